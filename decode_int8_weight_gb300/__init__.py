@@ -1,0 +1,253 @@
+"""Python binding of libq3i8.so: int8 weight-only Qwen3-family decode on GB300.
+
+Argument marshalling only.  Every step of the decode path runs in the CUDA
+kernels of ``libq3i8.so`` (built in-tree by ``build.py``); there is no CPU or
+PyTorch fallback.  If the library is missing, importing its functions raises.
+
+The call surface mirrors the C ABI in ``include/q3i8.h``:
+
+* ``Decoder(model, max_batch, max_ctx)``          -> ``q3i8_init``
+* ``Decoder.decode(prompts, max_new_tokens)``     -> ``q3i8_decode`` (host ids)
+* ``Decoder.decode_device(ids, lens, n, out)``    -> ``q3i8_decode_device``
+* ``Decoder.prefill`` / ``Decoder.step_logits``   -> teacher-forced checking
+* ``validate_dims``                               -> ``q3i8_validate_dims``
+* ``op_attention``                                -> ``q3i8_op_attention``
+
+A model is any object with ``shape`` (hidden, n_layers, n_heads, n_kv_heads,
+head_dim, intermediate, vocab, rope_theta, rms_eps), ``embed.q``/``embed.s``,
+``final_norm`` and ``layers[i]`` holding ``wq wk wv wo wg wu wd`` (each with
+int8 ``q`` [out, in] and fp32 ``s`` [out]) and the gains ``attn_norm
+ffn_norm q_norm k_norm``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libq3i8.so")
+
+STATUS = {0: "ok", 1: "unsupported_architecture", 2: "invalid_arguments", 3: "context_past_ceiling",
+          4: "no_device", 5: "out_of_memory", 6: "cuda_error", 7: "device_wait_timeout", 8: "invalid_state"}
+
+EXPORTS = ["q3i8_validate_dims", "q3i8_init", "q3i8_decode", "q3i8_decode_device", "q3i8_prefill",
+           "q3i8_step_logits", "q3i8_read_kv", "q3i8_step_bytes", "q3i8_step_launches", "q3i8_last_error",
+           "q3i8_status_name", "q3i8_destroy", "q3i8_op_attention_workspace", "q3i8_op_attention"]
+
+
+class Q3Error(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"{STATUS.get(code, code)}: {msg}")
+        self.code = code
+        self.status = STATUS.get(code, str(code))
+
+
+class Dims(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in
+                ("hidden", "n_layers", "n_heads", "n_kv_heads", "head_dim", "intermediate", "vocab")] + \
+               [("rope_theta", ctypes.c_float), ("rms_eps", ctypes.c_float)] + \
+               [(n, ctypes.c_int32) for n in ("max_batch", "max_ctx", "tie_word_embeddings", "attention_bias")]
+
+
+class Mat(ctypes.Structure):
+    _fields_ = [("w", ctypes.c_void_p), ("scale", ctypes.c_void_p)]
+
+
+class Layer(ctypes.Structure):
+    _fields_ = [(n, Mat) for n in ("q", "k", "v", "o", "gate", "up", "down")] + \
+               [(n, ctypes.c_void_p) for n in ("attn_norm", "ffn_norm", "q_norm", "k_norm")]
+
+
+class Stats(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_double) for n in ("prefill_ms", "decode_ms", "prefill_tokens_per_sec",
+                                               "decode_tokens_per_sec", "step_us")] + \
+               [("prefill_tokens", ctypes.c_int64), ("decode_steps", ctypes.c_int64)]
+
+    def as_dict(self):
+        return {f: getattr(self, f) for f, _ in self._fields_}
+
+
+_lib = None
+_lock = threading.Lock()
+
+
+def lib():
+    """The loaded libq3i8.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise ImportError(f"libq3i8.so is not built ({LIB_PATH}); run "
+                                  "`python -m decode_int8_weight_gb300.build`")
+            L = ctypes.CDLL(LIB_PATH)
+            vp, i32, i64, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+            L.q3i8_validate_dims.argtypes = [ctypes.POINTER(Dims), ctypes.c_char_p, sz]
+            L.q3i8_init.argtypes = [ctypes.POINTER(Dims), ctypes.POINTER(Mat), ctypes.POINTER(Layer), vp, vp,
+                                    ctypes.POINTER(vp)]
+            L.q3i8_decode.argtypes = [vp, i32, ctypes.POINTER(vp), vp, i32, i32, vp, vp, ctypes.POINTER(Stats)]
+            L.q3i8_decode_device.argtypes = [vp, i32, vp, vp, i32, vp, ctypes.POINTER(Stats)]
+            L.q3i8_prefill.argtypes = [vp, i32, ctypes.POINTER(vp), vp, vp]
+            L.q3i8_step_logits.argtypes = [vp, vp, vp]
+            L.q3i8_read_kv.argtypes = [vp, i32, i32, i32, vp, vp]
+            L.q3i8_step_bytes.restype = i64
+            L.q3i8_step_bytes.argtypes = [vp, i32, vp]
+            L.q3i8_step_launches.restype = i32
+            L.q3i8_step_launches.argtypes = [vp, i32]
+            L.q3i8_last_error.restype = ctypes.c_char_p
+            L.q3i8_last_error.argtypes = [vp]
+            L.q3i8_status_name.restype = ctypes.c_char_p
+            L.q3i8_status_name.argtypes = [ctypes.c_int]
+            L.q3i8_destroy.argtypes = [vp]
+            L.q3i8_op_attention_workspace.restype = sz
+            L.q3i8_op_attention_workspace.argtypes = [i32, i32, i32, i32]
+            L.q3i8_op_attention.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, vp, vp, sz, vp, vp]
+            _lib = L
+    return _lib
+
+
+def _check(rc: int, ctx=None):
+    if rc != 0:
+        raise Q3Error(rc, lib().q3i8_last_error(ctx).decode(errors="replace"))
+
+
+def _p(a: np.ndarray):
+    assert a.flags["C_CONTIGUOUS"]
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def make_dims(shape, max_batch: int = 1, max_ctx: int = 0, tie_word_embeddings: int = 1,
+              attention_bias: int = 0) -> Dims:
+    return Dims(shape.hidden, shape.n_layers, shape.n_heads, shape.n_kv_heads, shape.head_dim, shape.intermediate,
+                shape.vocab, shape.rope_theta, shape.rms_eps, max_batch, max_ctx, tie_word_embeddings,
+                attention_bias)
+
+
+def validate_dims(dims: Dims):
+    """(status, message) of the host-only architecture check (no GPU needed)."""
+    buf = ctypes.create_string_buffer(2048)
+    rc = lib().q3i8_validate_dims(ctypes.byref(dims), buf, len(buf))
+    return rc, buf.value.decode()
+
+
+def _tptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else None
+
+
+class Decoder:
+    """One q3i8 context: weights resident on the current CUDA device."""
+
+    def __init__(self, model, max_batch: int = 1, max_ctx: int = 0, stream=None):
+        sh = model.shape
+        self.shape = sh
+        self.max_batch = max_batch
+        dims = make_dims(sh, max_batch, max_ctx)
+        keep = []
+
+        def mat(m):
+            q = np.ascontiguousarray(m.q, np.int8)
+            s = np.ascontiguousarray(m.s, np.float32)
+            keep.extend([q, s])
+            return Mat(q.ctypes.data, s.ctypes.data)
+
+        def vec(a):
+            a = np.ascontiguousarray(a, np.float32)
+            keep.append(a)
+            return a.ctypes.data
+
+        layers = (Layer * sh.n_layers)()
+        for i, ly in enumerate(model.layers):
+            layers[i] = Layer(mat(ly.wq), mat(ly.wk), mat(ly.wv), mat(ly.wo), mat(ly.wg), mat(ly.wu), mat(ly.wd),
+                              vec(ly.attn_norm), vec(ly.ffn_norm), vec(ly.q_norm), vec(ly.k_norm))
+        emb = mat(model.embed)
+        fin = vec(model.final_norm)
+        h = ctypes.c_void_p()
+        rc = lib().q3i8_init(ctypes.byref(dims), ctypes.byref(emb), layers, ctypes.c_void_p(fin),
+                             ctypes.c_void_p(stream) if stream else None, ctypes.byref(h))
+        _check(rc, None)
+        self._h = h
+        del keep  # weights were copied to the device
+
+    def close(self):
+        if getattr(self, "_h", None):
+            lib().q3i8_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def _prompts(self, prompts):
+        arrs = [np.ascontiguousarray(p, np.int32) for p in prompts]
+        ptrs = (ctypes.c_void_p * len(arrs))(*[a.ctypes.data for a in arrs])
+        lens = np.array([a.size for a in arrs], np.int32)
+        return arrs, ptrs, lens
+
+    def decode(self, prompts, max_new_tokens: int, eos_id: int = -1):
+        """Greedy decode (host buffers).  Returns (ids [B, max_new], counts [B], stats dict)."""
+        arrs, ptrs, lens = self._prompts(prompts)
+        B = len(arrs)
+        out = np.zeros((B, max_new_tokens), np.int32)
+        counts = np.zeros(B, np.int32)
+        st = Stats()
+        rc = lib().q3i8_decode(self._h, B, ptrs, _p(lens), max_new_tokens, eos_id, _p(out), _p(counts),
+                               ctypes.byref(st))
+        _check(rc, self._h)
+        return out, counts, st.as_dict()
+
+    def decode_device(self, d_ids, lens, max_new_tokens: int, d_out):
+        """Greedy decode on device buffers (torch int32 CUDA tensors).  Returns stats."""
+        lens = np.ascontiguousarray(lens, np.int32)
+        st = Stats()
+        rc = lib().q3i8_decode_device(self._h, lens.size, _tptr(d_ids), _p(lens), max_new_tokens, _tptr(d_out),
+                                      ctypes.byref(st))
+        _check(rc, self._h)
+        return st.as_dict()
+
+    def prefill(self, prompts, want_logits: bool = True):
+        arrs, ptrs, lens = self._prompts(prompts)
+        out = np.zeros((len(arrs), self.shape.vocab), np.float32) if want_logits else None
+        rc = lib().q3i8_prefill(self._h, len(arrs), ptrs, _p(lens), _p(out) if out is not None else None)
+        _check(rc, self._h)
+        return out
+
+    def step_logits(self, tokens):
+        tokens = np.ascontiguousarray(tokens, np.int32)
+        out = np.zeros((tokens.size, self.shape.vocab), np.float32)
+        rc = lib().q3i8_step_logits(self._h, _p(tokens), _p(out))
+        _check(rc, self._h)
+        return out
+
+    def read_kv(self, layer: int, seq: int, n_pos: int):
+        sh = self.shape
+        k = np.zeros((sh.n_kv_heads, n_pos, sh.head_dim), np.uint16)
+        v = np.zeros_like(k)
+        _check(lib().q3i8_read_kv(self._h, layer, seq, n_pos, _p(k), _p(v)), self._h)
+        return k, v
+
+    def step_bytes(self, positions) -> int:
+        positions = np.ascontiguousarray(positions, np.int32)
+        return int(lib().q3i8_step_bytes(self._h, positions.size, _p(positions)))
+
+    def step_launches(self, B: int) -> int:
+        return int(lib().q3i8_step_launches(self._h, B))
+
+
+def op_attention_workspace(R: int, n_heads: int, hd: int, splits: int) -> int:
+    return int(lib().q3i8_op_attention_workspace(R, n_heads, hd, splits))
+
+
+def op_attention(q, k, v, row_seq, row_len, n_kv_heads: int, splits: int, out, workspace, status=None,
+                 stream=None):
+    """Split-KV decode attention on torch CUDA tensors (see q3i8_op_attention)."""
+    R, nh, hd = q.shape
+    cap = k.shape[2]
+    rc = lib().q3i8_op_attention(_tptr(q), _tptr(k), _tptr(v), _tptr(row_seq), _tptr(row_len), R, nh, n_kv_heads,
+                                 hd, cap, splits, _tptr(out), _tptr(workspace),
+                                 workspace.numel() * workspace.element_size(), _tptr(status),
+                                 ctypes.c_void_p(stream) if stream else None)
+    _check(rc, None)

@@ -1,0 +1,807 @@
+// q3i8 engine: the C ABI of include/q3i8.h on one GB300 (sm_103a).
+//
+// Owns the device copies of the weights (repacked at init), the bf16 KV
+// cache, the per-step device state (tokens, positions, step counter) and
+// one captured CUDA graph per batch size for the decode step.  The decode
+// loop replays that graph; next-token ids and positions stay on the device,
+// so nothing crosses to the host between steps.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <map>
+#include <string>
+#include <thread>
+#include <vector>
+
+#include "../../include/q3i8.h"
+#include "engine.h"
+#include "kernels.h"
+
+using namespace q3;
+
+static thread_local std::string g_tls_error;
+
+static int fail(q3i8_ctx* c, int code, const char* fmt, ...) {
+    char buf[1024];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    if (c) c->err = buf;
+    else g_tls_error = buf;
+    return code;
+}
+
+#define CK(c, call)                                                                                     \
+    do {                                                                                                \
+        cudaError_t e_ = (call);                                                                        \
+        if (e_ != cudaSuccess) {                                                                        \
+            int code_ = (e_ == cudaErrorMemoryAllocation) ? Q3_ERR_OOM : Q3_ERR_CUDA;                   \
+            return fail((c), code_, "%s failed: %s (%s:%d)", #call, cudaGetErrorString(e_), __FILE__,   \
+                        __LINE__);                                                                      \
+        }                                                                                               \
+    } while (0)
+
+// ------------------------------------------------------------------ validation
+
+extern "C" int q3i8_validate_dims(const q3i8_dims* d, char* msg, size_t msg_cap) {
+    std::string m;
+    int code = Q3_OK;
+    auto add = [&](int c, const std::string& s) {
+        if (!m.empty()) m += "; ";
+        m += s;
+        if (code == Q3_OK || c == Q3_ERR_INVALID_ARGUMENTS) code = c;
+    };
+    if (!d) {
+        add(Q3_ERR_INVALID_ARGUMENTS, "dims is NULL");
+    } else {
+        const int pos[] = {d->hidden, d->n_layers, d->n_heads, d->n_kv_heads, d->head_dim, d->intermediate, d->vocab};
+        const char* names[] = {"hidden", "n_layers", "n_heads", "n_kv_heads", "head_dim", "intermediate", "vocab"};
+        bool sizes_ok = true;
+        for (int i = 0; i < 7; ++i)
+            if (pos[i] <= 0) {
+                add(Q3_ERR_INVALID_ARGUMENTS, std::string(names[i]) + " must be positive");
+                sizes_ok = false;
+            }
+        if (sizes_ok) {
+            if (d->n_heads % d->n_kv_heads != 0)
+                add(Q3_ERR_UNSUPPORTED_ARCH, "GQA: n_heads (" + std::to_string(d->n_heads) +
+                                                 ") is not a multiple of n_kv_heads (" +
+                                                 std::to_string(d->n_kv_heads) + ")");
+            if (d->hidden % 32 != 0) add(Q3_ERR_UNSUPPORTED_ARCH, "tile alignment: hidden % 32 != 0");
+            if (d->intermediate % 32 != 0) add(Q3_ERR_UNSUPPORTED_ARCH, "tile alignment: intermediate % 32 != 0");
+            if ((d->n_heads * d->head_dim) % 32 != 0)
+                add(Q3_ERR_UNSUPPORTED_ARCH, "tile alignment: n_heads*head_dim % 32 != 0");
+            if (d->head_dim != 64 && d->head_dim != 128)
+                add(Q3_ERR_UNSUPPORTED_ARCH, "head_dim must be 64 or 128 for these kernels");
+            if (d->n_heads % d->n_kv_heads == 0) {
+                int gq = d->n_heads / d->n_kv_heads;
+                if (gq != 1 && gq != 2 && gq != 4 && gq != 8)
+                    add(Q3_ERR_UNSUPPORTED_ARCH, "n_heads/n_kv_heads must be 1, 2, 4 or 8 for these kernels");
+            }
+            if (d->hidden > 16384 || d->intermediate > 65536)
+                add(Q3_ERR_UNSUPPORTED_ARCH, "hidden above 16384 or intermediate above 65536");
+        }
+        if (d->tie_word_embeddings != 1) add(Q3_ERR_UNSUPPORTED_ARCH, "embeddings: tie_word_embeddings must be true");
+        if (d->attention_bias != 0) add(Q3_ERR_UNSUPPORTED_ARCH, "bias: attention bias is not supported");
+        if (!(d->rope_theta > 0.f)) add(Q3_ERR_INVALID_ARGUMENTS, "rope_theta must be positive");
+        if (!(d->rms_eps >= 0.f)) add(Q3_ERR_INVALID_ARGUMENTS, "rms_eps must be >= 0");
+        if (d->max_batch < 1 || d->max_batch > kMaxBatch)
+            add(Q3_ERR_INVALID_ARGUMENTS, "max_batch must be in [1, " + std::to_string(kMaxBatch) + "]");
+        if (d->max_ctx < 0 || d->max_ctx > kCtxCeiling)
+            add(Q3_ERR_CONTEXT, "max_ctx must be in [0, " + std::to_string(kCtxCeiling) + "]");
+    }
+    if (msg && msg_cap) {
+        snprintf(msg, msg_cap, "%s", m.c_str());
+    }
+    return code;
+}
+
+// ------------------------------------------------------------------ weights
+
+// [rows][K] int8 (row-major) -> fragment-order bytes (q + 128).
+static void pack_fragments(const int8_t* w, int rows, int K, uint8_t* out) {
+    const int tiles = rows / 16, pairs = K / 32;
+    auto work = [&](int t0, int t1) {
+        for (int tile = t0; tile < t1; ++tile)
+            for (int p = 0; p < pairs; ++p)
+                for (int lane = 0; lane < 32; ++lane) {
+                    const int g = lane >> 2, t = lane & 3;
+                    uint8_t* dst = out + (size_t)tile * 16 * K + (size_t)p * 512 + lane * 16;
+                    for (int ks = 0; ks < 2; ++ks) {
+                        const int k0 = p * 32 + ks * 16 + 2 * t;
+                        const int8_t* r0 = w + (size_t)(tile * 16 + g) * K;
+                        const int8_t* r8 = w + (size_t)(tile * 16 + g + 8) * K;
+                        const int8_t v[8] = {r0[k0], r0[k0 + 1], r8[k0], r8[k0 + 1],
+                                             r0[k0 + 8], r0[k0 + 9], r8[k0 + 8], r8[k0 + 9]};
+                        for (int j = 0; j < 8; ++j) dst[ks * 8 + j] = (uint8_t)((int)v[j] + 128);
+                    }
+                }
+    };
+    unsigned nt = std::max(1u, std::min(16u, std::thread::hardware_concurrency()));
+    if (tiles < 64) nt = 1;
+    std::vector<std::thread> th;
+    for (unsigned i = 0; i < nt; ++i) {
+        int t0 = (int)((long long)tiles * i / nt), t1 = (int)((long long)tiles * (i + 1) / nt);
+        th.emplace_back(work, t0, t1);
+    }
+    for (auto& x : th) x.join();
+}
+
+// Upload one (possibly fused) matrix given as host row blocks.
+int upload_matrix(q3i8_ctx* c, const std::vector<const int8_t*>& row_src, const std::vector<float>& scales, int K,
+                  int pad_rows, DevMat* m) {
+    const int rows = (int)row_src.size();
+    const int prow = ((rows + pad_rows - 1) / pad_rows) * pad_rows;
+    std::vector<int8_t> raw((size_t)prow * K, 0);
+    for (int r = 0; r < rows; ++r) memcpy(&raw[(size_t)r * K], row_src[r], K);
+    std::vector<float> sc(prow, 0.f);
+    std::copy(scales.begin(), scales.end(), sc.begin());
+    std::vector<uint8_t> frag((size_t)prow * K);
+    pack_fragments(raw.data(), prow, K, frag.data());
+    m->rows = prow;
+    m->valid_rows = rows;
+    m->cols = K;
+    CK(c, cudaMalloc(&m->raw, (size_t)prow * K));
+    CK(c, cudaMalloc(&m->frag, (size_t)prow * K));
+    CK(c, cudaMalloc(&m->scale, (size_t)prow * sizeof(float)));
+    CK(c, cudaMemcpy(m->raw, raw.data(), raw.size(), cudaMemcpyHostToDevice));
+    CK(c, cudaMemcpy(m->frag, frag.data(), frag.size(), cudaMemcpyHostToDevice));
+    CK(c, cudaMemcpy(m->scale, sc.data(), sc.size() * sizeof(float), cudaMemcpyHostToDevice));
+    c->weight_bytes_dev += 2 * (size_t)prow * K + (size_t)prow * 4;
+    return Q3_OK;
+}
+
+static int upload_vec(q3i8_ctx* c, const float* h, int n, float** d) {
+    CK(c, cudaMalloc(d, (size_t)n * sizeof(float)));
+    CK(c, cudaMemcpy(*d, h, (size_t)n * sizeof(float), cudaMemcpyHostToDevice));
+    return Q3_OK;
+}
+
+static void free_mat(DevMat& m) {
+    cudaFree(m.raw);
+    cudaFree(m.frag);
+    cudaFree(m.scale);
+    m = DevMat{};
+}
+
+// ------------------------------------------------------------------ buffers
+
+int ensure_capacity(q3i8_ctx* c, int need_ctx) {
+    if (need_ctx > kCtxCeiling)
+        return fail(c, Q3_ERR_CONTEXT, "context of %d positions exceeds the %d ceiling", need_ctx, kCtxCeiling);
+    int want = std::max(c->cap_request, need_ctx);
+    want = (want + kChunkPos - 1) / kChunkPos * kChunkPos;
+    if (c->kc && want <= c->cap) return Q3_OK;
+    drop_graphs(c);
+    cudaFree(c->kc);
+    cudaFree(c->vc);
+    cudaFree(c->rope);
+    c->kc = c->vc = nullptr;
+    c->rope = nullptr;
+    const q3i8_dims& d = c->d;
+    const size_t per = (size_t)d.n_layers * c->bmax * d.n_kv_heads * want * d.head_dim;
+    CK(c, cudaMalloc(&c->kc, per * 2));
+    CK(c, cudaMalloc(&c->vc, per * 2));
+    CK(c, cudaMemsetAsync(c->kc, 0, per * 2, c->stream));
+    CK(c, cudaMemsetAsync(c->vc, 0, per * 2, c->stream));
+    // RoPE table: frequency, angle, cos and sin in double, rounded to fp32
+    const int half = d.head_dim / 2;
+    std::vector<float2> tab((size_t)want * half);
+    for (int i = 0; i < half; ++i) {
+        const double freq = pow((double)d.rope_theta, -2.0 * (double)i / (double)d.head_dim);
+        for (int p = 0; p < want; ++p) {
+            const double ang = (double)p * freq;
+            tab[(size_t)p * half + i] = make_float2((float)cos(ang), (float)sin(ang));
+        }
+    }
+    CK(c, cudaMalloc(&c->rope, tab.size() * sizeof(float2)));
+    CK(c, cudaMemcpy(c->rope, tab.data(), tab.size() * sizeof(float2), cudaMemcpyHostToDevice));
+    c->cap = want;
+    return Q3_OK;
+}
+
+static int ensure_out(q3i8_ctx* c, int out_cap) {
+    if (c->out_ids && out_cap <= c->out_cap) return Q3_OK;
+    drop_graphs(c);
+    cudaFree(c->out_ids);
+    c->out_ids = nullptr;
+    int cap = std::max(out_cap, 256);
+    CK(c, cudaMalloc(&c->out_ids, (size_t)c->bmax * cap * sizeof(int32_t)));
+    c->out_cap = cap;
+    return Q3_OK;
+}
+
+static int ensure_prefill(q3i8_ctx* c, int M) {
+    if (M <= c->pf_rows) return Q3_OK;
+    const q3i8_dims& d = c->d;
+    const int H = d.hidden, I = d.intermediate, Dq = d.n_heads * d.head_dim, Dkv = d.n_kv_heads * d.head_dim;
+    for (float** p : {&c->pf_x, &c->pf_xn, &c->pf_qkv, &c->pf_q, &c->pf_o, &c->pf_y, &c->pf_gu, &c->pf_a, &c->pf_part})
+        cudaFree(*p), *p = nullptr;
+    cudaFree(c->pf_ids);
+    cudaFree(c->pf_seq);
+    cudaFree(c->pf_pos);
+    c->pf_rows = 0;
+    const size_t m = (size_t)M;
+    CK(c, cudaMalloc(&c->pf_x, m * H * 4));
+    CK(c, cudaMalloc(&c->pf_xn, m * std::max(H, I) * 4));
+    CK(c, cudaMalloc(&c->pf_qkv, m * (Dq + 2 * Dkv) * 4));
+    CK(c, cudaMalloc(&c->pf_q, m * Dq * 4));
+    CK(c, cudaMalloc(&c->pf_o, m * Dq * 4));
+    CK(c, cudaMalloc(&c->pf_y, m * H * 4));
+    CK(c, cudaMalloc(&c->pf_gu, m * 2 * I * 4));
+    CK(c, cudaMalloc(&c->pf_a, m * I * 4));
+    CK(c, cudaMalloc(&c->pf_part, attn_part_bytes(M, d.n_heads, d.head_dim, 1)));
+    CK(c, cudaMalloc(&c->pf_ids, m * 4));
+    CK(c, cudaMalloc(&c->pf_seq, m * 4));
+    CK(c, cudaMalloc(&c->pf_pos, m * 4));
+    c->pf_rows = M;
+    return Q3_OK;
+}
+
+void drop_graphs(q3i8_ctx* c) {
+    for (auto& kv : c->graphs) cudaGraphExecDestroy(kv.second);
+    c->graphs.clear();
+}
+
+// ------------------------------------------------------------------ init / destroy
+
+extern "C" int q3i8_init(const q3i8_dims* dims, const q3i8_mat* embed, const q3i8_layer* layers,
+                         const float* final_norm, void* cuda_stream, q3i8_ctx** out) {
+    if (out) *out = nullptr;
+    char msg[1024];
+    int rc = q3i8_validate_dims(dims, msg, sizeof msg);
+    if (rc != Q3_OK) return fail(nullptr, rc, "%s", msg);
+    if (!embed || !embed->w || !embed->scale || !layers || !final_norm || !out)
+        return fail(nullptr, Q3_ERR_INVALID_ARGUMENTS, "init: a required pointer is NULL");
+    for (int l = 0; l < dims->n_layers; ++l) {
+        const q3i8_layer& L = layers[l];
+        const q3i8_mat* ms[] = {&L.q, &L.k, &L.v, &L.o, &L.gate, &L.up, &L.down};
+        for (auto* m : ms)
+            if (!m->w || !m->scale) return fail(nullptr, Q3_ERR_INVALID_ARGUMENTS, "init: layer %d has a NULL matrix", l);
+        if (!L.attn_norm || !L.ffn_norm || !L.q_norm || !L.k_norm)
+            return fail(nullptr, Q3_ERR_INVALID_ARGUMENTS, "init: layer %d has a NULL norm gain", l);
+    }
+    int dev = 0, ndev = 0;
+    if (cudaGetDeviceCount(&ndev) != cudaSuccess || ndev == 0) {
+        cudaGetLastError();
+        return fail(nullptr, Q3_ERR_NO_DEVICE, "no CUDA device");
+    }
+    if (cudaGetDevice(&dev) != cudaSuccess) return fail(nullptr, Q3_ERR_NO_DEVICE, "cudaGetDevice failed");
+    cudaDeviceProp prop;
+    if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return fail(nullptr, Q3_ERR_NO_DEVICE, "no device properties");
+    if (!(prop.major == 10 && prop.minor == 3))
+        return fail(nullptr, Q3_ERR_NO_DEVICE, "device %s is sm_%d%d; this library is built for sm_103a", prop.name,
+                    prop.major, prop.minor);
+
+    q3i8_ctx* c = new q3i8_ctx();
+    c->d = *dims;
+    c->dev = dev;
+    c->num_sms = prop.multiProcessorCount;
+    c->bmax = dims->max_batch;
+    c->cap_request = dims->max_ctx > 0 ? dims->max_ctx : 512;
+    if (cuda_stream) {
+        c->stream = (cudaStream_t)cuda_stream;
+    } else {
+        if (cudaStreamCreateWithFlags(&c->stream, cudaStreamNonBlocking) != cudaSuccess) {
+            delete c;
+            return fail(nullptr, Q3_ERR_CUDA, "cudaStreamCreate failed");
+        }
+        c->own_stream = true;
+    }
+    rc = init_weights(c, embed, layers, final_norm);
+    if (rc == Q3_OK) rc = init_state(c);
+    if (rc == Q3_OK) rc = ensure_capacity(c, c->cap_request);
+    if (rc == Q3_OK) rc = ensure_out(c, 256);
+    if (rc == Q3_OK && cudaStreamSynchronize(c->stream) != cudaSuccess) rc = fail(c, Q3_ERR_CUDA, "init sync failed");
+    if (rc != Q3_OK) {
+        g_tls_error = c->err;
+        q3i8_destroy(c);
+        return rc;
+    }
+    *out = c;
+    return Q3_OK;
+}
+
+int init_weights(q3i8_ctx* c, const q3i8_mat* embed, const q3i8_layer* layers, const float* final_norm) {
+    const q3i8_dims& d = c->d;
+    const int H = d.hidden, I = d.intermediate, hd = d.head_dim;
+    const int Dq = d.n_heads * hd, Dkv = d.n_kv_heads * hd;
+    {
+        std::vector<const int8_t*> rows(d.vocab);
+        for (int r = 0; r < d.vocab; ++r) rows[r] = embed->w + (size_t)r * H;
+        std::vector<float> sc(embed->scale, embed->scale + d.vocab);
+        int rc = upload_matrix(c, rows, sc, H, 16, &c->embed);
+        if (rc) return rc;
+    }
+    int rc = upload_vec(c, final_norm, H, &c->final_norm);
+    if (rc) return rc;
+    c->layers.resize(d.n_layers);
+    for (int l = 0; l < d.n_layers; ++l) {
+        const q3i8_layer& L = layers[l];
+        DevLayer& D = c->layers[l];
+        std::vector<const int8_t*> rows;
+        std::vector<float> sc;
+        // fused QKV: rows of Wq, then Wk, then Wv
+        for (int r = 0; r < Dq; ++r) rows.push_back(L.q.w + (size_t)r * H), sc.push_back(L.q.scale[r]);
+        for (int r = 0; r < Dkv; ++r) rows.push_back(L.k.w + (size_t)r * H), sc.push_back(L.k.scale[r]);
+        for (int r = 0; r < Dkv; ++r) rows.push_back(L.v.w + (size_t)r * H), sc.push_back(L.v.scale[r]);
+        if ((rc = upload_matrix(c, rows, sc, H, 16, &D.qkv))) return rc;
+        rows.clear(), sc.clear();
+        for (int r = 0; r < H; ++r) rows.push_back(L.o.w + (size_t)r * Dq), sc.push_back(L.o.scale[r]);
+        if ((rc = upload_matrix(c, rows, sc, Dq, 16, &D.o))) return rc;
+        rows.clear(), sc.clear();
+        // fused gate/up: blocks of 16 rows = 8 gate units then the same 8 up units
+        for (int j = 0; j < I / 8; ++j) {
+            for (int r = 0; r < 8; ++r) rows.push_back(L.gate.w + (size_t)(8 * j + r) * H), sc.push_back(L.gate.scale[8 * j + r]);
+            for (int r = 0; r < 8; ++r) rows.push_back(L.up.w + (size_t)(8 * j + r) * H), sc.push_back(L.up.scale[8 * j + r]);
+        }
+        if ((rc = upload_matrix(c, rows, sc, H, 16, &D.gu))) return rc;
+        rows.clear(), sc.clear();
+        for (int r = 0; r < H; ++r) rows.push_back(L.down.w + (size_t)r * I), sc.push_back(L.down.scale[r]);
+        if ((rc = upload_matrix(c, rows, sc, I, 16, &D.down))) return rc;
+        if ((rc = upload_vec(c, L.attn_norm, H, &D.attn_norm))) return rc;
+        if ((rc = upload_vec(c, L.ffn_norm, H, &D.ffn_norm))) return rc;
+        if ((rc = upload_vec(c, L.q_norm, hd, &D.q_norm))) return rc;
+        if ((rc = upload_vec(c, L.k_norm, hd, &D.k_norm))) return rc;
+    }
+    return Q3_OK;
+}
+
+int init_state(q3i8_ctx* c) {
+    const q3i8_dims& d = c->d;
+    const int H = d.hidden, I = d.intermediate, Dq = d.n_heads * d.head_dim, Dkv = d.n_kv_heads * d.head_dim;
+    const int B = c->bmax, cols = 8 * ((B + 3) / 4);
+    CK(c, cudaMalloc(&c->tokens, B * 4));
+    CK(c, cudaMalloc(&c->pos, B * 4));
+    CK(c, cudaMalloc(&c->seq_ids, B * 4));
+    CK(c, cudaMalloc(&c->step, 4));
+    CK(c, cudaMalloc(&c->keys, B * 8));
+    CK(c, cudaMalloc(&c->counter, 4));
+    CK(c, cudaMalloc(&c->status, 4));
+    CK(c, cudaMalloc(&c->x, (size_t)B * H * 4));
+    CK(c, cudaMalloc(&c->qkv, (size_t)B * (Dq + 2 * Dkv) * 4));
+    CK(c, cudaMalloc(&c->qr, (size_t)B * Dq * 4));
+    c->dec_splits_max = 64;
+    CK(c, cudaMalloc(&c->part, attn_part_bytes(B, d.n_heads, d.head_dim, c->dec_splits_max)));
+    const int K = std::max(std::max(H, I), Dq);
+    CK(c, cudaMalloc(&c->xh, (size_t)cols * K * 2));
+    CK(c, cudaMalloc(&c->oh, (size_t)cols * Dq * 2));
+    CK(c, cudaMalloc(&c->ah, (size_t)cols * I * 2));
+    CK(c, cudaMalloc(&c->logits, (size_t)B * d.vocab * 4));
+    CK(c, cudaMemsetAsync(c->xh, 0, (size_t)cols * K * 2, c->stream));
+    CK(c, cudaMemsetAsync(c->oh, 0, (size_t)cols * Dq * 2, c->stream));
+    CK(c, cudaMemsetAsync(c->ah, 0, (size_t)cols * I * 2, c->stream));
+    CK(c, cudaMemsetAsync(c->keys, 0, B * 8, c->stream));
+    CK(c, cudaMemsetAsync(c->counter, 0, 4, c->stream));
+    CK(c, cudaMemsetAsync(c->status, 0, 4, c->stream));
+    CK(c, cudaMemsetAsync(c->step, 0, 4, c->stream));
+    std::vector<int32_t> ids(B);
+    for (int b = 0; b < B; ++b) ids[b] = b;
+    CK(c, cudaMemcpy(c->seq_ids, ids.data(), B * 4, cudaMemcpyHostToDevice));
+    return Q3_OK;
+}
+
+extern "C" void q3i8_destroy(q3i8_ctx* c) {
+    if (!c) return;
+    cudaStreamSynchronize(c->stream);
+    drop_graphs(c);
+    free_mat(c->embed);
+    for (auto& L : c->layers) {
+        free_mat(L.qkv), free_mat(L.o), free_mat(L.gu), free_mat(L.down);
+        cudaFree(L.attn_norm), cudaFree(L.ffn_norm), cudaFree(L.q_norm), cudaFree(L.k_norm);
+    }
+    void* ptrs[] = {c->final_norm, c->kc, c->vc, c->rope, c->tokens, c->pos, c->seq_ids, c->step, c->keys,
+                    c->counter, c->status, c->x, c->qkv, c->qr, c->part, c->xh, c->oh, c->ah, c->logits,
+                    c->out_ids, c->pf_x, c->pf_xn, c->pf_qkv, c->pf_q, c->pf_o, c->pf_y, c->pf_gu, c->pf_a,
+                    c->pf_part, c->pf_ids, c->pf_seq, c->pf_pos, c->pf_last};
+    for (void* p : ptrs) cudaFree(p);
+    if (c->ev0) cudaEventDestroy(c->ev0);
+    if (c->ev1) cudaEventDestroy(c->ev1);
+    if (c->ev2) cudaEventDestroy(c->ev2);
+    if (c->own_stream) cudaStreamDestroy(c->stream);
+    delete c;
+}
+
+// ------------------------------------------------------------------ the decode step
+
+int decode_splits(const q3i8_ctx* c, int B) {
+    int s = (2 * c->num_sms + B * c->d.n_kv_heads - 1) / (B * c->d.n_kv_heads);
+    s = std::min(s, c->cap / kChunkPos);
+    s = std::min(s, c->dec_splits_max);
+    return std::max(s, 1);
+}
+
+// Enqueue one decode step for B sequences: tokens[b] at positions pos[b].
+void enqueue_step(q3i8_ctx* c, int B, bool want_logits) {
+    const q3i8_dims& d = c->d;
+    const int H = d.hidden, I = d.intermediate, hd = d.head_dim, nh = d.n_heads, nkv = d.n_kv_heads;
+    const int Dq = nh * hd;
+    const size_t layer_kv = (size_t)c->bmax * nkv * c->cap * hd;
+    cudaStream_t st = c->stream;
+    const int splits = decode_splits(c, B);
+
+    launch_embed(c->tokens, B, c->embed.raw, c->embed.scale, H, c->x, st);
+    launch_rmsnorm(c->x, nullptr, B, H, c->layers[0].attn_norm, d.rms_eps, nullptr, c->xh, st);
+    for (int l = 0; l < d.n_layers; ++l) {
+        const DevLayer& L = c->layers[l];
+        GemvArgs a{};
+        a.B = B;
+        a.w = L.qkv.frag, a.scale = L.qkv.scale, a.rows = L.qkv.rows, a.K = H, a.xh = c->xh;
+        a.y = c->qkv, a.ldy = L.qkv.rows;
+        launch_gemv(a, kStore, gemv_grid(a.rows, kStore, c->num_sms), st);
+        launch_qk_rope_append(c->qkv, B, nh, nkv, hd, c->seq_ids, c->pos, L.q_norm, L.k_norm, d.rms_eps, c->rope,
+                              c->qr, c->kc + l * layer_kv, c->vc + l * layer_kv, c->cap, st);
+        launch_attention(c->qr, c->kc + l * layer_kv, c->vc + l * layer_kv, c->seq_ids, c->pos, 1, B, nh, nkv, hd,
+                         c->cap, splits, c->part, nullptr, c->oh, Dq, c->status, st);
+        a = GemvArgs{};
+        a.B = B;
+        a.w = L.o.frag, a.scale = L.o.scale, a.rows = L.o.rows, a.K = Dq, a.xh = c->oh;
+        a.y = c->x, a.ldy = H;
+        launch_gemv(a, kResid, gemv_grid(a.rows, kResid, c->num_sms), st);
+        launch_rmsnorm(c->x, nullptr, B, H, L.ffn_norm, d.rms_eps, nullptr, c->xh, st);
+        a = GemvArgs{};
+        a.B = B;
+        a.w = L.gu.frag, a.scale = L.gu.scale, a.rows = L.gu.rows, a.K = H, a.xh = c->xh;
+        a.yh = c->ah, a.ldyh = I;
+        launch_gemv(a, kSiluGate, gemv_grid(a.rows, kSiluGate, c->num_sms), st);
+        a = GemvArgs{};
+        a.B = B;
+        a.w = L.down.frag, a.scale = L.down.scale, a.rows = L.down.rows, a.K = I, a.xh = c->ah;
+        a.y = c->x, a.ldy = H;
+        launch_gemv(a, kResid, gemv_grid(a.rows, kResid, c->num_sms), st);
+        const float* g_next = (l + 1 < d.n_layers) ? c->layers[l + 1].attn_norm : c->final_norm;
+        launch_rmsnorm(c->x, nullptr, B, H, g_next, d.rms_eps, nullptr, c->xh, st);
+    }
+    enqueue_lm_head(c, B, true, want_logits ? c->logits : nullptr);
+}
+
+void enqueue_lm_head(q3i8_ctx* c, int B, bool advance_pos, float* logits) {
+    GemvArgs a{};
+    a.B = B;
+    a.w = c->embed.frag, a.scale = c->embed.scale, a.rows = c->embed.rows, a.K = c->d.hidden, a.xh = c->xh;
+    a.keys = c->keys, a.counter = c->counter, a.tokens = c->tokens, a.out_ids = c->out_ids, a.step = c->step;
+    a.out_cap = c->out_cap, a.pos = c->pos, a.advance_pos = advance_pos ? 1 : 0;
+    a.valid_rows = c->embed.valid_rows, a.logits = logits;
+    launch_gemv(a, kArgmax, gemv_grid(a.rows, kArgmax, c->num_sms), c->stream);
+}
+
+int step_launches(const q3i8_ctx* c) { return 2 + c->d.n_layers * 9 + 1; }
+
+// Graph of one decode step at batch B (captured on first use).
+static int get_graph(q3i8_ctx* c, int B, cudaGraphExec_t* out) {
+    auto it = c->graphs.find(B);
+    if (it != c->graphs.end()) {
+        *out = it->second;
+        return Q3_OK;
+    }
+    cudaGraph_t g;
+    CK(c, cudaStreamBeginCapture(c->stream, cudaStreamCaptureModeThreadLocal));
+    enqueue_step(c, B, false);
+    cudaError_t e = cudaStreamEndCapture(c->stream, &g);
+    if (e != cudaSuccess) return fail(c, Q3_ERR_CUDA, "graph capture failed: %s", cudaGetErrorString(e));
+    cudaGraphExec_t ex;
+    e = cudaGraphInstantiate(&ex, g, 0);
+    cudaGraphDestroy(g);
+    if (e != cudaSuccess) return fail(c, Q3_ERR_CUDA, "graph instantiate failed: %s", cudaGetErrorString(e));
+    c->graphs[B] = ex;
+    *out = ex;
+    return Q3_OK;
+}
+
+// ------------------------------------------------------------------ prefill
+
+// Prefill B prompts given back to back in device memory; leaves the first
+// generated token of each sequence in tokens[] / out_ids[:, 0] (step = 1)
+// and pos[b] = prompt length.
+static int run_prefill(q3i8_ctx* c, int B, const int32_t* d_ids, const int32_t* lens, float* d_logits) {
+    const q3i8_dims& d = c->d;
+    const int H = d.hidden, I = d.intermediate, hd = d.head_dim, nh = d.n_heads, nkv = d.n_kv_heads;
+    const int Dq = nh * hd, Dkv = nkv * hd;
+    int M = 0, maxlen = 0;
+    for (int b = 0; b < B; ++b) M += lens[b], maxlen = std::max(maxlen, lens[b]);
+    int rc = ensure_prefill(c, M);
+    if (rc) return rc;
+    cudaStream_t st = c->stream;
+    std::vector<int32_t> seq(M), pos(M), last(B), plen(lens, lens + B);
+    for (int b = 0, r = 0; b < B; ++b) {
+        for (int t = 0; t < lens[b]; ++t, ++r) seq[r] = b, pos[r] = t;
+        last[b] = r - 1;
+    }
+    if (!c->pf_last) CK(c, cudaMalloc(&c->pf_last, kMaxBatch * 4));
+    CK(c, cudaMemcpyAsync(c->pf_seq, seq.data(), M * 4, cudaMemcpyHostToDevice, st));
+    CK(c, cudaMemcpyAsync(c->pf_pos, pos.data(), M * 4, cudaMemcpyHostToDevice, st));
+    CK(c, cudaMemcpyAsync(c->pf_last, last.data(), B * 4, cudaMemcpyHostToDevice, st));
+    CK(c, cudaMemcpyAsync(c->pos, plen.data(), B * 4, cudaMemcpyHostToDevice, st));
+    CK(c, cudaMemsetAsync(c->step, 0, 4, st));
+    CK(c, cudaMemsetAsync(c->status, 0, 4, st));
+    const size_t layer_kv = (size_t)c->bmax * nkv * c->cap * hd;
+
+    launch_embed(d_ids, M, c->embed.raw, c->embed.scale, H, c->pf_x, st);
+    for (int l = 0; l < d.n_layers; ++l) {
+        const DevLayer& L = c->layers[l];
+        launch_rmsnorm(c->pf_x, nullptr, M, H, L.attn_norm, d.rms_eps, c->pf_xn, nullptr, st);
+        launch_gemm_f32(c->pf_xn, M, H, L.qkv.raw, L.qkv.scale, L.qkv.rows, c->pf_qkv, L.qkv.rows, st);
+        launch_qk_rope_append(c->pf_qkv, M, nh, nkv, hd, c->pf_seq, c->pf_pos, L.q_norm, L.k_norm, d.rms_eps,
+                              c->rope, c->pf_q, c->kc + l * layer_kv, c->vc + l * layer_kv, c->cap, st);
+        launch_attention(c->pf_q, c->kc + l * layer_kv, c->vc + l * layer_kv, c->pf_seq, c->pf_pos, 1, M, nh, nkv,
+                         hd, c->cap, 1, c->pf_part, c->pf_o, nullptr, 0, c->status, st);
+        launch_gemm_f32(c->pf_o, M, Dq, L.o.raw, L.o.scale, H, c->pf_y, H, st);
+        launch_add(c->pf_x, c->pf_y, (size_t)M * H, st);
+        launch_rmsnorm(c->pf_x, nullptr, M, H, L.ffn_norm, d.rms_eps, c->pf_xn, nullptr, st);
+        launch_gemm_f32(c->pf_xn, M, H, L.gu.raw, L.gu.scale, 2 * I, c->pf_gu, 2 * I, st);
+        launch_silu_gate(c->pf_gu, M, I, c->pf_a, st);
+        launch_gemm_f32(c->pf_a, M, I, L.down.raw, L.down.scale, H, c->pf_y, H, st);
+        launch_add(c->pf_x, c->pf_y, (size_t)M * H, st);
+        (void)Dkv;
+    }
+    launch_rmsnorm(c->pf_x, c->pf_last, B, H, c->final_norm, d.rms_eps, nullptr, c->xh, st);
+    enqueue_lm_head(c, B, false, d_logits);
+    CK(c, cudaGetLastError());
+    c->active_B = B;
+    c->seq_len.assign(lens, lens + B);
+    (void)maxlen;
+    return Q3_OK;
+}
+
+static int check_status(q3i8_ctx* c) {
+    int32_t st = 0;
+    CK(c, cudaMemcpyAsync(&st, c->status, 4, cudaMemcpyDeviceToHost, c->stream));
+    CK(c, cudaStreamSynchronize(c->stream));
+    if (st != 0) {
+        cudaMemsetAsync(c->status, 0, 4, c->stream);
+        return fail(c, Q3_ERR_TIMEOUT, "a bounded device wait gave up (status %d)", st);
+    }
+    return Q3_OK;
+}
+
+static int validate_prompts(q3i8_ctx* c, int B, const int32_t* lens, int max_new, int* need) {
+    if (B < 1 || B > c->bmax) return fail(c, Q3_ERR_INVALID_ARGUMENTS, "B=%d outside [1, max_batch=%d]", B, c->bmax);
+    if (!lens) return fail(c, Q3_ERR_INVALID_ARGUMENTS, "prompt_lens is NULL");
+    if (max_new < 1) return fail(c, Q3_ERR_INVALID_ARGUMENTS, "max_new_tokens < 1");
+    int mx = 0;
+    for (int b = 0; b < B; ++b) {
+        if (lens[b] < 1) return fail(c, Q3_ERR_INVALID_ARGUMENTS, "sequence %d: empty prompt", b);
+        mx = std::max(mx, lens[b]);
+    }
+    const long long n = (long long)mx + max_new;
+    if (n > kCtxCeiling)
+        return fail(c, Q3_ERR_CONTEXT, "prompt (%d) + new tokens (%d) exceeds the %d-position ceiling", mx, max_new,
+                    kCtxCeiling);
+    *need = (int)n;
+    return Q3_OK;
+}
+
+static int ensure_events(q3i8_ctx* c) {
+    if (!c->ev0) {
+        CK(c, cudaEventCreate(&c->ev0));
+        CK(c, cudaEventCreate(&c->ev1));
+        CK(c, cudaEventCreate(&c->ev2));
+    }
+    return Q3_OK;
+}
+
+static int decode_core(q3i8_ctx* c, int B, const int32_t* d_ids, const int32_t* lens, int max_new,
+                       q3i8_stats* stats) {
+    int rc = ensure_events(c);
+    if (rc) return rc;
+    CK(c, cudaEventRecord(c->ev0, c->stream));
+    rc = run_prefill(c, B, d_ids, lens, nullptr);
+    if (rc) return rc;
+    CK(c, cudaEventRecord(c->ev1, c->stream));
+    if (max_new > 1) {
+        cudaGraphExec_t g;
+        rc = get_graph(c, B, &g);
+        if (rc) return rc;
+        for (int i = 1; i < max_new; ++i) CK(c, cudaGraphLaunch(g, c->stream));
+    }
+    CK(c, cudaEventRecord(c->ev2, c->stream));
+    rc = check_status(c);
+    if (rc) return rc;
+    for (int b = 0; b < B; ++b) c->seq_len[b] += max_new - 1;
+    if (stats) {
+        float pf = 0, dc = 0;
+        CK(c, cudaEventElapsedTime(&pf, c->ev0, c->ev1));
+        CK(c, cudaEventElapsedTime(&dc, c->ev1, c->ev2));
+        long long ptoks = 0;
+        for (int b = 0; b < B; ++b) ptoks += lens[b];
+        stats->prefill_ms = pf;
+        stats->decode_ms = dc;
+        stats->prefill_tokens = ptoks;
+        stats->decode_steps = max_new - 1;
+        stats->prefill_tokens_per_sec = pf > 0 ? ptoks / (pf * 1e-3) : 0;
+        stats->decode_tokens_per_sec = (dc > 0 && max_new > 1) ? (double)B * (max_new - 1) / (dc * 1e-3) : 0;
+        stats->step_us = max_new > 1 ? dc * 1e3 / (max_new - 1) : 0;
+    }
+    return Q3_OK;
+}
+
+extern "C" int q3i8_decode_device(q3i8_ctx* c, int32_t B, const int32_t* d_prompt_ids, const int32_t* prompt_lens,
+                                  int32_t max_new_tokens, int32_t* d_out_ids, q3i8_stats* stats) {
+    if (!c) return fail(nullptr, Q3_ERR_INVALID_ARGUMENTS, "ctx is NULL");
+    int need = 0;
+    int rc = validate_prompts(c, B, prompt_lens, max_new_tokens, &need);
+    if (rc) return rc;
+    if (!d_prompt_ids || !d_out_ids) return fail(c, Q3_ERR_INVALID_ARGUMENTS, "device id buffer is NULL");
+    if ((rc = ensure_capacity(c, need))) return rc;
+    if ((rc = ensure_out(c, max_new_tokens))) return rc;
+    if ((rc = decode_core(c, B, d_prompt_ids, prompt_lens, max_new_tokens, stats))) return rc;
+    CK(c, cudaMemcpy2DAsync(d_out_ids, (size_t)max_new_tokens * 4, c->out_ids, (size_t)c->out_cap * 4,
+                            (size_t)max_new_tokens * 4, B, cudaMemcpyDeviceToDevice, c->stream));
+    CK(c, cudaStreamSynchronize(c->stream));
+    return Q3_OK;
+}
+
+extern "C" int q3i8_decode(q3i8_ctx* c, int32_t B, const int32_t* const* prompt_ids, const int32_t* prompt_lens,
+                           int32_t max_new_tokens, int32_t eos_id, int32_t* out_ids, int32_t* out_counts,
+                           q3i8_stats* stats) {
+    if (!c) return fail(nullptr, Q3_ERR_INVALID_ARGUMENTS, "ctx is NULL");
+    int need = 0;
+    int rc = validate_prompts(c, B, prompt_lens, max_new_tokens, &need);
+    if (rc) return rc;
+    if (!prompt_ids || !out_ids) return fail(c, Q3_ERR_INVALID_ARGUMENTS, "prompt_ids or out_ids is NULL");
+    std::vector<int32_t> all;
+    for (int b = 0; b < B; ++b) {
+        if (!prompt_ids[b]) return fail(c, Q3_ERR_INVALID_ARGUMENTS, "prompt_ids[%d] is NULL", b);
+        for (int t = 0; t < prompt_lens[b]; ++t) {
+            const int32_t id = prompt_ids[b][t];
+            if (id < 0 || id >= c->d.vocab)
+                return fail(c, Q3_ERR_INVALID_ARGUMENTS, "sequence %d position %d: id %d outside [0, %d)", b, t, id,
+                            c->d.vocab);
+            all.push_back(id);
+        }
+    }
+    if ((rc = ensure_capacity(c, need))) return rc;
+    if ((rc = ensure_out(c, max_new_tokens))) return rc;
+    if ((rc = ensure_prefill(c, (int)all.size()))) return rc;
+    CK(c, cudaMemcpyAsync(c->pf_ids, all.data(), all.size() * 4, cudaMemcpyHostToDevice, c->stream));
+    if ((rc = decode_core(c, B, c->pf_ids, prompt_lens, max_new_tokens, stats))) return rc;
+    CK(c, cudaMemcpy2DAsync(out_ids, (size_t)max_new_tokens * 4, c->out_ids, (size_t)c->out_cap * 4,
+                            (size_t)max_new_tokens * 4, B, cudaMemcpyDeviceToHost, c->stream));
+    CK(c, cudaStreamSynchronize(c->stream));
+    for (int b = 0; b < B; ++b) {
+        int n = max_new_tokens;
+        if (eos_id >= 0)
+            for (int i = 0; i < max_new_tokens; ++i)
+                if (out_ids[(size_t)b * max_new_tokens + i] == eos_id) {
+                    n = i + 1;
+                    break;
+                }
+        if (out_counts) out_counts[b] = n;
+    }
+    return Q3_OK;
+}
+
+extern "C" int q3i8_prefill(q3i8_ctx* c, int32_t B, const int32_t* const* prompt_ids, const int32_t* prompt_lens,
+                            float* last_logits) {
+    if (!c) return fail(nullptr, Q3_ERR_INVALID_ARGUMENTS, "ctx is NULL");
+    int need = 0;
+    int rc = validate_prompts(c, B, prompt_lens, 1, &need);
+    if (rc) return rc;
+    if (!prompt_ids) return fail(c, Q3_ERR_INVALID_ARGUMENTS, "prompt_ids is NULL");
+    std::vector<int32_t> all;
+    for (int b = 0; b < B; ++b) {
+        if (!prompt_ids[b]) return fail(c, Q3_ERR_INVALID_ARGUMENTS, "prompt_ids[%d] is NULL", b);
+        for (int t = 0; t < prompt_lens[b]; ++t) {
+            const int32_t id = prompt_ids[b][t];
+            if (id < 0 || id >= c->d.vocab)
+                return fail(c, Q3_ERR_INVALID_ARGUMENTS, "sequence %d position %d: id %d outside [0, %d)", b, t, id,
+                            c->d.vocab);
+            all.push_back(id);
+        }
+    }
+    if ((rc = ensure_capacity(c, need))) return rc;
+    if ((rc = ensure_out(c, 256))) return rc;
+    if ((rc = ensure_prefill(c, (int)all.size()))) return rc;
+    CK(c, cudaMemcpyAsync(c->pf_ids, all.data(), all.size() * 4, cudaMemcpyHostToDevice, c->stream));
+    if ((rc = run_prefill(c, B, c->pf_ids, prompt_lens, last_logits ? c->logits : nullptr))) return rc;
+    if (last_logits)
+        CK(c, cudaMemcpyAsync(last_logits, c->logits, (size_t)B * c->d.vocab * 4, cudaMemcpyDeviceToHost, c->stream));
+    return check_status(c);
+}
+
+extern "C" int q3i8_step_logits(q3i8_ctx* c, const int32_t* tokens, float* logits) {
+    if (!c) return fail(nullptr, Q3_ERR_INVALID_ARGUMENTS, "ctx is NULL");
+    if (c->active_B <= 0) return fail(c, Q3_ERR_STATE, "q3i8_step_logits before q3i8_prefill");
+    if (!tokens || !logits) return fail(c, Q3_ERR_INVALID_ARGUMENTS, "tokens or logits is NULL");
+    const int B = c->active_B;
+    for (int b = 0; b < B; ++b) {
+        if (tokens[b] < 0 || tokens[b] >= c->d.vocab)
+            return fail(c, Q3_ERR_INVALID_ARGUMENTS, "token %d of sequence %d outside [0, %d)", tokens[b], b,
+                        c->d.vocab);
+        if (c->seq_len[b] + 1 > c->cap)
+            return fail(c, Q3_ERR_STATE, "sequence %d is at the context capacity (%d)", b, c->cap);
+    }
+    CK(c, cudaMemcpyAsync(c->tokens, tokens, B * 4, cudaMemcpyHostToDevice, c->stream));
+    enqueue_step(c, B, true);
+    CK(c, cudaGetLastError());
+    CK(c, cudaMemcpyAsync(logits, c->logits, (size_t)B * c->d.vocab * 4, cudaMemcpyDeviceToHost, c->stream));
+    int rc = check_status(c);
+    if (rc) return rc;
+    for (int b = 0; b < B; ++b) c->seq_len[b] += 1;
+    return Q3_OK;
+}
+
+extern "C" int q3i8_read_kv(q3i8_ctx* c, int32_t layer, int32_t seq, int32_t n_pos, uint16_t* k, uint16_t* v) {
+    if (!c) return fail(nullptr, Q3_ERR_INVALID_ARGUMENTS, "ctx is NULL");
+    const q3i8_dims& d = c->d;
+    if (layer < 0 || layer >= d.n_layers || seq < 0 || seq >= c->bmax || n_pos < 0 || n_pos > c->cap || !k || !v)
+        return fail(c, Q3_ERR_INVALID_ARGUMENTS, "read_kv: argument out of range");
+    CK(c, cudaStreamSynchronize(c->stream));
+    const int hd = d.head_dim, nkv = d.n_kv_heads;
+    for (int g = 0; g < nkv; ++g) {
+        const size_t src = ((((size_t)layer * c->bmax + seq) * nkv + g) * c->cap) * hd;
+        CK(c, cudaMemcpy(k + (size_t)g * n_pos * hd, c->kc + src, (size_t)n_pos * hd * 2, cudaMemcpyDeviceToHost));
+        CK(c, cudaMemcpy(v + (size_t)g * n_pos * hd, c->vc + src, (size_t)n_pos * hd * 2, cudaMemcpyDeviceToHost));
+    }
+    return Q3_OK;
+}
+
+extern "C" int64_t q3i8_step_bytes(const q3i8_ctx* c, int32_t B, const int32_t* positions) {
+    if (!c) return -1;
+    const q3i8_dims& d = c->d;
+    const int64_t H = d.hidden, I = d.intermediate, L = d.n_layers, hd = d.head_dim;
+    const int64_t Dq = d.n_heads * hd, Dkv = d.n_kv_heads * hd;
+    const int64_t w = (int64_t)d.vocab * H + L * ((Dq + 2 * Dkv) * H + H * Dq + 2 * I * H + H * I);
+    const int64_t s = 4 * ((int64_t)d.vocab + L * ((Dq + 2 * Dkv) + H + 2 * I + H));
+    const int64_t g = 4 * (L * (2 * H + 2 * hd) + H);
+    int64_t kv = 0;
+    for (int b = 0; b < B; ++b) kv += (int64_t)(positions ? positions[b] + 1 : 1) * L * 2 * Dkv * 2;
+    kv += (int64_t)B * L * 2 * Dkv * 2;
+    return w + s + g + kv;
+}
+
+extern "C" int32_t q3i8_step_launches(const q3i8_ctx* c, int32_t B) {
+    (void)B;
+    return c ? step_launches(c) : 0;
+}
+
+extern "C" const char* q3i8_last_error(const q3i8_ctx* c) { return c ? c->err.c_str() : g_tls_error.c_str(); }
+
+extern "C" const char* q3i8_status_name(int s) {
+    switch (s) {
+        case Q3_OK: return "ok";
+        case Q3_ERR_UNSUPPORTED_ARCH: return "unsupported_architecture";
+        case Q3_ERR_INVALID_ARGUMENTS: return "invalid_arguments";
+        case Q3_ERR_CONTEXT: return "context_past_ceiling";
+        case Q3_ERR_NO_DEVICE: return "no_device";
+        case Q3_ERR_OOM: return "out_of_memory";
+        case Q3_ERR_CUDA: return "cuda_error";
+        case Q3_ERR_TIMEOUT: return "device_wait_timeout";
+        case Q3_ERR_STATE: return "invalid_state";
+        default: return "unknown_status";
+    }
+}
+
+// ------------------------------------------------------------------ ops
+
+extern "C" size_t q3i8_op_attention_workspace(int32_t R, int32_t n_heads, int32_t hd, int32_t splits) {
+    if (R <= 0 || n_heads <= 0 || hd <= 0 || splits <= 0) return 0;
+    return attn_part_bytes(R, n_heads, hd, splits);
+}
+
+extern "C" int q3i8_op_attention(const float* q, const uint16_t* k, const uint16_t* v, const int32_t* row_seq,
+                                 const int32_t* row_len, int32_t R, int32_t n_heads, int32_t n_kv_heads, int32_t hd,
+                                 int32_t cap, int32_t splits, float* out, void* workspace, size_t ws_bytes,
+                                 int32_t* d_status, void* cuda_stream) {
+    if (!q || !k || !v || !row_seq || !row_len || !out || !workspace)
+        return fail(nullptr, Q3_ERR_INVALID_ARGUMENTS, "op_attention: NULL pointer");
+    if (R < 1 || n_heads < 1 || n_kv_heads < 1 || n_heads % n_kv_heads || (hd != 64 && hd != 128) || cap < 64 ||
+        cap % 64 || splits < 1 || splits > 64)
+        return fail(nullptr, Q3_ERR_INVALID_ARGUMENTS, "op_attention: unsupported sizes");
+    if (ws_bytes < attn_part_bytes(R, n_heads, hd, splits) || ((uintptr_t)workspace & 15))
+        return fail(nullptr, Q3_ERR_INVALID_ARGUMENTS, "op_attention: workspace too small or misaligned");
+    if (((uintptr_t)k & 15) || ((uintptr_t)v & 15))
+        return fail(nullptr, Q3_ERR_INVALID_ARGUMENTS, "op_attention: K/V caches must be 16-byte aligned");
+    int rc = launch_attention(q, (const __nv_bfloat16*)k, (const __nv_bfloat16*)v, row_seq, row_len, 0, R, n_heads,
+                              n_kv_heads, hd, cap, splits, (float*)workspace, out, nullptr, 0, d_status,
+                              (cudaStream_t)cuda_stream);
+    if (rc) return fail(nullptr, Q3_ERR_INVALID_ARGUMENTS, "op_attention: unsupported head_dim/group");
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(nullptr, Q3_ERR_CUDA, "op_attention launch: %s", cudaGetErrorString(e));
+    return Q3_OK;
+}

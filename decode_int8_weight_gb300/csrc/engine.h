@@ -1,0 +1,82 @@
+// Internal state of a q3i8 context (host side of libq3i8.so).
+#pragma once
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <map>
+#include <string>
+#include <vector>
+
+#include "../../include/q3i8.h"
+
+namespace q3 {
+constexpr int kMaxBatch = 32;      // GEMV activation operand: 4 sequences per 8-column MMA tile, 8 tiles
+constexpr int kCtxCeiling = 65536; // "Model-agnostic LLM inference", section "Long context"
+constexpr int kChunkPos = 64;      // KV positions per attention stage; the cache capacity is a multiple
+
+struct DevMat {
+    int8_t* raw = nullptr;     // [rows][cols] row-major int8 (prefill GEMM)
+    uint8_t* frag = nullptr;   // fragment-order bytes (decode GEMV)
+    float* scale = nullptr;    // [rows]
+    int rows = 0, valid_rows = 0, cols = 0;
+};
+
+struct DevLayer {
+    DevMat qkv, o, gu, down;   // qkv: Wq;Wk;Wv rows.  gu: 16-row blocks of 8 gate + 8 up units
+    float *attn_norm = nullptr, *ffn_norm = nullptr, *q_norm = nullptr, *k_norm = nullptr;
+};
+}  // namespace q3
+
+struct q3i8_ctx {
+    q3i8_dims d{};
+    int dev = 0, num_sms = 0, bmax = 0;
+    cudaStream_t stream = nullptr;
+    bool own_stream = false;
+    std::string err;
+    size_t weight_bytes_dev = 0;
+
+    q3::DevMat embed;
+    std::vector<q3::DevLayer> layers;
+    float* final_norm = nullptr;
+
+    // KV cache [L][bmax][n_kv][cap][hd] bf16 and the RoPE table [cap][hd/2]
+    int cap = 0, cap_request = 512;
+    __nv_bfloat16 *kc = nullptr, *vc = nullptr;
+    float2* rope = nullptr;
+
+    // per-step device state
+    int32_t *tokens = nullptr, *pos = nullptr, *seq_ids = nullptr, *step = nullptr, *status = nullptr;
+    unsigned long long* keys = nullptr;
+    unsigned int* counter = nullptr;
+    int32_t* out_ids = nullptr;  // [bmax][out_cap]
+    int out_cap = 0;
+
+    // decode activations
+    float *x = nullptr, *qkv = nullptr, *qr = nullptr, *part = nullptr, *logits = nullptr;
+    __half *xh = nullptr, *oh = nullptr, *ah = nullptr;
+    int dec_splits_max = 64;
+
+    // prefill buffers (grow-only)
+    int pf_rows = 0;
+    float *pf_x = nullptr, *pf_xn = nullptr, *pf_qkv = nullptr, *pf_q = nullptr, *pf_o = nullptr, *pf_y = nullptr,
+          *pf_gu = nullptr, *pf_a = nullptr, *pf_part = nullptr;
+    int32_t *pf_ids = nullptr, *pf_seq = nullptr, *pf_pos = nullptr, *pf_last = nullptr;
+
+    std::map<int, cudaGraphExec_t> graphs;  // decode step graph per batch size
+    cudaEvent_t ev0 = nullptr, ev1 = nullptr, ev2 = nullptr;
+
+    int active_B = 0;            // sequences of the last prefill
+    std::vector<int> seq_len;    // host copy of each sequence's filled positions
+};
+
+int upload_matrix(q3i8_ctx* c, const std::vector<const int8_t*>& row_src, const std::vector<float>& scales, int K,
+                  int pad_rows, q3::DevMat* m);
+int init_weights(q3i8_ctx* c, const q3i8_mat* embed, const q3i8_layer* layers, const float* final_norm);
+int init_state(q3i8_ctx* c);
+int ensure_capacity(q3i8_ctx* c, int need_ctx);
+void drop_graphs(q3i8_ctx* c);
+int decode_splits(const q3i8_ctx* c, int B);
+void enqueue_step(q3i8_ctx* c, int B, bool want_logits);
+void enqueue_lm_head(q3i8_ctx* c, int B, bool advance_pos, float* logits);
+int step_launches(const q3i8_ctx* c);

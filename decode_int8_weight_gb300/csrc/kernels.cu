@@ -1,0 +1,643 @@
+// q3i8 kernels: decode step pieces and the plain prefill pieces (sm_103a).
+//
+// The decoder block computed here is the Qwen3 family's ("Model-agnostic LLM
+// inference", section "Supported models"): RMSNorm -> QKV -> per-head
+// RMSNorm on Q and K -> RoPE -> KV append (bf16) -> grouped-query attention
+// -> O + residual -> RMSNorm -> SiLU-gated FFN + residual, then a final
+// RMSNorm and the tied lm_head with a fused argmax ("Run local LLM decode",
+// section "Limitations": every token is the argmax at its step).
+#include "common.cuh"
+#include "kernels.h"
+
+namespace q3 {
+
+size_t packed_offset(int row, int k, int K) {
+    int tile = row >> 4, r = row & 15, g = r & 7, hi_row = r >> 3;
+    int pair = k >> 5, kin = k & 31, kstep = kin >> 4, kk = kin & 15;
+    int t = (kk & 7) >> 1, hi_k = kk >> 3, sub = kk & 1;
+    int lane = 4 * g + t;
+    int byte = 4 * hi_k + 2 * hi_row + sub;
+    return (size_t)tile * 16 * K + (size_t)pair * 512 + lane * 16 + kstep * 8 + byte;
+}
+
+// =====================================================================
+// int8 weight GEMV / skinny GEMM on the tensor cores.
+//
+// y[b][row] = scale[row] * sum_k q[row][k] * x[b][k] for B <= 4*NT rows of
+// activations.  Each warp takes every 8th pair of k-steps of a 16-row
+// weight tile (split-K inside the CTA); one 16-byte streaming load per lane
+// carries the tile's bytes for two m16n8k16 MMAs, converted to f16 in
+// registers (exact for |q| <= 127).  The activation operand holds each
+// sequence as two f16 columns (hi and lo parts of the fp32 value), so one
+// weight tile serves all B sequences and the fp32 value is kept to ~22 bits.
+// The 8 warps' partial sums meet in shared memory; the epilogue applies the
+// row scale and the mode's fusion.
+// =====================================================================
+template <int NT, int MODE>
+__global__ void __launch_bounds__(256) gemv_kernel(GemvArgs a) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane >> 2, t = lane & 3;
+    const int n_tiles = a.rows >> 4;
+    const int kpairs = a.K >> 5;
+    __shared__ float red[8][NT][32][2];
+    __shared__ unsigned long long best[4 * NT];
+    __shared__ int is_last;
+
+    if (MODE == kArgmax) {
+        for (int i = threadIdx.x; i < 4 * NT; i += blockDim.x) best[i] = 0ull;
+        __syncthreads();
+    }
+    for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
+        float acc[NT][4];
+#pragma unroll
+        for (int n = 0; n < NT; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
+        const uint8_t* wt = a.w + (size_t)tile * 16 * a.K + lane * 16;
+#pragma unroll 4
+        for (int p = warp; p < kpairs; p += 8) {
+            uint4 wv = ld_stream_u4(wt + (size_t)p * 512);
+            uint32_t A0[4], A1[4];
+            u8x4_to_f16x2x2(wv.x, A0[0], A0[1]);
+            u8x4_to_f16x2x2(wv.y, A0[2], A0[3]);
+            u8x4_to_f16x2x2(wv.z, A1[0], A1[1]);
+            u8x4_to_f16x2x2(wv.w, A1[2], A1[3]);
+            const int k0 = p * 32 + 2 * t;
+#pragma unroll
+            for (int n = 0; n < NT; ++n) {
+                const __half* xr = a.xh + (size_t)(8 * n + g) * a.K + k0;
+                uint32_t b0 = *reinterpret_cast<const uint32_t*>(xr);
+                uint32_t b1 = *reinterpret_cast<const uint32_t*>(xr + 8);
+                uint32_t b2 = *reinterpret_cast<const uint32_t*>(xr + 16);
+                uint32_t b3 = *reinterpret_cast<const uint32_t*>(xr + 24);
+                mma_f16_16816(acc[n], A0, b0, b1);
+                mma_f16_16816(acc[n], A1, b2, b3);
+            }
+        }
+#pragma unroll
+        for (int n = 0; n < NT; ++n) {
+            red[warp][n][lane][0] = acc[n][0] + acc[n][1];  // row g,   sequence 4n+t (hi + lo)
+            red[warp][n][lane][1] = acc[n][2] + acc[n][3];  // row g+8, sequence 4n+t
+        }
+        __syncthreads();
+        if (MODE == kSiluGate) {
+            // tile rows 0..7 are gate rows, 8..15 the up rows of the same 8 units
+            for (int i = threadIdx.x; i < NT * 32; i += blockDim.x) {
+                const int n = i >> 5, ln = i & 31, gg = ln >> 2, b = 4 * n + (ln & 3);
+                float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+                for (int w = 0; w < 8; ++w) {
+                    s0 += red[w][n][ln][0];
+                    s1 += red[w][n][ln][1];
+                }
+                if (b < a.B) {
+                    const int rg = tile * 16 + gg;
+                    const float gate = a.scale[rg] * s0;
+                    const float up = a.scale[rg + 8] * s1;
+                    const float v = (gate / (1.0f + expf(-gate))) * up;
+                    const int idx = tile * 8 + gg;
+                    __half hi, lo;
+                    split_f16(v, hi, lo);
+                    a.yh[(size_t)(2 * b) * a.ldyh + idx] = hi;
+                    a.yh[(size_t)(2 * b + 1) * a.ldyh + idx] = lo;
+                }
+            }
+        } else {
+            for (int i = threadIdx.x; i < NT * 64; i += blockDim.x) {
+                const int n = i >> 6, ln = (i & 63) >> 1, half = i & 1, gg = ln >> 2, b = 4 * n + (ln & 3);
+                float sum = 0.f;
+#pragma unroll
+                for (int w = 0; w < 8; ++w) sum += red[w][n][ln][half];
+                if (b < a.B) {
+                    const int row = tile * 16 + gg + 8 * half;
+                    const float v = a.scale[row] * sum;
+                    if (MODE == kStore) {
+                        a.y[(size_t)b * a.ldy + row] = v;
+                    } else if (MODE == kResid) {
+                        float* p = a.y + (size_t)b * a.ldy + row;
+                        *p = *p + v;
+                    } else {
+                        if (row < a.valid_rows) {
+                            if (a.logits) a.logits[(size_t)b * a.valid_rows + row] = v;
+                            atomicMax(&best[b], argmax_key(v, (uint32_t)row));
+                        }
+                    }
+                }
+            }
+        }
+        __syncthreads();
+    }
+    if (MODE == kArgmax) {
+        // block result -> grid result; the last block to finish publishes the tokens
+        if (threadIdx.x < a.B) atomicMax(&a.keys[threadIdx.x], best[threadIdx.x]);
+        __threadfence();
+        __syncthreads();
+        if (threadIdx.x == 0) is_last = (atomicAdd(a.counter, 1u) == gridDim.x - 1);
+        __syncthreads();
+        if (is_last) {
+            __threadfence();
+            const int step = *reinterpret_cast<volatile int32_t*>(a.step);
+            if (threadIdx.x < a.B) {
+                const int b = threadIdx.x;
+                const unsigned long long k = atomicExch(&a.keys[b], 0ull);
+                const int tok = (int)argmax_key_index(k);
+                a.tokens[b] = tok;
+                if (step < a.out_cap) a.out_ids[(size_t)b * a.out_cap + step] = tok;
+                if (a.advance_pos) a.pos[b] += 1;
+            }
+            __syncthreads();
+            if (threadIdx.x == 0) {
+                *a.step = step + 1;
+                *a.counter = 0u;
+            }
+        }
+    }
+}
+
+template <int NT>
+static void launch_gemv_nt(const GemvArgs& a, int mode, int grid, cudaStream_t st) {
+    switch (mode) {
+        case kStore: gemv_kernel<NT, kStore><<<grid, 256, 0, st>>>(a); break;
+        case kResid: gemv_kernel<NT, kResid><<<grid, 256, 0, st>>>(a); break;
+        case kSiluGate: gemv_kernel<NT, kSiluGate><<<grid, 256, 0, st>>>(a); break;
+        default: gemv_kernel<NT, kArgmax><<<grid, 256, 0, st>>>(a); break;
+    }
+}
+
+void launch_gemv(const GemvArgs& a, int mode, int grid, cudaStream_t st) {
+    const int nt = (a.B + 3) / 4;
+    if (nt <= 1) launch_gemv_nt<1>(a, mode, grid, st);
+    else if (nt <= 2) launch_gemv_nt<2>(a, mode, grid, st);
+    else if (nt <= 4) launch_gemv_nt<4>(a, mode, grid, st);
+    else launch_gemv_nt<8>(a, mode, grid, st);
+}
+
+int gemv_grid(int rows, int mode, int num_sms) {
+    const int tiles = rows / 16;
+    if (mode == kArgmax) return tiles < num_sms * 8 ? tiles : num_sms * 8;
+    return tiles;
+}
+
+// =====================================================================
+// Embedding gather from the tied int8 table: x = float(q[tok]) * s[tok].
+// =====================================================================
+__global__ void embed_kernel(const int32_t* ids, const int8_t* E, const float* sE, int H, float* x) {
+    const int r = blockIdx.x;
+    const int tok = ids[r];
+    const float s = sE[tok];
+    const int8_t* row = E + (size_t)tok * H;
+    for (int i = threadIdx.x; i < H; i += blockDim.x) x[(size_t)r * H + i] = (float)row[i] * s;
+}
+
+void launch_embed(const int32_t* ids, int n, const int8_t* E, const float* sE, int H, float* x, cudaStream_t st) {
+    if (n > 0) embed_kernel<<<n, 256, 0, st>>>(ids, E, sE, H, x);
+}
+
+// =====================================================================
+// RMSNorm: y = x / sqrt(mean(x^2) + eps) * g, one row per CTA.  Writes fp32
+// rows (xn, [n][H]) and/or f16 hi/lo planes (xh, columns 2i and 2i+1).
+// =====================================================================
+__global__ void rmsnorm_kernel(const float* x, const int32_t* rows, int H, const float* g, float eps, float* xn,
+                               __half* xh) {
+    __shared__ float part[32];
+    __shared__ float s_inv;
+    const int i = blockIdx.x;
+    const int r = rows ? rows[i] : i;
+    const float* xr = x + (size_t)r * H;
+    float ss = 0.f;
+    for (int k = threadIdx.x; k < H; k += blockDim.x) ss += xr[k] * xr[k];
+    ss = warp_sum(ss);
+    if ((threadIdx.x & 31) == 0) part[threadIdx.x >> 5] = ss;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float tot = 0.f;
+        for (int w = 0; w < (int)(blockDim.x >> 5); ++w) tot += part[w];
+        s_inv = 1.0f / sqrtf(tot / (float)H + eps);
+    }
+    __syncthreads();
+    const float inv = s_inv;
+    for (int k = threadIdx.x; k < H; k += blockDim.x) {
+        const float v = __fmul_rn(__fmul_rn(xr[k], inv), g[k]);
+        if (xn) xn[(size_t)i * H + k] = v;
+        if (xh) {
+            __half hi, lo;
+            split_f16(v, hi, lo);
+            xh[(size_t)(2 * i) * H + k] = hi;
+            xh[(size_t)(2 * i + 1) * H + k] = lo;
+        }
+    }
+}
+
+void launch_rmsnorm(const float* x, const int32_t* rows, int n, int H, const float* g, float eps, float* xn,
+                    __half* xh, cudaStream_t st) {
+    if (n > 0) rmsnorm_kernel<<<n, 256, 0, st>>>(x, rows, H, g, eps, xn, xh);
+}
+
+// =====================================================================
+// Per-head RMSNorm on Q and K, RoPE (rotate-half, theta^(-2i/hd)), and the
+// bf16 KV append at each row's position.  One warp per head; lane l holds
+// elements l + 32j, so both members of every rotation pair sit in one lane.
+// =====================================================================
+template <int HD>
+__global__ void qk_rope_append_kernel(const float* qkv, int nh, int nkv, const int32_t* row_seq,
+                                      const int32_t* row_pos, const float* q_norm, const float* k_norm, float eps,
+                                      const float2* rope_cs, float* q_out, __nv_bfloat16* kc, __nv_bfloat16* vc,
+                                      int cap) {
+    constexpr int E = HD / 32;
+    const int r = blockIdx.x;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int seq = row_seq[r], pos = row_pos[r];
+    const int width = (nh + 2 * nkv) * HD;
+    const float* row = qkv + (size_t)r * width;
+    const float2* cs = rope_cs + (size_t)pos * (HD / 2);
+    for (int h = warp; h < nh + nkv; h += (blockDim.x >> 5)) {
+        const bool is_q = h < nh;
+        const float* src = row + (size_t)h * HD;  // q heads, then k heads
+        const float* gain = is_q ? q_norm : k_norm;
+        float v[E];
+        float ss = 0.f;
+#pragma unroll
+        for (int j = 0; j < E; ++j) {
+            v[j] = src[lane + 32 * j];
+            ss += v[j] * v[j];
+        }
+        ss = warp_sum(ss);
+        const float inv = 1.0f / sqrtf(ss / (float)HD + eps);
+#pragma unroll
+        for (int j = 0; j < E; ++j) v[j] = __fmul_rn(__fmul_rn(v[j], inv), gain[lane + 32 * j]);
+#pragma unroll
+        for (int j = 0; j < E / 2; ++j) {
+            const float2 c = cs[lane + 32 * j];  // (cos, sin) of pair lane + 32j
+            const float a0 = v[j], b0 = v[j + E / 2];
+            v[j] = __fsub_rn(__fmul_rn(a0, c.x), __fmul_rn(b0, c.y));
+            v[j + E / 2] = __fadd_rn(__fmul_rn(b0, c.x), __fmul_rn(a0, c.y));
+        }
+        if (is_q) {
+            float* dst = q_out + ((size_t)r * nh + h) * HD;
+#pragma unroll
+            for (int j = 0; j < E; ++j) dst[lane + 32 * j] = v[j];
+        } else {
+            const int gk = h - nh;
+            const size_t slot = (((size_t)seq * nkv + gk) * cap + pos) * HD;
+            const float* vsrc = row + (size_t)(nh + nkv + gk) * HD;
+#pragma unroll
+            for (int j = 0; j < E; ++j) {
+                kc[slot + lane + 32 * j] = __float2bfloat16_rn(v[j]);
+                vc[slot + lane + 32 * j] = __float2bfloat16_rn(vsrc[lane + 32 * j]);
+            }
+        }
+    }
+}
+
+void launch_qk_rope_append(const float* qkv, int R, int nh, int nkv, int hd, const int32_t* row_seq,
+                           const int32_t* row_pos, const float* q_norm, const float* k_norm, float eps,
+                           const float2* rope_cs, float* q_out, __nv_bfloat16* kc, __nv_bfloat16* vc, int cap,
+                           cudaStream_t st) {
+    if (R <= 0) return;
+    int threads = 32 * (nh + nkv);
+    if (threads > 512) threads = 512;
+    if (hd == 128)
+        qk_rope_append_kernel<128><<<R, threads, 0, st>>>(qkv, nh, nkv, row_seq, row_pos, q_norm, k_norm, eps,
+                                                          rope_cs, q_out, kc, vc, cap);
+    else
+        qk_rope_append_kernel<64><<<R, threads, 0, st>>>(qkv, nh, nkv, row_seq, row_pos, q_norm, k_norm, eps,
+                                                         rope_cs, q_out, kc, vc, cap);
+}
+
+// =====================================================================
+// Split-KV grouped-query decode attention.
+//
+// CTA (split, kv head g, row r) covers a contiguous slice of the row's
+// positions.  K and V are staged 64 positions at a time into shared memory
+// by 1-D bulk copies (TMA) on an mbarrier, two stages deep.  The GROUP query
+// heads that share kv head g are processed together, so every K/V byte is
+// read once per group.  Warp w scores positions 16w..16w+15 of each chunk
+// (lane l holds dims HD/32 * l ..), keeps an online softmax (running max,
+// sum, weighted V), and the four warps merge their states in shared memory.
+// The per-split states (acc[HD], m, l) go to `part`; the merge kernel
+// combines the splits.
+// =====================================================================
+constexpr int kChunk = 64;
+
+template <int HD>
+struct AttnSmem {
+    __nv_bfloat16 k[2][kChunk * HD];
+    __nv_bfloat16 v[2][kChunk * HD];
+    uint64_t bar[2];
+};
+
+template <int HD, int GROUP>
+__global__ void __launch_bounds__(128) attn_split_kernel(const float* q, const __nv_bfloat16* kc,
+                                                         const __nv_bfloat16* vc, const int32_t* row_seq,
+                                                         const int32_t* row_len, int len_add, int nh, int nkv,
+                                                         int cap, int splits, float* part, int32_t* status) {
+    constexpr int D = HD / 32;  // dims per lane
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    AttnSmem<HD>& sm = *reinterpret_cast<AttnSmem<HD>*>(smem_raw);
+    __shared__ float wm[4][GROUP], wl[4][GROUP];
+    __shared__ float wacc[4][GROUP][HD];
+
+    const int sp = blockIdx.x, g = blockIdx.y, r = blockIdx.z;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int len = row_len[r] + len_add, seq = row_seq[r];
+    int per = (len + splits - 1) / splits;
+    per = (per + kChunk - 1) / kChunk * kChunk;
+    const int start = sp * per;
+    const int end = min(len, start + per);
+    float* outp = part + ((size_t)r * nh + (size_t)g * GROUP) * splits * (HD + 2);
+    if (start >= end) {
+        for (int i = threadIdx.x; i < GROUP * (HD + 2); i += blockDim.x) {
+            const int h = i / (HD + 2), e = i % (HD + 2);
+            outp[((size_t)h * splits + sp) * (HD + 2) + e] = (e == HD) ? -INFINITY : 0.f;
+        }
+        return;
+    }
+    const int nchunks = (end - start + kChunk - 1) / kChunk;
+    const size_t head_base = ((size_t)seq * nkv + g) * cap * HD;
+    const __nv_bfloat16* kb = kc + head_base + (size_t)start * HD;
+    const __nv_bfloat16* vb = vc + head_base + (size_t)start * HD;
+    constexpr uint32_t kBytes = kChunk * HD * 2;
+
+    if (threadIdx.x == 0) {
+        mbar_init(&sm.bar[0], 1);
+        mbar_init(&sm.bar[1], 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        for (int c = 0; c < 2 && c < nchunks; ++c) {
+            mbar_arrive_expect_tx(&sm.bar[c], 2 * kBytes);
+            bulk_g2s(sm.k[c], kb + (size_t)c * kChunk * HD, kBytes, &sm.bar[c]);
+            bulk_g2s(sm.v[c], vb + (size_t)c * kChunk * HD, kBytes, &sm.bar[c]);
+        }
+    }
+
+    float qr[GROUP][D];
+#pragma unroll
+    for (int h = 0; h < GROUP; ++h)
+#pragma unroll
+        for (int d = 0; d < D; ++d) qr[h][d] = q[((size_t)r * nh + g * GROUP + h) * HD + lane * D + d];
+    const float scale = 1.0f / sqrtf((float)HD);
+    float m[GROUP], l[GROUP], acc[GROUP][D];
+#pragma unroll
+    for (int h = 0; h < GROUP; ++h) {
+        m[h] = -INFINITY;
+        l[h] = 0.f;
+#pragma unroll
+        for (int d = 0; d < D; ++d) acc[h][d] = 0.f;
+    }
+
+    bool ok = true;
+    for (int c = 0; c < nchunks; ++c) {
+        const int s = c & 1;
+        if (!mbar_wait_bounded(&sm.bar[s], (c >> 1) & 1)) {
+            ok = false;
+            break;
+        }
+        const int p0 = start + c * kChunk + warp * 16;
+        float sc[GROUP][16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const __nv_bfloat16* krow = sm.k[s] + (size_t)(warp * 16 + i) * HD + lane * D;
+            float kv[D];
+            if constexpr (D == 4) {
+                uint2 raw = *reinterpret_cast<const uint2*>(krow);
+                kv[0] = bf16_bits_to_float(raw.x & 0xffff);
+                kv[1] = bf16_bits_to_float(raw.x >> 16);
+                kv[2] = bf16_bits_to_float(raw.y & 0xffff);
+                kv[3] = bf16_bits_to_float(raw.y >> 16);
+            } else {
+                uint32_t raw = *reinterpret_cast<const uint32_t*>(krow);
+                kv[0] = bf16_bits_to_float(raw & 0xffff);
+                kv[1] = bf16_bits_to_float(raw >> 16);
+            }
+#pragma unroll
+            for (int h = 0; h < GROUP; ++h) {
+                float dot = 0.f;
+#pragma unroll
+                for (int d = 0; d < D; ++d) dot += qr[h][d] * kv[d];
+                dot = warp_sum(dot);
+                sc[h][i] = (p0 + i < end) ? dot * scale : -INFINITY;
+            }
+        }
+#pragma unroll
+        for (int h = 0; h < GROUP; ++h) {
+            float cm = sc[h][0];
+#pragma unroll
+            for (int i = 1; i < 16; ++i) cm = fmaxf(cm, sc[h][i]);
+            const float mn = fmaxf(m[h], cm);
+            if (mn == -INFINITY) continue;
+            const float corr = (m[h] == -INFINITY) ? 0.f : expf(m[h] - mn);
+            l[h] *= corr;
+#pragma unroll
+            for (int d = 0; d < D; ++d) acc[h][d] *= corr;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const float p = (sc[h][i] == -INFINITY) ? 0.f : expf(sc[h][i] - mn);
+                l[h] += p;
+                const __nv_bfloat16* vrow = sm.v[s] + (size_t)(warp * 16 + i) * HD + lane * D;
+#pragma unroll
+                for (int d = 0; d < D; ++d) acc[h][d] += p * __bfloat162float(vrow[d]);
+            }
+            m[h] = mn;
+        }
+        __syncthreads();  // every warp is done with stage s
+        if (threadIdx.x == 0 && c + 2 < nchunks) {
+            mbar_arrive_expect_tx(&sm.bar[s], 2 * kBytes);
+            bulk_g2s(sm.k[s], kb + (size_t)(c + 2) * kChunk * HD, kBytes, &sm.bar[s]);
+            bulk_g2s(sm.v[s], vb + (size_t)(c + 2) * kChunk * HD, kBytes, &sm.bar[s]);
+        }
+    }
+    if (!ok) {
+        // a bounded wait gave up: record it, give the other copy a bounded
+        // chance to land, and leave without writing results
+        if (threadIdx.x == 0) {
+            set_status(status, kStatusTimeout);
+            for (int s = 0; s < 2; ++s) mbar_wait_bounded(&sm.bar[s], 0);
+        }
+        return;
+    }
+    // merge the four warps' online-softmax states
+    if (lane == 0)
+        for (int h = 0; h < GROUP; ++h) {
+            wm[warp][h] = m[h];
+            wl[warp][h] = l[h];
+        }
+#pragma unroll
+    for (int h = 0; h < GROUP; ++h)
+#pragma unroll
+        for (int d = 0; d < D; ++d) wacc[warp][h][lane * D + d] = acc[h][d];
+    __syncthreads();
+    for (int i = threadIdx.x; i < GROUP * HD; i += blockDim.x) {
+        const int h = i / HD, d = i % HD;
+        float M = -INFINITY;
+        for (int w = 0; w < 4; ++w) M = fmaxf(M, wm[w][h]);
+        float L = 0.f, A = 0.f;
+        for (int w = 0; w < 4; ++w) {
+            if (wm[w][h] == -INFINITY) continue;
+            const float f = expf(wm[w][h] - M);
+            L += wl[w][h] * f;
+            A += wacc[w][h][d] * f;
+        }
+        float* o = outp + ((size_t)h * splits + sp) * (HD + 2);
+        o[d] = A;
+        if (d == 0) {
+            o[HD] = M;
+            o[HD + 1] = L;
+        }
+    }
+}
+
+// out[r][h][:] = sum_s acc_s e^{m_s - M} / sum_s l_s e^{m_s - M}
+template <int HD>
+__global__ void attn_merge_kernel(const float* part, int nh, int splits, float* out, __half* outh, int ldh) {
+    const int rh = blockIdx.x;  // r * nh + h
+    const int d = threadIdx.x;
+    const float* p = part + (size_t)rh * splits * (HD + 2);
+    float M = -INFINITY;
+    for (int s = 0; s < splits; ++s) M = fmaxf(M, p[(size_t)s * (HD + 2) + HD]);
+    float L = 0.f, A = 0.f;
+    for (int s = 0; s < splits; ++s) {
+        const float ms = p[(size_t)s * (HD + 2) + HD];
+        if (ms == -INFINITY) continue;
+        const float f = expf(ms - M);
+        L += p[(size_t)s * (HD + 2) + HD + 1] * f;
+        A += p[(size_t)s * (HD + 2) + d] * f;
+    }
+    const float o = A / L;
+    const int r = rh / nh, h = rh % nh;
+    if (out) out[(size_t)rh * HD + d] = o;
+    if (outh) {
+        __half hi, lo;
+        split_f16(o, hi, lo);
+        outh[(size_t)(2 * r) * ldh + h * HD + d] = hi;
+        outh[(size_t)(2 * r + 1) * ldh + h * HD + d] = lo;
+    }
+}
+
+size_t attn_part_bytes(int R, int nh, int hd, int splits) { return (size_t)R * nh * splits * (hd + 2) * sizeof(float); }
+
+template <int HD, int GROUP>
+static void launch_attn_t(const float* q, const __nv_bfloat16* k, const __nv_bfloat16* v, const int32_t* row_seq,
+                          const int32_t* row_len, int len_add, int R, int nh, int nkv, int cap, int splits,
+                          float* part, int32_t* status, cudaStream_t st) {
+    static bool attr_set = false;
+    const int smem = (int)sizeof(AttnSmem<HD>);
+    if (!attr_set) {
+        cudaFuncSetAttribute(attn_split_kernel<HD, GROUP>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        attr_set = true;
+    }
+    dim3 grid(splits, nkv, R);
+    attn_split_kernel<HD, GROUP><<<grid, 128, smem, st>>>(q, k, v, row_seq, row_len, len_add, nh, nkv, cap, splits,
+                                                          part, status);
+}
+
+int launch_attention(const float* q, const __nv_bfloat16* k, const __nv_bfloat16* v, const int32_t* row_seq,
+                     const int32_t* row_len, int len_add, int R, int nh, int nkv, int hd, int cap, int splits,
+                     float* part, float* out, __half* outh, int ldh, int32_t* status, cudaStream_t st) {
+    if (R <= 0) return 0;
+    const int group = nh / nkv;
+#define Q3_ATTN_CASE(HDV, GV)                                                                         \
+    if (hd == HDV && group == GV) {                                                                   \
+        launch_attn_t<HDV, GV>(q, k, v, row_seq, row_len, len_add, R, nh, nkv, cap, splits, part, status, st); \
+        attn_merge_kernel<HDV><<<R * nh, HDV, 0, st>>>(part, nh, splits, out, outh, ldh);              \
+        return 0;                                                                                     \
+    }
+    Q3_ATTN_CASE(128, 1)
+    Q3_ATTN_CASE(128, 2)
+    Q3_ATTN_CASE(128, 4)
+    Q3_ATTN_CASE(128, 8)
+    Q3_ATTN_CASE(64, 1)
+    Q3_ATTN_CASE(64, 2)
+    Q3_ATTN_CASE(64, 4)
+    Q3_ATTN_CASE(64, 8)
+#undef Q3_ATTN_CASE
+    return -1;  // unsupported head_dim / group
+}
+
+// =====================================================================
+// Plain prefill pieces (CUDA cores, fp32): Y = (X . W^T) * s over int8 W.
+// =====================================================================
+__global__ void __launch_bounds__(256) gemm_f32_kernel(const float* X, int M, int K, const int8_t* W, const float* s,
+                                                       int N, float* Y, int ldy) {
+    __shared__ float Xs[32][64 + 4];
+    __shared__ float Ws[32][64 + 4];
+    const int m0 = blockIdx.y * 64, n0 = blockIdx.x * 64;
+    const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+    float acc[4][4] = {};
+    for (int k0 = 0; k0 < K; k0 += 32) {
+        for (int i = threadIdx.x; i < 64 * 32; i += 256) {
+            const int mm = i >> 5, kk = i & 31;
+            Xs[kk][mm] = (m0 + mm < M) ? X[(size_t)(m0 + mm) * K + k0 + kk] : 0.f;
+            Ws[kk][mm] = (n0 + mm < N) ? (float)W[(size_t)(n0 + mm) * K + k0 + kk] : 0.f;
+        }
+        __syncthreads();
+#pragma unroll 8
+        for (int kk = 0; kk < 32; ++kk) {
+            float av[4], bv[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                av[i] = Xs[kk][ty * 4 + i];
+                bv[i] = Ws[kk][tx * 4 + i];
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) acc[i][j] += av[i] * bv[j];
+        }
+        __syncthreads();
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int m = m0 + ty * 4 + i;
+        if (m >= M) continue;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int n = n0 + tx * 4 + j;
+            if (n < N) Y[(size_t)m * ldy + n] = s[n] * acc[i][j];
+        }
+    }
+}
+
+void launch_gemm_f32(const float* X, int M, int K, const int8_t* W, const float* s, int N, float* Y, int ldy,
+                     cudaStream_t st) {
+    if (M <= 0) return;
+    dim3 grid((N + 63) / 64, (M + 63) / 64);
+    gemm_f32_kernel<<<grid, 256, 0, st>>>(X, M, K, W, s, N, Y, ldy);
+}
+
+__global__ void add_kernel(float* x, const float* y, size_t n) {
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x)
+        x[i] = x[i] + y[i];
+}
+
+void launch_add(float* x, const float* y, size_t n, cudaStream_t st) {
+    if (n) add_kernel<<<(unsigned)((n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096), 256, 0, st>>>(x, y, n);
+}
+
+// gu rows come from the fused gate/up matrix: in each block of 16 outputs the
+// first 8 are gate units 8j..8j+7 and the next 8 the matching up units.
+__global__ void silu_gate_kernel(const float* gu, int M, int I, float* a) {
+    const size_t n = (size_t)M * I;
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
+        const size_t m = i / I;
+        const int u = (int)(i % I);
+        const size_t base = m * (size_t)(2 * I) + (size_t)(u >> 3) * 16 + (u & 7);
+        const float gate = gu[base], up = gu[base + 8];
+        a[i] = (gate / (1.0f + expf(-gate))) * up;
+    }
+}
+
+void launch_silu_gate(const float* gu, int M, int I, float* a, cudaStream_t st) {
+    const size_t n = (size_t)M * I;
+    if (n) silu_gate_kernel<<<(unsigned)((n + 255) / 256 < 8192 ? (n + 255) / 256 : 8192), 256, 0, st>>>(gu, M, I, a);
+}
+
+__global__ void gather_rows_kernel(const float* src, const int32_t* rows, int H, float* dst) {
+    const int i = blockIdx.x;
+    for (int k = threadIdx.x; k < H; k += blockDim.x) dst[(size_t)i * H + k] = src[(size_t)rows[i] * H + k];
+}
+
+void launch_gather_rows(const float* src, const int32_t* rows, int n, int H, float* dst, cudaStream_t st) {
+    if (n > 0) gather_rows_kernel<<<n, 256, 0, st>>>(src, rows, H, dst);
+}
+
+}  // namespace q3

@@ -1,0 +1,70 @@
+// Launchers of the q3i8 kernels (host side, internal to libq3i8.so).
+#pragma once
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace q3 {
+
+// Packed int8 weight layout used by the decode GEMV ("fragment order"):
+// 16-row tiles; inside a tile, pairs of 16-wide k-steps; inside a pair, 32
+// lanes x 16 bytes.  Lane l = 4g + t holds, per k-step k0, the bytes
+// W[g][k0+2t], W[g][k0+2t+1], W[g+8][k0+2t], W[g+8][k0+2t+1],
+// W[g][k0+2t+8], W[g][k0+2t+9], W[g+8][k0+2t+8], W[g+8][k0+2t+9],
+// each stored as q + 128.  These are exactly the A-operand registers of an
+// m16n8k16 tensor-core MMA, so one 16-byte load feeds two MMAs.
+size_t packed_offset(int row, int k, int K);  // byte offset of W[row][k]
+
+enum GemvMode { kStore = 0, kResid = 1, kSiluGate = 2, kArgmax = 3 };
+
+struct GemvArgs {
+    const uint8_t* w;     // packed fragments, rows x K
+    const float* scale;   // [rows]
+    int rows, K;
+    const __half* xh;     // [8*NT][K] f16 planes: column 2b = hi, 2b+1 = lo of sequence b
+    int B;                // sequences (<= 4*NT)
+    float* y;             // kStore: y[b*ldy + row] = s*acc; kResid: y[b*ldy + row] += s*acc
+    int ldy;
+    __half* yh;           // kSiluGate: planes [8*NT][ldyh] of a = silu(gate)*up
+    int ldyh;
+    // kArgmax (lm_head): block-then-grid argmax, lowest index on ties
+    unsigned long long* keys;  // [B], zero between launches
+    unsigned int* counter;     // zero between launches
+    int32_t* tokens;           // [B] next token
+    int32_t* out_ids;          // [B][out_cap], column = *step
+    int32_t* step;             // device step counter (incremented)
+    int out_cap;
+    int32_t* pos;              // [B] positions, += 1 when advance_pos
+    int advance_pos;
+    int valid_rows;            // rows >= valid_rows (padding) take no part in the argmax
+    float* logits;             // optional [B][valid_rows]
+};
+
+void launch_gemv(const GemvArgs& a, int mode, int grid, cudaStream_t st);
+int gemv_grid(int rows, int mode, int num_sms);
+
+void launch_embed(const int32_t* ids, int n, const int8_t* E, const float* sE, int H, float* x, cudaStream_t st);
+
+// RMSNorm of rows (row map optional) -> fp32 rows and/or f16 hi/lo planes.
+void launch_rmsnorm(const float* x, const int32_t* rows, int n, int H, const float* g, float eps, float* xn,
+                    __half* xh, cudaStream_t st);
+
+void launch_qk_rope_append(const float* qkv, int R, int nh, int nkv, int hd, const int32_t* row_seq,
+                           const int32_t* row_pos, const float* q_norm, const float* k_norm, float eps,
+                           const float2* rope_cs, float* q_out, __nv_bfloat16* kc, __nv_bfloat16* vc, int cap,
+                           cudaStream_t st);
+
+size_t attn_part_bytes(int R, int nh, int hd, int splits);
+// Attends positions 0 .. row_len[r] + len_add - 1 of sequence row_seq[r].
+int launch_attention(const float* q, const __nv_bfloat16* k, const __nv_bfloat16* v, const int32_t* row_seq,
+                     const int32_t* row_len, int len_add, int R, int nh, int nkv, int hd, int cap, int splits,
+                     float* part, float* out, __half* outh, int ldh, int32_t* status, cudaStream_t st);
+
+void launch_gemm_f32(const float* X, int M, int K, const int8_t* W, const float* s, int N, float* Y, int ldy,
+                     cudaStream_t st);
+void launch_add(float* x, const float* y, size_t n, cudaStream_t st);
+void launch_silu_gate(const float* gu, int M, int I, float* a, cudaStream_t st);
+void launch_gather_rows(const float* src, const int32_t* rows, int n, int H, float* dst, cudaStream_t st);
+
+}  // namespace q3

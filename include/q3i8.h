@@ -1,0 +1,224 @@
+/*
+ * q3i8 -- int8 weight-only Qwen3-family decode on one NVIDIA GB300 (sm_103a).
+ *
+ * C ABI of libq3i8.so.  Plain pointers and sizes only.
+ *
+ * The operation ("Model-agnostic LLM inference" and "Run local LLM decode"):
+ * prompt token ids in, greedy generated token ids out, for a Qwen3-family
+ * decoder (grouped-query attention with RMSNorm on Q/K, RoPE, SiLU-gated
+ * FFN, tied embeddings, no attention bias; "Model-agnostic LLM inference",
+ * section "Supported models") whose weights are int8 with one fp32 scale per
+ * output row (same page, section "The quantized load cache").  A prefill
+ * reads each whole prompt and builds the KV cache; each decode step then
+ * sweeps the weights once for all B sequences and ends in an argmax
+ * ("LLM inference overview", sections "Results" and "Workload
+ * characteristics"; "Run local LLM decode", section "Limitations": greedy,
+ * every token is the argmax at its step).  The KV cache is bf16.
+ *
+ * Numerics: fp32 accumulation over exact int8 weights; K and V are rounded to
+ * bf16 (nearest even) when stored and read back rounded.  Argmax ties go to
+ * the lowest token id.
+ *
+ * Errors: every entry point returns a status (Q3_OK == 0).  The message of
+ * the last failure on a context is q3i8_last_error(ctx); failures before a
+ * context exists put their message in q3i8_last_error(NULL) (per thread).
+ * Validation failures are reported before any device work starts.
+ *
+ * Threading: a context is bound to one device and one CUDA stream and is not
+ * thread-safe; use one context per host thread.
+ */
+#ifndef Q3I8_H
+#define Q3I8_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---------------------------------------------------------------- status */
+enum {
+    Q3_OK = 0,
+    /* The model shape is outside the supported family or alignment gates
+     * ("Model-agnostic LLM inference", section "Supported models": GQA
+     * heads % kv_heads == 0; hidden, intermediate and heads*head_dim each a
+     * multiple of 32; tied embeddings; no attention bias).  The message lists
+     * every mismatch, not just the first.  These kernels also need
+     * head_dim in {64, 128}. */
+    Q3_ERR_UNSUPPORTED_ARCH = 1,
+    /* Empty or out-of-range prompt ids, max_new_tokens < 1, B outside
+     * [1, max_batch], NULL where an array is required ("Model-agnostic LLM
+     * inference", section "Errors", invalid_arguments). */
+    Q3_ERR_INVALID_ARGUMENTS = 2,
+    /* prompt + new tokens above the 65,536-position ceiling ("Model-agnostic
+     * LLM inference", section "Long context"). */
+    Q3_ERR_CONTEXT = 3,
+    /* No CUDA device, or a device that is not sm_103. */
+    Q3_ERR_NO_DEVICE = 4,
+    /* Device memory allocation failed. */
+    Q3_ERR_OOM = 5,
+    /* Any other CUDA runtime failure (the message names the call). */
+    Q3_ERR_CUDA = 6,
+    /* A bounded device-side wait gave up; the kernel returned early and the
+     * results of that call are invalid.  The context stays usable. */
+    Q3_ERR_TIMEOUT = 7,
+    /* Call order: q3i8_step_logits before any prefill, or a step past the
+     * context's capacity. */
+    Q3_ERR_STATE = 8
+};
+
+/* ---------------------------------------------------------------- model */
+typedef struct q3i8_dims {
+    int32_t hidden;             /* H */
+    int32_t n_layers;           /* L */
+    int32_t n_heads;            /* query heads */
+    int32_t n_kv_heads;         /* key/value heads (GQA) */
+    int32_t head_dim;           /* 64 or 128 */
+    int32_t intermediate;       /* I (FFN width) */
+    int32_t vocab;              /* V (tied embedding rows) */
+    float rope_theta;           /* 1e6 for Qwen3 */
+    float rms_eps;              /* 1e-6 for Qwen3 */
+    int32_t max_batch;          /* most sequences per call, 1..64 */
+    int32_t max_ctx;            /* initial per-sequence KV capacity in positions
+                                   (0 means 512); raised automatically up to
+                                   65,536 when a call needs more */
+    int32_t tie_word_embeddings;/* must be 1 */
+    int32_t attention_bias;     /* must be 0 */
+} q3i8_dims;
+
+/* One linear layer in nn.Linear order: w is [out][in] row-major int8,
+ * scale is [out] fp32; y = scale * (w . x). */
+typedef struct q3i8_mat {
+    const int8_t* w;
+    const float* scale;
+} q3i8_mat;
+
+/* One decoder layer.  q: [n_heads*head_dim][H], k and v: [n_kv*head_dim][H],
+ * o: [H][n_heads*head_dim], gate and up: [I][H], down: [H][I].
+ * Norm gains are fp32: attn_norm and ffn_norm [H], q_norm and k_norm
+ * [head_dim] (shared by all heads). */
+typedef struct q3i8_layer {
+    q3i8_mat q, k, v, o, gate, up, down;
+    const float* attn_norm;
+    const float* ffn_norm;
+    const float* q_norm;
+    const float* k_norm;
+} q3i8_layer;
+
+typedef struct q3i8_stats {
+    double prefill_ms;              /* device time of the prefill (CUDA events) */
+    double decode_ms;               /* device time of the decode steps */
+    double prefill_tokens_per_sec;  /* prompt tokens / prefill time */
+    double decode_tokens_per_sec;   /* tokens from decode steps / decode time */
+    double step_us;                 /* mean decode step */
+    int64_t prefill_tokens;
+    int64_t decode_steps;
+} q3i8_stats;
+
+typedef struct q3i8_ctx q3i8_ctx;
+
+/* ---------------------------------------------------------------- calls */
+
+/* Host-only check of a model shape against the architecture gates ("Model-
+ * agnostic LLM inference", section "Supported models").  Touches no GPU.
+ * On failure writes every mismatch, separated by "; ", into msg (always
+ * NUL-terminated when msg_cap > 0) and returns Q3_ERR_UNSUPPORTED_ARCH (or
+ * Q3_ERR_INVALID_ARGUMENTS for non-positive sizes or a bad max_batch). */
+int q3i8_validate_dims(const q3i8_dims* dims, char* msg, size_t msg_cap);
+
+/* Create a context on the current CUDA device.  Copies every weight from
+ * the caller's HOST arrays into library-owned device memory (repacked for
+ * the kernels), so the caller may free them on return; weights then stay
+ * resident for every later call ("Model-agnostic LLM inference", section
+ * "Convert once, decode many times": loaded weights stay resident).
+ *   embed       [vocab][H] int8 + [vocab] scales: embedding table and, tied,
+ *               the lm_head.
+ *   layers      [n_layers] host array of layer descriptors.
+ *   final_norm  [H] fp32 gain of the last RMSNorm.
+ *   cuda_stream cudaStream_t to run on (NULL = a stream the context creates).
+ * On success *out receives the context (free with q3i8_destroy). */
+int q3i8_init(const q3i8_dims* dims, const q3i8_mat* embed, const q3i8_layer* layers,
+              const float* final_norm, void* cuda_stream, q3i8_ctx** out);
+
+/* Greedy decode of B sequences ("Run local LLM decode", section "Read the
+ * result"; "LLM inference overview": batched decode sweeps the weights once
+ * per step for all B sequences).  HOST buffers:
+ *   prompt_ids[b]  pointer to prompt_lens[b] token ids of sequence b.
+ *   out_ids        [B][max_new_tokens] generated ids, row b for sequence b.
+ *   out_counts     [B] number of valid ids per row: max_new_tokens, or up to
+ *                  and including the first eos_id when eos_id >= 0.
+ *   stats          optional timings (NULL to skip).
+ * Resets the KV cache, prefills every prompt, runs max_new_tokens-1 decode
+ * steps (each one replay of a captured CUDA graph) and copies the ids back
+ * once at the end.  Context sizing: max(512, longest prompt + new tokens),
+ * raised automatically up to 65,536 positions ("Model-agnostic LLM
+ * inference", section "Long context"). */
+int q3i8_decode(q3i8_ctx* ctx, int32_t B, const int32_t* const* prompt_ids, const int32_t* prompt_lens,
+                int32_t max_new_tokens, int32_t eos_id, int32_t* out_ids, int32_t* out_counts,
+                q3i8_stats* stats);
+
+/* As q3i8_decode, with DEVICE buffers: d_prompt_ids holds the B prompts back
+ * to back (sum of prompt_lens ids, sequence 0 first); d_out_ids receives
+ * [B][max_new_tokens] ids.  prompt_lens stays a host array.  Nothing is
+ * copied between host and device except the per-call row tables; returns
+ * after the device work has finished. */
+int q3i8_decode_device(q3i8_ctx* ctx, int32_t B, const int32_t* d_prompt_ids, const int32_t* prompt_lens,
+                       int32_t max_new_tokens, int32_t* d_out_ids, q3i8_stats* stats);
+
+/* Teacher-forced checking interface (the pages' step-by-step session).
+ * q3i8_prefill resets the KV cache and runs the B prompts (HOST ids); when
+ * last_logits is not NULL it receives the fp32 logits [B][vocab] of each
+ * prompt's last position.  Each q3i8_step_logits then appends tokens[b]
+ * (HOST, [B]) at the next position of sequence b and writes the fp32 logits
+ * [B][vocab] for the position after it into the HOST buffer logits. */
+int q3i8_prefill(q3i8_ctx* ctx, int32_t B, const int32_t* const* prompt_ids, const int32_t* prompt_lens,
+                 float* last_logits);
+int q3i8_step_logits(q3i8_ctx* ctx, const int32_t* tokens, float* logits);
+
+/* Copy the cached K and V (bf16 bit patterns) of one layer and sequence for
+ * positions [0, n_pos) into HOST arrays k and v, each [n_kv_heads][n_pos]
+ * [head_dim].  For checking. */
+int q3i8_read_kv(q3i8_ctx* ctx, int32_t layer, int32_t seq, int32_t n_pos, uint16_t* k, uint16_t* v);
+
+/* Algorithmic HBM bytes of one decode step: weights + scales + norm gains
+ * read once, plus the K/V read for sum_b (pos_b + 1) positions and written
+ * for B positions. */
+int64_t q3i8_step_bytes(const q3i8_ctx* ctx, int32_t B, const int32_t* positions);
+
+/* Kernel launches of one decode step at batch B (the captured graph). */
+int32_t q3i8_step_launches(const q3i8_ctx* ctx, int32_t B);
+
+const char* q3i8_last_error(const q3i8_ctx* ctx);
+const char* q3i8_status_name(int status);
+void q3i8_destroy(q3i8_ctx* ctx);
+
+/* ---------------------------------------------------------------- ops
+ * Single kernels on caller-owned DEVICE memory, for checking each kernel in
+ * isolation.  All run on `cuda_stream` (NULL = legacy default stream) and
+ * return after enqueueing (no synchronisation).
+ */
+
+/* Split-KV grouped-query decode attention (the attention step of the
+ * "Supported models" block, one query position per row):
+ *   q       [R][n_heads][hd] fp32 queries (already normed and rotated).
+ *   k, v    bf16 caches [n_seq][n_kv][cap][hd] (cap a multiple of 64).
+ *   row_seq [R] int32 sequence of each row; row_len [R] int32 positions
+ *           0..row_len-1 attended (1 <= row_len <= cap).
+ *   out     [R][n_heads][hd] fp32.
+ *   splits  KV splits per (row, kv head), 1..64.
+ *   workspace, ws_bytes: device scratch for the partial softmax states,
+ *           at least q3i8_op_attention_workspace(R, n_heads, hd, splits)
+ *           bytes, 16-byte aligned; contents need no initialisation.
+ *   d_status device int32 set non-zero if a bounded wait gave up (may be
+ *           NULL). */
+size_t q3i8_op_attention_workspace(int32_t R, int32_t n_heads, int32_t hd, int32_t splits);
+int q3i8_op_attention(const float* q, const uint16_t* k, const uint16_t* v, const int32_t* row_seq,
+                      const int32_t* row_len, int32_t R, int32_t n_heads, int32_t n_kv_heads, int32_t hd,
+                      int32_t cap, int32_t splits, float* out, void* workspace, size_t ws_bytes,
+                      int32_t* d_status, void* cuda_stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif
