@@ -34,7 +34,7 @@ STATUS = {0: "ok", 1: "unsupported_architecture", 2: "invalid_arguments", 3: "co
           4: "no_device", 5: "out_of_memory", 6: "cuda_error", 7: "device_wait_timeout", 8: "invalid_state"}
 
 EXPORTS = ["q3i8_validate_dims", "q3i8_init", "q3i8_decode", "q3i8_decode_device", "q3i8_prefill",
-           "q3i8_step_logits", "q3i8_read_kv", "q3i8_step_bytes", "q3i8_step_launches", "q3i8_last_error",
+           "q3i8_step_logits", "q3i8_read_kv", "q3i8_step_bytes", "q3i8_step_launches", "q3i8_launch_count", "q3i8_last_error",
            "q3i8_status_name", "q3i8_destroy", "q3i8_op_attention_workspace", "q3i8_op_attention"]
 
 
@@ -96,6 +96,8 @@ def lib():
             L.q3i8_step_bytes.argtypes = [vp, i32, vp]
             L.q3i8_step_launches.restype = i32
             L.q3i8_step_launches.argtypes = [vp, i32]
+            L.q3i8_launch_count.restype = i64
+            L.q3i8_launch_count.argtypes = [vp]
             L.q3i8_last_error.restype = ctypes.c_char_p
             L.q3i8_last_error.argtypes = [vp]
             L.q3i8_status_name.restype = ctypes.c_char_p
@@ -235,6 +237,9 @@ class Decoder:
 
     def step_launches(self, B: int) -> int:
         return int(lib().q3i8_step_launches(self._h, B))
+
+    def launch_count(self) -> int:
+        return int(lib().q3i8_launch_count(self._h))
 
 
 def op_attention_workspace(R: int, n_heads: int, hd: int, splits: int) -> int:

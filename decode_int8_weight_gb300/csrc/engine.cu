@@ -471,6 +471,7 @@ void enqueue_lm_head(q3i8_ctx* c, int B, bool advance_pos, float* logits) {
 }
 
 int step_launches(const q3i8_ctx* c) { return 2 + c->d.n_layers * 9 + 1; }
+int prefill_launches(const q3i8_ctx* c) { return 1 + c->d.n_layers * 12 + 2; }
 
 // Graph of one decode step at batch B (captured on first use).
 static int get_graph(q3i8_ctx* c, int B, cudaGraphExec_t* out) {
@@ -542,6 +543,7 @@ static int run_prefill(q3i8_ctx* c, int B, const int32_t* d_ids, const int32_t* 
     launch_rmsnorm(c->pf_x, c->pf_last, B, H, c->final_norm, d.rms_eps, nullptr, c->xh, st);
     enqueue_lm_head(c, B, false, d_logits);
     CK(c, cudaGetLastError());
+    c->launches += prefill_launches(c);
     c->active_B = B;
     c->seq_len.assign(lens, lens + B);
     (void)maxlen;
@@ -598,6 +600,7 @@ static int decode_core(q3i8_ctx* c, int B, const int32_t* d_ids, const int32_t* 
         rc = get_graph(c, B, &g);
         if (rc) return rc;
         for (int i = 1; i < max_new; ++i) CK(c, cudaGraphLaunch(g, c->stream));
+        c->launches += (int64_t)(max_new - 1) * step_launches(c);
     }
     CK(c, cudaEventRecord(c->ev2, c->stream));
     rc = check_status(c);
@@ -718,6 +721,7 @@ extern "C" int q3i8_step_logits(q3i8_ctx* c, const int32_t* tokens, float* logit
     }
     CK(c, cudaMemcpyAsync(c->tokens, tokens, B * 4, cudaMemcpyHostToDevice, c->stream));
     enqueue_step(c, B, true);
+    c->launches += step_launches(c);
     CK(c, cudaGetLastError());
     CK(c, cudaMemcpyAsync(logits, c->logits, (size_t)B * c->d.vocab * 4, cudaMemcpyDeviceToHost, c->stream));
     int rc = check_status(c);
@@ -759,6 +763,8 @@ extern "C" int32_t q3i8_step_launches(const q3i8_ctx* c, int32_t B) {
     (void)B;
     return c ? step_launches(c) : 0;
 }
+
+extern "C" int64_t q3i8_launch_count(const q3i8_ctx* c) { return c ? c->launches : 0; }
 
 extern "C" const char* q3i8_last_error(const q3i8_ctx* c) { return c ? c->err.c_str() : g_tls_error.c_str(); }
 

@@ -66,6 +66,7 @@ struct q3i8_ctx {
     std::map<int, cudaGraphExec_t> graphs;  // decode step graph per batch size
     cudaEvent_t ev0 = nullptr, ev1 = nullptr, ev2 = nullptr;
 
+    int64_t launches = 0;        // kernels launched (graph replays counted per node)
     int active_B = 0;            // sequences of the last prefill
     std::vector<int> seq_len;    // host copy of each sequence's filled positions
 };
@@ -80,3 +81,4 @@ int decode_splits(const q3i8_ctx* c, int B);
 void enqueue_step(q3i8_ctx* c, int B, bool want_logits);
 void enqueue_lm_head(q3i8_ctx* c, int B, bool advance_pos, float* logits);
 int step_launches(const q3i8_ctx* c);
+int prefill_launches(const q3i8_ctx* c);

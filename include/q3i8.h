@@ -189,6 +189,9 @@ int64_t q3i8_step_bytes(const q3i8_ctx* ctx, int32_t B, const int32_t* positions
 /* Kernel launches of one decode step at batch B (the captured graph). */
 int32_t q3i8_step_launches(const q3i8_ctx* ctx, int32_t B);
 
+/* Kernels this context has launched so far (graph replays counted per node). */
+int64_t q3i8_launch_count(const q3i8_ctx* ctx);
+
 const char* q3i8_last_error(const q3i8_ctx* ctx);
 const char* q3i8_status_name(int status);
 void q3i8_destroy(q3i8_ctx* ctx);
