@@ -20,6 +20,7 @@
 #include "../../include/q3i8.h"
 #include "engine.h"
 #include "kernels.h"
+#include "persistent.h"
 
 using namespace q3;
 
@@ -103,15 +104,19 @@ extern "C" int q3i8_validate_dims(const q3i8_dims* d, char* msg, size_t msg_cap)
 
 // ------------------------------------------------------------------ weights
 
-// [rows][K] int8 (row-major) -> fragment-order bytes (q + 128).
-static void pack_fragments(const int8_t* w, int rows, int K, uint8_t* out) {
+// [rows][K] int8 (row-major) + scales -> tile blobs (header of 16 scales,
+// then fragment-order bytes q + 128).
+static void pack_fragments(const int8_t* w, const float* scale, int rows, int K, uint8_t* out) {
     const int tiles = rows / 16, pairs = K / 32;
     auto work = [&](int t0, int t1) {
-        for (int tile = t0; tile < t1; ++tile)
+        for (int tile = t0; tile < t1; ++tile) {
+            uint8_t* hdr = out + (size_t)tile * tile_blob_bytes(K);
+            memset(hdr, 0, kTileHeader);
+            memcpy(hdr, scale + (size_t)tile * 16, 16 * sizeof(float));
             for (int p = 0; p < pairs; ++p)
                 for (int lane = 0; lane < 32; ++lane) {
                     const int g = lane >> 2, t = lane & 3;
-                    uint8_t* dst = out + (size_t)tile * 16 * K + (size_t)p * 512 + lane * 16;
+                    uint8_t* dst = hdr + kTileHeader + (size_t)p * 512 + lane * 16;
                     for (int ks = 0; ks < 2; ++ks) {
                         const int k0 = p * 32 + ks * 16 + 2 * t;
                         const int8_t* r0 = w + (size_t)(tile * 16 + g) * K;
@@ -121,6 +126,7 @@ static void pack_fragments(const int8_t* w, int rows, int K, uint8_t* out) {
                         for (int j = 0; j < 8; ++j) dst[ks * 8 + j] = (uint8_t)((int)v[j] + 128);
                     }
                 }
+        }
     };
     unsigned nt = std::max(1u, std::min(16u, std::thread::hardware_concurrency()));
     if (tiles < 64) nt = 1;
@@ -141,13 +147,13 @@ int upload_matrix(q3i8_ctx* c, const std::vector<const int8_t*>& row_src, const 
     for (int r = 0; r < rows; ++r) memcpy(&raw[(size_t)r * K], row_src[r], K);
     std::vector<float> sc(prow, 0.f);
     std::copy(scales.begin(), scales.end(), sc.begin());
-    std::vector<uint8_t> frag((size_t)prow * K);
-    pack_fragments(raw.data(), prow, K, frag.data());
+    std::vector<uint8_t> frag((size_t)(prow / 16) * tile_blob_bytes(K));
+    pack_fragments(raw.data(), sc.data(), prow, K, frag.data());
     m->rows = prow;
     m->valid_rows = rows;
     m->cols = K;
     CK(c, cudaMalloc(&m->raw, (size_t)prow * K));
-    CK(c, cudaMalloc(&m->frag, (size_t)prow * K));
+    CK(c, cudaMalloc(&m->frag, frag.size()));
     CK(c, cudaMalloc(&m->scale, (size_t)prow * sizeof(float)));
     CK(c, cudaMemcpy(m->raw, raw.data(), raw.size(), cudaMemcpyHostToDevice));
     CK(c, cudaMemcpy(m->frag, frag.data(), frag.size(), cudaMemcpyHostToDevice));
@@ -297,6 +303,7 @@ extern "C" int q3i8_init(const q3i8_dims* dims, const q3i8_mat* embed, const q3i
     if (rc == Q3_OK) rc = init_state(c);
     if (rc == Q3_OK) rc = ensure_capacity(c, c->cap_request);
     if (rc == Q3_OK) rc = ensure_out(c, 256);
+    if (rc == Q3_OK) rc = persistent_setup(c);
     if (rc == Q3_OK && cudaStreamSynchronize(c->stream) != cudaSuccess) rc = fail(c, Q3_ERR_CUDA, "init sync failed");
     if (rc != Q3_OK) {
         g_tls_error = c->err;
@@ -398,7 +405,8 @@ extern "C" void q3i8_destroy(q3i8_ctx* c) {
     void* ptrs[] = {c->final_norm, c->kc, c->vc, c->rope, c->tokens, c->pos, c->seq_ids, c->step, c->keys,
                     c->counter, c->status, c->x, c->qkv, c->qr, c->part, c->xh, c->oh, c->ah, c->logits,
                     c->out_ids, c->pf_x, c->pf_xn, c->pf_qkv, c->pf_q, c->pf_o, c->pf_y, c->pf_gu, c->pf_a,
-                    c->pf_part, c->pf_ids, c->pf_seq, c->pf_pos, c->pf_last};
+                    c->pf_part, c->pf_ids, c->pf_seq, c->pf_pos, c->pf_last, c->d_mats, c->d_gains,
+                    c->p_epoch, c->p_keys, c->p_exit, c->p_attn_cnt, c->p_abort, c->p_diag, c->p_ll, c->p_part};
     for (void* p : ptrs) cudaFree(p);
     if (c->ev0) cudaEventDestroy(c->ev0);
     if (c->ev1) cudaEventDestroy(c->ev1);
@@ -470,7 +478,112 @@ void enqueue_lm_head(q3i8_ctx* c, int B, bool advance_pos, float* logits) {
     launch_gemv(a, kArgmax, gemv_grid(a.rows, kArgmax, c->num_sms), c->stream);
 }
 
-int step_launches(const q3i8_ctx* c) { return 2 + c->d.n_layers * 9 + 1; }
+// ------------------------------------------------------------------ persistent step
+
+int persistent_setup(q3i8_ctx* c) {
+    const char* env = getenv("Q3I8_DECODE_PATH");
+    if (env && strcmp(env, "chained") == 0) return Q3_OK;
+    if (!persistent_supported(c->d)) return Q3_OK;
+    int optin = 0;
+    CK(c, cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, c->dev));
+    const int ns = persistent_slots(optin);
+    if (ns < 4) return Q3_OK;
+    const q3i8_dims& d = c->d;
+    const int L = d.n_layers, H = d.hidden, I = d.intermediate, hd = d.head_dim;
+    const int Dq = d.n_heads * hd, Dkv = d.n_kv_heads * hd, B = c->bmax, G = c->num_sms;
+    std::vector<const uint8_t*> mats(4 * L);
+    std::vector<const float*> gains(4 * L);
+    for (int l = 0; l < L; ++l) {
+        mats[4 * l + 0] = c->layers[l].qkv.frag;
+        mats[4 * l + 1] = c->layers[l].o.frag;
+        mats[4 * l + 2] = c->layers[l].gu.frag;
+        mats[4 * l + 3] = c->layers[l].down.frag;
+        gains[4 * l + 0] = c->layers[l].attn_norm;
+        gains[4 * l + 1] = c->layers[l].ffn_norm;
+        gains[4 * l + 2] = c->layers[l].q_norm;
+        gains[4 * l + 3] = c->layers[l].k_norm;
+    }
+    CK(c, cudaMalloc(&c->d_mats, mats.size() * sizeof(void*)));
+    CK(c, cudaMalloc(&c->d_gains, gains.size() * sizeof(void*)));
+    CK(c, cudaMemcpy(c->d_mats, mats.data(), mats.size() * sizeof(void*), cudaMemcpyHostToDevice));
+    CK(c, cudaMemcpy(c->d_gains, gains.data(), gains.size() * sizeof(void*), cudaMemcpyHostToDevice));
+    CK(c, cudaMalloc(&c->p_epoch, 4));
+    CK(c, cudaMalloc(&c->p_keys, B * 8));
+    CK(c, cudaMalloc(&c->p_exit, 4));
+    CK(c, cudaMalloc(&c->p_attn_cnt, (size_t)L * B * d.n_kv_heads * 4));
+    CK(c, cudaMalloc(&c->p_abort, 4));
+    CK(c, cudaMalloc(&c->p_diag, 8 * 4));
+    const size_t words = (size_t)B * (3 * H + H / 8 + (Dq + 2 * Dkv) + Dq + I);
+    c->p_ll_bytes = words * 8;
+    CK(c, cudaMalloc(&c->p_ll, c->p_ll_bytes));
+    CK(c, cudaMemset(c->p_ll, 0, c->p_ll_bytes));
+    CK(c, cudaMalloc(&c->p_part, (size_t)B * d.n_kv_heads * G * 2 * (hd + 2) * sizeof(float)));
+    c->p_grid = G;
+    c->p_ns = ns;
+    if (int rc = persistent_reset(c)) return rc;
+    const uint32_t one = 1;
+    CK(c, cudaMemcpy(c->p_epoch, &one, 4, cudaMemcpyHostToDevice));
+    c->use_persistent = true;
+    return Q3_OK;
+}
+
+// Clear the persistent kernel's between-step state (after init or a timeout)
+// and move to a fresh epoch so that no flagged word of an interrupted step
+// can match.
+int persistent_reset(q3i8_ctx* c) {
+    const q3i8_dims& d = c->d;
+    CK(c, cudaMemset(c->p_keys, 0, c->bmax * 8));
+    CK(c, cudaMemset(c->p_exit, 0, 4));
+    CK(c, cudaMemset(c->p_attn_cnt, 0, (size_t)d.n_layers * c->bmax * d.n_kv_heads * 4));
+    CK(c, cudaMemset(c->p_abort, 0, 4));
+    CK(c, cudaMemset(c->p_diag, 0, 8 * 4));
+    uint32_t e = 0;
+    CK(c, cudaMemcpy(&e, c->p_epoch, 4, cudaMemcpyDeviceToHost));
+    e = (e < 1 ? 1 : e) + 2;
+    CK(c, cudaMemcpy(c->p_epoch, &e, 4, cudaMemcpyHostToDevice));
+    return Q3_OK;
+}
+
+cudaError_t enqueue_persistent(q3i8_ctx* c, int B, float* logits) {
+    const q3i8_dims& d = c->d;
+    const int H = d.hidden, I = d.intermediate, hd = d.head_dim;
+    const int Dq = d.n_heads * hd, Dkv = d.n_kv_heads * hd, bm = c->bmax;
+    PParams P{};
+    P.B = B, P.bmax = bm, P.H = H, P.I = I, P.L = d.n_layers, P.nh = d.n_heads, P.nkv = d.n_kv_heads, P.hd = hd;
+    P.cap = c->cap, P.vocab = d.vocab, P.vpad = c->embed.rows, P.qkv_rows = c->layers[0].qkv.rows, P.ns = c->p_ns;
+    P.eps = d.rms_eps;
+    P.mats = c->d_mats, P.lm = c->embed.frag, P.emb_raw = c->embed.raw, P.emb_scale = c->embed.scale;
+    P.gains = c->d_gains, P.final_norm = c->final_norm, P.rope = c->rope, P.kc = c->kc, P.vc = c->vc;
+    P.tokens = c->tokens, P.pos = c->pos, P.step = c->step, P.out_ids = c->out_ids, P.out_cap = c->out_cap;
+    P.advance_pos = 1, P.epoch = c->p_epoch, P.keys = c->p_keys, P.exit_cnt = c->p_exit;
+    P.attn_cnt = c->p_attn_cnt, P.status = c->status, P.abort_flag = c->p_abort, P.diag = c->p_diag;
+    P.logits = logits;
+    LLw* w = reinterpret_cast<LLw*>(c->p_ll);
+    P.x = w, w += (size_t)bm * H;
+    P.pl_attn = w, w += (size_t)bm * H;
+    P.pl_ffn = w, w += (size_t)bm * H;
+    P.ss_attn = w, w += (size_t)bm * (H / 16);
+    P.ss_ffn = w, w += (size_t)bm * (H / 16);
+    P.qkv = w, w += (size_t)bm * (Dq + 2 * Dkv);
+    P.pl_o = w, w += (size_t)bm * Dq;
+    P.pl_a = w;
+    P.part = c->p_part;
+    return launch_persistent_step(P, c->p_grid, c->stream);
+}
+
+// One decode step on the context's stream: the persistent kernel when the
+// shape allows it, else the chained kernels.
+static int enqueue_decode_step(q3i8_ctx* c, int B, bool want_logits) {
+    if (c->use_persistent) {
+        cudaError_t e = enqueue_persistent(c, B, want_logits ? c->logits : nullptr);
+        if (e != cudaSuccess) return fail(c, Q3_ERR_CUDA, "persistent step launch: %s", cudaGetErrorString(e));
+        return Q3_OK;
+    }
+    enqueue_step(c, B, want_logits);
+    return Q3_OK;
+}
+
+int step_launches(const q3i8_ctx* c) { return c->use_persistent ? 1 : 2 + c->d.n_layers * 9 + 1; }
 int prefill_launches(const q3i8_ctx* c) { return 1 + c->d.n_layers * 12 + 2; }
 
 // Graph of one decode step at batch B (captured on first use).
@@ -482,8 +595,12 @@ static int get_graph(q3i8_ctx* c, int B, cudaGraphExec_t* out) {
     }
     cudaGraph_t g;
     CK(c, cudaStreamBeginCapture(c->stream, cudaStreamCaptureModeThreadLocal));
-    enqueue_step(c, B, false);
+    const int rc = enqueue_decode_step(c, B, false);
     cudaError_t e = cudaStreamEndCapture(c->stream, &g);
+    if (rc != Q3_OK) {
+        if (e == cudaSuccess) cudaGraphDestroy(g);
+        return rc;
+    }
     if (e != cudaSuccess) return fail(c, Q3_ERR_CUDA, "graph capture failed: %s", cudaGetErrorString(e));
     cudaGraphExec_t ex;
     e = cudaGraphInstantiate(&ex, g, 0);
@@ -556,7 +673,15 @@ static int check_status(q3i8_ctx* c) {
     CK(c, cudaStreamSynchronize(c->stream));
     if (st != 0) {
         cudaMemsetAsync(c->status, 0, 4, c->stream);
-        return fail(c, Q3_ERR_TIMEOUT, "a bounded device wait gave up (status %d)", st);
+        cudaStreamSynchronize(c->stream);
+        int32_t dg[8] = {0};
+        if (c->use_persistent) {
+            cudaMemcpy(dg, c->p_diag, sizeof dg, cudaMemcpyDeviceToHost);
+            persistent_reset(c);
+        }
+        return fail(c, Q3_ERR_TIMEOUT,
+                    "a bounded device wait gave up (status %d; site %d cta %d warp %d layer %d phase %d aux %d)", st,
+                    dg[0], dg[1], dg[2], dg[3], dg[4], dg[5]);
     }
     return Q3_OK;
 }
@@ -720,7 +845,7 @@ extern "C" int q3i8_step_logits(q3i8_ctx* c, const int32_t* tokens, float* logit
             return fail(c, Q3_ERR_STATE, "sequence %d is at the context capacity (%d)", b, c->cap);
     }
     CK(c, cudaMemcpyAsync(c->tokens, tokens, B * 4, cudaMemcpyHostToDevice, c->stream));
-    enqueue_step(c, B, true);
+    if (int rc0 = enqueue_decode_step(c, B, true)) return rc0;
     c->launches += step_launches(c);
     CK(c, cudaGetLastError());
     CK(c, cudaMemcpyAsync(logits, c->logits, (size_t)B * c->d.vocab * 4, cudaMemcpyDeviceToHost, c->stream));

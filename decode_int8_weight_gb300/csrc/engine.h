@@ -63,6 +63,20 @@ struct q3i8_ctx {
           *pf_gu = nullptr, *pf_a = nullptr, *pf_part = nullptr;
     int32_t *pf_ids = nullptr, *pf_seq = nullptr, *pf_pos = nullptr, *pf_last = nullptr;
 
+    // persistent decode step (one cooperative kernel per step)
+    bool use_persistent = false;
+    int p_grid = 0, p_ns = 0;
+    const uint8_t** d_mats = nullptr;     // device [L*4]
+    const float** d_gains = nullptr;      // device [L*4]
+    uint32_t* p_epoch = nullptr;
+    unsigned long long* p_keys = nullptr;
+    unsigned int *p_exit = nullptr, *p_attn_cnt = nullptr;
+    int32_t* p_abort = nullptr;
+    int32_t* p_diag = nullptr;
+    void* p_ll = nullptr;                 // all flagged-word buffers
+    float* p_part = nullptr;
+    size_t p_ll_bytes = 0;
+
     std::map<int, cudaGraphExec_t> graphs;  // decode step graph per batch size
     cudaEvent_t ev0 = nullptr, ev1 = nullptr, ev2 = nullptr;
 
@@ -81,4 +95,7 @@ int decode_splits(const q3i8_ctx* c, int B);
 void enqueue_step(q3i8_ctx* c, int B, bool want_logits);
 void enqueue_lm_head(q3i8_ctx* c, int B, bool advance_pos, float* logits);
 int step_launches(const q3i8_ctx* c);
+int persistent_setup(q3i8_ctx* c);
+int persistent_reset(q3i8_ctx* c);
+cudaError_t enqueue_persistent(q3i8_ctx* c, int B, float* logits);
 int prefill_launches(const q3i8_ctx* c);

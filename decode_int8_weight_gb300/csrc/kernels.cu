@@ -17,7 +17,8 @@ size_t packed_offset(int row, int k, int K) {
     int t = (kk & 7) >> 1, hi_k = kk >> 3, sub = kk & 1;
     int lane = 4 * g + t;
     int byte = 4 * hi_k + 2 * hi_row + sub;
-    return (size_t)tile * 16 * K + (size_t)pair * 512 + lane * 16 + kstep * 8 + byte;
+    return (size_t)tile * (kTileHeader + 16 * (size_t)K) + kTileHeader + (size_t)pair * 512 + lane * 16 + kstep * 8 +
+           byte;
 }
 
 // =====================================================================
@@ -51,7 +52,7 @@ __global__ void __launch_bounds__(256) gemv_kernel(GemvArgs a) {
         float acc[NT][4];
 #pragma unroll
         for (int n = 0; n < NT; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
-        const uint8_t* wt = a.w + (size_t)tile * 16 * a.K + lane * 16;
+        const uint8_t* wt = a.w + (size_t)tile * (kTileHeader + 16 * (size_t)a.K) + kTileHeader + lane * 16;
 #pragma unroll 4
         for (int p = warp; p < kpairs; p += 8) {
             uint4 wv = ld_stream_u4(wt + (size_t)p * 512);

@@ -7,19 +7,23 @@
 
 namespace q3 {
 
-// Packed int8 weight layout used by the decode GEMV ("fragment order"):
-// 16-row tiles; inside a tile, pairs of 16-wide k-steps; inside a pair, 32
-// lanes x 16 bytes.  Lane l = 4g + t holds, per k-step k0, the bytes
-// W[g][k0+2t], W[g][k0+2t+1], W[g+8][k0+2t], W[g+8][k0+2t+1],
-// W[g][k0+2t+8], W[g][k0+2t+9], W[g+8][k0+2t+8], W[g+8][k0+2t+9],
-// each stored as q + 128.  These are exactly the A-operand registers of an
-// m16n8k16 tensor-core MMA, so one 16-byte load feeds two MMAs.
-size_t packed_offset(int row, int k, int K);  // byte offset of W[row][k]
+// Packed int8 weight layout of the decode GEMVs ("tile blobs"): one blob per
+// 16-row tile, 128 + 16*K bytes: a 128-byte header (the 16 fp32 row scales,
+// then zeros) followed by the tile's weights in fragment order -- pairs of
+// 16-wide k-steps; inside a pair, 32 lanes x 16 bytes.  Lane l = 4g + t
+// holds, per k-step k0, the bytes W[g][k0+2t], W[g][k0+2t+1], W[g+8][k0+2t],
+// W[g+8][k0+2t+1], W[g][k0+2t+8], W[g][k0+2t+9], W[g+8][k0+2t+8],
+// W[g+8][k0+2t+9], each stored as q + 128.  These are exactly the A-operand
+// registers of an m16n8k16 tensor-core MMA, so one 16-byte load feeds two
+// MMAs, and a tile is one contiguous run of bytes for a bulk copy.
+constexpr int kTileHeader = 128;
+size_t packed_offset(int row, int k, int K);  // byte offset of W[row][k] in the blob sequence
+__host__ __device__ inline size_t tile_blob_bytes(int K) { return kTileHeader + 16 * (size_t)K; }
 
 enum GemvMode { kStore = 0, kResid = 1, kSiluGate = 2, kArgmax = 3 };
 
 struct GemvArgs {
-    const uint8_t* w;     // packed fragments, rows x K
+    const uint8_t* w;     // tile blobs, rows x K
     const float* scale;   // [rows]
     int rows, K;
     const __half* xh;     // [8*NT][K] f16 planes: column 2b = hi, 2b+1 = lo of sequence b
