@@ -28,14 +28,14 @@ import threading
 import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "_build", "libq3i8.so")
+LIB_PATH = os.environ.get("Q3I8_LIB") or os.path.join(_HERE, "_build", "libq3i8.so")
 
 STATUS = {0: "ok", 1: "unsupported_architecture", 2: "invalid_arguments", 3: "context_past_ceiling",
           4: "no_device", 5: "out_of_memory", 6: "cuda_error", 7: "device_wait_timeout", 8: "invalid_state"}
 
 EXPORTS = ["q3i8_validate_dims", "q3i8_init", "q3i8_decode", "q3i8_decode_device", "q3i8_prefill",
            "q3i8_step_logits", "q3i8_read_kv", "q3i8_step_bytes", "q3i8_step_launches", "q3i8_launch_count", "q3i8_last_error",
-           "q3i8_status_name", "q3i8_destroy", "q3i8_op_attention_workspace", "q3i8_op_attention"]
+           "q3i8_status_name", "q3i8_destroy", "q3i8_trace_step", "q3i8_op_attention_workspace", "q3i8_op_attention"]
 
 
 class Q3Error(RuntimeError):
@@ -103,6 +103,7 @@ def lib():
             L.q3i8_status_name.restype = ctypes.c_char_p
             L.q3i8_status_name.argtypes = [ctypes.c_int]
             L.q3i8_destroy.argtypes = [vp]
+            L.q3i8_trace_step.argtypes = [vp, vp, vp, sz, ctypes.POINTER(i32), ctypes.POINTER(i32)]
             L.q3i8_op_attention_workspace.restype = sz
             L.q3i8_op_attention_workspace.argtypes = [i32, i32, i32, i32]
             L.q3i8_op_attention.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, vp, vp, sz, vp, vp]
@@ -237,6 +238,16 @@ class Decoder:
 
     def step_launches(self, B: int) -> int:
         return int(lib().q3i8_step_launches(self._h, B))
+
+    def trace_step(self, tokens):
+        """One traced decode step: per-CTA %globaltimer stamps [grid, stride] (ns)."""
+        tokens = np.ascontiguousarray(tokens, np.int32)
+        grid, stride = ctypes.c_int32(), ctypes.c_int32()
+        lib().q3i8_trace_step(self._h, _p(tokens), None, 0, ctypes.byref(grid), ctypes.byref(stride))
+        out = np.zeros((grid.value, stride.value), np.uint64)
+        _check(lib().q3i8_trace_step(self._h, _p(tokens), _p(out), out.size, ctypes.byref(grid),
+                                     ctypes.byref(stride)), self._h)
+        return out
 
     def launch_count(self) -> int:
         return int(lib().q3i8_launch_count(self._h))

@@ -28,6 +28,16 @@ Q3_DEV void u8x4_to_f16x2x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
     asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(hi) : "r"(b), "r"(magic));
 }
 
+// Same bytes -> f16x2 words {1024 + u0, 1024 + u1}, {1024 + u2, 1024 + u3}:
+// one byte permute per pair and no subtraction.  A GEMV fed these operands
+// computes sum (q + 1152) x = (W . x) + 1152 * sum x; the caller subtracts
+// 1152 * sum x once per output.
+Q3_DEV void u8x4_to_biased(uint32_t w, uint32_t& lo, uint32_t& hi) {
+    lo = __byte_perm(w, 0x64646464u, 0x4140);
+    hi = __byte_perm(w, 0x64646464u, 0x4342);
+}
+constexpr float kBias = 1152.0f;
+
 // v = hi + lo with hi = f16(v), lo = f16(v - hi): about 22 significant bits.
 Q3_DEV void split_f16(float v, __half& hi, __half& lo) {
     hi = __float2half_rn(v);
@@ -115,6 +125,30 @@ Q3_DEV void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) 
             smem_u32(dst)),
         "l"(src), "r"(bytes), "r"(smem_u32(bar))
         : "memory");
+}
+
+// ------------------------------------------------------------- shared-memory loads
+// Explicit shared-space loads (32-bit shared addresses), so that hot loops
+// never go through generic addressing.
+Q3_DEV uint4 lds128(uint32_t a) {
+    uint4 r;
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "r"(a));
+    return r;
+}
+Q3_DEV uint32_t lds32(uint32_t a) {
+    uint32_t r;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(r) : "r"(a));
+    return r;
+}
+Q3_DEV float lds_f32(uint32_t a) {
+    float r;
+    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(r) : "r"(a));
+    return r;
+}
+Q3_DEV uint2 lds64(uint32_t a) {
+    uint2 r;
+    asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(r.x), "=r"(r.y) : "r"(a));
+    return r;
 }
 
 // ------------------------------------------------------------- misc

@@ -406,7 +406,7 @@ extern "C" void q3i8_destroy(q3i8_ctx* c) {
                     c->counter, c->status, c->x, c->qkv, c->qr, c->part, c->xh, c->oh, c->ah, c->logits,
                     c->out_ids, c->pf_x, c->pf_xn, c->pf_qkv, c->pf_q, c->pf_o, c->pf_y, c->pf_gu, c->pf_a,
                     c->pf_part, c->pf_ids, c->pf_seq, c->pf_pos, c->pf_last, c->d_mats, c->d_gains,
-                    c->p_epoch, c->p_keys, c->p_exit, c->p_attn_cnt, c->p_abort, c->p_diag, c->p_ll, c->p_part};
+                    c->p_epoch, c->p_keys, c->p_exit, c->p_attn_cnt, c->p_abort, c->p_diag, c->p_ll, c->p_part, c->p_trace};
     for (void* p : ptrs) cudaFree(p);
     if (c->ev0) cudaEventDestroy(c->ev0);
     if (c->ev1) cudaEventDestroy(c->ev1);
@@ -484,11 +484,15 @@ int persistent_setup(q3i8_ctx* c) {
     const char* env = getenv("Q3I8_DECODE_PATH");
     if (env && strcmp(env, "chained") == 0) return Q3_OK;
     if (!persistent_supported(c->d)) return Q3_OK;
+    if (c->d.hidden / 16 > 4 * c->num_sms || c->d.hidden > 4096) return Q3_OK;  // resident H-row tiles
     int optin = 0;
     CK(c, cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, c->dev));
-    const int ns = persistent_slots(optin);
-    if (ns < 4) return Q3_OK;
     const q3i8_dims& d = c->d;
+    c->p_kmax = std::max(std::max(d.hidden, d.intermediate), d.n_heads * d.head_dim);
+    c->p_optin = optin;
+    for (int b = 1; b <= c->bmax; ++b)
+        if (persistent_slots(optin, b, c->p_kmax) < 4) return Q3_OK;
+    const int ns = persistent_slots(optin, 1, c->p_kmax);
     const int L = d.n_layers, H = d.hidden, I = d.intermediate, hd = d.head_dim;
     const int Dq = d.n_heads * hd, Dkv = d.n_kv_heads * hd, B = c->bmax, G = c->num_sms;
     std::vector<const uint8_t*> mats(4 * L);
@@ -517,7 +521,7 @@ int persistent_setup(q3i8_ctx* c) {
     c->p_ll_bytes = words * 8;
     CK(c, cudaMalloc(&c->p_ll, c->p_ll_bytes));
     CK(c, cudaMemset(c->p_ll, 0, c->p_ll_bytes));
-    CK(c, cudaMalloc(&c->p_part, (size_t)B * d.n_kv_heads * G * 2 * (hd + 2) * sizeof(float)));
+    CK(c, cudaMalloc(&c->p_part, (size_t)B * d.n_kv_heads * (G + 1) * 2 * (hd + 2) * sizeof(float)));
     c->p_grid = G;
     c->p_ns = ns;
     if (int rc = persistent_reset(c)) return rc;
@@ -544,13 +548,14 @@ int persistent_reset(q3i8_ctx* c) {
     return Q3_OK;
 }
 
-cudaError_t enqueue_persistent(q3i8_ctx* c, int B, float* logits) {
+cudaError_t enqueue_persistent(q3i8_ctx* c, int B, float* logits, unsigned long long* trace) {
     const q3i8_dims& d = c->d;
     const int H = d.hidden, I = d.intermediate, hd = d.head_dim;
     const int Dq = d.n_heads * hd, Dkv = d.n_kv_heads * hd, bm = c->bmax;
     PParams P{};
     P.B = B, P.bmax = bm, P.H = H, P.I = I, P.L = d.n_layers, P.nh = d.n_heads, P.nkv = d.n_kv_heads, P.hd = hd;
-    P.cap = c->cap, P.vocab = d.vocab, P.vpad = c->embed.rows, P.qkv_rows = c->layers[0].qkv.rows, P.ns = c->p_ns;
+    P.cap = c->cap, P.vocab = d.vocab, P.vpad = c->embed.rows, P.qkv_rows = c->layers[0].qkv.rows;
+    P.kmax = c->p_kmax, P.ns = persistent_slots(c->p_optin, B, c->p_kmax);
     P.eps = d.rms_eps;
     P.mats = c->d_mats, P.lm = c->embed.frag, P.emb_raw = c->embed.raw, P.emb_scale = c->embed.scale;
     P.gains = c->d_gains, P.final_norm = c->final_norm, P.rope = c->rope, P.kc = c->kc, P.vc = c->vc;
@@ -558,6 +563,7 @@ cudaError_t enqueue_persistent(q3i8_ctx* c, int B, float* logits) {
     P.advance_pos = 1, P.epoch = c->p_epoch, P.keys = c->p_keys, P.exit_cnt = c->p_exit;
     P.attn_cnt = c->p_attn_cnt, P.status = c->status, P.abort_flag = c->p_abort, P.diag = c->p_diag;
     P.logits = logits;
+    P.trace = trace;
     LLw* w = reinterpret_cast<LLw*>(c->p_ll);
     P.x = w, w += (size_t)bm * H;
     P.pl_attn = w, w += (size_t)bm * H;
@@ -849,6 +855,32 @@ extern "C" int q3i8_step_logits(q3i8_ctx* c, const int32_t* tokens, float* logit
     c->launches += step_launches(c);
     CK(c, cudaGetLastError());
     CK(c, cudaMemcpyAsync(logits, c->logits, (size_t)B * c->d.vocab * 4, cudaMemcpyDeviceToHost, c->stream));
+    int rc = check_status(c);
+    if (rc) return rc;
+    for (int b = 0; b < B; ++b) c->seq_len[b] += 1;
+    return Q3_OK;
+}
+
+extern "C" int q3i8_trace_step(q3i8_ctx* c, const int32_t* tokens, uint64_t* stamps, size_t cap, int32_t* grid,
+                               int32_t* stride) {
+    if (!c) return fail(nullptr, Q3_ERR_INVALID_ARGUMENTS, "ctx is NULL");
+    if (!c->use_persistent) return fail(c, Q3_ERR_STATE, "trace_step: this context uses the chained step kernels");
+    if (c->active_B <= 0) return fail(c, Q3_ERR_STATE, "trace_step before q3i8_prefill");
+    const int st = trace_stride(c->d.n_layers);
+    const size_t n = (size_t)c->p_grid * st;
+    if (grid) *grid = c->p_grid;
+    if (stride) *stride = st;
+    if (!stamps || !tokens || cap < n) return fail(c, Q3_ERR_STATE, "trace_step: need %zu stamps", n);
+    const int B = c->active_B;
+    for (int b = 0; b < B; ++b)
+        if (c->seq_len[b] + 1 > c->cap) return fail(c, Q3_ERR_STATE, "sequence %d is at the context capacity", b);
+    if (!c->p_trace) CK(c, cudaMalloc(&c->p_trace, n * 8));
+    CK(c, cudaMemsetAsync(c->p_trace, 0, n * 8, c->stream));
+    CK(c, cudaMemcpyAsync(c->tokens, tokens, B * 4, cudaMemcpyHostToDevice, c->stream));
+    cudaError_t e = enqueue_persistent(c, B, nullptr, c->p_trace);
+    if (e != cudaSuccess) return fail(c, Q3_ERR_CUDA, "trace_step launch: %s", cudaGetErrorString(e));
+    c->launches += 1;
+    CK(c, cudaMemcpyAsync(stamps, c->p_trace, n * 8, cudaMemcpyDeviceToHost, c->stream));
     int rc = check_status(c);
     if (rc) return rc;
     for (int b = 0; b < B; ++b) c->seq_len[b] += 1;

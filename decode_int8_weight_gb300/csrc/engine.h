@@ -65,7 +65,7 @@ struct q3i8_ctx {
 
     // persistent decode step (one cooperative kernel per step)
     bool use_persistent = false;
-    int p_grid = 0, p_ns = 0;
+    int p_grid = 0, p_ns = 0, p_kmax = 0, p_optin = 0;
     const uint8_t** d_mats = nullptr;     // device [L*4]
     const float** d_gains = nullptr;      // device [L*4]
     uint32_t* p_epoch = nullptr;
@@ -73,6 +73,7 @@ struct q3i8_ctx {
     unsigned int *p_exit = nullptr, *p_attn_cnt = nullptr;
     int32_t* p_abort = nullptr;
     int32_t* p_diag = nullptr;
+    unsigned long long* p_trace = nullptr;  // set only for a traced step
     void* p_ll = nullptr;                 // all flagged-word buffers
     float* p_part = nullptr;
     size_t p_ll_bytes = 0;
@@ -97,5 +98,5 @@ void enqueue_lm_head(q3i8_ctx* c, int B, bool advance_pos, float* logits);
 int step_launches(const q3i8_ctx* c);
 int persistent_setup(q3i8_ctx* c);
 int persistent_reset(q3i8_ctx* c);
-cudaError_t enqueue_persistent(q3i8_ctx* c, int B, float* logits);
+cudaError_t enqueue_persistent(q3i8_ctx* c, int B, float* logits, unsigned long long* trace = nullptr);
 int prefill_launches(const q3i8_ctx* c);

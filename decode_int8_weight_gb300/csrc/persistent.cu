@@ -23,10 +23,13 @@
 //
 // Intermediate values travel between CTAs as 8-byte words {payload, flag}
 // written with one 64-bit store; flag is the (step, layer, phase) epoch, so a
-// consumer polls the very words it needs and no counters, fences or grid
-// barriers sit on the dependency path.  Every wait is bounded; a wait that
-// gives up records status 7 and raises an abort flag that ends every wait in
-// the grid, and the CTA drains its in-flight copies before returning.
+// consumer checks the very words it reads and no counters, fences or grid
+// barriers sit on the dependency path.  For B <= 4 a CTA copies a phase's
+// whole input vector into shared memory once (after one warp has sampled a
+// few words of it), and every tile of the phase reads its MMA operands from
+// there.  Every wait is bounded; a wait that gives up records where, raises
+// status 7 and an abort flag that ends every wait in the grid, and the CTA
+// drains its in-flight copies before returning.
 #include "common.cuh"
 #include "engine.h"
 #include "kernels.h"
@@ -36,10 +39,13 @@ namespace q3 {
 
 constexpr int kSlotBytes = kTileHeader + 16384;  // header + 32 k-pairs of fragments
 constexpr int kKpPerChunk = 32;
-constexpr int kCWarps = 8;
+constexpr int kCWarps = 4;
 constexpr int kCThreads = 32 * kCWarps;
 constexpr int kThreads = kCThreads + 32;
 constexpr int kKvChunk = 64;
+constexpr int kStagePad = 4;  // u32 padding per staged column (bank spread)
+constexpr int kMaxSlots = 12;
+constexpr int kMaxHTiles = 4;  // H-row tiles per CTA (H <= 64 * grid)
 
 // phase ids inside a layer (epoch = base + 8 * layer + phase)
 enum { kPhEmbed = 0, kPhQkv = 1, kPhAtt = 2, kPhO = 3, kPhGu = 4, kPhDown = 5 };
@@ -55,20 +61,32 @@ Q3_DEV unsigned long long ll_get(const LLw* p) {
     return v;
 }
 
+// two adjacent words (16-byte aligned); each word is checked on its own
+Q3_DEV void ll_get2(const LLw* p, unsigned long long& a, unsigned long long& b) {
+    asm volatile("ld.relaxed.gpu.global.v2.b64 {%0, %1}, [%2];" : "=l"(a), "=l"(b) : "l"(p) : "memory");
+}
+
 Q3_DEV float ld_cg_f32(const float* p) {
     float v;
     asm volatile("ld.relaxed.gpu.global.f32 %0, [%1];" : "=f"(v) : "l"(p) : "memory");
     return v;
 }
 
+Q3_DEV void mbar_arrive_cnt(uint64_t* bar, uint32_t n) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(n) : "memory");
+}
+
 struct Shared {
-    float red[kCWarps][8][32][2];   // per-warp partial sums of a tile (NT <= 8)
     float scl[16];                  // row scales of the current tile
     float rnorm[kMaxBatch];         // 1/rms per sequence for the current phase
     float sq[kMaxBatch][16];        // x^2 of the current tile's rows
     float gx[kMaxBatch][16];        // gain * x (or silu(gate) * up) of the current tile
+    float xres[kMaxHTiles][16][kMaxBatch];  // residual rows of this CTA's H-row tiles
+    float ssp[4 * 256];                     // per-tile sums of squares, B <= 4, H <= 4096 (staged path)
+    float xsum[kMaxBatch];                  // sum of the staged operand values per sequence (bias correction)
+    float xsum_w[kCWarps][4];
     unsigned long long best[kMaxBatch];
-    float qs[8][128];               // normed + rotated queries of one kv group
+    float qs[2][128];               // normed + rotated queries of one kv group (GROUP <= 2)
     float kp[128], vp[128];         // bf16-rounded K/V of the new position
     float wm[kCWarps][8], wl[kCWarps][8];
     float wacc[kCWarps][2][128];    // per-warp attention accumulators (GROUP <= 2)
@@ -86,11 +104,15 @@ struct Ctl {
     uint8_t* ring;
     uint64_t* full;
     uint64_t* empty;
+    float* red;        // [8 warps][NT][32][2] partial sums of a tile
+    uint32_t* stage;   // [2B][stage_ld] staged f16-pair words of the phase input (NT == 1)
+    int stage_ld;
     int ns;
     uint32_t used;     // consumer slot counter (per warp, identical sequence)
     uint32_t cphase;   // consumer-barrier phase
     int warp, lane, tid;
     int layer, phase;  // position in the schedule (diagnostics)
+    int dcount;        // detail stamps recorded so far
 };
 
 Q3_DEV bool aborted(const Ctl& c) {
@@ -120,27 +142,73 @@ Q3_DEV void raise_abort(Ctl& c, int site, uint32_t aux) {
     atomicExch(c.P->abort_flag, 1);
 }
 
-// Shared polling discipline: true when ready() holds, false on abort/timeout.
-template <class F>
-Q3_DEV bool poll(Ctl& c, int site, uint32_t aux, int sleep_ns, F ready) {
+// Slow paths of every wait, out of line so that each call site costs a test
+// and a call; they take scalars only, so that the caller's control block
+// stays in registers.  `diag` packs (warp, layer, phase) for the record.
+struct WaitCtx {
+    const PParams* P;
+    int* sh_abort;
+    int diag;  // warp | layer << 8 | (phase + 1) << 16
+};
+
+Q3_DEV bool aborted_w(const WaitCtx& w) {
+    return *reinterpret_cast<volatile int*>(w.sh_abort) || *reinterpret_cast<volatile int32_t*>(w.P->abort_flag);
+}
+
+Q3_DEV void raise_abort_w(const WaitCtx& w, int site, uint32_t aux) {
+    *w.sh_abort = 1;
+    if (atomicCAS(w.P->status, 0, kStatusTimeout) == 0) {
+        int32_t* d = w.P->diag;
+        d[0] = site, d[1] = blockIdx.x, d[2] = w.diag & 255, d[3] = (w.diag >> 8) & 255, d[4] = (w.diag >> 16) - 1;
+        d[5] = (int32_t)aux;
+    }
+    atomicExch(w.P->abort_flag, 1);
+}
+
+__device__ __noinline__ bool poll_mbar(const PParams* P, int* sh_abort, int diag, uint64_t* bar, uint32_t parity,
+                                       int site) {
+    const WaitCtx w{P, sh_abort, diag};
     uint64_t t0 = 0;
     for (uint32_t i = 0;; ++i) {
-        if (ready()) return true;
+        if (mbar_try_wait(bar, parity)) return true;
         if ((i & 255) == 255) {
-            if (aborted(c)) return false;
+            if (aborted_w(w)) return false;
             const uint64_t now = global_ns();
             if (t0 == 0) t0 = now;
             else if (now - t0 > kWaitNs || i > kSpinLimit * 16) {
-                raise_abort(c, site, aux);
+                raise_abort_w(w, site, parity);
                 return false;
             }
         }
-        if (i > 16) __nanosleep(sleep_ns);
+        if (i > 16) __nanosleep(32);
     }
 }
 
+__device__ __noinline__ unsigned long long poll_word(const PParams* P, int* sh_abort, int diag, const LLw* p,
+                                                     uint32_t flag) {
+    const WaitCtx w{P, sh_abort, diag};
+    uint64_t t0 = 0;
+    for (uint32_t i = 0;; ++i) {
+        const unsigned long long v = ll_get(p);
+        if ((uint32_t)(v >> 32) == flag) return v;
+        if ((i & 255) == 255) {
+            if (aborted_w(w)) return 0ull;
+            const uint64_t now = global_ns();
+            if (t0 == 0) t0 = now;
+            else if (now - t0 > kWaitNs || i > kSpinLimit * 16) {
+                raise_abort_w(w, kSiteWord, flag);
+                return 0ull;
+            }
+        }
+        if (i > 4) __nanosleep(20);
+    }
+}
+
+Q3_DEV int diag_of(const Ctl& c) { return c.warp | (c.layer & 255) << 8 | (c.phase + 1) << 16; }
+
 Q3_DEV bool mbar_wait_ctl(Ctl& c, uint64_t* bar, uint32_t parity, int site) {
-    return poll(c, site, parity, 32, [&] { return mbar_try_wait(bar, parity); });
+    if (mbar_try_wait(bar, parity)) return true;
+    return poll_mbar(c.P, &c.sh->abort, diag_of(c), bar, parity, site);
 }
 
 // all eight consumer warps meet (mbarrier based, so that it can time out)
@@ -153,12 +221,15 @@ Q3_DEV bool cbar_sync(Ctl& c) {
     return ok;
 }
 
-Q3_DEV bool slot_wait(Ctl& c, uint8_t*& slot) {
-    const int s = (int)(c.used % c.ns);
-    if (!mbar_wait_ctl(c, &c.full[s], (c.used / c.ns) & 1, kSiteFull)) return false;
+// Ring slot number u (all consumer warps count slots identically).
+Q3_DEV bool slot_wait_at(Ctl& c, uint32_t u, uint8_t*& slot) {
+    const int s = (int)(u % c.ns);
+    if (!mbar_wait_ctl(c, &c.full[s], (u / c.ns) & 1, kSiteFull)) return false;
     slot = c.ring + (size_t)s * kSlotBytes;
     return true;
 }
+
+Q3_DEV bool slot_wait(Ctl& c, uint8_t*& slot) { return slot_wait_at(c, c.used, slot); }
 
 Q3_DEV void slot_release(Ctl& c) {
     const int s = (int)(c.used % c.ns);
@@ -168,14 +239,12 @@ Q3_DEV void slot_release(Ctl& c) {
 }
 
 // Re-poll *p until the word already loaded into v carries `flag`.  Callers
-// issue all their loads first (ll_get) and settle them afterwards, so the
-// L2 round trips of one wait overlap.
+// issue all their loads first and settle them afterwards, so the L2 round
+// trips of one wait overlap.
 Q3_DEV bool ll_settle(Ctl& c, const LLw* p, uint32_t flag, unsigned long long& v) {
     if ((uint32_t)(v >> 32) == flag) return true;
-    return poll(c, kSiteWord, flag, 20, [&] {
-        v = ll_get(p);
-        return (uint32_t)(v >> 32) == flag;
-    });
+    v = poll_word(c.P, &c.sh->abort, diag_of(c), p, flag);
+    return (uint32_t)(v >> 32) == flag;
 }
 
 // wait until *p carries `flag`; return its payload
@@ -186,40 +255,60 @@ Q3_DEV bool ll_wait(Ctl& c, const LLw* p, uint32_t flag, uint32_t& out) {
     return true;
 }
 
+Q3_DEV void stamp(const Ctl& c, int idx) {
+    if (c.P->trace && (c.warp == kCWarps || c.tid == 0))
+        c.P->trace[(size_t)blockIdx.x * trace_stride(c.P->L) + idx] = global_ns();
+}
+
+// detail stamp inside the traced layer (consumer thread 0 only)
+Q3_DEV void dstamp(Ctl& c, int event) {
+    if (!c.P->trace || c.layer != kTraceDetailLayer) return;
+    if (c.tid == 0 && c.dcount < 32) {
+        unsigned long long* t = c.P->trace + (size_t)blockIdx.x * trace_stride(c.P->L) + trace_detail_base(c.P->L);
+        t[2 * c.dcount] = clock64();
+        t[2 * c.dcount + 1] = (unsigned long long)(16 * c.phase + event);
+    }
+    c.dcount++;
+}
+
 // ------------------------------------------------------------------ schedule
 // Tile t of a phase instance goes to CTA (t + rot) mod G, rot running over
 // the step so that every CTA gets the same share of bytes.
 Q3_DEV int first_tile(int cta, int rot, int G) { return ((cta - rot) % G + G) % G; }
 
-// Attention work of a layer: chunk list ordered by (sequence, kv head, chunk),
-// CTA i owns chunks [floor(i T / G), floor((i + 1) T / G)).
+// Attention work of a layer: units (sequence b, kv head g, split) in that
+// order, each covering up to Q consecutive 64-position chunks of b's cache;
+// Q = max(4, ceil(T / G)) with T the total chunk count, so short contexts
+// take one unit per (b, g) and long ones split evenly over the grid.  Unit u
+// goes to CTA u mod G.  Splits of one (b, g) merge their softmax states.
 struct AttnSched {
-    int T, G, nkv, B;
+    int B, nkv, G, Q, U;
     const int* nchunk;  // per sequence
-    Q3_DEV long long start(int i) const { return (long long)i * T / G; }
-    Q3_DEV int cta_of(long long j) const {
-        int i = (int)((j * G) / T);
-        while (i > 0 && start(i) > j) --i;
-        while (i + 1 < G && start(i + 1) <= j) ++i;
-        return i;
+    Q3_DEV void init(int B_, int nkv_, int G_, const int* nch) {
+        B = B_, nkv = nkv_, G = G_, nchunk = nch;
+        long long T = 0;
+        for (int b = 0; b < B; ++b) T += (long long)nkv * nchunk[b];
+        Q = (int)((T + G - 1) / G);
+        if (Q < 4) Q = 4;
+        U = 0;
+        for (int b = 0; b < B; ++b) U += nkv * nsplit(b);
     }
-    // chunk j -> (b, g, c, first chunk of (b, g))
-    Q3_DEV void locate(long long j, int& b, int& g, int& cc, long long& s0) const {
-        long long base = 0;
+    Q3_DEV int nsplit(int b) const { return (nchunk[b] + Q - 1) / Q; }
+    Q3_DEV void locate(int u, int& b, int& g, int& split) const {
+        int base = 0;
         for (b = 0; b < B; ++b) {
-            const long long n = (long long)nkv * nchunk[b];
-            if (j < base + n) break;
+            const int n = nkv * nsplit(b);
+            if (u < base + n) break;
             base += n;
         }
-        const int C = nchunk[b];
-        g = (int)((j - base) / C);
-        cc = (int)((j - base) % C);
-        s0 = base + (long long)g * C;
+        const int ns = nsplit(b);
+        g = (u - base) / ns;
+        split = (u - base) % ns;
     }
 };
 
 // ------------------------------------------------------------------ producer
-__device__ __noinline__ void produce(Ctl& c) {
+Q3_DEV void produce(Ctl& c) {
     const PParams& P = *c.P;
     Shared& sh = *c.sh;
     const int cta = blockIdx.x, G = gridDim.x;
@@ -255,24 +344,30 @@ __device__ __noinline__ void produce(Ctl& c) {
     };
     const int H = P.H, I = P.I, hd = P.hd;
     const int Dq = P.nh * hd;
-    int rot = (P.H / 16) % G;  // the embedding phase's tiles come first
-    AttnSched as{0, G, P.nkv, P.B, sh.nchunk};
-    for (int b = 0; b < P.B; ++b) as.T += P.nkv * sh.nchunk[b];
-    const long long a0 = as.start(cta), a1 = as.start(cta + 1);
+    // QKV, gate/up and lm_head tiles rotate over the grid starting after the
+    // CTAs that own the H-row tiles (embedding, O, down)
+    int rot = (P.H / 16) % G;
+    AttnSched as;
+    as.init(P.B, P.nkv, G, sh.nchunk);
     const uint32_t kvbytes = (uint32_t)(kKvChunk * hd * 2);
     for (int l = 0; l < P.L && ok; ++l) {
         put_phase(P.mats[4 * l + 0], P.qkv_rows / 16, H, rot);
-        for (long long j = a0; j < a1 && ok; ++j) {
-            int b, g, cc;
-            long long s0;
-            as.locate(j, b, g, cc, s0);
-            const size_t base = ((((size_t)l * P.bmax + b) * P.nkv + g) * P.cap + (size_t)cc * kKvChunk) * hd;
-            put(P.kc + base, kvbytes);
-            put(P.vc + base, kvbytes);
+        for (int u = cta; u < as.U && ok; u += G) {
+            int b, g, split;
+            as.locate(u, b, g, split);
+            const int c0 = split * as.Q, c1 = min(sh.nchunk[b], c0 + as.Q);
+            for (int cc = c0; cc < c1 && ok; ++cc) {
+                const size_t base = ((((size_t)l * P.bmax + b) * P.nkv + g) * P.cap + (size_t)cc * kKvChunk) * hd;
+                put(P.kc + base, kvbytes);
+                put(P.vc + base, kvbytes);
+            }
         }
-        put_phase(P.mats[4 * l + 1], H / 16, Dq, rot);
+        int fixed = 0;  // O and down: H-row tile t always on CTA t mod G
+        put_phase(P.mats[4 * l + 1], H / 16, Dq, fixed);
         put_phase(P.mats[4 * l + 2], 2 * I / 16, H, rot);
-        put_phase(P.mats[4 * l + 3], H / 16, I, rot);
+        fixed = 0;
+        put_phase(P.mats[4 * l + 3], H / 16, I, fixed);
+        stamp(c, 2 + 6 * l + 5);
     }
     put_phase(P.lm, P.vpad / 16, H, rot);
     sh.prod_done = 1;
@@ -281,7 +376,7 @@ __device__ __noinline__ void produce(Ctl& c) {
 // ------------------------------------------------------------------ consumer pieces
 
 // 1/rms(x) per sequence from the per-tile partial sums of squares
-Q3_DEV bool load_rnorm(Ctl& c, const LLw* ss, uint32_t flag) {
+Q3_DEV bool rnorm_from(Ctl& c, const LLw* ss, uint32_t flag) {
     const PParams& P = *c.P;
     const int ntiles = P.H / 16;
     for (int b = c.warp; b < P.B; b += kCWarps) {
@@ -301,14 +396,100 @@ Q3_DEV bool load_rnorm(Ctl& c, const LLw* ss, uint32_t flag) {
         acc = warp_sum(acc);
         if (c.lane == 0) c.sh->rnorm[b] = 1.0f / sqrtf(acc / (float)P.H + P.eps);
     }
+    return true;
+}
+
+Q3_DEV bool load_rnorm(Ctl& c, const LLw* ss, uint32_t flag) {
+    if (!rnorm_from(c, ss, flag)) return false;
     return cbar_sync(c);
 }
 
-// One 16-row weight tile against the activation planes plane[b][k]
-// ({f16 hi, f16 lo} of each value); leaves per-warp sums in sh.red and the
-// row scales in sh.scl (visible to all consumer threads on return).
+// Copy the phase input (plane words of 2B columns x K/2 pairs) into shared
+// memory as plain f16 pairs, and 1/rms per sequence when ss is given.  All
+// loads of a batch -- plane words and the partial sums of squares -- are
+// issued before any is checked, so a stage costs one round trip when its
+// input is ready.
+Q3_DEV bool stage_plane(Ctl& c, const LLw* plane, int K, uint32_t flag, const LLw* ss, uint32_t sflag) {
+    const PParams& P = *c.P;
+    const int half = K >> 1;
+    const int npair = P.B * half;  // (hi word, lo word) pairs are not adjacent; load word pairs of one part
+    const int nss = ss ? P.B * (P.H / 16) : 0;
+    // sums of squares: thread i < nss loads word (j = i / B, b = i % B)
+    unsigned long long sv = 0;
+    if (c.tid < nss) sv = ll_get(ss + (size_t)(c.tid / P.B) * P.bmax + c.tid % P.B);
+    constexpr int U = 8;
+    float xs[4] = {0.f, 0.f, 0.f, 0.f};  // B <= 4 on this path
+    for (int base = c.tid; base < npair; base += kCThreads * U) {
+        unsigned long long v[U][2];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int q = base + u * kCThreads;
+            if (q < npair) ll_get2(plane + 2 * q, v[u][0], v[u][1]);
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int q = base + u * kCThreads;
+            if (q >= npair) continue;
+            const int w0 = 2 * q;
+            if (!ll_settle(c, plane + w0, flag, v[u][0])) return false;
+            if (!ll_settle(c, plane + w0 + 1, flag, v[u][1])) return false;
+            const int col = w0 / half, k2 = w0 - col * half;
+            uint32_t* d = c.stage + (size_t)col * c.stage_ld + k2;
+            d[0] = (uint32_t)v[u][0];
+            d[1] = (uint32_t)v[u][1];
+            const __half2 h0 = *reinterpret_cast<const __half2*>(&d[0]);
+            const __half2 h1 = *reinterpret_cast<const __half2*>(&d[1]);
+            const float part = (__low2float(h0) + __high2float(h0)) + (__low2float(h1) + __high2float(h1));
+            const int bb = col >> 1;
+#pragma unroll
+            for (int q2 = 0; q2 < 4; ++q2)
+                if (q2 == bb) xs[q2] += part;
+        }
+    }
+    // per-sequence sums of the operand values (hi + lo), fixed order
+#pragma unroll
+    for (int q2 = 0; q2 < 4; ++q2) {
+        const float w = warp_sum(xs[q2]);
+        if (c.lane == 0) c.sh->xsum_w[c.warp][q2] = w;
+    }
+    if (ss) {
+        // each sequence's H/16 partial sums, in a fixed order: thread-local
+        // words go through shared memory and thread b < B adds them up
+        float* part = c.sh->ssp;
+        if (c.tid < nss) {
+            if (!ll_settle(c, ss + (size_t)(c.tid / P.B) * P.bmax + c.tid % P.B, sflag, sv)) return false;
+            part[c.tid] = __uint_as_float((uint32_t)sv);
+        }
+        for (int i = c.tid + kCThreads; i < nss; i += kCThreads) {
+            uint32_t u32;
+            if (!ll_wait(c, ss + (size_t)(i / P.B) * P.bmax + i % P.B, sflag, u32)) return false;
+            part[i] = __uint_as_float(u32);
+        }
+        if (!cbar_sync(c)) return false;
+        if (c.tid < P.B) {
+            float acc = 0.f;
+            for (int j = 0; j < P.H / 16; ++j) acc += part[j * P.B + c.tid];
+            c.sh->rnorm[c.tid] = 1.0f / sqrtf(acc / (float)P.H + P.eps);
+        }
+    } else {
+        if (!cbar_sync(c)) return false;
+    }
+    if (c.tid < P.B) {
+        float t4 = 0.f;
+#pragma unroll
+        for (int w = 0; w < kCWarps; ++w) t4 += c.sh->xsum_w[w][c.tid];
+        c.sh->xsum[c.tid] = kBias * t4;
+    }
+    return cbar_sync(c);
+}
+
+// One 16-row weight tile against the activation planes ({f16 hi, f16 lo}
+// pairs of each value); split-K over the eight warps.  Leaves per-warp sums
+// in c.red and the row scales in sh.scl (visible to all consumer threads on
+// return).  NT == 1 reads the operands from the staged copy in shared
+// memory, larger NT straight from the flagged words in global memory.
 template <int NT>
-__device__ __noinline__ bool gemv_tile(Ctl& c, int K, const LLw* plane, uint32_t flag) {
+Q3_DEV bool gemv_tile(Ctl& c, int K, const LLw* plane, uint32_t flag) {
     const PParams& P = *c.P;
     const int KP = K >> 5;
     const int nchunks = (KP + kKpPerChunk - 1) / kKpPerChunk;
@@ -316,77 +497,218 @@ __device__ __noinline__ bool gemv_tile(Ctl& c, int K, const LLw* plane, uint32_t
     float acc[NT][4];
 #pragma unroll
     for (int n = 0; n < NT; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
-    constexpr int KB = NT == 1 ? 4 : (NT == 2 ? 2 : 1);  // k-pairs whose operands are in flight together
+    dstamp(c, 8);
     for (int j = 0; j < nchunks; ++j) {
         uint8_t* slot;
         if (!slot_wait(c, slot)) return false;
+        dstamp(c, 4);
         if (j == 0 && c.warp == 0 && c.lane < 16) c.sh->scl[c.lane] = reinterpret_cast<const float*>(slot)[c.lane];
         const uint8_t* fb = slot + (j == 0 ? kTileHeader : 0);
         const int kp_end = min(KP, kKpPerChunk * (j + 1));
-        for (int i0 = 0; i0 < 4; i0 += KB) {
-            // B operand: the four {v(k), v(k+1)} words of this lane's column
-            // (sequence 4n + g/2, hi part for even g, lo part for odd g)
-            unsigned long long raw[KB][NT][4];
+        if constexpr (NT == 1) {
+            const bool live = (g >> 1) < P.B;
+            const uint32_t sca = smem_u32(c.stage + (size_t)g * c.stage_ld + t);
+            const uint32_t fa = smem_u32(fb) + c.lane * 16;
+            float a4[4][4];
 #pragma unroll
-            for (int i = 0; i < KB; ++i) {
-                const int p = kKpPerChunk * j + c.warp + 8 * (i0 + i);
+            for (int q = 0; q < 4; ++q) a4[q][0] = a4[q][1] = a4[q][2] = a4[q][3] = 0.f;
 #pragma unroll
-                for (int n = 0; n < NT; ++n) {
-                    const int b = 4 * n + (g >> 1);
-                    if (p < kp_end && b < P.B) {
-                        const LLw* base = plane + (size_t)(2 * b + (g & 1)) * (K >> 1) + 16 * p + t;
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) raw[i][n][e] = ll_get(base + 4 * e);
-                    }
-                }
+            for (int i = 0; i < kKpPerChunk / kCWarps; ++i) {
+                const int p = kKpPerChunk * j + c.warp + kCWarps * i;
+                if (p >= kp_end) continue;
+                const uint4 wv = lds128(fa + (p - kKpPerChunk * j) * 512);
+                uint32_t A0[4], A1[4];
+                u8x4_to_biased(wv.x, A0[0], A0[1]);
+                u8x4_to_biased(wv.y, A0[2], A0[3]);
+                u8x4_to_biased(wv.z, A1[0], A1[1]);
+                u8x4_to_biased(wv.w, A1[2], A1[3]);
+                const uint32_t ba = sca + 4 * 16 * p;
+                const uint32_t b0 = live ? lds32(ba) : 0u, b1 = live ? lds32(ba + 16) : 0u;
+                const uint32_t b2 = live ? lds32(ba + 32) : 0u, b3 = live ? lds32(ba + 48) : 0u;
+                mma_f16_16816(a4[(2 * i) & 3], A0, b0, b1);
+                mma_f16_16816(a4[(2 * i + 1) & 3], A1, b2, b3);
             }
 #pragma unroll
-            for (int i = 0; i < KB; ++i) {
-                const int p = kKpPerChunk * j + c.warp + 8 * (i0 + i);
-                if (p >= kp_end) continue;
+            for (int e = 0; e < 4; ++e) acc[0][e] += (a4[0][e] + a4[1][e]) + (a4[2][e] + a4[3][e]);
+        } else {
+            constexpr int KB = NT == 2 ? 4 : (NT == 4 ? 2 : 1);  // k-pairs with operands in flight together
+            for (int i0 = 0; i0 < kKpPerChunk / kCWarps; i0 += KB) {
+                // B operand: the four {v(k), v(k+1)} words of this lane's column
+                // (sequence 4n + g/2, hi part for even g, lo part for odd g)
+                unsigned long long raw[KB][NT][4];
 #pragma unroll
-                for (int n = 0; n < NT; ++n) {
-                    const int b = 4 * n + (g >> 1);
-                    if (b < P.B) {
-                        const LLw* base = plane + (size_t)(2 * b + (g & 1)) * (K >> 1) + 16 * p + t;
+                for (int i = 0; i < KB; ++i) {
+                    const int p = kKpPerChunk * j + c.warp + kCWarps * (i0 + i);
 #pragma unroll
-                        for (int e = 0; e < 4; ++e)
-                            if (!ll_settle(c, base + 4 * e, flag, raw[i][n][e])) return false;
+                    for (int n = 0; n < NT; ++n) {
+                        const int b = 4 * n + (g >> 1);
+                        if (p < kp_end && b < P.B) {
+                            const LLw* base = plane + (size_t)(2 * b + (g & 1)) * (K >> 1) + 16 * p + t;
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) raw[i][n][e] = ll_get(base + 4 * e);
+                        }
                     }
                 }
-                const uint4 wv = *reinterpret_cast<const uint4*>(fb + (size_t)(p - kKpPerChunk * j) * 512 + c.lane * 16);
-                uint32_t A0[4], A1[4];
-                u8x4_to_f16x2x2(wv.x, A0[0], A0[1]);
-                u8x4_to_f16x2x2(wv.y, A0[2], A0[3]);
-                u8x4_to_f16x2x2(wv.z, A1[0], A1[1]);
-                u8x4_to_f16x2x2(wv.w, A1[2], A1[3]);
 #pragma unroll
-                for (int n = 0; n < NT; ++n) {
-                    const bool live = 4 * n + (g >> 1) < P.B;
-                    const uint32_t b0 = live ? (uint32_t)raw[i][n][0] : 0u;
-                    const uint32_t b1 = live ? (uint32_t)raw[i][n][1] : 0u;
-                    const uint32_t b2 = live ? (uint32_t)raw[i][n][2] : 0u;
-                    const uint32_t b3 = live ? (uint32_t)raw[i][n][3] : 0u;
-                    mma_f16_16816(acc[n], A0, b0, b1);
-                    mma_f16_16816(acc[n], A1, b2, b3);
+                for (int i = 0; i < KB; ++i) {
+                    const int p = kKpPerChunk * j + c.warp + kCWarps * (i0 + i);
+                    if (p >= kp_end) continue;
+#pragma unroll
+                    for (int n = 0; n < NT; ++n) {
+                        const int b = 4 * n + (g >> 1);
+                        if (b < P.B) {
+                            const LLw* base = plane + (size_t)(2 * b + (g & 1)) * (K >> 1) + 16 * p + t;
+#pragma unroll
+                            for (int e = 0; e < 4; ++e)
+                                if (!ll_settle(c, base + 4 * e, flag, raw[i][n][e])) return false;
+                        }
+                    }
+                    const uint4 wv =
+                        *reinterpret_cast<const uint4*>(fb + (size_t)(p - kKpPerChunk * j) * 512 + c.lane * 16);
+                    uint32_t A0[4], A1[4];
+                    u8x4_to_f16x2x2(wv.x, A0[0], A0[1]);
+                    u8x4_to_f16x2x2(wv.y, A0[2], A0[3]);
+                    u8x4_to_f16x2x2(wv.z, A1[0], A1[1]);
+                    u8x4_to_f16x2x2(wv.w, A1[2], A1[3]);
+#pragma unroll
+                    for (int n = 0; n < NT; ++n) {
+                        const bool live = 4 * n + (g >> 1) < P.B;
+                        const uint32_t b0 = live ? (uint32_t)raw[i][n][0] : 0u;
+                        const uint32_t b1 = live ? (uint32_t)raw[i][n][1] : 0u;
+                        const uint32_t b2 = live ? (uint32_t)raw[i][n][2] : 0u;
+                        const uint32_t b3 = live ? (uint32_t)raw[i][n][3] : 0u;
+                        mma_f16_16816(acc[n], A0, b0, b1);
+                        mma_f16_16816(acc[n], A1, b2, b3);
+                    }
                 }
             }
         }
         slot_release(c);
+        dstamp(c, 5);
     }
+    float* red = c.red + (size_t)c.warp * NT * 64;
 #pragma unroll
     for (int n = 0; n < NT; ++n) {
-        c.sh->red[c.warp][n][c.lane][0] = acc[n][0] + acc[n][1];
-        c.sh->red[c.warp][n][c.lane][1] = acc[n][2] + acc[n][3];
+        red[(n * 32 + c.lane) * 2 + 0] = acc[n][0] + acc[n][1];
+        red[(n * 32 + c.lane) * 2 + 1] = acc[n][2] + acc[n][3];
     }
     return cbar_sync(c);
 }
 
-Q3_DEV float red_sum(const Shared& sh, int n, int ln, int half) {
+// Cross-warp sum of a split-K tile's partial results; with NT == 1 the
+// operands were biased (u8x4_to_biased) and the bias term is removed here.
+template <int NT>
+Q3_DEV float red_sum(const Ctl& c, int n, int ln, int half) {
     float s = 0.f;
 #pragma unroll
-    for (int w = 0; w < kCWarps; ++w) s += sh.red[w][n][ln][half];
+    for (int w = 0; w < kCWarps; ++w) s += c.red[((size_t)w * NT * 32 + n * 32 + ln) * 2 + half];
+    if constexpr (NT == 1) s -= c.sh->xsum[ln & 3];
     return s;
+}
+
+// Per-warp tiles for NT == 1 (B <= 4): warp w of the CTA takes every
+// kCWarps-th of the CTA's tiles in this phase, runs the whole K with four
+// independent MMA accumulator chains and does its own epilogue, so the
+// phase needs no CTA barrier.  The slots of the CTA's tile i are
+// used + i*nsl ...; each is released by its warp alone (arrival count
+// kCWarps) and every warp advances `used` past all of them at the end.
+enum WarpMode { kWmQkv = 0, kWmGu = 1, kWmLm = 2 };
+
+Q3_DEV void put_pair(LLw* plane, int K, int b, int k, float v0, float v1, uint32_t f);
+
+template <int MODE>
+Q3_DEV bool warp_tiles(Ctl& c, int t0, int ntiles, int G, int K, uint32_t fout) {
+    const PParams& P = *c.P;
+    Shared& sh = *c.sh;
+    const int KP = K >> 5, nsl = (KP + kKpPerChunk - 1) / kKpPerChunk;
+    const int g = c.lane >> 2, t = c.lane & 3;
+    const bool live = (g >> 1) < P.B;
+    const uint32_t sca = smem_u32(c.stage + (size_t)g * c.stage_ld + t);  // B operand column of this lane
+    int count = 0;
+    for (int tile = t0; tile < ntiles; tile += G, ++count) {
+        if ((count & (kCWarps - 1)) != c.warp) continue;
+        float a[4][4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) a[q][0] = a[q][1] = a[q][2] = a[q][3] = 0.f;
+        float s_lo = 0.f, s_hi = 0.f;
+        for (int j = 0; j < nsl; ++j) {
+            const uint32_t u = c.used + (uint32_t)(count * nsl + j);
+            uint8_t* slot;
+            if (!slot_wait_at(c, u, slot)) return false;
+            const uint32_t sa = smem_u32(slot);
+            if (j == 0) {
+                s_lo = lds_f32(sa + 4 * g);
+                s_hi = lds_f32(sa + 4 * (g + 8));
+            }
+            const uint32_t fa = sa + (j == 0 ? kTileHeader : 0) + c.lane * 16;
+            const int p0 = kKpPerChunk * j, np = min(KP - p0, kKpPerChunk);
+            {
+#pragma unroll 2
+                for (int i = 0; i < np; i += 2) {
+                    // k-pairs p and p+1: four k-steps on four independent chains
+                    const uint32_t ba = sca + 4 * 16 * (p0 + i);
+                    const bool two = i + 1 < np;  // a slot may end on an odd k-pair
+                    const uint4 w0 = lds128(fa + i * 512);
+                    const uint4 w1 = two ? lds128(fa + (i + 1) * 512) : w0;
+                    uint32_t bb[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) bb[e] = (live && (e < 4 || two)) ? lds32(ba + 16 * e) : 0u;
+                    uint32_t A[4];
+                    u8x4_to_biased(w0.x, A[0], A[1]);
+                    u8x4_to_biased(w0.y, A[2], A[3]);
+                    mma_f16_16816(a[0], A, bb[0], bb[1]);
+                    u8x4_to_biased(w0.z, A[0], A[1]);
+                    u8x4_to_biased(w0.w, A[2], A[3]);
+                    mma_f16_16816(a[1], A, bb[2], bb[3]);
+                    // (a missing second k-pair multiplies zero operands)
+                    u8x4_to_biased(w1.x, A[0], A[1]);
+                    u8x4_to_biased(w1.y, A[2], A[3]);
+                    mma_f16_16816(a[2], A, bb[4], bb[5]);
+                    u8x4_to_biased(w1.z, A[0], A[1]);
+                    u8x4_to_biased(w1.w, A[2], A[3]);
+                    mma_f16_16816(a[3], A, bb[6], bb[7]);
+                }
+            }
+            __syncwarp();
+            if (c.lane == 0) mbar_arrive_cnt(&c.empty[u % c.ns], kCWarps);
+        }
+        // lane (g, t): rows g and g+8 of the tile for sequence t (hi + lo columns)
+        const float bias = t < P.B ? sh.xsum[t] : 0.f;
+        const float v0 =
+            (((a[0][0] + a[0][1]) + (a[1][0] + a[1][1])) + ((a[2][0] + a[2][1]) + (a[3][0] + a[3][1]))) - bias;
+        const float v1 =
+            (((a[0][2] + a[0][3]) + (a[1][2] + a[1][3])) + ((a[2][2] + a[2][3]) + (a[3][2] + a[3][3]))) - bias;
+        const float r = t < P.B ? sh.rnorm[t] : 0.f;
+        if constexpr (MODE == kWmQkv) {
+            if (t < P.B) {
+                LLw* dst = P.qkv + (size_t)t * P.qkv_rows + 16 * tile + g;
+                ll_put(dst, __float_as_uint(s_lo * r * v0), fout);
+                ll_put(dst + 8, __float_as_uint(s_hi * r * v1), fout);
+            }
+        } else if constexpr (MODE == kWmGu) {
+            // rows g / g+8 are gate / up of unit 8*tile + g; lane + 4 holds unit g + 1
+            const float gate = s_lo * r * v0, up = s_hi * r * v1;
+            const float act = (gate / (1.0f + expf(-gate))) * up;
+            const float nxt = __shfl_down_sync(0xffffffffu, act, 4);
+            if (t < P.B && (g & 1) == 0) put_pair(P.pl_a, P.I, t, 8 * tile + g, act, nxt, fout);
+        } else {
+            if (t < P.B) {
+                const int row = 16 * tile + g;
+                const float z0 = s_lo * r * v0, z1 = s_hi * r * v1;
+                if (row < P.vocab) {
+                    if (P.logits) P.logits[(size_t)t * P.vocab + row] = z0;
+                    atomicMax(&sh.best[t], argmax_key(z0, (uint32_t)row));
+                }
+                if (row + 8 < P.vocab) {
+                    if (P.logits) P.logits[(size_t)t * P.vocab + row + 8] = z1;
+                    atomicMax(&sh.best[t], argmax_key(z1, (uint32_t)(row + 8)));
+                }
+            }
+        }
+    }
+    c.used += (uint32_t)(count * nsl);
+    // the staged input and 1/rms stay in use until every warp is done
+    return cbar_sync(c);
 }
 
 // Activation planes: plane[(2b + part) * (K/2) + k/2] = {v(k), v(k+1)} as
@@ -403,30 +725,26 @@ Q3_DEV void put_pair(LLw* plane, int K, int b, int k, float v0, float v1, uint32
 }
 
 // Residual epilogue shared by O, DOWN (from GEMV sums) and the embedding
-// phase (from the gathered row): x = x_prev + v; writes x and stages
-// gain * x and x^2 for finish_rows.
-Q3_DEV bool resid_store(Ctl& c, int tile, int row_in_tile, int b, float v, bool add_prev, uint32_t fprev,
-                        uint32_t fcur, const float* gain) {
-    const PParams& P = *c.P;
-    const int row = 16 * tile + row_in_tile;
-    float xn = v;
-    if (add_prev) {
-        uint32_t xp;
-        if (!ll_wait(c, P.x + (size_t)b * P.H + row, fprev, xp)) return false;
-        xn = __uint_as_float(xp) + v;
-    }
-    ll_put(P.x + (size_t)b * P.H + row, __float_as_uint(xn), fcur);
-    c.sh->gx[b][row_in_tile] = gain[row] * xn;
+// phase (from the gathered row).  H-row tile t lives on CTA t mod G in all
+// three phases, so the residual rows stay in this CTA's shared memory
+// (slot ti = t / G) from the embedding to the last layer: x = x_prev + v;
+// stages gain * x and x^2 for finish_rows.
+Q3_DEV void resid_store(Ctl& c, int tile, int row_in_tile, int b, float v, bool add_prev, const float* gain) {
+    float& xr = c.sh->xres[tile / gridDim.x][row_in_tile][b];
+    const float xn = add_prev ? xr + v : v;
+    xr = xn;
+    c.sh->gx[b][row_in_tile] = gain[16 * tile + row_in_tile] * xn;
     c.sh->sq[b][row_in_tile] = xn * xn;
-    return true;
 }
 
 // After resid_store: publish the planes of gain * x and the tile's sum of x^2.
 Q3_DEV bool finish_rows(Ctl& c, int tile, LLw* plane_out, LLw* ss_out, uint32_t fcur) {
+    dstamp(c, 6);
     if (!cbar_sync(c)) return false;
+    dstamp(c, 7);
     const PParams& P = *c.P;
-    if (c.tid < P.B * 8) {
-        const int b = c.tid >> 3, j = c.tid & 7;
+    for (int i = c.tid; i < P.B * 8; i += kCThreads) {
+        const int b = i >> 3, j = i & 7;
         put_pair(plane_out, P.H, b, 16 * tile + 2 * j, c.sh->gx[b][2 * j], c.sh->gx[b][2 * j + 1], fcur);
     }
     if (c.tid < P.B) {
@@ -438,13 +756,10 @@ Q3_DEV bool finish_rows(Ctl& c, int tile, LLw* plane_out, LLw* ss_out, uint32_t 
 }
 
 // ------------------------------------------------------------------ attention segment
-// The CTAs first..first+span-1 cover the chunks of (b, g); the ones whose
-// chunk range is empty (start(i) == start(i+1)) do not take part, so
-// narrive counts the others and the merge skips their slots.
+// One attention unit: chunks [c0, c1) of (b, g), split `split` of nsplit.
 template <int HD, int GROUP>
-__device__ __noinline__ bool attn_segment(Ctl& c, const AttnSched& as, int l, int b, int g, int c0, int c1, int first,
-                                          int span, int narrive, uint32_t fqkv, uint32_t fatt) {
-    const int seg = blockIdx.x - first;
+Q3_DEV bool attn_segment(Ctl& c, int l, int b, int g, int c0, int c1, int split, int nsplit,
+                                          uint32_t fqkv, uint32_t fatt) {
     constexpr int D = HD / 32;
     constexpr int E = HD / 32;
     const PParams& P = *c.P;
@@ -545,16 +860,15 @@ __device__ __noinline__ bool attn_segment(Ctl& c, const AttnSched& as, int l, in
     };
     for (int cc = c0; cc < c1; ++cc) {
         uint8_t *ks, *vs;
-        if (!slot_wait(c, ks)) return false;
-        c.used++;
-        const bool okv = slot_wait(c, vs);
-        c.used--;
-        if (!okv) return false;
+        if (!slot_wait_at(c, c.used, ks)) return false;
+        if (!slot_wait_at(c, c.used + 1, vs)) return false;
+#pragma unroll 1
+        for (int half = 0; half < kKvChunk / (8 * kCWarps); ++half) {
         float sc[GROUP][8];
         float vv[8][D];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-            const int r = c.warp * 8 + i;
+            const int r = (c.warp * (kKvChunk / (8 * kCWarps)) + half) * 8 + i;
             const int pa = cc * kKvChunk + r;
             const __nv_bfloat16* kr = reinterpret_cast<const __nv_bfloat16*>(ks) + (size_t)r * HD + c.lane * D;
             const __nv_bfloat16* vr = reinterpret_cast<const __nv_bfloat16*>(vs) + (size_t)r * HD + c.lane * D;
@@ -574,6 +888,7 @@ __device__ __noinline__ bool attn_segment(Ctl& c, const AttnSched& as, int l, in
             }
         }
         absorb(sc, vv);
+        }
         slot_release(c);
         slot_release(c);
     }
@@ -595,7 +910,8 @@ __device__ __noinline__ bool attn_segment(Ctl& c, const AttnSched& as, int l, in
         }
         absorb(sc, vv);
     }
-    // 3) merge the eight warps, publish this split's state
+    // 3) merge the eight warps; a single split writes the output directly,
+    //    otherwise it publishes its state and the last split merges them
     if (c.lane == 0)
         for (int h = 0; h < GROUP; ++h) {
             sh.wm[c.warp][h] = m[h];
@@ -606,7 +922,7 @@ __device__ __noinline__ bool attn_segment(Ctl& c, const AttnSched& as, int l, in
 #pragma unroll
         for (int d = 0; d < D; ++d) sh.wacc[c.warp][h][c.lane * D + d] = acc[h][d];
     if (!cbar_sync(c)) return false;
-    float* part = P.part + (((size_t)b * P.nkv + g) * gridDim.x + seg) * GROUP * (HD + 2);
+    float* part = P.part + (((size_t)b * P.nkv + g) * (gridDim.x + 1) + split) * GROUP * (HD + 2);
     for (int i = c.tid; i < GROUP * HD; i += kCThreads) {
         const int h = i / HD, d = i % HD;
         float M = -INFINITY;
@@ -618,31 +934,35 @@ __device__ __noinline__ bool attn_segment(Ctl& c, const AttnSched& as, int l, in
             L += sh.wl[w][h] * f;
             A += sh.wacc[w][h][d] * f;
         }
-        part[h * (HD + 2) + d] = A;
-        if (d == 0) {
-            part[h * (HD + 2) + HD] = M;
-            part[h * (HD + 2) + HD + 1] = L;
+        if (nsplit == 1) {
+            const float o = A / L;
+            const float o1 = __shfl_xor_sync(0xffffffffu, o, 1);
+            if ((d & 1) == 0) put_pair(P.pl_o, P.nh * HD, b, (g * GROUP + h) * HD + d, o, o1, fatt);
+        } else {
+            part[h * (HD + 2) + d] = A;
+            if (d == 0) {
+                part[h * (HD + 2) + HD] = M;
+                part[h * (HD + 2) + HD + 1] = L;
+            }
         }
     }
-    __threadfence();
+    if (nsplit == 1) return cbar_sync(c);
     if (!cbar_sync(c)) return false;
     if (c.tid == 0) {
+        __threadfence();  // the barrier made every thread's partial visible to this one
         const unsigned int old = atomicAdd(P.attn_cnt + ((size_t)l * P.bmax + b) * P.nkv + g, 1u);
-        sh.flag_last = (old == (unsigned)(narrive - 1));
+        sh.flag_last = (old == (unsigned)(nsplit - 1));
+        if (sh.flag_last) __threadfence();
     }
     if (!cbar_sync(c)) return false;
     if (sh.flag_last) {
-        __threadfence();
-        const float* p0 = P.part + (((size_t)b * P.nkv + g) * gridDim.x) * GROUP * (HD + 2);
+        const float* p0 = P.part + (((size_t)b * P.nkv + g) * (gridDim.x + 1)) * GROUP * (HD + 2);
         for (int i = c.tid; i < GROUP * HD; i += kCThreads) {
             const int h = i / HD, d = i % HD;
             float M = -INFINITY;
-            for (int s = 0; s < span; ++s)
-                if (as.start(first + s + 1) > as.start(first + s))
-                    M = fmaxf(M, ld_cg_f32(p0 + ((size_t)s * GROUP + h) * (HD + 2) + HD));
+            for (int s = 0; s < nsplit; ++s) M = fmaxf(M, ld_cg_f32(p0 + ((size_t)s * GROUP + h) * (HD + 2) + HD));
             float L = 0.f, A = 0.f;
-            for (int s = 0; s < span; ++s) {
-                if (as.start(first + s + 1) <= as.start(first + s)) continue;
+            for (int s = 0; s < nsplit; ++s) {
                 const float* ps = p0 + ((size_t)s * GROUP + h) * (HD + 2);
                 const float ms = ld_cg_f32(ps + HD);
                 if (ms == -INFINITY) continue;
@@ -667,27 +987,32 @@ Q3_DEV void consume(Ctl& c) {
     const int H = P.H, I = P.I, B = P.B, Dq = P.nh * HD;
     const uint32_t eb = *reinterpret_cast<volatile uint32_t*>(P.epoch) * 1024u;
     auto ep = [&](int l, int ph) { return eb + 8u * (uint32_t)l + (uint32_t)ph; };
-    int rot = 0;
+    // get this phase's input ready: staged copy (NT == 1) or 1/rms only
+    auto prepare = [&](const LLw* plane, int K, uint32_t flag, const LLw* ss, uint32_t sflag) -> bool {
+        if constexpr (NT == 1) return stage_plane(c, plane, K, flag, ss, sflag);
+        if (ss) return load_rnorm(c, ss, sflag);
+        return true;
+    };
+    int rot = (H / 16) % G;  // rotation of the QKV / gate-up / lm_head tiles
 
     // embedding gather (phase 0): x = E[tok] * s, planes of g_attn(0) * x
     {
         const int ntiles = H / 16;
         const uint32_t f = ep(0, kPhEmbed);
-        for (int t = first_tile(cta, rot, G); t < ntiles; t += G) {
+        for (int t = cta; t < ntiles; t += G) {
             for (int i = c.tid; i < B * 16; i += kCThreads) {
                 const int b = i >> 4, r = i & 15, k = 16 * t + r;
                 const int tok = P.tokens[b];
                 const float v = (float)P.emb_raw[(size_t)tok * H + k] * P.emb_scale[tok];
-                if (!resid_store(c, t, r, b, v, false, 0, f, P.gains[0])) return;
+                resid_store(c, t, r, b, v, false, P.gains[0]);
             }
             if (!finish_rows(c, t, P.pl_attn, P.ss_attn, f)) return;
             if (!cbar_sync(c)) return;
         }
-        rot = (rot + ntiles) % G;
+        stamp(c, 1);
     }
-    AttnSched as{0, G, P.nkv, B, sh.nchunk};
-    for (int b = 0; b < B; ++b) as.T += P.nkv * sh.nchunk[b];
-    const long long a0 = as.start(cta), a1 = as.start(cta + 1);
+    AttnSched as;
+    as.init(B, P.nkv, G, sh.nchunk);
 
     for (int l = 0; l < P.L; ++l) {
         const uint32_t f_in = l == 0 ? ep(0, kPhEmbed) : ep(l - 1, kPhDown);
@@ -697,97 +1022,116 @@ Q3_DEV void consume(Ctl& c) {
         {
             const int ntiles = P.qkv_rows / 16;
             int t = first_tile(cta, rot, G);
-            if (t < ntiles && !load_rnorm(c, P.ss_attn, f_in)) return;
+            if (t < ntiles && !prepare(P.pl_attn, H, f_in, P.ss_attn, f_in)) return;
+            dstamp(c, 1);
+            if constexpr (NT == 1) {
+                if (!warp_tiles<kWmQkv>(c, t, ntiles, G, H, ep(l, kPhQkv))) return;
+                t = ntiles;
+            }
             for (; t < ntiles; t += G) {
                 if (!gemv_tile<NT>(c, H, P.pl_attn, f_in)) return;
+                dstamp(c, 2);
                 for (int i = c.tid; i < NT * 64; i += kCThreads) {
                     const int n = i >> 6, ln = (i & 63) >> 1, half = i & 1, b = 4 * n + (ln & 3);
                     if (b >= B) continue;
                     const int rr = (ln >> 2) + 8 * half;
-                    const float v = sh.scl[rr] * sh.rnorm[b] * red_sum(sh, n, ln, half);
+                    const float v = sh.scl[rr] * sh.rnorm[b] * red_sum<NT>(c, n, ln, half);
                     ll_put(P.qkv + (size_t)b * P.qkv_rows + 16 * t + rr, __float_as_uint(v), ep(l, kPhQkv));
                 }
                 if (!cbar_sync(c)) return;
+                dstamp(c, 3);
             }
             rot = (rot + ntiles) % G;
+            stamp(c, 2 + 6 * l + 0);
         }
         // ---- attention
         c.phase = kPhAtt;
-        for (long long j = a0; j < a1;) {
-            int b, g, cc;
-            long long s0;
-            as.locate(j, b, g, cc, s0);
-            const long long seg_end = s0 + sh.nchunk[b] < a1 ? s0 + sh.nchunk[b] : a1;
-            const int first = as.cta_of(s0), last = as.cta_of(s0 + sh.nchunk[b] - 1);
-            int narrive = 0;
-            for (int i = first; i <= last; ++i) narrive += as.start(i + 1) > as.start(i);
-            const int c1 = cc + (int)(seg_end - j);
-            if (!attn_segment<HD, GROUP>(c, as, l, b, g, cc, c1, first, last - first + 1, narrive, ep(l, kPhQkv),
-                                         ep(l, kPhAtt)))
+        for (int u = cta; u < as.U; u += G) {
+            int b, g, split;
+            as.locate(u, b, g, split);
+            const int c0 = split * as.Q, c1 = min(sh.nchunk[b], c0 + as.Q);
+            if (!attn_segment<HD, GROUP>(c, l, b, g, c0, c1, split, as.nsplit(b), ep(l, kPhQkv), ep(l, kPhAtt)))
                 return;
-            j = seg_end;
         }
+        stamp(c, 2 + 6 * l + 1);
         // ---- O projection + residual
         c.phase = kPhO;
         {
             const int ntiles = H / 16;
-            const uint32_t fprev = l == 0 ? ep(0, kPhEmbed) : ep(l - 1, kPhDown);
-            for (int t = first_tile(cta, rot, G); t < ntiles; t += G) {
+            int t = cta;
+            if (t < ntiles && !prepare(P.pl_o, Dq, ep(l, kPhAtt), nullptr, 0)) return;
+            dstamp(c, 1);
+            for (; t < ntiles; t += G) {
                 if (!gemv_tile<NT>(c, Dq, P.pl_o, ep(l, kPhAtt))) return;
+                dstamp(c, 2);
                 for (int i = c.tid; i < NT * 64; i += kCThreads) {
                     const int n = i >> 6, ln = (i & 63) >> 1, half = i & 1, b = 4 * n + (ln & 3);
                     if (b >= B) continue;
                     const int rr = (ln >> 2) + 8 * half;
-                    const float v = sh.scl[rr] * red_sum(sh, n, ln, half);
-                    if (!resid_store(c, t, rr, b, v, true, fprev, ep(l, kPhO), P.gains[4 * l + 1])) return;
+                    const float v = sh.scl[rr] * red_sum<NT>(c, n, ln, half);
+                    resid_store(c, t, rr, b, v, true, P.gains[4 * l + 1]);
                 }
                 if (!finish_rows(c, t, P.pl_ffn, P.ss_ffn, ep(l, kPhO))) return;
                 if (!cbar_sync(c)) return;
+                dstamp(c, 3);
             }
-            rot = (rot + ntiles) % G;
+            stamp(c, 2 + 6 * l + 2);
         }
         // ---- gate/up + SiLU
         c.phase = kPhGu;
         {
             const int ntiles = 2 * I / 16;
             int t = first_tile(cta, rot, G);
-            if (t < ntiles && !load_rnorm(c, P.ss_ffn, ep(l, kPhO))) return;
+            if (t < ntiles && !prepare(P.pl_ffn, H, ep(l, kPhO), P.ss_ffn, ep(l, kPhO))) return;
+            dstamp(c, 1);
+            if constexpr (NT == 1) {
+                if (!warp_tiles<kWmGu>(c, t, ntiles, G, H, ep(l, kPhGu))) return;
+                t = ntiles;
+            }
             for (; t < ntiles; t += G) {
                 if (!gemv_tile<NT>(c, H, P.pl_ffn, ep(l, kPhO))) return;
+                dstamp(c, 2);
                 for (int i = c.tid; i < NT * 32; i += kCThreads) {
                     const int n = i >> 5, ln = i & 31, gg = ln >> 2, b = 4 * n + (ln & 3);
                     if (b >= B) continue;
-                    const float gate = sh.scl[gg] * sh.rnorm[b] * red_sum(sh, n, ln, 0);
-                    const float up = sh.scl[gg + 8] * sh.rnorm[b] * red_sum(sh, n, ln, 1);
+                    const float gate = sh.scl[gg] * sh.rnorm[b] * red_sum<NT>(c, n, ln, 0);
+                    const float up = sh.scl[gg + 8] * sh.rnorm[b] * red_sum<NT>(c, n, ln, 1);
                     sh.gx[b][gg] = (gate / (1.0f + expf(-gate))) * up;
                 }
                 if (!cbar_sync(c)) return;
-                if (c.tid < B * 4) {
-                    const int b = c.tid >> 2, jj = c.tid & 3;
+                for (int i = c.tid; i < B * 4; i += kCThreads) {
+                    const int b = i >> 2, jj = i & 3;
                     put_pair(P.pl_a, I, b, 8 * t + 2 * jj, sh.gx[b][2 * jj], sh.gx[b][2 * jj + 1], ep(l, kPhGu));
                 }
                 if (!cbar_sync(c)) return;
+                dstamp(c, 3);
             }
             rot = (rot + ntiles) % G;
+            stamp(c, 2 + 6 * l + 3);
         }
         // ---- down + residual
         c.phase = kPhDown;
         {
             const int ntiles = H / 16;
             const float* gnext = l + 1 < P.L ? P.gains[4 * (l + 1)] : P.final_norm;
-            for (int t = first_tile(cta, rot, G); t < ntiles; t += G) {
+            int t = cta;
+            if (t < ntiles && !prepare(P.pl_a, I, ep(l, kPhGu), nullptr, 0)) return;
+            dstamp(c, 1);
+            for (; t < ntiles; t += G) {
                 if (!gemv_tile<NT>(c, I, P.pl_a, ep(l, kPhGu))) return;
+                dstamp(c, 2);
                 for (int i = c.tid; i < NT * 64; i += kCThreads) {
                     const int n = i >> 6, ln = (i & 63) >> 1, half = i & 1, b = 4 * n + (ln & 3);
                     if (b >= B) continue;
                     const int rr = (ln >> 2) + 8 * half;
-                    const float v = sh.scl[rr] * red_sum(sh, n, ln, half);
-                    if (!resid_store(c, t, rr, b, v, true, ep(l, kPhO), ep(l, kPhDown), gnext)) return;
+                    const float v = sh.scl[rr] * red_sum<NT>(c, n, ln, half);
+                    resid_store(c, t, rr, b, v, true, gnext);
                 }
                 if (!finish_rows(c, t, P.pl_attn, P.ss_attn, ep(l, kPhDown))) return;
                 if (!cbar_sync(c)) return;
+                dstamp(c, 3);
             }
-            rot = (rot + ntiles) % G;
+            stamp(c, 2 + 6 * l + 4);
         }
     }
     // ---- lm_head + argmax
@@ -798,21 +1142,27 @@ Q3_DEV void consume(Ctl& c) {
         const uint32_t f = ep(P.L - 1, kPhDown);
         if (c.tid < kMaxBatch) sh.best[c.tid] = 0ull;
         int t = first_tile(cta, rot, G);
-        if (t < ntiles && !load_rnorm(c, P.ss_attn, f)) return;
+        if (t < ntiles && !prepare(P.pl_attn, H, f, P.ss_attn, f)) return;
         if (!cbar_sync(c)) return;
-        for (; t < ntiles; t += G) {
-            if (!gemv_tile<NT>(c, H, P.pl_attn, f)) return;
-            for (int i = c.tid; i < NT * 64; i += kCThreads) {
-                const int n = i >> 6, ln = (i & 63) >> 1, half = i & 1, b = 4 * n + (ln & 3);
-                if (b >= B) continue;
-                const int rr = (ln >> 2) + 8 * half, row = 16 * t + rr;
-                if (row >= P.vocab) continue;
-                const float z = sh.scl[rr] * sh.rnorm[b] * red_sum(sh, n, ln, half);
-                if (P.logits) P.logits[(size_t)b * P.vocab + row] = z;
-                atomicMax(&sh.best[b], argmax_key(z, (uint32_t)row));
+        if constexpr (NT == 1) {
+            if (!warp_tiles<kWmLm>(c, t, ntiles, G, H, 0u)) return;
+        } else {
+            for (; t < ntiles; t += G) {
+                if (!gemv_tile<NT>(c, H, P.pl_attn, f)) return;
+                for (int i = c.tid; i < NT * 64; i += kCThreads) {
+                    const int n = i >> 6, ln = (i & 63) >> 1, half = i & 1, b = 4 * n + (ln & 3);
+                    if (b >= B) continue;
+                    const int rr = (ln >> 2) + 8 * half, row = 16 * t + rr;
+                    if (row >= P.vocab) continue;
+                    const float z = sh.scl[rr] * sh.rnorm[b] * red_sum<NT>(c, n, ln, half);
+                    if (P.logits) P.logits[(size_t)b * P.vocab + row] = z;
+                    atomicMax(&sh.best[b], argmax_key(z, (uint32_t)row));
+                }
+                if (!cbar_sync(c)) return;
             }
-            if (!cbar_sync(c)) return;
         }
+        if (!cbar_sync(c)) return;
+        stamp(c, 2 + 6 * P.L);
         if (c.tid < B) atomicMax(&P.keys[c.tid], sh.best[c.tid]);
         __threadfence();
         if (!cbar_sync(c)) return;
@@ -840,6 +1190,25 @@ Q3_DEV void consume(Ctl& c) {
     }
 }
 
+// ------------------------------------------------------------------ layout of the dynamic shared memory
+// [ring: ns slots][red: 8 x NT x 32 x 2 floats][stage (NT == 1): 2B x ld u32][full, empty mbarriers]
+struct DynLayout {
+    size_t ring, red, stage, bars, total;
+    int stage_ld;
+};
+
+__host__ __device__ inline DynLayout dyn_layout(int ns, int NT, int B, int kmax) {
+    DynLayout d;
+    d.ring = 0;
+    d.red = d.ring + (size_t)ns * kSlotBytes;
+    d.stage = d.red + (size_t)kCWarps * NT * 64 * sizeof(float);
+    d.stage_ld = kmax / 2 + kStagePad;
+    const size_t stage_bytes = NT == 1 ? (size_t)2 * B * d.stage_ld * sizeof(uint32_t) : 0;
+    d.bars = (d.stage + stage_bytes + 15) / 16 * 16;
+    d.total = d.bars + 2 * (size_t)ns * sizeof(uint64_t);
+    return d;
+}
+
 template <int NT, int HD, int GROUP>
 __global__ void __launch_bounds__(kThreads, 1) persistent_step_kernel(PParams P) {
     extern __shared__ __align__(128) uint8_t dsm[];
@@ -847,11 +1216,15 @@ __global__ void __launch_bounds__(kThreads, 1) persistent_step_kernel(PParams P)
     __shared__ PParams sP;
     if (threadIdx.x == 0) sP = P;
     const int ns = P.ns;
+    const DynLayout dl = dyn_layout(ns, NT, P.B, P.kmax);
     Ctl c;
     c.P = &sP;
     c.sh = &sh;
-    c.ring = dsm;
-    c.full = reinterpret_cast<uint64_t*>(dsm + (size_t)ns * kSlotBytes);
+    c.ring = dsm + dl.ring;
+    c.red = reinterpret_cast<float*>(dsm + dl.red);
+    c.stage = reinterpret_cast<uint32_t*>(dsm + dl.stage);
+    c.stage_ld = dl.stage_ld;
+    c.full = reinterpret_cast<uint64_t*>(dsm + dl.bars);
     c.empty = c.full + ns;
     c.ns = ns;
     c.used = 0;
@@ -861,6 +1234,7 @@ __global__ void __launch_bounds__(kThreads, 1) persistent_step_kernel(PParams P)
     c.tid = threadIdx.x;
     c.layer = -1;
     c.phase = -1;
+    c.dcount = 0;
     if (threadIdx.x == 0) {
         for (int s = 0; s < ns; ++s) {
             mbar_init(&c.full[s], 1);
@@ -883,21 +1257,29 @@ __global__ void __launch_bounds__(kThreads, 1) persistent_step_kernel(PParams P)
         if (c.lane == 0) produce(c);
         return;
     }
+    stamp(c, 0);
     consume<NT, HD, GROUP>(c);
+    stamp(c, 3 + 6 * P.L);
     if (sh.abort && c.tid == 0) {
         // give every copy still in flight a bounded chance to land
         for (uint32_t i = 0; i < kSpinLimit && !sh.prod_done; ++i) __nanosleep(64);
         const uint32_t issued = sh.issued;
         for (uint32_t u = c.used; u < issued; ++u) mbar_wait_bounded(&c.full[u % ns], (u / ns) & 1);
-        (void)global_ns;
     }
 }
 
 // ------------------------------------------------------------------ host side
+static int nt_of(int B) { return B <= 4 ? 1 : B <= 8 ? 2 : B <= 16 ? 4 : 8; }
+
 template <int NT, int HD, int GROUP>
 static cudaError_t launch_t(const PParams& P, int grid, size_t smem, cudaStream_t st) {
     auto kern = persistent_step_kernel<NT, HD, GROUP>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    // shared-memory carveout just large enough (percent of the maximum), the rest stays L1
+    const size_t need = smem + sizeof(Shared) + sizeof(PParams) + 1024;
+    int carve = (int)((need * 100 + 232447) / 232448);
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, carve > 100 ? 100 : carve);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
@@ -914,11 +1296,12 @@ static cudaError_t launch_t(const PParams& P, int grid, size_t smem, cudaStream_
 
 template <int HD, int GROUP>
 static cudaError_t launch_hg(const PParams& P, int grid, size_t smem, cudaStream_t st) {
-    const int nt = (P.B + 3) / 4;
-    if (nt <= 1) return launch_t<1, HD, GROUP>(P, grid, smem, st);
-    if (nt <= 2) return launch_t<2, HD, GROUP>(P, grid, smem, st);
-    if (nt <= 4) return launch_t<4, HD, GROUP>(P, grid, smem, st);
-    return launch_t<8, HD, GROUP>(P, grid, smem, st);
+    switch (nt_of(P.B)) {
+        case 1: return launch_t<1, HD, GROUP>(P, grid, smem, st);
+        case 2: return launch_t<2, HD, GROUP>(P, grid, smem, st);
+        case 4: return launch_t<4, HD, GROUP>(P, grid, smem, st);
+        default: return launch_t<8, HD, GROUP>(P, grid, smem, st);
+    }
 }
 
 bool persistent_supported(const q3i8_dims& d) {
@@ -926,18 +1309,21 @@ bool persistent_supported(const q3i8_dims& d) {
     return (d.head_dim == 128 || d.head_dim == 64) && group == 2 && d.n_layers <= 127;
 }
 
-size_t persistent_static_smem() { return sizeof(Shared); }
-
-int persistent_slots(int max_optin_smem) {
-    const int avail = max_optin_smem - (int)sizeof(Shared) - 1024;
-    int ns = avail / (kSlotBytes + 16);
-    return ns > 12 ? 12 : ns;
+// Ring slots for batch B: as many as fit (at most kMaxSlots) after the
+// static shared memory, the reduction buffer and the staged input.  The ring
+// should hold more than one layer's share of a CTA's weight tiles (about ten
+// 16.5 KB slots for the CTAs that also own O and down tiles), so that a
+// layer's last weights are loaded before its consumers reach them.
+int persistent_slots(int max_optin_smem, int B, int kmax) {
+    const int nt = nt_of(B);
+    const int fixed = (int)(sizeof(Shared) + sizeof(PParams)) + 1024;
+    for (int ns = kMaxSlots; ns >= 2; --ns)
+        if ((int)dyn_layout(ns, nt, B, kmax).total + fixed <= max_optin_smem) return ns;
+    return 0;
 }
 
-size_t persistent_dyn_smem(int ns) { return (size_t)ns * kSlotBytes + 2 * (size_t)ns * sizeof(uint64_t); }
-
 cudaError_t launch_persistent_step(const PParams& P, int grid, cudaStream_t st) {
-    const size_t smem = persistent_dyn_smem(P.ns);
+    const size_t smem = dyn_layout(P.ns, nt_of(P.B), P.B, P.kmax).total;
     if (P.hd == 128) return launch_hg<128, 2>(P, grid, smem, st);
     return launch_hg<64, 2>(P, grid, smem, st);
 }

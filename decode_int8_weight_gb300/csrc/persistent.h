@@ -15,7 +15,7 @@ struct LLw {
 };
 
 struct PParams {
-    int B, bmax, H, I, L, nh, nkv, hd, cap, vocab, vpad, qkv_rows, ns;
+    int B, bmax, H, I, L, nh, nkv, hd, cap, vocab, vpad, qkv_rows, ns, kmax;
     float eps;
     const uint8_t* const* mats;   // [L*4] tile blobs: qkv, o, gate/up, down
     const uint8_t* lm;            // tile blobs of the tied embedding (lm_head)
@@ -39,6 +39,7 @@ struct PParams {
     int32_t* status;              // 0, or 7 when a bounded wait gave up
     int32_t* abort_flag;          // raised with status; ends every wait in the grid
     int32_t* diag;                // [8] first failed wait: site, cta, warp, layer, phase, aux
+    unsigned long long* trace;    // optional [grid][trace_stride] globaltimer stamps
     float* logits;                // optional [B][vocab]
     LLw* x;                       // [bmax][H] residual stream
     LLw* pl_attn;                 // [bmax][H] {hi, lo} of g * x feeding QKV / lm_head
@@ -48,13 +49,20 @@ struct PParams {
     LLw* qkv;                     // [bmax][qkv_rows] fp32 projections
     LLw* pl_o;                    // [bmax][nh*hd] {hi, lo} of the attention output
     LLw* pl_a;                    // [bmax][I] {hi, lo} of silu(gate) * up
-    float* part;                  // [bmax][nkv][grid][2][hd+2] split-KV softmax states
+    float* part;                  // [bmax][nkv][grid+1][2][hd+2] split-KV softmax states
 };
 
+// Trace record of one CTA: [0] start, [1] embedding done, per layer l at
+// 2 + 6l: QKV, attention, O, gate/up, down done and the producer's last
+// issue of the layer; then the lm_head done and the exit; then up to 32
+// (time, event) pairs inside layer kTraceDetailLayer (event = 16 * phase +
+// {1: input staged, 2: tile GEMV done, 3: tile epilogue done}).
+constexpr int kTraceDetailLayer = 5;
+__host__ __device__ inline int trace_detail_base(int L) { return 4 + 6 * L; }
+__host__ __device__ inline int trace_stride(int L) { return 4 + 6 * L + 64; }
+
 bool persistent_supported(const q3i8_dims& d);
-size_t persistent_static_smem();
-int persistent_slots(int max_optin_smem);
-size_t persistent_dyn_smem(int ns);
+int persistent_slots(int max_optin_smem, int B, int kmax);
 cudaError_t launch_persistent_step(const PParams& P, int grid, cudaStream_t st);
 
 }  // namespace q3

@@ -192,6 +192,15 @@ int32_t q3i8_step_launches(const q3i8_ctx* ctx, int32_t B);
 /* Kernels this context has launched so far (graph replays counted per node). */
 int64_t q3i8_launch_count(const q3i8_ctx* ctx);
 
+/* Diagnostics: run ONE decode step (as q3i8_step_logits would, without
+ * logits) with %globaltimer stamps recorded at every phase boundary of the
+ * persistent step kernel, and copy them to the HOST array stamps
+ * [grid][stride] (nanoseconds).  *grid and *stride receive the shape.  Needs a
+ * prior q3i8_prefill; returns Q3_ERR_STATE when the context decodes with the
+ * chained kernels or when cap is too small. */
+int q3i8_trace_step(q3i8_ctx* ctx, const int32_t* tokens, uint64_t* stamps, size_t cap, int32_t* grid,
+                    int32_t* stride);
+
 const char* q3i8_last_error(const q3i8_ctx* ctx);
 const char* q3i8_status_name(int status);
 void q3i8_destroy(q3i8_ctx* ctx);
