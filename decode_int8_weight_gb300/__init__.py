@@ -12,6 +12,7 @@ The call surface mirrors the C ABI in ``include/q3i8.h``:
 * ``Decoder.prefill`` / ``Decoder.step_logits``   -> teacher-forced checking
 * ``validate_dims``                               -> ``q3i8_validate_dims``
 * ``op_attention``                                -> ``q3i8_op_attention``
+* ``op_attention_static``                         -> ``q3i8_op_attention_static``
 
 A model is any object with ``shape`` (hidden, n_layers, n_heads, n_kv_heads,
 head_dim, intermediate, vocab, rope_theta, rms_eps), ``embed.q``/``embed.s``,
@@ -35,7 +36,8 @@ STATUS = {0: "ok", 1: "unsupported_architecture", 2: "invalid_arguments", 3: "co
 
 EXPORTS = ["q3i8_validate_dims", "q3i8_init", "q3i8_decode", "q3i8_decode_device", "q3i8_prefill",
            "q3i8_step_logits", "q3i8_read_kv", "q3i8_step_bytes", "q3i8_step_launches", "q3i8_launch_count", "q3i8_last_error",
-           "q3i8_status_name", "q3i8_destroy", "q3i8_trace_step", "q3i8_op_attention_workspace", "q3i8_op_attention"]
+           "q3i8_status_name", "q3i8_destroy", "q3i8_trace_step", "q3i8_op_attention_workspace", "q3i8_op_attention",
+           "q3i8_op_attention_static"]
 
 
 class Q3Error(RuntimeError):
@@ -107,6 +109,7 @@ def lib():
             L.q3i8_op_attention_workspace.restype = sz
             L.q3i8_op_attention_workspace.argtypes = [i32, i32, i32, i32]
             L.q3i8_op_attention.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, vp, vp, sz, vp, vp]
+            L.q3i8_op_attention_static.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, vp, vp, vp]
             _lib = L
     return _lib
 
@@ -266,4 +269,20 @@ def op_attention(q, k, v, row_seq, row_len, n_kv_heads: int, splits: int, out, w
                                  hd, cap, splits, _tptr(out), _tptr(workspace),
                                  workspace.numel() * workspace.element_size(), _tptr(status),
                                  ctypes.c_void_p(stream) if stream else None)
+    _check(rc, None)
+
+
+#: Largest scratch, in bytes, that ``op_attention_static`` may need.
+OP_ATTENTION_STATIC_SCRATCH_BYTES = 4 << 20
+
+
+def op_attention_static(q, k, v, row_seq, row_len, n_kv_heads: int, splits: int, out, status=None, stream=None):
+    """``op_attention`` without a workspace: the partial states go to scratch
+    compiled into the library, so nothing is allocated (see
+    q3i8_op_attention_static).  Calls that overlap on one device race."""
+    R, nh, hd = q.shape
+    cap = k.shape[2]
+    rc = lib().q3i8_op_attention_static(_tptr(q), _tptr(k), _tptr(v), _tptr(row_seq), _tptr(row_len), R, nh,
+                                        n_kv_heads, hd, cap, splits, _tptr(out), _tptr(status),
+                                        ctypes.c_void_p(stream) if stream else None)
     _check(rc, None)

@@ -37,6 +37,13 @@ static int fail(q3i8_ctx* c, int code, const char* fmt, ...) {
     return code;
 }
 
+// Records an error of a call that has no context; q3i8_last_error(NULL)
+// returns it on the same thread.
+int q3_report_error(int code, const char* msg) {
+    g_tls_error = msg;
+    return code;
+}
+
 #define CK(c, call)                                                                                     \
     do {                                                                                                \
         cudaError_t e_ = (call);                                                                        \

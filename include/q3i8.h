@@ -230,6 +230,31 @@ int q3i8_op_attention(const float* q, const uint16_t* k, const uint16_t* v, cons
                       int32_t cap, int32_t splits, float* out, void* workspace, size_t ws_bytes,
                       int32_t* d_status, void* cuda_stream);
 
+/* Upper limit, in bytes, of the scratch q3i8_op_attention_static may use:
+ * attention_workspace(R, n_heads, hd, splits) must not exceed it. */
+#define Q3I8_OP_ATTENTION_STATIC_SCRATCH_BYTES (4u << 20)
+
+/* q3i8_op_attention without a workspace argument and without allocating.
+ * The pages have no counterpart of this call: it exists for callers that
+ * cannot hand over device memory, e.g. a plain C host program with no device
+ * allocator of its own, or code that must not call cudaMalloc/cudaFree
+ * between steps because cudaFree synchronises the whole device.
+ *
+ * Arguments, layouts and results are those of q3i8_op_attention.  The
+ * partial softmax states live in one scratch array compiled into the library
+ * (Q3I8_OP_ATTENTION_STATIC_SCRATCH_BYTES per device); nothing in it has to
+ * start at zero, since every state is written before it is read.
+ *
+ * The first call on each device (the caller's current device) looks up the
+ * scratch array's device address; make that first call before any stream
+ * capture begins.  Calls that overlap in time on the same device (two
+ * streams, two threads) share the scratch and race: serialise them, e.g. on
+ * one stream.  Returns Q3_ERR_INVALID_ARGUMENTS (with a message naming the
+ * limit) when the sizes need more scratch than the limit. */
+int q3i8_op_attention_static(const float* q, const uint16_t* k, const uint16_t* v, const int32_t* row_seq,
+                             const int32_t* row_len, int32_t R, int32_t n_heads, int32_t n_kv_heads, int32_t hd,
+                             int32_t cap, int32_t splits, float* out, int32_t* d_status, void* cuda_stream);
+
 #ifdef __cplusplus
 }
 #endif
