@@ -48,7 +48,7 @@ constexpr int kMaxSlots = 12;
 constexpr int kMaxHTiles = 4;  // H-row tiles per CTA (H <= 64 * grid)
 
 // phase ids inside a layer (epoch = base + 8 * layer + phase)
-enum { kPhEmbed = 0, kPhQkv = 1, kPhAtt = 2, kPhO = 3, kPhGu = 4, kPhDown = 5 };
+enum { kPhEmbed = 0, kPhQkv = 1, kPhAtt = 2, kPhO = 3, kPhGu = 4, kPhDown = 5, kPhLm = 6 };
 
 Q3_DEV void ll_put(LLw* p, uint32_t payload, uint32_t flag) {
     const unsigned long long v = ((unsigned long long)flag << 32) | payload;
@@ -202,6 +202,25 @@ __device__ __noinline__ unsigned long long poll_word(const PParams* P, int* sh_a
         }
         if (i > 4) __nanosleep(20);
     }
+}
+
+// One round of a batched poll found words still stale: sleep briefly and,
+// every 64 rounds, check the abort flag and the time limit.  Returns the
+// updated start time, or ~0 when the wait has to give up.
+__device__ __noinline__ uint64_t poll_tick(const PParams* P, int* sh_abort, int diag, uint32_t i, uint64_t t0,
+                                           uint32_t flag) {
+    const WaitCtx w{P, sh_abort, diag};
+    if ((i & 63) == 63) {
+        if (aborted_w(w)) return ~0ull;
+        const uint64_t now = global_ns();
+        if (t0 == 0) return now;
+        if (now - t0 > kWaitNs || i > kSpinLimit * 16) {
+            raise_abort_w(w, kSiteWord, flag);
+            return ~0ull;
+        }
+    }
+    if (i > 2) __nanosleep(20);
+    return t0;
 }
 
 Q3_DEV int diag_of(const Ctl& c) { return c.warp | (c.layer & 255) << 8 | (c.phase + 1) << 16; }
@@ -417,22 +436,40 @@ Q3_DEV bool stage_plane(Ctl& c, const LLw* plane, int K, uint32_t flag, const LL
     // sums of squares: thread i < nss loads word (j = i / B, b = i % B)
     unsigned long long sv = 0;
     if (c.tid < nss) sv = ll_get(ss + (size_t)(c.tid / P.B) * P.bmax + c.tid % P.B);
-    constexpr int U = 8;
+    constexpr int U = 12;
     float xs[4] = {0.f, 0.f, 0.f, 0.f};  // B <= 4 on this path
+    const unsigned long long done = (unsigned long long)flag << 32;
     for (int base = c.tid; base < npair; base += kCThreads * U) {
         unsigned long long v[U][2];
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             const int q = base + u * kCThreads;
             if (q < npair) ll_get2(plane + 2 * q, v[u][0], v[u][1]);
+            else v[u][0] = v[u][1] = done;
+        }
+        // words still stale are re-read together, so a round costs one
+        // round trip however many of them were early
+        uint64_t t0 = 0;
+        for (uint32_t i = 0;; ++i) {
+            bool stale = false;
+#pragma unroll
+            for (int u = 0; u < U; ++u)
+                stale |= ((uint32_t)(v[u][0] >> 32) != flag) | ((uint32_t)(v[u][1] >> 32) != flag);
+            if (!stale) break;
+            t0 = poll_tick(c.P, &c.sh->abort, diag_of(c), i, t0, flag);
+            if (t0 == ~0ull) return false;
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int q = base + u * kCThreads;
+                if (((uint32_t)(v[u][0] >> 32) != flag) | ((uint32_t)(v[u][1] >> 32) != flag))
+                    ll_get2(plane + 2 * q, v[u][0], v[u][1]);
+            }
         }
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             const int q = base + u * kCThreads;
             if (q >= npair) continue;
             const int w0 = 2 * q;
-            if (!ll_settle(c, plane + w0, flag, v[u][0])) return false;
-            if (!ll_settle(c, plane + w0 + 1, flag, v[u][1])) return false;
             const int col = w0 / half, k2 = w0 - col * half;
             uint32_t* d = c.stage + (size_t)col * c.stage_ld + k2;
             d[0] = (uint32_t)v[u][0];
@@ -616,8 +653,7 @@ enum WarpMode { kWmQkv = 0, kWmGu = 1, kWmLm = 2 };
 
 Q3_DEV void put_pair(LLw* plane, int K, int b, int k, float v0, float v1, uint32_t f);
 
-template <int MODE>
-Q3_DEV bool warp_tiles(Ctl& c, int t0, int ntiles, int G, int K, uint32_t fout) {
+Q3_DEV bool warp_tiles(Ctl& c, int mode, int t0, int ntiles, int G, int K, uint32_t fout) {
     const PParams& P = *c.P;
     Shared& sh = *c.sh;
     const int KP = K >> 5, nsl = (KP + kKpPerChunk - 1) / kKpPerChunk;
@@ -679,13 +715,13 @@ Q3_DEV bool warp_tiles(Ctl& c, int t0, int ntiles, int G, int K, uint32_t fout) 
         const float v1 =
             (((a[0][2] + a[0][3]) + (a[1][2] + a[1][3])) + ((a[2][2] + a[2][3]) + (a[3][2] + a[3][3]))) - bias;
         const float r = t < P.B ? sh.rnorm[t] : 0.f;
-        if constexpr (MODE == kWmQkv) {
+        if (mode == kWmQkv) {
             if (t < P.B) {
                 LLw* dst = P.qkv + (size_t)t * P.qkv_rows + 16 * tile + g;
                 ll_put(dst, __float_as_uint(s_lo * r * v0), fout);
                 ll_put(dst + 8, __float_as_uint(s_hi * r * v1), fout);
             }
-        } else if constexpr (MODE == kWmGu) {
+        } else if (mode == kWmGu) {
             // rows g / g+8 are gate / up of unit 8*tile + g; lane + 4 holds unit g + 1
             const float gate = s_lo * r * v0, up = s_hi * r * v1;
             const float act = (gate / (1.0f + expf(-gate))) * up;
@@ -782,11 +818,20 @@ Q3_DEV bool attn_segment(Ctl& c, int l, int b, int g, int c0, int c1, int split,
             unsigned long long raw[E];
 #pragma unroll
             for (int e = 0; e < E; ++e) raw[e] = ll_get(qp + 32 * e);
+            uint64_t t0 = 0;
+            for (uint32_t i = 0;; ++i) {
+                bool stale = false;
 #pragma unroll
-            for (int e = 0; e < E; ++e) {
-                if (!ll_settle(c, qp + 32 * e, fqkv, raw[e])) return false;
-                v[e] = __uint_as_float((uint32_t)raw[e]);
+                for (int e = 0; e < E; ++e) stale |= (uint32_t)(raw[e] >> 32) != fqkv;
+                if (!stale) break;
+                t0 = poll_tick(c.P, &c.sh->abort, diag_of(c), i, t0, fqkv);
+                if (t0 == ~0ull) return false;
+#pragma unroll
+                for (int e = 0; e < E; ++e)
+                    if ((uint32_t)(raw[e] >> 32) != fqkv) raw[e] = ll_get(qp + 32 * e);
             }
+#pragma unroll
+            for (int e = 0; e < E; ++e) v[e] = __uint_as_float((uint32_t)raw[e]);
         }
         if (h <= GROUP) {
             const float* gain = h < GROUP ? qn : kn;
@@ -987,12 +1032,6 @@ Q3_DEV void consume(Ctl& c) {
     const int H = P.H, I = P.I, B = P.B, Dq = P.nh * HD;
     const uint32_t eb = *reinterpret_cast<volatile uint32_t*>(P.epoch) * 1024u;
     auto ep = [&](int l, int ph) { return eb + 8u * (uint32_t)l + (uint32_t)ph; };
-    // get this phase's input ready: staged copy (NT == 1) or 1/rms only
-    auto prepare = [&](const LLw* plane, int K, uint32_t flag, const LLw* ss, uint32_t sflag) -> bool {
-        if constexpr (NT == 1) return stage_plane(c, plane, K, flag, ss, sflag);
-        if (ss) return load_rnorm(c, ss, sflag);
-        return true;
-    };
     int rot = (H / 16) % G;  // rotation of the QKV / gate-up / lm_head tiles
 
     // embedding gather (phase 0): x = E[tok] * s, planes of g_attn(0) * x
@@ -1013,179 +1052,134 @@ Q3_DEV void consume(Ctl& c) {
     }
     AttnSched as;
     as.init(B, P.nkv, G, sh.nchunk);
+    if (c.tid < kMaxBatch) sh.best[c.tid] = 0ull;
 
-    for (int l = 0; l < P.L; ++l) {
-        const uint32_t f_in = l == 0 ? ep(0, kPhEmbed) : ep(l - 1, kPhDown);
-        c.layer = l;
-        // ---- QKV
-        c.phase = kPhQkv;
-        {
-            const int ntiles = P.qkv_rows / 16;
-            int t = first_tile(cta, rot, G);
-            if (t < ntiles && !prepare(P.pl_attn, H, f_in, P.ss_attn, f_in)) return;
-            dstamp(c, 1);
-            if constexpr (NT == 1) {
-                if (!warp_tiles<kWmQkv>(c, t, ntiles, G, H, ep(l, kPhQkv))) return;
-                t = ntiles;
+    // Every phase of every layer, then the lm_head, runs through the same
+    // loop body, so each piece of code exists once in the kernel: the
+    // per-layer code walk then stays small enough for the instruction cache.
+    const int nph = 5 * P.L + 1;
+#pragma unroll 1
+    for (int it = 0; it < nph; ++it) {
+        const int l = it < 5 * P.L ? it / 5 : P.L - 1;
+        const int ph = it < 5 * P.L ? kPhQkv + it % 5 : kPhLm;
+        c.layer = it < 5 * P.L ? l : P.L;
+        c.phase = ph;
+        if (ph == kPhAtt) {
+            for (int u = cta; u < as.U; u += G) {
+                int b, g, split;
+                as.locate(u, b, g, split);
+                const int c0 = split * as.Q, c1 = min(sh.nchunk[b], c0 + as.Q);
+                if (!attn_segment<HD, GROUP>(c, l, b, g, c0, c1, split, as.nsplit(b), ep(l, kPhQkv),
+                                             ep(l, kPhAtt)))
+                    return;
             }
-            for (; t < ntiles; t += G) {
-                if (!gemv_tile<NT>(c, H, P.pl_attn, f_in)) return;
-                dstamp(c, 2);
-                for (int i = c.tid; i < NT * 64; i += kCThreads) {
-                    const int n = i >> 6, ln = (i & 63) >> 1, half = i & 1, b = 4 * n + (ln & 3);
-                    if (b >= B) continue;
-                    const int rr = (ln >> 2) + 8 * half;
-                    const float v = sh.scl[rr] * sh.rnorm[b] * red_sum<NT>(c, n, ln, half);
-                    ll_put(P.qkv + (size_t)b * P.qkv_rows + 16 * t + rr, __float_as_uint(v), ep(l, kPhQkv));
-                }
-                if (!cbar_sync(c)) return;
-                dstamp(c, 3);
-            }
-            rot = (rot + ntiles) % G;
-            stamp(c, 2 + 6 * l + 0);
+            stamp(c, 2 + 6 * l + 1);
+            continue;
         }
-        // ---- attention
-        c.phase = kPhAtt;
-        for (int u = cta; u < as.U; u += G) {
-            int b, g, split;
-            as.locate(u, b, g, split);
-            const int c0 = split * as.Q, c1 = min(sh.nchunk[b], c0 + as.Q);
-            if (!attn_segment<HD, GROUP>(c, l, b, g, c0, c1, split, as.nsplit(b), ep(l, kPhQkv), ep(l, kPhAtt)))
-                return;
+        // this phase's input and shape
+        const bool rowtiles = ph == kPhO || ph == kPhDown;  // H-row tiles: split-K GEMV + residual
+        const int K = ph == kPhO ? Dq : ph == kPhDown ? I : H;
+        const int ntiles = rowtiles ? H / 16 : ph == kPhQkv ? P.qkv_rows / 16 : ph == kPhGu ? 2 * I / 16 : P.vpad / 16;
+        const LLw* in = ph == kPhO ? P.pl_o : ph == kPhGu ? P.pl_ffn : ph == kPhDown ? P.pl_a : P.pl_attn;
+        const uint32_t fin = (ph == kPhQkv || ph == kPhLm) ? (ph == kPhQkv && l == 0 ? ep(0, kPhEmbed)
+                                                              : ep(ph == kPhQkv ? l - 1 : l, kPhDown))
+                                                           : ep(l, ph - 1);
+        const LLw* ss = ph == kPhO || ph == kPhDown ? nullptr : ph == kPhGu ? P.ss_ffn : P.ss_attn;
+        const uint32_t fout = ph == kPhLm ? 0u : ep(l, ph);
+        int t = rowtiles ? cta : first_tile(cta, rot, G);
+        if (t < ntiles) {
+            bool ok;
+            if constexpr (NT == 1) ok = stage_plane(c, in, K, fin, ss, fin);
+            else ok = ss ? load_rnorm(c, ss, fin) : true;
+            if (!ok) return;
         }
-        stamp(c, 2 + 6 * l + 1);
-        // ---- O projection + residual
-        c.phase = kPhO;
-        {
-            const int ntiles = H / 16;
-            int t = cta;
-            if (t < ntiles && !prepare(P.pl_o, Dq, ep(l, kPhAtt), nullptr, 0)) return;
-            dstamp(c, 1);
+        dstamp(c, 1);
+        if (rowtiles) {
+            const float* gain = ph == kPhO ? P.gains[4 * l + 1] : (l + 1 < P.L ? P.gains[4 * (l + 1)] : P.final_norm);
+            LLw* plo = ph == kPhO ? P.pl_ffn : P.pl_attn;
+            LLw* sso = ph == kPhO ? P.ss_ffn : P.ss_attn;
             for (; t < ntiles; t += G) {
-                if (!gemv_tile<NT>(c, Dq, P.pl_o, ep(l, kPhAtt))) return;
-                dstamp(c, 2);
-                for (int i = c.tid; i < NT * 64; i += kCThreads) {
-                    const int n = i >> 6, ln = (i & 63) >> 1, half = i & 1, b = 4 * n + (ln & 3);
-                    if (b >= B) continue;
-                    const int rr = (ln >> 2) + 8 * half;
-                    const float v = sh.scl[rr] * red_sum<NT>(c, n, ln, half);
-                    resid_store(c, t, rr, b, v, true, P.gains[4 * l + 1]);
-                }
-                if (!finish_rows(c, t, P.pl_ffn, P.ss_ffn, ep(l, kPhO))) return;
-                if (!cbar_sync(c)) return;
-                dstamp(c, 3);
-            }
-            stamp(c, 2 + 6 * l + 2);
-        }
-        // ---- gate/up + SiLU
-        c.phase = kPhGu;
-        {
-            const int ntiles = 2 * I / 16;
-            int t = first_tile(cta, rot, G);
-            if (t < ntiles && !prepare(P.pl_ffn, H, ep(l, kPhO), P.ss_ffn, ep(l, kPhO))) return;
-            dstamp(c, 1);
-            if constexpr (NT == 1) {
-                if (!warp_tiles<kWmGu>(c, t, ntiles, G, H, ep(l, kPhGu))) return;
-                t = ntiles;
-            }
-            for (; t < ntiles; t += G) {
-                if (!gemv_tile<NT>(c, H, P.pl_ffn, ep(l, kPhO))) return;
-                dstamp(c, 2);
-                for (int i = c.tid; i < NT * 32; i += kCThreads) {
-                    const int n = i >> 5, ln = i & 31, gg = ln >> 2, b = 4 * n + (ln & 3);
-                    if (b >= B) continue;
-                    const float gate = sh.scl[gg] * sh.rnorm[b] * red_sum<NT>(c, n, ln, 0);
-                    const float up = sh.scl[gg + 8] * sh.rnorm[b] * red_sum<NT>(c, n, ln, 1);
-                    sh.gx[b][gg] = (gate / (1.0f + expf(-gate))) * up;
-                }
-                if (!cbar_sync(c)) return;
-                for (int i = c.tid; i < B * 4; i += kCThreads) {
-                    const int b = i >> 2, jj = i & 3;
-                    put_pair(P.pl_a, I, b, 8 * t + 2 * jj, sh.gx[b][2 * jj], sh.gx[b][2 * jj + 1], ep(l, kPhGu));
-                }
-                if (!cbar_sync(c)) return;
-                dstamp(c, 3);
-            }
-            rot = (rot + ntiles) % G;
-            stamp(c, 2 + 6 * l + 3);
-        }
-        // ---- down + residual
-        c.phase = kPhDown;
-        {
-            const int ntiles = H / 16;
-            const float* gnext = l + 1 < P.L ? P.gains[4 * (l + 1)] : P.final_norm;
-            int t = cta;
-            if (t < ntiles && !prepare(P.pl_a, I, ep(l, kPhGu), nullptr, 0)) return;
-            dstamp(c, 1);
-            for (; t < ntiles; t += G) {
-                if (!gemv_tile<NT>(c, I, P.pl_a, ep(l, kPhGu))) return;
+                if (!gemv_tile<NT>(c, K, in, fin)) return;
                 dstamp(c, 2);
                 for (int i = c.tid; i < NT * 64; i += kCThreads) {
                     const int n = i >> 6, ln = (i & 63) >> 1, half = i & 1, b = 4 * n + (ln & 3);
                     if (b >= B) continue;
                     const int rr = (ln >> 2) + 8 * half;
                     const float v = sh.scl[rr] * red_sum<NT>(c, n, ln, half);
-                    resid_store(c, t, rr, b, v, true, gnext);
+                    resid_store(c, t, rr, b, v, true, gain);
                 }
-                if (!finish_rows(c, t, P.pl_attn, P.ss_attn, ep(l, kPhDown))) return;
+                if (!finish_rows(c, t, plo, sso, fout)) return;
                 if (!cbar_sync(c)) return;
                 dstamp(c, 3);
             }
-            stamp(c, 2 + 6 * l + 4);
-        }
-    }
-    // ---- lm_head + argmax
-    c.layer = P.L;
-    c.phase = 6;
-    {
-        const int ntiles = P.vpad / 16;
-        const uint32_t f = ep(P.L - 1, kPhDown);
-        if (c.tid < kMaxBatch) sh.best[c.tid] = 0ull;
-        int t = first_tile(cta, rot, G);
-        if (t < ntiles && !prepare(P.pl_attn, H, f, P.ss_attn, f)) return;
-        if (!cbar_sync(c)) return;
-        if constexpr (NT == 1) {
-            if (!warp_tiles<kWmLm>(c, t, ntiles, G, H, 0u)) return;
         } else {
-            for (; t < ntiles; t += G) {
-                if (!gemv_tile<NT>(c, H, P.pl_attn, f)) return;
-                for (int i = c.tid; i < NT * 64; i += kCThreads) {
-                    const int n = i >> 6, ln = (i & 63) >> 1, half = i & 1, b = 4 * n + (ln & 3);
-                    if (b >= B) continue;
-                    const int rr = (ln >> 2) + 8 * half, row = 16 * t + rr;
-                    if (row >= P.vocab) continue;
-                    const float z = sh.scl[rr] * sh.rnorm[b] * red_sum<NT>(c, n, ln, half);
-                    if (P.logits) P.logits[(size_t)b * P.vocab + row] = z;
-                    atomicMax(&sh.best[b], argmax_key(z, (uint32_t)row));
+            const int mode = ph == kPhQkv ? kWmQkv : ph == kPhGu ? kWmGu : kWmLm;
+            if constexpr (NT == 1) {
+                if (!warp_tiles(c, mode, t, ntiles, G, H, fout)) return;
+            } else {
+                for (; t < ntiles; t += G) {
+                    if (!gemv_tile<NT>(c, H, in, fin)) return;
+                    dstamp(c, 2);
+                    if (mode == kWmGu) {
+                        for (int i = c.tid; i < NT * 32; i += kCThreads) {
+                            const int n = i >> 5, ln = i & 31, gg = ln >> 2, b = 4 * n + (ln & 3);
+                            if (b >= B) continue;
+                            const float gate = sh.scl[gg] * sh.rnorm[b] * red_sum<NT>(c, n, ln, 0);
+                            const float up = sh.scl[gg + 8] * sh.rnorm[b] * red_sum<NT>(c, n, ln, 1);
+                            sh.gx[b][gg] = (gate / (1.0f + expf(-gate))) * up;
+                        }
+                        if (!cbar_sync(c)) return;
+                        for (int i = c.tid; i < B * 4; i += kCThreads) {
+                            const int b = i >> 2, jj = i & 3;
+                            put_pair(P.pl_a, I, b, 8 * t + 2 * jj, sh.gx[b][2 * jj], sh.gx[b][2 * jj + 1], fout);
+                        }
+                    } else {
+                        for (int i = c.tid; i < NT * 64; i += kCThreads) {
+                            const int n = i >> 6, ln = (i & 63) >> 1, half = i & 1, b = 4 * n + (ln & 3);
+                            if (b >= B) continue;
+                            const int rr = (ln >> 2) + 8 * half, row = 16 * t + rr;
+                            const float v = sh.scl[rr] * sh.rnorm[b] * red_sum<NT>(c, n, ln, half);
+                            if (mode == kWmQkv) {
+                                ll_put(P.qkv + (size_t)b * P.qkv_rows + row, __float_as_uint(v), fout);
+                            } else if (row < P.vocab) {
+                                if (P.logits) P.logits[(size_t)b * P.vocab + row] = v;
+                                atomicMax(&sh.best[b], argmax_key(v, (uint32_t)row));
+                            }
+                        }
+                    }
+                    if (!cbar_sync(c)) return;
+                    dstamp(c, 3);
                 }
-                if (!cbar_sync(c)) return;
             }
+            rot = (rot + ntiles) % G;
         }
-        if (!cbar_sync(c)) return;
-        stamp(c, 2 + 6 * P.L);
-        if (c.tid < B) atomicMax(&P.keys[c.tid], sh.best[c.tid]);
+        if (ph != kPhLm) stamp(c, 2 + 6 * l + (ph - kPhQkv));
+    }
+    // ---- argmax over the grid; the last CTA to finish closes the step
+    if (!cbar_sync(c)) return;
+    stamp(c, 2 + 6 * P.L);
+    if (c.tid < B) atomicMax(&P.keys[c.tid], sh.best[c.tid]);
+    __threadfence();
+    if (!cbar_sync(c)) return;
+    if (c.tid == 0) sh.flag_last = (atomicAdd(P.exit_cnt, 1u) == (unsigned)(G - 1));
+    if (!cbar_sync(c)) return;
+    if (sh.flag_last) {
         __threadfence();
-        if (!cbar_sync(c)) return;
-        if (c.tid == 0) sh.flag_last = (atomicAdd(P.exit_cnt, 1u) == (unsigned)(G - 1));
-        if (!cbar_sync(c)) return;
-        if (sh.flag_last) {
-            __threadfence();
-            const int step = *reinterpret_cast<volatile int32_t*>(P.step);
-            if (c.tid < B) {
-                const int b = c.tid;
-                const unsigned long long k = atomicExch(&P.keys[b], 0ull);
-                const int tok = (int)argmax_key_index(k);
-                P.tokens[b] = tok;
-                if (step < P.out_cap) P.out_ids[(size_t)b * P.out_cap + step] = tok;
-                if (P.advance_pos) P.pos[b] += 1;
-            }
-            const int ncnt = P.L * P.bmax * P.nkv;
-            for (int i = c.tid; i < ncnt; i += kCThreads) P.attn_cnt[i] = 0u;
-            if (c.tid == 0) {
-                *P.step = step + 1;
-                *P.epoch = *P.epoch + 1u;
-                *P.exit_cnt = 0u;
-            }
+        const int step = *reinterpret_cast<volatile int32_t*>(P.step);
+        if (c.tid < B) {
+            const int b = c.tid;
+            const unsigned long long k = atomicExch(&P.keys[b], 0ull);
+            const int tok = (int)argmax_key_index(k);
+            P.tokens[b] = tok;
+            if (step < P.out_cap) P.out_ids[(size_t)b * P.out_cap + step] = tok;
+            if (P.advance_pos) P.pos[b] += 1;
+        }
+        const int ncnt = P.L * P.bmax * P.nkv;
+        for (int i = c.tid; i < ncnt; i += kCThreads) P.attn_cnt[i] = 0u;
+        if (c.tid == 0) {
+            *P.step = step + 1;
+            *P.epoch = *P.epoch + 1u;
+            *P.exit_cnt = 0u;
         }
     }
 }
