@@ -404,13 +404,23 @@ Q3_DEV bool rnorm_from(Ctl& c, const LLw* ss, uint32_t flag) {
             unsigned long long raw[4];
 #pragma unroll
             for (int u = 0; u < 4; ++u)
-                if (j0 + 32 * u < ntiles) raw[u] = ll_get(ss + (size_t)(j0 + 32 * u) * P.bmax + b);
+                raw[u] = j0 + 32 * u < ntiles ? ll_get(ss + (size_t)(j0 + 32 * u) * P.bmax + b)
+                                              : (unsigned long long)flag << 32;
+            uint64_t t0 = 0;
+            for (uint32_t i = 0;; ++i) {
+                bool stale = false;
+#pragma unroll
+                for (int u = 0; u < 4; ++u) stale |= (uint32_t)(raw[u] >> 32) != flag;
+                if (!stale) break;
+                t0 = poll_tick(c.P, &c.sh->abort, diag_of(c), i, t0, flag);
+                if (t0 == ~0ull) return false;
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                    if ((uint32_t)(raw[u] >> 32) != flag) raw[u] = ll_get(ss + (size_t)(j0 + 32 * u) * P.bmax + b);
+            }
 #pragma unroll
             for (int u = 0; u < 4; ++u)
-                if (j0 + 32 * u < ntiles) {
-                    if (!ll_settle(c, ss + (size_t)(j0 + 32 * u) * P.bmax + b, flag, raw[u])) return false;
-                    acc += __uint_as_float((uint32_t)raw[u]);
-                }
+                if (j0 + 32 * u < ntiles) acc += __uint_as_float((uint32_t)raw[u]);
         }
         acc = warp_sum(acc);
         if (c.lane == 0) c.sh->rnorm[b] = 1.0f / sqrtf(acc / (float)P.H + P.eps);
@@ -579,10 +589,35 @@ Q3_DEV bool gemv_tile(Ctl& c, int K, const LLw* plane, uint32_t flag) {
 #pragma unroll
                     for (int n = 0; n < NT; ++n) {
                         const int b = 4 * n + (g >> 1);
-                        if (p < kp_end && b < P.B) {
+                        const LLw* base = plane + (size_t)(2 * b + (g & 1)) * (K >> 1) + 16 * p + t;
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            raw[i][n][e] = (p < kp_end && b < P.B) ? ll_get(base + 4 * e) : (unsigned long long)flag << 32;
+                    }
+                }
+                // stale words are re-read together: one round trip per round
+                uint64_t t0 = 0;
+                for (uint32_t it = 0;; ++it) {
+                    bool stale = false;
+#pragma unroll
+                    for (int i = 0; i < KB; ++i)
+#pragma unroll
+                        for (int n = 0; n < NT; ++n)
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) stale |= (uint32_t)(raw[i][n][e] >> 32) != flag;
+                    if (!stale) break;
+                    t0 = poll_tick(c.P, &c.sh->abort, diag_of(c), it, t0, flag);
+                    if (t0 == ~0ull) return false;
+#pragma unroll
+                    for (int i = 0; i < KB; ++i) {
+                        const int p = kKpPerChunk * j + c.warp + kCWarps * (i0 + i);
+#pragma unroll
+                        for (int n = 0; n < NT; ++n) {
+                            const int b = 4 * n + (g >> 1);
                             const LLw* base = plane + (size_t)(2 * b + (g & 1)) * (K >> 1) + 16 * p + t;
 #pragma unroll
-                            for (int e = 0; e < 4; ++e) raw[i][n][e] = ll_get(base + 4 * e);
+                            for (int e = 0; e < 4; ++e)
+                                if ((uint32_t)(raw[i][n][e] >> 32) != flag) raw[i][n][e] = ll_get(base + 4 * e);
                         }
                     }
                 }
@@ -590,16 +625,6 @@ Q3_DEV bool gemv_tile(Ctl& c, int K, const LLw* plane, uint32_t flag) {
                 for (int i = 0; i < KB; ++i) {
                     const int p = kKpPerChunk * j + c.warp + kCWarps * (i0 + i);
                     if (p >= kp_end) continue;
-#pragma unroll
-                    for (int n = 0; n < NT; ++n) {
-                        const int b = 4 * n + (g >> 1);
-                        if (b < P.B) {
-                            const LLw* base = plane + (size_t)(2 * b + (g & 1)) * (K >> 1) + 16 * p + t;
-#pragma unroll
-                            for (int e = 0; e < 4; ++e)
-                                if (!ll_settle(c, base + 4 * e, flag, raw[i][n][e])) return false;
-                        }
-                    }
                     const uint4 wv =
                         *reinterpret_cast<const uint4*>(fb + (size_t)(p - kKpPerChunk * j) * 512 + c.lane * 16);
                     uint32_t A0[4], A1[4];
@@ -765,12 +790,16 @@ Q3_DEV void put_pair(LLw* plane, int K, int b, int k, float v0, float v1, uint32
 // three phases, so the residual rows stay in this CTA's shared memory
 // (slot ti = t / G) from the embedding to the last layer: x = x_prev + v;
 // stages gain * x and x^2 for finish_rows.
-Q3_DEV void resid_store(Ctl& c, int tile, int row_in_tile, int b, float v, bool add_prev, const float* gain) {
+Q3_DEV void resid_store_g(Ctl& c, int tile, int row_in_tile, int b, float v, bool add_prev, float gain) {
     float& xr = c.sh->xres[tile / gridDim.x][row_in_tile][b];
     const float xn = add_prev ? xr + v : v;
     xr = xn;
-    c.sh->gx[b][row_in_tile] = gain[16 * tile + row_in_tile] * xn;
+    c.sh->gx[b][row_in_tile] = gain * xn;
     c.sh->sq[b][row_in_tile] = xn * xn;
+}
+
+Q3_DEV void resid_store(Ctl& c, int tile, int row_in_tile, int b, float v, bool add_prev, const float* gain) {
+    resid_store_g(c, tile, row_in_tile, b, v, add_prev, gain[16 * tile + row_in_tile]);
 }
 
 // After resid_store: publish the planes of gain * x and the tile's sum of x^2.
@@ -813,6 +842,16 @@ Q3_DEV bool attn_segment(Ctl& c, int l, int b, int g, int c0, int c1, int split,
         else if (h == GROUP) src = (P.nh + g) * HD;
         else src = (P.nh + P.nkv + g) * HD;
         float v[E];
+        // gains and rotation of this head, fetched along with its words
+        float gn[E];
+        float2 rp[E / 2];
+        if (h <= GROUP) {
+            const float* gain = h < GROUP ? qn : kn;
+#pragma unroll
+            for (int e = 0; e < E; ++e) gn[e] = gain[c.lane + 32 * e];
+#pragma unroll
+            for (int e = 0; e < E / 2; ++e) rp[e] = cs[c.lane + 32 * e];
+        }
         {
             const LLw* qp = P.qkv + (size_t)b * P.qkv_rows + src + c.lane;
             unsigned long long raw[E];
@@ -834,17 +873,16 @@ Q3_DEV bool attn_segment(Ctl& c, int l, int b, int g, int c0, int c1, int split,
             for (int e = 0; e < E; ++e) v[e] = __uint_as_float((uint32_t)raw[e]);
         }
         if (h <= GROUP) {
-            const float* gain = h < GROUP ? qn : kn;
             float ss = 0.f;
 #pragma unroll
             for (int e = 0; e < E; ++e) ss += v[e] * v[e];
             ss = warp_sum(ss);
             const float inv = 1.0f / sqrtf(ss / (float)HD + P.eps);
 #pragma unroll
-            for (int e = 0; e < E; ++e) v[e] = __fmul_rn(__fmul_rn(v[e], inv), gain[c.lane + 32 * e]);
+            for (int e = 0; e < E; ++e) v[e] = __fmul_rn(__fmul_rn(v[e], inv), gn[e]);
 #pragma unroll
             for (int e = 0; e < E / 2; ++e) {
-                const float2 r = cs[c.lane + 32 * e];
+                const float2 r = rp[e];
                 const float a0 = v[e], b0 = v[e + E / 2];
                 v[e] = __fsub_rn(__fmul_rn(a0, r.x), __fmul_rn(b0, r.y));
                 v[e + E / 2] = __fadd_rn(__fmul_rn(b0, r.x), __fmul_rn(a0, r.y));
@@ -1098,15 +1136,26 @@ Q3_DEV void consume(Ctl& c) {
             const float* gain = ph == kPhO ? P.gains[4 * l + 1] : (l + 1 < P.L ? P.gains[4 * (l + 1)] : P.final_norm);
             LLw* plo = ph == kPhO ? P.pl_ffn : P.pl_attn;
             LLw* sso = ph == kPhO ? P.ss_ffn : P.ss_attn;
+            constexpr int kEpi = (NT * 64 + kCThreads - 1) / kCThreads;  // epilogue items per thread
             for (; t < ntiles; t += G) {
+                // this thread's gain values, fetched before the GEMV hides their latency
+                float gv[kEpi];
+#pragma unroll
+                for (int j = 0; j < kEpi; ++j) {
+                    const int i = c.tid + j * kCThreads;
+                    const int rr = (((i & 63) >> 1) >> 2) + 8 * (i & 1);
+                    gv[j] = i < NT * 64 ? gain[16 * t + rr] : 0.f;
+                }
                 if (!gemv_tile<NT>(c, K, in, fin)) return;
                 dstamp(c, 2);
-                for (int i = c.tid; i < NT * 64; i += kCThreads) {
+#pragma unroll
+                for (int j = 0; j < kEpi; ++j) {
+                    const int i = c.tid + j * kCThreads;
                     const int n = i >> 6, ln = (i & 63) >> 1, half = i & 1, b = 4 * n + (ln & 3);
-                    if (b >= B) continue;
+                    if (i >= NT * 64 || b >= B) continue;
                     const int rr = (ln >> 2) + 8 * half;
                     const float v = sh.scl[rr] * red_sum<NT>(c, n, ln, half);
-                    resid_store(c, t, rr, b, v, true, gain);
+                    resid_store_g(c, t, rr, b, v, true, gv[j]);
                 }
                 if (!finish_rows(c, t, plo, sso, fout)) return;
                 if (!cbar_sync(c)) return;
