@@ -147,7 +147,7 @@ static void pack_fragments(const int8_t* w, const float* scale, int rows, int K,
 
 // Upload one (possibly fused) matrix given as host row blocks.
 int upload_matrix(q3i8_ctx* c, const std::vector<const int8_t*>& row_src, const std::vector<float>& scales, int K,
-                  int pad_rows, DevMat* m) {
+                  int pad_rows, DevMat* m, bool keep_raw) {
     const int rows = (int)row_src.size();
     const int prow = ((rows + pad_rows - 1) / pad_rows) * pad_rows;
     std::vector<int8_t> raw((size_t)prow * K, 0);
@@ -159,13 +159,15 @@ int upload_matrix(q3i8_ctx* c, const std::vector<const int8_t*>& row_src, const 
     m->rows = prow;
     m->valid_rows = rows;
     m->cols = K;
-    CK(c, cudaMalloc(&m->raw, (size_t)prow * K));
+    if (keep_raw) {
+        CK(c, cudaMalloc(&m->raw, (size_t)prow * K));
+        CK(c, cudaMemcpy(m->raw, raw.data(), raw.size(), cudaMemcpyHostToDevice));
+    }
     CK(c, cudaMalloc(&m->frag, frag.size()));
     CK(c, cudaMalloc(&m->scale, (size_t)prow * sizeof(float)));
-    CK(c, cudaMemcpy(m->raw, raw.data(), raw.size(), cudaMemcpyHostToDevice));
     CK(c, cudaMemcpy(m->frag, frag.data(), frag.size(), cudaMemcpyHostToDevice));
     CK(c, cudaMemcpy(m->scale, sc.data(), sc.size() * sizeof(float), cudaMemcpyHostToDevice));
-    c->weight_bytes_dev += 2 * (size_t)prow * K + (size_t)prow * 4;
+    c->weight_bytes_dev += (keep_raw ? 2 : 1) * (size_t)prow * K + (size_t)prow * 4;
     return Q3_OK;
 }
 
@@ -233,21 +235,19 @@ static int ensure_prefill(q3i8_ctx* c, int M) {
     if (M <= c->pf_rows) return Q3_OK;
     const q3i8_dims& d = c->d;
     const int H = d.hidden, I = d.intermediate, Dq = d.n_heads * d.head_dim, Dkv = d.n_kv_heads * d.head_dim;
-    for (float** p : {&c->pf_x, &c->pf_xn, &c->pf_qkv, &c->pf_q, &c->pf_o, &c->pf_y, &c->pf_gu, &c->pf_a, &c->pf_part})
-        cudaFree(*p), *p = nullptr;
+    for (float** p : {&c->pf_x, &c->pf_qkv, &c->pf_q, &c->pf_part}) cudaFree(*p), *p = nullptr;
+    for (__half** p : {&c->pf_xh, &c->pf_oh, &c->pf_ah}) cudaFree(*p), *p = nullptr;
     cudaFree(c->pf_ids);
     cudaFree(c->pf_seq);
     cudaFree(c->pf_pos);
     c->pf_rows = 0;
     const size_t m = (size_t)M;
     CK(c, cudaMalloc(&c->pf_x, m * H * 4));
-    CK(c, cudaMalloc(&c->pf_xn, m * std::max(H, I) * 4));
     CK(c, cudaMalloc(&c->pf_qkv, m * (Dq + 2 * Dkv) * 4));
     CK(c, cudaMalloc(&c->pf_q, m * Dq * 4));
-    CK(c, cudaMalloc(&c->pf_o, m * Dq * 4));
-    CK(c, cudaMalloc(&c->pf_y, m * H * 4));
-    CK(c, cudaMalloc(&c->pf_gu, m * 2 * I * 4));
-    CK(c, cudaMalloc(&c->pf_a, m * I * 4));
+    CK(c, cudaMalloc(&c->pf_xh, 2 * m * H * 2));
+    CK(c, cudaMalloc(&c->pf_oh, 2 * m * Dq * 2));
+    CK(c, cudaMalloc(&c->pf_ah, 2 * m * I * 2));
     CK(c, cudaMalloc(&c->pf_part, attn_part_bytes(M, d.n_heads, d.head_dim, 1)));
     CK(c, cudaMalloc(&c->pf_ids, m * 4));
     CK(c, cudaMalloc(&c->pf_seq, m * 4));
@@ -329,7 +329,7 @@ int init_weights(q3i8_ctx* c, const q3i8_mat* embed, const q3i8_layer* layers, c
         std::vector<const int8_t*> rows(d.vocab);
         for (int r = 0; r < d.vocab; ++r) rows[r] = embed->w + (size_t)r * H;
         std::vector<float> sc(embed->scale, embed->scale + d.vocab);
-        int rc = upload_matrix(c, rows, sc, H, 16, &c->embed);
+        int rc = upload_matrix(c, rows, sc, H, 16, &c->embed, true);
         if (rc) return rc;
     }
     int rc = upload_vec(c, final_norm, H, &c->final_norm);
@@ -344,20 +344,20 @@ int init_weights(q3i8_ctx* c, const q3i8_mat* embed, const q3i8_layer* layers, c
         for (int r = 0; r < Dq; ++r) rows.push_back(L.q.w + (size_t)r * H), sc.push_back(L.q.scale[r]);
         for (int r = 0; r < Dkv; ++r) rows.push_back(L.k.w + (size_t)r * H), sc.push_back(L.k.scale[r]);
         for (int r = 0; r < Dkv; ++r) rows.push_back(L.v.w + (size_t)r * H), sc.push_back(L.v.scale[r]);
-        if ((rc = upload_matrix(c, rows, sc, H, 16, &D.qkv))) return rc;
+        if ((rc = upload_matrix(c, rows, sc, H, 16, &D.qkv, false))) return rc;
         rows.clear(), sc.clear();
         for (int r = 0; r < H; ++r) rows.push_back(L.o.w + (size_t)r * Dq), sc.push_back(L.o.scale[r]);
-        if ((rc = upload_matrix(c, rows, sc, Dq, 16, &D.o))) return rc;
+        if ((rc = upload_matrix(c, rows, sc, Dq, 16, &D.o, false))) return rc;
         rows.clear(), sc.clear();
         // fused gate/up: blocks of 16 rows = 8 gate units then the same 8 up units
         for (int j = 0; j < I / 8; ++j) {
             for (int r = 0; r < 8; ++r) rows.push_back(L.gate.w + (size_t)(8 * j + r) * H), sc.push_back(L.gate.scale[8 * j + r]);
             for (int r = 0; r < 8; ++r) rows.push_back(L.up.w + (size_t)(8 * j + r) * H), sc.push_back(L.up.scale[8 * j + r]);
         }
-        if ((rc = upload_matrix(c, rows, sc, H, 16, &D.gu))) return rc;
+        if ((rc = upload_matrix(c, rows, sc, H, 16, &D.gu, false))) return rc;
         rows.clear(), sc.clear();
         for (int r = 0; r < H; ++r) rows.push_back(L.down.w + (size_t)r * I), sc.push_back(L.down.scale[r]);
-        if ((rc = upload_matrix(c, rows, sc, I, 16, &D.down))) return rc;
+        if ((rc = upload_matrix(c, rows, sc, I, 16, &D.down, false))) return rc;
         if ((rc = upload_vec(c, L.attn_norm, H, &D.attn_norm))) return rc;
         if ((rc = upload_vec(c, L.ffn_norm, H, &D.ffn_norm))) return rc;
         if ((rc = upload_vec(c, L.q_norm, hd, &D.q_norm))) return rc;
@@ -411,7 +411,7 @@ extern "C" void q3i8_destroy(q3i8_ctx* c) {
     }
     void* ptrs[] = {c->final_norm, c->kc, c->vc, c->rope, c->tokens, c->pos, c->seq_ids, c->step, c->keys,
                     c->counter, c->status, c->x, c->qkv, c->qr, c->part, c->xh, c->oh, c->ah, c->logits,
-                    c->out_ids, c->pf_x, c->pf_xn, c->pf_qkv, c->pf_q, c->pf_o, c->pf_y, c->pf_gu, c->pf_a,
+                    c->out_ids, c->pf_x, c->pf_qkv, c->pf_q, c->pf_xh, c->pf_oh, c->pf_ah,
                     c->pf_part, c->pf_ids, c->pf_seq, c->pf_pos, c->pf_last, c->d_mats, c->d_gains,
                     c->p_epoch, c->p_keys, c->p_exit, c->p_attn_cnt, c->p_abort, c->p_diag, c->p_ll, c->p_part, c->p_trace};
     for (void* p : ptrs) cudaFree(p);
@@ -597,7 +597,13 @@ static int enqueue_decode_step(q3i8_ctx* c, int B, bool want_logits) {
 }
 
 int step_launches(const q3i8_ctx* c) { return c->use_persistent ? 1 : 2 + c->d.n_layers * 9 + 1; }
-int prefill_launches(const q3i8_ctx* c) { return 1 + c->d.n_layers * 12 + 2; }
+// Kernels of one prefill over M prompt rows: embed; per layer 2 RMSNorms, the
+// QK-norm/RoPE/append, attention split + merge and 4 projections per chunk
+// of kPrefillChunk rows; final RMSNorm and lm_head.
+int prefill_launches(const q3i8_ctx* c, int M) {
+    const int chunks = (M + kPrefillChunk - 1) / kPrefillChunk;
+    return 1 + c->d.n_layers * (5 + 4 * chunks) + 2;
+}
 
 // Graph of one decode step at batch B (captured on first use).
 static int get_graph(q3i8_ctx* c, int B, cudaGraphExec_t* out) {
@@ -652,28 +658,38 @@ static int run_prefill(q3i8_ctx* c, int B, const int32_t* d_ids, const int32_t* 
     CK(c, cudaMemsetAsync(c->status, 0, 4, st));
     const size_t layer_kv = (size_t)c->bmax * nkv * c->cap * hd;
 
+    // One projection over all prompt rows: the decode GEMV (tensor-core MMA,
+    // one weight sweep per chunk of up to kPrefillChunk rows).
+    auto project = [&](const DevMat& W, int K, const __half* xh, int mode, float* y, int ldy, __half* yh, int ldyh) {
+        for (int m0 = 0; m0 < M; m0 += kPrefillChunk) {
+            GemvArgs a{};
+            a.B = std::min(kPrefillChunk, M - m0);
+            a.w = W.frag, a.scale = W.scale, a.rows = W.rows, a.K = K;
+            a.xh = xh + (size_t)2 * m0 * K;
+            if (y) a.y = y + (size_t)m0 * ldy, a.ldy = ldy;
+            if (yh) a.yh = yh + (size_t)2 * m0 * ldyh, a.ldyh = ldyh;
+            launch_gemv(a, mode, gemv_grid(a.rows, mode, c->num_sms), st);
+        }
+    };
     launch_embed(d_ids, M, c->embed.raw, c->embed.scale, H, c->pf_x, st);
     for (int l = 0; l < d.n_layers; ++l) {
         const DevLayer& L = c->layers[l];
-        launch_rmsnorm(c->pf_x, nullptr, M, H, L.attn_norm, d.rms_eps, c->pf_xn, nullptr, st);
-        launch_gemm_f32(c->pf_xn, M, H, L.qkv.raw, L.qkv.scale, L.qkv.rows, c->pf_qkv, L.qkv.rows, st);
+        launch_rmsnorm(c->pf_x, nullptr, M, H, L.attn_norm, d.rms_eps, nullptr, c->pf_xh, st);
+        project(L.qkv, H, c->pf_xh, kStore, c->pf_qkv, L.qkv.rows, nullptr, 0);
         launch_qk_rope_append(c->pf_qkv, M, nh, nkv, hd, c->pf_seq, c->pf_pos, L.q_norm, L.k_norm, d.rms_eps,
                               c->rope, c->pf_q, c->kc + l * layer_kv, c->vc + l * layer_kv, c->cap, st);
         launch_attention(c->pf_q, c->kc + l * layer_kv, c->vc + l * layer_kv, c->pf_seq, c->pf_pos, 1, M, nh, nkv,
-                         hd, c->cap, 1, c->pf_part, c->pf_o, nullptr, 0, c->status, st);
-        launch_gemm_f32(c->pf_o, M, Dq, L.o.raw, L.o.scale, H, c->pf_y, H, st);
-        launch_add(c->pf_x, c->pf_y, (size_t)M * H, st);
-        launch_rmsnorm(c->pf_x, nullptr, M, H, L.ffn_norm, d.rms_eps, c->pf_xn, nullptr, st);
-        launch_gemm_f32(c->pf_xn, M, H, L.gu.raw, L.gu.scale, 2 * I, c->pf_gu, 2 * I, st);
-        launch_silu_gate(c->pf_gu, M, I, c->pf_a, st);
-        launch_gemm_f32(c->pf_a, M, I, L.down.raw, L.down.scale, H, c->pf_y, H, st);
-        launch_add(c->pf_x, c->pf_y, (size_t)M * H, st);
+                         hd, c->cap, 1, c->pf_part, nullptr, c->pf_oh, Dq, c->status, st);
+        project(L.o, Dq, c->pf_oh, kResid, c->pf_x, H, nullptr, 0);
+        launch_rmsnorm(c->pf_x, nullptr, M, H, L.ffn_norm, d.rms_eps, nullptr, c->pf_xh, st);
+        project(L.gu, H, c->pf_xh, kSiluGate, nullptr, 0, c->pf_ah, I);
+        project(L.down, I, c->pf_ah, kResid, c->pf_x, H, nullptr, 0);
         (void)Dkv;
     }
     launch_rmsnorm(c->pf_x, c->pf_last, B, H, c->final_norm, d.rms_eps, nullptr, c->xh, st);
     enqueue_lm_head(c, B, false, d_logits);
     CK(c, cudaGetLastError());
-    c->launches += prefill_launches(c);
+    c->launches += prefill_launches(c, M);
     c->active_B = B;
     c->seq_len.assign(lens, lens + B);
     (void)maxlen;

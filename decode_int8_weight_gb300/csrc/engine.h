@@ -16,7 +16,7 @@ constexpr int kCtxCeiling = 65536; // "Model-agnostic LLM inference", section "L
 constexpr int kChunkPos = 64;      // KV positions per attention stage; the cache capacity is a multiple
 
 struct DevMat {
-    int8_t* raw = nullptr;     // [rows][cols] row-major int8 (prefill GEMM)
+    int8_t* raw = nullptr;     // [rows][cols] row-major int8 (embedding table only: the gather)
     uint8_t* frag = nullptr;   // fragment-order bytes (decode GEMV)
     float* scale = nullptr;    // [rows]
     int rows = 0, valid_rows = 0, cols = 0;
@@ -59,8 +59,8 @@ struct q3i8_ctx {
 
     // prefill buffers (grow-only)
     int pf_rows = 0;
-    float *pf_x = nullptr, *pf_xn = nullptr, *pf_qkv = nullptr, *pf_q = nullptr, *pf_o = nullptr, *pf_y = nullptr,
-          *pf_gu = nullptr, *pf_a = nullptr, *pf_part = nullptr;
+    float *pf_x = nullptr, *pf_qkv = nullptr, *pf_q = nullptr, *pf_part = nullptr;
+    __half *pf_xh = nullptr, *pf_oh = nullptr, *pf_ah = nullptr;  // [2M][K] hi/lo planes of the prompt rows
     int32_t *pf_ids = nullptr, *pf_seq = nullptr, *pf_pos = nullptr, *pf_last = nullptr;
 
     // persistent decode step (one cooperative kernel per step)
@@ -87,7 +87,7 @@ struct q3i8_ctx {
 };
 
 int upload_matrix(q3i8_ctx* c, const std::vector<const int8_t*>& row_src, const std::vector<float>& scales, int K,
-                  int pad_rows, q3::DevMat* m);
+                  int pad_rows, q3::DevMat* m, bool keep_raw);
 int init_weights(q3i8_ctx* c, const q3i8_mat* embed, const q3i8_layer* layers, const float* final_norm);
 int init_state(q3i8_ctx* c);
 int ensure_capacity(q3i8_ctx* c, int need_ctx);
@@ -99,4 +99,5 @@ int step_launches(const q3i8_ctx* c);
 int persistent_setup(q3i8_ctx* c);
 int persistent_reset(q3i8_ctx* c);
 cudaError_t enqueue_persistent(q3i8_ctx* c, int B, float* logits, unsigned long long* trace = nullptr);
-int prefill_launches(const q3i8_ctx* c);
+constexpr int kPrefillChunk = 32;  // prompt rows per weight sweep of a prefill projection
+int prefill_launches(const q3i8_ctx* c, int M);

@@ -554,91 +554,5 @@ int launch_attention(const float* q, const __nv_bfloat16* k, const __nv_bfloat16
     return -1;  // unsupported head_dim / group
 }
 
-// =====================================================================
-// Plain prefill pieces (CUDA cores, fp32): Y = (X . W^T) * s over int8 W.
-// =====================================================================
-__global__ void __launch_bounds__(256) gemm_f32_kernel(const float* X, int M, int K, const int8_t* W, const float* s,
-                                                       int N, float* Y, int ldy) {
-    __shared__ float Xs[32][64 + 4];
-    __shared__ float Ws[32][64 + 4];
-    const int m0 = blockIdx.y * 64, n0 = blockIdx.x * 64;
-    const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
-    float acc[4][4] = {};
-    for (int k0 = 0; k0 < K; k0 += 32) {
-        for (int i = threadIdx.x; i < 64 * 32; i += 256) {
-            const int mm = i >> 5, kk = i & 31;
-            Xs[kk][mm] = (m0 + mm < M) ? X[(size_t)(m0 + mm) * K + k0 + kk] : 0.f;
-            Ws[kk][mm] = (n0 + mm < N) ? (float)W[(size_t)(n0 + mm) * K + k0 + kk] : 0.f;
-        }
-        __syncthreads();
-#pragma unroll 8
-        for (int kk = 0; kk < 32; ++kk) {
-            float av[4], bv[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                av[i] = Xs[kk][ty * 4 + i];
-                bv[i] = Ws[kk][tx * 4 + i];
-            }
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-#pragma unroll
-                for (int j = 0; j < 4; ++j) acc[i][j] += av[i] * bv[j];
-        }
-        __syncthreads();
-    }
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const int m = m0 + ty * 4 + i;
-        if (m >= M) continue;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int n = n0 + tx * 4 + j;
-            if (n < N) Y[(size_t)m * ldy + n] = s[n] * acc[i][j];
-        }
-    }
-}
-
-void launch_gemm_f32(const float* X, int M, int K, const int8_t* W, const float* s, int N, float* Y, int ldy,
-                     cudaStream_t st) {
-    if (M <= 0) return;
-    dim3 grid((N + 63) / 64, (M + 63) / 64);
-    gemm_f32_kernel<<<grid, 256, 0, st>>>(X, M, K, W, s, N, Y, ldy);
-}
-
-__global__ void add_kernel(float* x, const float* y, size_t n) {
-    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x)
-        x[i] = x[i] + y[i];
-}
-
-void launch_add(float* x, const float* y, size_t n, cudaStream_t st) {
-    if (n) add_kernel<<<(unsigned)((n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096), 256, 0, st>>>(x, y, n);
-}
-
-// gu rows come from the fused gate/up matrix: in each block of 16 outputs the
-// first 8 are gate units 8j..8j+7 and the next 8 the matching up units.
-__global__ void silu_gate_kernel(const float* gu, int M, int I, float* a) {
-    const size_t n = (size_t)M * I;
-    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
-        const size_t m = i / I;
-        const int u = (int)(i % I);
-        const size_t base = m * (size_t)(2 * I) + (size_t)(u >> 3) * 16 + (u & 7);
-        const float gate = gu[base], up = gu[base + 8];
-        a[i] = (gate / (1.0f + expf(-gate))) * up;
-    }
-}
-
-void launch_silu_gate(const float* gu, int M, int I, float* a, cudaStream_t st) {
-    const size_t n = (size_t)M * I;
-    if (n) silu_gate_kernel<<<(unsigned)((n + 255) / 256 < 8192 ? (n + 255) / 256 : 8192), 256, 0, st>>>(gu, M, I, a);
-}
-
-__global__ void gather_rows_kernel(const float* src, const int32_t* rows, int H, float* dst) {
-    const int i = blockIdx.x;
-    for (int k = threadIdx.x; k < H; k += blockDim.x) dst[(size_t)i * H + k] = src[(size_t)rows[i] * H + k];
-}
-
-void launch_gather_rows(const float* src, const int32_t* rows, int n, int H, float* dst, cudaStream_t st) {
-    if (n > 0) gather_rows_kernel<<<n, 256, 0, st>>>(src, rows, H, dst);
-}
 
 }  // namespace q3

@@ -65,10 +65,4 @@ int launch_attention(const float* q, const __nv_bfloat16* k, const __nv_bfloat16
                      const int32_t* row_len, int len_add, int R, int nh, int nkv, int hd, int cap, int splits,
                      float* part, float* out, __half* outh, int ldh, int32_t* status, cudaStream_t st);
 
-void launch_gemm_f32(const float* X, int M, int K, const int8_t* W, const float* s, int N, float* Y, int ldy,
-                     cudaStream_t st);
-void launch_add(float* x, const float* y, size_t n, cudaStream_t st);
-void launch_silu_gate(const float* gu, int M, int I, float* a, cudaStream_t st);
-void launch_gather_rows(const float* src, const int32_t* rows, int n, int H, float* dst, cudaStream_t st);
-
 }  // namespace q3
