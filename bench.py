@@ -17,6 +17,7 @@ the host cores on a bounded sample of the same workload (rank 0 only).
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import os
 import statistics
@@ -31,6 +32,21 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 import synth  # noqa: E402
+
+# DRAM bytes (read + write) of one decode-step launch, from an ncu capture of
+# the persistent step kernel (profiles/persistent_step_0.6b-b1-p32-n128.md).
+# A figure holds only for the kernel sources it was taken on, identified by
+# kernel_source_id(); for any other build the roofline reports null.
+NCU_TRAFFIC = {("b7fc21b5eb8c160f", "0.6b-b1-p32-n128", 1): 611_159_040}
+
+
+def kernel_source_id() -> str:
+    h = hashlib.sha256()
+    for f in ("persistent.cu", "persistent.h", "common.cuh"):
+        with open(os.path.join(ROOT, "decode_int8_weight_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
 
 METRIC = "decode tok/s at B=1/8/32 (Qwen3-0.6B shape) and achieved HBM GB/s per step"
 DEFAULT_WORKLOAD = "0.6b-b1-p32-n128"
@@ -309,7 +325,8 @@ def run_gpu(args, w):
             "step_us": step_us, "prefill_tok_s": pf_tok_s,
             "step_bytes": {"weights": weight_bytes, "kv_mean": step_bytes - weight_bytes, "total_mean": step_bytes},
             "roofline": {"kernel": "decode step (CUDA graph replay)", "bound": "hbm", "achieved": achieved,
-                         "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak, "traffic": None,
+                         "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
+                         "traffic": NCU_TRAFFIC.get((kernel_source_id(), w.name, B)), "traffic_unit": "bytes/launch",
                          "peak_kind": peak_kind},
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_val, "unit": "tok/s", "h2d_bytes_per_step": int(flat.nbytes + 8 * flat.size + 12 * B),
