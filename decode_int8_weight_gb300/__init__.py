@@ -11,6 +11,7 @@ The call surface mirrors the C ABI in ``include/q3i8.h``:
 * ``Decoder.decode_device(ids, lens, n, out)``    -> ``q3i8_decode_device``
 * ``Decoder.prefill`` / ``Decoder.step_logits``   -> teacher-forced checking
 * ``validate_dims``                               -> ``q3i8_validate_dims``
+* ``op_gemm_i8``                                  -> ``q3i8_op_gemm_i8``
 * ``op_attention``                                -> ``q3i8_op_attention``
 * ``op_attention_static``                         -> ``q3i8_op_attention_static``
 
@@ -36,7 +37,7 @@ STATUS = {0: "ok", 1: "unsupported_architecture", 2: "invalid_arguments", 3: "co
 
 EXPORTS = ["q3i8_validate_dims", "q3i8_init", "q3i8_decode", "q3i8_decode_device", "q3i8_prefill",
            "q3i8_step_logits", "q3i8_read_kv", "q3i8_step_bytes", "q3i8_step_launches", "q3i8_launch_count", "q3i8_last_error",
-           "q3i8_status_name", "q3i8_destroy", "q3i8_trace_step", "q3i8_op_attention_workspace", "q3i8_op_attention",
+           "q3i8_status_name", "q3i8_destroy", "q3i8_trace_step", "q3i8_op_gemm_i8", "q3i8_op_attention_workspace", "q3i8_op_attention",
            "q3i8_op_attention_static"]
 
 
@@ -106,6 +107,7 @@ def lib():
             L.q3i8_status_name.argtypes = [ctypes.c_int]
             L.q3i8_destroy.argtypes = [vp]
             L.q3i8_trace_step.argtypes = [vp, vp, vp, sz, ctypes.POINTER(i32), ctypes.POINTER(i32)]
+            L.q3i8_op_gemm_i8.argtypes = [vp, vp, vp, i32, i32, i32, vp, vp, vp]
             L.q3i8_op_attention_workspace.restype = sz
             L.q3i8_op_attention_workspace.argtypes = [i32, i32, i32, i32]
             L.q3i8_op_attention.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, vp, vp, sz, vp, vp]
@@ -254,6 +256,17 @@ class Decoder:
 
     def launch_count(self) -> int:
         return int(lib().q3i8_launch_count(self._h))
+
+
+def op_gemm_i8(a_planes, w, scale, y, status=None, stream=None):
+    """Tensor-core projection on torch CUDA tensors (see q3i8_op_gemm_i8): a_planes [M, 2K] (f16 bits as int16 or
+    float16), w [N, K] int8, scale [N] fp32, y [M, N] fp32."""
+    M, K2 = a_planes.shape
+    N, K = w.shape
+    assert K2 == 2 * K
+    rc = lib().q3i8_op_gemm_i8(_tptr(a_planes), _tptr(w), _tptr(scale), M, N, K, _tptr(y), _tptr(status),
+                               ctypes.c_void_p(stream) if stream else None)
+    _check(rc, None)
 
 
 def op_attention_workspace(R: int, n_heads: int, hd: int, splits: int) -> int:

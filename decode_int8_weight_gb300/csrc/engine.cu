@@ -344,20 +344,20 @@ int init_weights(q3i8_ctx* c, const q3i8_mat* embed, const q3i8_layer* layers, c
         for (int r = 0; r < Dq; ++r) rows.push_back(L.q.w + (size_t)r * H), sc.push_back(L.q.scale[r]);
         for (int r = 0; r < Dkv; ++r) rows.push_back(L.k.w + (size_t)r * H), sc.push_back(L.k.scale[r]);
         for (int r = 0; r < Dkv; ++r) rows.push_back(L.v.w + (size_t)r * H), sc.push_back(L.v.scale[r]);
-        if ((rc = upload_matrix(c, rows, sc, H, 16, &D.qkv, false))) return rc;
+        if ((rc = upload_matrix(c, rows, sc, H, 16, &D.qkv, true))) return rc;
         rows.clear(), sc.clear();
         for (int r = 0; r < H; ++r) rows.push_back(L.o.w + (size_t)r * Dq), sc.push_back(L.o.scale[r]);
-        if ((rc = upload_matrix(c, rows, sc, Dq, 16, &D.o, false))) return rc;
+        if ((rc = upload_matrix(c, rows, sc, Dq, 16, &D.o, true))) return rc;
         rows.clear(), sc.clear();
         // fused gate/up: blocks of 16 rows = 8 gate units then the same 8 up units
         for (int j = 0; j < I / 8; ++j) {
             for (int r = 0; r < 8; ++r) rows.push_back(L.gate.w + (size_t)(8 * j + r) * H), sc.push_back(L.gate.scale[8 * j + r]);
             for (int r = 0; r < 8; ++r) rows.push_back(L.up.w + (size_t)(8 * j + r) * H), sc.push_back(L.up.scale[8 * j + r]);
         }
-        if ((rc = upload_matrix(c, rows, sc, H, 16, &D.gu, false))) return rc;
+        if ((rc = upload_matrix(c, rows, sc, H, 16, &D.gu, true))) return rc;
         rows.clear(), sc.clear();
         for (int r = 0; r < H; ++r) rows.push_back(L.down.w + (size_t)r * I), sc.push_back(L.down.scale[r]);
-        if ((rc = upload_matrix(c, rows, sc, I, 16, &D.down, false))) return rc;
+        if ((rc = upload_matrix(c, rows, sc, I, 16, &D.down, true))) return rc;
         if ((rc = upload_vec(c, L.attn_norm, H, &D.attn_norm))) return rc;
         if ((rc = upload_vec(c, L.ffn_norm, H, &D.ffn_norm))) return rc;
         if ((rc = upload_vec(c, L.q_norm, hd, &D.q_norm))) return rc;
@@ -598,11 +598,16 @@ static int enqueue_decode_step(q3i8_ctx* c, int B, bool want_logits) {
 
 int step_launches(const q3i8_ctx* c) { return c->use_persistent ? 1 : 2 + c->d.n_layers * 9 + 1; }
 // Kernels of one prefill over M prompt rows: embed; per layer 2 RMSNorms, the
-// QK-norm/RoPE/append, attention split + merge and 4 projections per chunk
-// of kPrefillChunk rows; final RMSNorm and lm_head.
+// QK-norm/RoPE/append, attention split + merge and the 4 projections (one
+// tensor-core GEMM each, or one GEMV per chunk of kPrefillChunk rows); final
+// RMSNorm and lm_head.
 int prefill_launches(const q3i8_ctx* c, int M) {
+    const q3i8_dims& d = c->d;
     const int chunks = (M + kPrefillChunk - 1) / kPrefillChunk;
-    return 1 + c->d.n_layers * (5 + 4 * chunks) + 2;
+    auto per = [&](int N, int K) { return M > kPrefillChunk && tc_gemm_supported(N, K) ? 1 : chunks; };
+    const int H = d.hidden, I = d.intermediate, Dq = d.n_heads * d.head_dim, Dkv = d.n_kv_heads * d.head_dim;
+    const int proj = per(Dq + 2 * Dkv, H) + per(H, Dq) + per(2 * I, H) + per(H, I);
+    return 1 + d.n_layers * (5 + proj) + 2;
 }
 
 // Graph of one decode step at batch B (captured on first use).
@@ -658,9 +663,16 @@ static int run_prefill(q3i8_ctx* c, int B, const int32_t* d_ids, const int32_t* 
     CK(c, cudaMemsetAsync(c->status, 0, 4, st));
     const size_t layer_kv = (size_t)c->bmax * nkv * c->cap * hd;
 
-    // One projection over all prompt rows: the decode GEMV (tensor-core MMA,
-    // one weight sweep per chunk of up to kPrefillChunk rows).
+    // One projection over all prompt rows: the tcgen05 GEMM when there is
+    // more than one chunk of rows, else the decode GEMV (one weight sweep per
+    // chunk of up to kPrefillChunk rows).
+    int tc_rc = 0;
     auto project = [&](const DevMat& W, int K, const __half* xh, int mode, float* y, int ldy, __half* yh, int ldyh) {
+        if (M > kPrefillChunk && W.raw && tc_gemm_supported(W.rows, K)) {
+            const int rc = launch_tc_gemm(xh, W.raw, W.scale, M, W.rows, K, mode, y, ldy, yh, ldyh, c->status, st);
+            if (rc == 0) return;
+            tc_rc = rc;
+        }
         for (int m0 = 0; m0 < M; m0 += kPrefillChunk) {
             GemvArgs a{};
             a.B = std::min(kPrefillChunk, M - m0);
@@ -686,6 +698,7 @@ static int run_prefill(q3i8_ctx* c, int B, const int32_t* d_ids, const int32_t* 
         project(L.down, I, c->pf_ah, kResid, c->pf_x, H, nullptr, 0);
         (void)Dkv;
     }
+    if (tc_rc) return fail(c, Q3_ERR_CUDA, "prefill: tensor-core GEMM could not be set up (%d)", tc_rc);
     launch_rmsnorm(c->pf_x, c->pf_last, B, H, c->final_norm, d.rms_eps, nullptr, c->xh, st);
     enqueue_lm_head(c, B, false, d_logits);
     CK(c, cudaGetLastError());
@@ -964,6 +977,21 @@ extern "C" const char* q3i8_status_name(int s) {
 }
 
 // ------------------------------------------------------------------ ops
+
+extern "C" int q3i8_op_gemm_i8(const uint16_t* a_planes, const int8_t* w, const float* scale, int32_t M, int32_t N,
+                               int32_t K, float* y, int32_t* d_status, void* cuda_stream) {
+    if (!a_planes || !w || !scale || !y) return fail(nullptr, Q3_ERR_INVALID_ARGUMENTS, "op_gemm_i8: NULL pointer");
+    if (M < 1 || !tc_gemm_supported(N, K))
+        return fail(nullptr, Q3_ERR_INVALID_ARGUMENTS, "op_gemm_i8: needs M >= 1, N %% 128 == 0, K %% 64 == 0");
+    if (((uintptr_t)a_planes & 15) || ((uintptr_t)w & 15) || ((uintptr_t)y & 15))
+        return fail(nullptr, Q3_ERR_INVALID_ARGUMENTS, "op_gemm_i8: buffers must be 16-byte aligned");
+    const int rc = launch_tc_gemm(reinterpret_cast<const __half*>(a_planes), w, scale, M, N, K, kStore, y, N, nullptr,
+                                  0, d_status, (cudaStream_t)cuda_stream);
+    if (rc) return fail(nullptr, Q3_ERR_CUDA, "op_gemm_i8: tensor-core GEMM could not be set up (%d)", rc);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(nullptr, Q3_ERR_CUDA, "op_gemm_i8 launch: %s", cudaGetErrorString(e));
+    return Q3_OK;
+}
 
 extern "C" size_t q3i8_op_attention_workspace(int32_t R, int32_t n_heads, int32_t hd, int32_t splits) {
     if (R <= 0 || n_heads <= 0 || hd <= 0 || splits <= 0) return 0;

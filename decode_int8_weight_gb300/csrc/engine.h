@@ -16,7 +16,7 @@ constexpr int kCtxCeiling = 65536; // "Model-agnostic LLM inference", section "L
 constexpr int kChunkPos = 64;      // KV positions per attention stage; the cache capacity is a multiple
 
 struct DevMat {
-    int8_t* raw = nullptr;     // [rows][cols] row-major int8 (embedding table only: the gather)
+    int8_t* raw = nullptr;     // [rows][cols] row-major int8 (embedding gather, prefill tensor-core GEMM)
     uint8_t* frag = nullptr;   // fragment-order bytes (decode GEMV)
     float* scale = nullptr;    // [rows]
     int rows = 0, valid_rows = 0, cols = 0;
@@ -99,5 +99,6 @@ int step_launches(const q3i8_ctx* c);
 int persistent_setup(q3i8_ctx* c);
 int persistent_reset(q3i8_ctx* c);
 cudaError_t enqueue_persistent(q3i8_ctx* c, int B, float* logits, unsigned long long* trace = nullptr);
-constexpr int kPrefillChunk = 32;  // prompt rows per weight sweep of a prefill projection
+constexpr int kPrefillChunk = 32;  // prompt rows per weight sweep of a prefill projection on the GEMV
+// prefills longer than this many rows run their projections on the tcgen05 GEMM
 int prefill_launches(const q3i8_ctx* c, int M);

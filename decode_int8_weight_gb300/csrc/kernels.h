@@ -65,4 +65,14 @@ int launch_attention(const float* q, const __nv_bfloat16* k, const __nv_bfloat16
                      const int32_t* row_len, int len_add, int R, int nh, int nkv, int hd, int cap, int splits,
                      float* part, float* out, __half* outh, int ldh, int32_t* status, cudaStream_t st);
 
+// Prefill projection on tcgen05 tensor cores: Y = s * (x . W^T) over M rows.
+// a_planes: [M][2K] f16, row m = hi(m, :) then lo(m, :); w: [N][K] int8
+// row-major.  mode kStore: y[m*ldy + n] = ...; kResid: y[...] += ...;
+// kSiluGate (fused gate/up rows): hi/lo planes of silu(gate)*up into
+// yh[(2m + part) * ldyh + unit].  Needs N % 128 == 0 and K % 64 == 0.
+// Returns 0 when launched, < 0 when the arguments do not fit.
+bool tc_gemm_supported(int N, int K);
+int launch_tc_gemm(const __half* a_planes, const int8_t* w, const float* scale, int M, int N, int K, int mode,
+                   float* y, int ldy, __half* yh, int ldyh, int32_t* status, cudaStream_t st);
+
 }  // namespace q3

@@ -211,6 +211,19 @@ void q3i8_destroy(q3i8_ctx* ctx);
  * return after enqueueing (no synchronisation).
  */
 
+/* Dense int8-weight projection on the tcgen05 tensor cores, the contraction
+ * of the prefill ("LLM inference overview", section "Workload
+ * characteristics": each prompt projection is one wide matmul):
+ *   y[m][n] = scale[n] * sum_k w[n][k] * x[m][k],  m < M, n < N.
+ *   a_planes [M][2K] f16 bit patterns: row m holds hi(m, 0..K-1) then
+ *            lo(m, 0..K-1), with x = hi + lo (hi = f16(x), lo = f16(x - hi)).
+ *   w        [N][K] int8 row-major; scale [N] fp32; y [M][N] fp32.
+ *   N % 128 == 0, K % 64 == 0, M >= 1; all buffers 16-byte aligned.
+ *   d_status device int32 set non-zero if a bounded wait gave up (may be
+ *            NULL). */
+int q3i8_op_gemm_i8(const uint16_t* a_planes, const int8_t* w, const float* scale, int32_t M, int32_t N, int32_t K,
+                    float* y, int32_t* d_status, void* cuda_stream);
+
 /* Split-KV grouped-query decode attention (the attention step of the
  * "Supported models" block, one query position per row):
  *   q       [R][n_heads][hd] fp32 queries (already normed and rotated).

@@ -90,3 +90,41 @@ def test_attention_rejects_bad_sizes(pkg):
     with pytest.raises(pkg.Q3Error):
         pkg.op_attention(q, k, k, torch.zeros(1, dtype=torch.int32, device=dev),
                          torch.ones(1, dtype=torch.int32, device=dev), 2, 1, q, ws)
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 128, 64), (100, 256, 1024), (128, 128, 128), (300, 1024, 3072),
+                                   (513, 384, 2048)])
+def test_tc_gemm_vs_oracle(pkg, M, N, K):
+    """The tcgen05 prefill projection against the oracle's int8 matmul on the value it multiplies (hi + lo,
+    exact in fp32): several tiles, a ragged last row tile, a single row."""
+    import torch
+
+    rng = np.random.default_rng(M * 7 + N + K)
+    x = (rng.standard_normal((M, K)) * 1.5).astype(np.float32)
+    hi = x.astype(np.float16)
+    lo = (x - hi.astype(np.float32)).astype(np.float16)
+    xs = hi.astype(np.float32) + lo.astype(np.float32)
+    q = rng.integers(-127, 128, (N, K), dtype=np.int8)
+    s = (rng.random(N) * 0.02 + 1e-3).astype(np.float32)
+    ref = oracle.matmul_i8(q, s, xs, nthreads=oracle.default_threads())
+    dev = torch.device("cuda")
+    planes = torch.from_numpy(np.ascontiguousarray(np.concatenate([hi, lo], axis=1)).view(np.int16)).to(dev)
+    y = torch.full((M, N), float("nan"), device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    pkg.op_gemm_i8(planes, torch.from_numpy(q).to(dev), torch.from_numpy(s).to(dev), y, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    got = y.cpu().numpy()
+    # two fp32 sums of the same K exact products in different orders (and the tensor core's own
+    # accumulation): |err| <= 4 K eps32 sum|terms|; a layout or indexing error is O(sum|terms|)
+    bound = 4 * K * 6e-8 * (s[None, :] * (np.abs(xs) @ np.abs(q.astype(np.float32)).T)) + 1e-6
+    assert np.all(np.abs(got - ref) <= bound), float(np.max(np.abs(got - ref) - bound))
+
+
+def test_tc_gemm_rejects_bad_shapes(pkg):
+    import torch
+
+    dev = torch.device("cuda")
+    with pytest.raises(pkg.Q3Error):
+        pkg.op_gemm_i8(torch.zeros(4, 192, dtype=torch.int16, device=dev), torch.zeros(100, 96, dtype=torch.int8,
+                       device=dev), torch.ones(100, device=dev), torch.zeros(4, 100, device=dev))
