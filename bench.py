@@ -17,6 +17,7 @@ the host cores on a bounded sample of the same workload (rank 0 only).
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import os
@@ -231,6 +232,31 @@ def run_reference(args, w):
 
 # ---------------------------------------------------------------- GPU arm
 
+def batched_sweep(q3, dev, hbm_peak, batches=(8, 16, 32)):
+    """Decode jobs of the batched workloads (one untimed job, then one timed): decode tok/s, step time and the
+    step's HBM roofline fraction, with the KV bytes of each sequence's positions."""
+    import torch
+
+    out = {}
+    for B in batches:
+        wb = synth.WORKLOADS[f"0.6b-b{B}-p16to256-n128"]
+        mb = synth.make_model(wb.shape, wb.weight_seed)
+        pb = synth.prompts(wb)
+        lens = np.array([len(p) for p in pb], np.int32)
+        dec = q3.Decoder(mb, max_batch=B, max_ctx=wb.max_ctx)
+        d_ids = torch.from_numpy(np.concatenate(pb).astype(np.int32)).to(dev)
+        d_out = torch.empty((B, wb.new_tokens), dtype=torch.int32, device=dev)
+        dec.decode_device(d_ids, lens, wb.new_tokens, d_out)
+        st = dec.decode_device(d_ids, lens, wb.new_tokens, d_out)
+        sb = float(np.mean([dec.step_bytes(lens + i) for i in range(wb.new_tokens - 1)]))
+        gbs = sb / (st["step_us"] * 1e-6) / 1e9
+        out[f"b{B}"] = {"decode_tok_s": st["decode_tokens_per_sec"], "step_us": st["step_us"],
+                        "step_bytes_mean": sb, "achieved_gbs": gbs, "frac": gbs / hbm_peak,
+                        "prefill_tok_s": st["prefill_tokens_per_sec"]}
+        dec.close()
+    return out
+
+
 def run_gpu(args, w):
     import torch
 
@@ -287,6 +313,9 @@ def run_gpu(args, w):
     hbm_peak, peak_kind = peaks()
     achieved = step_bytes / (step_us * 1e-6) / 1e9 if step_us > 0 else 0.0
 
+    # the batched decode workloads (B = 8 / 16 / 32), outside the timed region
+    batched = batched_sweep(q3, dev, hbm_peak) if (rank == 0 and not args.no_batched and w.batch == 1) else None
+
     # e2e through the public API with host buffers
     out_e2e = None
     e2e_times = []
@@ -331,6 +360,7 @@ def run_gpu(args, w):
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_val, "unit": "tok/s", "h2d_bytes_per_step": int(flat.nbytes + 8 * flat.size + 12 * B),
                     "d2h_bytes_per_step": int(n_tok * 4), "ids_match_device_run": same},
+            "batched_decode": batched,
             "gpu_launches": int(launches),
             "wall_s": wall,
             "clocks": clocks,
@@ -352,8 +382,13 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS))
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-batched", action="store_true", help="skip the B = 8 / 16 / 32 decode jobs")
+    ap.add_argument("--new-tokens", type=int, default=None,
+                    help="override the workload's generated tokens per sequence (e.g. to profile its prefill)")
     args = ap.parse_args()
     w = synth.WORKLOADS[args.workload]
+    if args.new_tokens is not None:
+        w = dataclasses.replace(w, new_tokens=max(1, args.new_tokens))
     if args.impl == "reference":
         return run_reference(args, w)
     return run_gpu(args, w)

@@ -248,6 +248,9 @@ static int ensure_prefill(q3i8_ctx* c, int M) {
     CK(c, cudaMalloc(&c->pf_xh, 2 * m * H * 2));
     CK(c, cudaMalloc(&c->pf_oh, 2 * m * Dq * 2));
     CK(c, cudaMalloc(&c->pf_ah, 2 * m * I * 2));
+    cudaFree(c->pf_blocks);
+    c->pf_blocks_cap = M / 32 + kMaxBatch + 1;
+    CK(c, cudaMalloc(&c->pf_blocks, (size_t)c->pf_blocks_cap * sizeof(int4)));
     CK(c, cudaMalloc(&c->pf_part, attn_part_bytes(M, d.n_heads, d.head_dim, 1)));
     CK(c, cudaMalloc(&c->pf_ids, m * 4));
     CK(c, cudaMalloc(&c->pf_seq, m * 4));
@@ -411,7 +414,7 @@ extern "C" void q3i8_destroy(q3i8_ctx* c) {
     }
     void* ptrs[] = {c->final_norm, c->kc, c->vc, c->rope, c->tokens, c->pos, c->seq_ids, c->step, c->keys,
                     c->counter, c->status, c->x, c->qkv, c->qr, c->part, c->xh, c->oh, c->ah, c->logits,
-                    c->out_ids, c->pf_x, c->pf_qkv, c->pf_q, c->pf_xh, c->pf_oh, c->pf_ah,
+                    c->out_ids, c->pf_x, c->pf_qkv, c->pf_q, c->pf_xh, c->pf_oh, c->pf_ah, c->pf_blocks,
                     c->pf_part, c->pf_ids, c->pf_seq, c->pf_pos, c->pf_last, c->d_mats, c->d_gains,
                     c->p_epoch, c->p_keys, c->p_exit, c->p_attn_cnt, c->p_abort, c->p_diag, c->p_ll, c->p_part, c->p_trace};
     for (void* p : ptrs) cudaFree(p);
@@ -607,7 +610,8 @@ int prefill_launches(const q3i8_ctx* c, int M) {
     auto per = [&](int N, int K) { return M > kPrefillChunk && tc_gemm_supported(N, K) ? 1 : chunks; };
     const int H = d.hidden, I = d.intermediate, Dq = d.n_heads * d.head_dim, Dkv = d.n_kv_heads * d.head_dim;
     const int proj = per(Dq + 2 * Dkv, H) + per(H, Dq) + per(2 * I, H) + per(H, I);
-    return 1 + d.n_layers * (5 + proj) + 2;
+    const int attn = attn_prefill_supported(d.n_heads, d.n_kv_heads, d.head_dim) ? 1 : 2;
+    return 1 + d.n_layers * (3 + attn + proj) + 2;
 }
 
 // Graph of one decode step at batch B (captured on first use).
@@ -683,6 +687,17 @@ static int run_prefill(q3i8_ctx* c, int B, const int32_t* d_ids, const int32_t* 
             launch_gemv(a, mode, gemv_grid(a.rows, mode, c->num_sms), st);
         }
     };
+    // causal attention: the tensor-core kernel over 32-position query blocks
+    // where the shape allows, else the split kernel with one split per row
+    int nblk = 0;
+    const bool tc_attn = attn_prefill_supported(nh, nkv, hd);
+    if (tc_attn) {
+        std::vector<int4> blk(c->pf_blocks_cap);
+        nblk = attn_prefill_blocks(lens, B, blk.data(), c->pf_blocks_cap);
+        if (nblk > c->pf_blocks_cap) return fail(c, Q3_ERR_STATE, "prefill: query block table too small");
+        CK(c, cudaMemcpyAsync(c->pf_blocks, blk.data(), (size_t)nblk * sizeof(int4), cudaMemcpyHostToDevice, st));
+        CK(c, cudaStreamSynchronize(st));  // blk is a host temporary
+    }
     launch_embed(d_ids, M, c->embed.raw, c->embed.scale, H, c->pf_x, st);
     for (int l = 0; l < d.n_layers; ++l) {
         const DevLayer& L = c->layers[l];
@@ -690,8 +705,14 @@ static int run_prefill(q3i8_ctx* c, int B, const int32_t* d_ids, const int32_t* 
         project(L.qkv, H, c->pf_xh, kStore, c->pf_qkv, L.qkv.rows, nullptr, 0);
         launch_qk_rope_append(c->pf_qkv, M, nh, nkv, hd, c->pf_seq, c->pf_pos, L.q_norm, L.k_norm, d.rms_eps,
                               c->rope, c->pf_q, c->kc + l * layer_kv, c->vc + l * layer_kv, c->cap, st);
-        launch_attention(c->pf_q, c->kc + l * layer_kv, c->vc + l * layer_kv, c->pf_seq, c->pf_pos, 1, M, nh, nkv,
-                         hd, c->cap, 1, c->pf_part, nullptr, c->pf_oh, Dq, c->status, st);
+        if (tc_attn) {
+            if (launch_attn_prefill(c->pf_q, c->kc + l * layer_kv, c->vc + l * layer_kv, c->pf_blocks, nblk, nh, nkv,
+                                    hd, c->cap, c->pf_oh, Dq, st))
+                return fail(c, Q3_ERR_CUDA, "prefill attention could not be launched");
+        } else {
+            launch_attention(c->pf_q, c->kc + l * layer_kv, c->vc + l * layer_kv, c->pf_seq, c->pf_pos, 1, M, nh,
+                             nkv, hd, c->cap, 1, c->pf_part, nullptr, c->pf_oh, Dq, c->status, st);
+        }
         project(L.o, Dq, c->pf_oh, kResid, c->pf_x, H, nullptr, 0);
         launch_rmsnorm(c->pf_x, nullptr, M, H, L.ffn_norm, d.rms_eps, nullptr, c->pf_xh, st);
         project(L.gu, H, c->pf_xh, kSiluGate, nullptr, 0, c->pf_ah, I);

@@ -61,6 +61,8 @@ struct q3i8_ctx {
     int pf_rows = 0;
     float *pf_x = nullptr, *pf_qkv = nullptr, *pf_q = nullptr, *pf_part = nullptr;
     __half *pf_xh = nullptr, *pf_oh = nullptr, *pf_ah = nullptr;  // [2M][K] hi/lo planes of the prompt rows
+    int4* pf_blocks = nullptr;  // query blocks of the tensor-core prefill attention
+    int pf_blocks_cap = 0;
     int32_t *pf_ids = nullptr, *pf_seq = nullptr, *pf_pos = nullptr, *pf_last = nullptr;
 
     // persistent decode step (one cooperative kernel per step)

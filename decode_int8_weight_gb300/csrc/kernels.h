@@ -65,6 +65,16 @@ int launch_attention(const float* q, const __nv_bfloat16* k, const __nv_bfloat16
                      const int32_t* row_len, int len_add, int R, int nh, int nkv, int hd, int cap, int splits,
                      float* part, float* out, __half* outh, int ldh, int32_t* status, cudaStream_t st);
 
+// Causal prefill attention on tensor cores (GROUP == 2, hd == 128): blocks
+// of 32 prompt positions of one sequence, {sequence, first position, flat
+// row of the sequence's position 0, length}, built by attn_prefill_blocks
+// (returns the count; writes at most cap_blocks).  Output: hi/lo f16 planes
+// outh[(2r + part) * ldh + head * hd + d].
+bool attn_prefill_supported(int nh, int nkv, int hd);
+int attn_prefill_blocks(const int32_t* lens, int B, int4* out, int cap_blocks);
+int launch_attn_prefill(const float* q, const __nv_bfloat16* kc, const __nv_bfloat16* vc, const int4* blocks,
+                        int nblocks, int nh, int nkv, int hd, int cap, __half* outh, int ldh, cudaStream_t st);
+
 // Prefill projection on tcgen05 tensor cores: Y = s * (x . W^T) over M rows.
 // a_planes: [M][2K] f16, row m = hi(m, :) then lo(m, :); w: [N][K] int8
 // row-major.  mode kStore: y[m*ldy + n] = ...; kResid: y[...] += ...;

@@ -458,16 +458,19 @@ Q3_DEV bool stage_plane(Ctl& c, const LLw* plane, int K, uint32_t flag, const LL
             else v[u][0] = v[u][1] = done;
         }
         // words still stale are re-read together, so a round costs one
-        // round trip however many of them were early
+        // round trip however many of them were early; this thread's sum of
+        // squares word (first batch) rides along
+        const bool own_ss = base == c.tid && c.tid < nss;
         uint64_t t0 = 0;
         for (uint32_t i = 0;; ++i) {
-            bool stale = false;
+            bool stale = own_ss && (uint32_t)(sv >> 32) != sflag;
 #pragma unroll
             for (int u = 0; u < U; ++u)
                 stale |= ((uint32_t)(v[u][0] >> 32) != flag) | ((uint32_t)(v[u][1] >> 32) != flag);
             if (!stale) break;
             t0 = poll_tick(c.P, &c.sh->abort, diag_of(c), i, t0, flag);
             if (t0 == ~0ull) return false;
+            if (own_ss && (uint32_t)(sv >> 32) != sflag) sv = ll_get(ss + (size_t)(c.tid / P.B) * P.bmax + c.tid % P.B);
 #pragma unroll
             for (int u = 0; u < U; ++u) {
                 const int q = base + u * kCThreads;
@@ -559,21 +562,30 @@ Q3_DEV bool gemv_tile(Ctl& c, int K, const LLw* plane, uint32_t flag) {
             float a4[4][4];
 #pragma unroll
             for (int q = 0; q < 4; ++q) a4[q][0] = a4[q][1] = a4[q][2] = a4[q][3] = 0.f;
+            // every operand of this warp's k-pairs is loaded before the first
+            // MMA, so the shared-memory latency is paid once per slot
+            constexpr int NI = kKpPerChunk / kCWarps;
+            uint4 wv[NI];
+            uint32_t bq[NI][4];
 #pragma unroll
-            for (int i = 0; i < kKpPerChunk / kCWarps; ++i) {
+            for (int i = 0; i < NI; ++i) {
                 const int p = kKpPerChunk * j + c.warp + kCWarps * i;
-                if (p >= kp_end) continue;
-                const uint4 wv = lds128(fa + (p - kKpPerChunk * j) * 512);
-                uint32_t A0[4], A1[4];
-                u8x4_to_biased(wv.x, A0[0], A0[1]);
-                u8x4_to_biased(wv.y, A0[2], A0[3]);
-                u8x4_to_biased(wv.z, A1[0], A1[1]);
-                u8x4_to_biased(wv.w, A1[2], A1[3]);
+                const bool in = p < kp_end;
                 const uint32_t ba = sca + 4 * 16 * p;
-                const uint32_t b0 = live ? lds32(ba) : 0u, b1 = live ? lds32(ba + 16) : 0u;
-                const uint32_t b2 = live ? lds32(ba + 32) : 0u, b3 = live ? lds32(ba + 48) : 0u;
-                mma_f16_16816(a4[(2 * i) & 3], A0, b0, b1);
-                mma_f16_16816(a4[(2 * i + 1) & 3], A1, b2, b3);
+                wv[i] = in ? lds128(fa + (p - kKpPerChunk * j) * 512) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) bq[i][e] = (in && live) ? lds32(ba + 16 * e) : 0u;
+            }
+#pragma unroll
+            for (int i = 0; i < NI; ++i) {
+                // a k-pair past the end multiplies zero operands
+                uint32_t A0[4], A1[4];
+                u8x4_to_biased(wv[i].x, A0[0], A0[1]);
+                u8x4_to_biased(wv[i].y, A0[2], A0[3]);
+                u8x4_to_biased(wv[i].z, A1[0], A1[1]);
+                u8x4_to_biased(wv[i].w, A1[2], A1[3]);
+                mma_f16_16816(a4[(2 * i) & 3], A0, bq[i][0], bq[i][1]);
+                mma_f16_16816(a4[(2 * i + 1) & 3], A1, bq[i][2], bq[i][3]);
             }
 #pragma unroll
             for (int e = 0; e < 4; ++e) acc[0][e] += (a4[0][e] + a4[1][e]) + (a4[2][e] + a4[3][e]);
@@ -703,31 +715,31 @@ Q3_DEV bool warp_tiles(Ctl& c, int mode, int t0, int ntiles, int G, int K, uint3
             }
             const uint32_t fa = sa + (j == 0 ? kTileHeader : 0) + c.lane * 16;
             const int p0 = kKpPerChunk * j, np = min(KP - p0, kKpPerChunk);
-            {
-#pragma unroll 2
-                for (int i = 0; i < np; i += 2) {
-                    // k-pairs p and p+1: four k-steps on four independent chains
-                    const uint32_t ba = sca + 4 * 16 * (p0 + i);
-                    const bool two = i + 1 < np;  // a slot may end on an odd k-pair
-                    const uint4 w0 = lds128(fa + i * 512);
-                    const uint4 w1 = two ? lds128(fa + (i + 1) * 512) : w0;
-                    uint32_t bb[8];
+            // groups of 8 k-pairs: all operands of a group are loaded before
+            // its 16 MMAs (four independent accumulator chains), so the
+            // shared-memory latency is paid once per group; k-pairs past the
+            // end of the slot multiply zero operands
+#pragma unroll 1
+            for (int i0 = 0; i0 < np; i0 += 8) {
+                uint4 wv[8];
+                uint32_t bq[8][4];
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) bb[e] = (live && (e < 4 || two)) ? lds32(ba + 16 * e) : 0u;
+                for (int i = 0; i < 8; ++i) {
+                    const bool in = i0 + i < np;
+                    const uint32_t ba = sca + 4 * 16 * (p0 + i0 + i);
+                    wv[i] = in ? lds128(fa + (i0 + i) * 512) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) bq[i][e] = (in && live) ? lds32(ba + 16 * e) : 0u;
+                }
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
                     uint32_t A[4];
-                    u8x4_to_biased(w0.x, A[0], A[1]);
-                    u8x4_to_biased(w0.y, A[2], A[3]);
-                    mma_f16_16816(a[0], A, bb[0], bb[1]);
-                    u8x4_to_biased(w0.z, A[0], A[1]);
-                    u8x4_to_biased(w0.w, A[2], A[3]);
-                    mma_f16_16816(a[1], A, bb[2], bb[3]);
-                    // (a missing second k-pair multiplies zero operands)
-                    u8x4_to_biased(w1.x, A[0], A[1]);
-                    u8x4_to_biased(w1.y, A[2], A[3]);
-                    mma_f16_16816(a[2], A, bb[4], bb[5]);
-                    u8x4_to_biased(w1.z, A[0], A[1]);
-                    u8x4_to_biased(w1.w, A[2], A[3]);
-                    mma_f16_16816(a[3], A, bb[6], bb[7]);
+                    u8x4_to_biased(wv[i].x, A[0], A[1]);
+                    u8x4_to_biased(wv[i].y, A[2], A[3]);
+                    mma_f16_16816(a[(2 * i) & 3], A, bq[i][0], bq[i][1]);
+                    u8x4_to_biased(wv[i].z, A[0], A[1]);
+                    u8x4_to_biased(wv[i].w, A[2], A[3]);
+                    mma_f16_16816(a[(2 * i + 1) & 3], A, bq[i][2], bq[i][3]);
                 }
             }
             __syncwarp();
