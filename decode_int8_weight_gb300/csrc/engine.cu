@@ -538,6 +538,11 @@ int persistent_setup(q3i8_ctx* c) {
     const uint32_t one = 1;
     CK(c, cudaMemcpy(c->p_epoch, &one, 4, cudaMemcpyHostToDevice));
     c->use_persistent = true;
+    // B <= 4 stages each phase's whole input in shared memory and is the
+    // measured winner; at B >= 8 the chained kernels are faster (the
+    // persistent path then reads its operands from the flagged words)
+    c->p_max_batch = 4;
+    if (const char* mb = getenv("Q3I8_PERSISTENT_MAX_BATCH")) c->p_max_batch = std::max(1, atoi(mb));
     return Q3_OK;
 }
 
@@ -589,8 +594,10 @@ cudaError_t enqueue_persistent(q3i8_ctx* c, int B, float* logits, unsigned long 
 
 // One decode step on the context's stream: the persistent kernel when the
 // shape allows it, else the chained kernels.
+static bool persistent_for(const q3i8_ctx* c, int B) { return c->use_persistent && B <= c->p_max_batch; }
+
 static int enqueue_decode_step(q3i8_ctx* c, int B, bool want_logits) {
-    if (c->use_persistent) {
+    if (persistent_for(c, B)) {
         cudaError_t e = enqueue_persistent(c, B, want_logits ? c->logits : nullptr);
         if (e != cudaSuccess) return fail(c, Q3_ERR_CUDA, "persistent step launch: %s", cudaGetErrorString(e));
         return Q3_OK;
@@ -599,7 +606,7 @@ static int enqueue_decode_step(q3i8_ctx* c, int B, bool want_logits) {
     return Q3_OK;
 }
 
-int step_launches(const q3i8_ctx* c) { return c->use_persistent ? 1 : 2 + c->d.n_layers * 9 + 1; }
+int step_launches(const q3i8_ctx* c, int B) { return persistent_for(c, B) ? 1 : 2 + c->d.n_layers * 9 + 1; }
 // Kernels of one prefill over M prompt rows: embed; per layer 2 RMSNorms, the
 // QK-norm/RoPE/append, attention split + merge and the 4 projections (one
 // tensor-core GEMM each, or one GEMV per chunk of kPrefillChunk rows); final
@@ -788,7 +795,7 @@ static int decode_core(q3i8_ctx* c, int B, const int32_t* d_ids, const int32_t* 
         rc = get_graph(c, B, &g);
         if (rc) return rc;
         for (int i = 1; i < max_new; ++i) CK(c, cudaGraphLaunch(g, c->stream));
-        c->launches += (int64_t)(max_new - 1) * step_launches(c);
+        c->launches += (int64_t)(max_new - 1) * step_launches(c, B);
     }
     CK(c, cudaEventRecord(c->ev2, c->stream));
     rc = check_status(c);
@@ -909,7 +916,7 @@ extern "C" int q3i8_step_logits(q3i8_ctx* c, const int32_t* tokens, float* logit
     }
     CK(c, cudaMemcpyAsync(c->tokens, tokens, B * 4, cudaMemcpyHostToDevice, c->stream));
     if (int rc0 = enqueue_decode_step(c, B, true)) return rc0;
-    c->launches += step_launches(c);
+    c->launches += step_launches(c, B);
     CK(c, cudaGetLastError());
     CK(c, cudaMemcpyAsync(logits, c->logits, (size_t)B * c->d.vocab * 4, cudaMemcpyDeviceToHost, c->stream));
     int rc = check_status(c);
@@ -921,8 +928,9 @@ extern "C" int q3i8_step_logits(q3i8_ctx* c, const int32_t* tokens, float* logit
 extern "C" int q3i8_trace_step(q3i8_ctx* c, const int32_t* tokens, uint64_t* stamps, size_t cap, int32_t* grid,
                                int32_t* stride) {
     if (!c) return fail(nullptr, Q3_ERR_INVALID_ARGUMENTS, "ctx is NULL");
-    if (!c->use_persistent) return fail(c, Q3_ERR_STATE, "trace_step: this context uses the chained step kernels");
     if (c->active_B <= 0) return fail(c, Q3_ERR_STATE, "trace_step before q3i8_prefill");
+    if (!persistent_for(c, c->active_B))
+        return fail(c, Q3_ERR_STATE, "trace_step: this batch decodes with the chained step kernels");
     const int st = trace_stride(c->d.n_layers);
     const size_t n = (size_t)c->p_grid * st;
     if (grid) *grid = c->p_grid;
@@ -974,8 +982,7 @@ extern "C" int64_t q3i8_step_bytes(const q3i8_ctx* c, int32_t B, const int32_t* 
 }
 
 extern "C" int32_t q3i8_step_launches(const q3i8_ctx* c, int32_t B) {
-    (void)B;
-    return c ? step_launches(c) : 0;
+    return c ? step_launches(c, B) : 0;
 }
 
 extern "C" int64_t q3i8_launch_count(const q3i8_ctx* c) { return c ? c->launches : 0; }

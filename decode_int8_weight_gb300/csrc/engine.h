@@ -67,6 +67,7 @@ struct q3i8_ctx {
 
     // persistent decode step (one cooperative kernel per step)
     bool use_persistent = false;
+    int p_max_batch = 4;  // largest B decoded by the persistent kernel; larger B take the chained kernels
     int p_grid = 0, p_ns = 0, p_kmax = 0, p_optin = 0;
     const uint8_t** d_mats = nullptr;     // device [L*4]
     const float** d_gains = nullptr;      // device [L*4]
@@ -97,7 +98,7 @@ void drop_graphs(q3i8_ctx* c);
 int decode_splits(const q3i8_ctx* c, int B);
 void enqueue_step(q3i8_ctx* c, int B, bool want_logits);
 void enqueue_lm_head(q3i8_ctx* c, int B, bool advance_pos, float* logits);
-int step_launches(const q3i8_ctx* c);
+int step_launches(const q3i8_ctx* c, int B);
 int persistent_setup(q3i8_ctx* c);
 int persistent_reset(q3i8_ctx* c);
 cudaError_t enqueue_persistent(q3i8_ctx* c, int B, float* logits, unsigned long long* trace = nullptr);

@@ -113,6 +113,14 @@ def test_0p6b_b8_ragged(pkg):
     _teacher_forced_check(pkg, "0.6b-b8-p16to256-n128", steps=24)
 
 
+def test_0p6b_b8_persistent_operands_from_words(pkg, monkeypatch):
+    # B > 4 decodes with the chained kernels by default; this keeps the
+    # persistent kernel's wide-batch path (operands read from the flagged
+    # words) under test
+    monkeypatch.setenv("Q3I8_PERSISTENT_MAX_BATCH", "32")
+    _teacher_forced_check(pkg, "0.6b-b8-p16to256-n128", steps=12)
+
+
 def test_decode_is_deterministic(pkg):
     w = synth.WORKLOADS["tiny-b1-p8-n16"]
     m, _ = model_for(w.name)
