@@ -442,6 +442,9 @@ void enqueue_step(q3i8_ctx* c, int B, bool want_logits) {
     const size_t layer_kv = (size_t)c->bmax * nkv * c->cap * hd;
     cudaStream_t st = c->stream;
     const int splits = decode_splits(c, B);
+    // the residual projections have only hidden/16 tiles: from 5 sequences on
+    // (wide operands) their K is split over 4 CTAs per tile (atomic adds)
+    const int ks_resid = B > 4 ? 4 : 1;
 
     launch_embed(c->tokens, B, c->embed.raw, c->embed.scale, H, c->x, st);
     launch_rmsnorm(c->x, nullptr, B, H, c->layers[0].attn_norm, d.rms_eps, nullptr, c->xh, st);
@@ -459,8 +462,8 @@ void enqueue_step(q3i8_ctx* c, int B, bool want_logits) {
         a = GemvArgs{};
         a.B = B;
         a.w = L.o.frag, a.scale = L.o.scale, a.rows = L.o.rows, a.K = Dq, a.xh = c->oh;
-        a.y = c->x, a.ldy = H;
-        launch_gemv(a, kResid, gemv_grid(a.rows, kResid, c->num_sms), st);
+        a.y = c->x, a.ldy = H, a.ksplit = ks_resid;
+        launch_gemv(a, kResid, gemv_grid(a.rows, kResid, c->num_sms) * ks_resid, st);
         launch_rmsnorm(c->x, nullptr, B, H, L.ffn_norm, d.rms_eps, nullptr, c->xh, st);
         a = GemvArgs{};
         a.B = B;
@@ -470,8 +473,8 @@ void enqueue_step(q3i8_ctx* c, int B, bool want_logits) {
         a = GemvArgs{};
         a.B = B;
         a.w = L.down.frag, a.scale = L.down.scale, a.rows = L.down.rows, a.K = I, a.xh = c->ah;
-        a.y = c->x, a.ldy = H;
-        launch_gemv(a, kResid, gemv_grid(a.rows, kResid, c->num_sms), st);
+        a.y = c->x, a.ldy = H, a.ksplit = ks_resid;
+        launch_gemv(a, kResid, gemv_grid(a.rows, kResid, c->num_sms) * ks_resid, st);
         const float* g_next = (l + 1 < d.n_layers) ? c->layers[l + 1].attn_norm : c->final_norm;
         launch_rmsnorm(c->x, nullptr, B, H, g_next, d.rms_eps, nullptr, c->xh, st);
     }

@@ -48,13 +48,17 @@ __global__ void __launch_bounds__(256) gemv_kernel(GemvArgs a) {
         for (int i = threadIdx.x; i < 4 * NT; i += blockDim.x) best[i] = 0ull;
         __syncthreads();
     }
-    for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
+    // work item = (tile, K part); residual tiles may be split over ks CTAs
+    const int ks = (MODE == kResid && a.ksplit > 1) ? a.ksplit : 1;
+    for (int item = blockIdx.x; item < n_tiles * ks; item += gridDim.x) {
+        const int tile = item / ks, part = item - tile * ks;
+        const int p_lo = (int)((long long)kpairs * part / ks), p_hi = (int)((long long)kpairs * (part + 1) / ks);
         float acc[NT][4];
 #pragma unroll
         for (int n = 0; n < NT; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
         const uint8_t* wt = a.w + (size_t)tile * (kTileHeader + 16 * (size_t)a.K) + kTileHeader + lane * 16;
 #pragma unroll 4
-        for (int p = warp; p < kpairs; p += 8) {
+        for (int p = p_lo + warp; p < p_hi; p += 8) {
             uint4 wv = ld_stream_u4(wt + (size_t)p * 512);
             uint32_t A0[4], A1[4];
             u8x4_to_f16x2x2(wv.x, A0[0], A0[1]);
@@ -114,7 +118,8 @@ __global__ void __launch_bounds__(256) gemv_kernel(GemvArgs a) {
                         a.y[(size_t)b * a.ldy + row] = v;
                     } else if (MODE == kResid) {
                         float* p = a.y + (size_t)b * a.ldy + row;
-                        *p = *p + v;
+                        if (ks > 1) atomicAdd(p, v);
+                        else *p = *p + v;
                     } else {
                         if (row < a.valid_rows) {
                             if (a.logits) a.logits[(size_t)b * a.valid_rows + row] = v;

@@ -43,6 +43,7 @@ struct GemvArgs {
     int advance_pos;
     int valid_rows;            // rows >= valid_rows (padding) take no part in the argmax
     float* logits;             // optional [B][valid_rows]
+    int ksplit;                // kResid only: K split over this many CTAs per tile, summed by atomicAdd (0 = 1)
 };
 
 void launch_gemv(const GemvArgs& a, int mode, int grid, cudaStream_t st);
