@@ -372,7 +372,7 @@ int init_weights(q3i8_ctx* c, const q3i8_mat* embed, const q3i8_layer* layers, c
 int init_state(q3i8_ctx* c) {
     const q3i8_dims& d = c->d;
     const int H = d.hidden, I = d.intermediate, Dq = d.n_heads * d.head_dim, Dkv = d.n_kv_heads * d.head_dim;
-    const int B = c->bmax, cols = 8 * ((B + 3) / 4);
+    const int B = c->bmax;
     CK(c, cudaMalloc(&c->tokens, B * 4));
     CK(c, cudaMalloc(&c->pos, B * 4));
     CK(c, cudaMalloc(&c->seq_ids, B * 4));
@@ -386,13 +386,16 @@ int init_state(q3i8_ctx* c) {
     c->dec_splits_max = 64;
     CK(c, cudaMalloc(&c->part, attn_part_bytes(B, d.n_heads, d.head_dim, c->dec_splits_max)));
     const int K = std::max(std::max(H, I), Dq);
-    CK(c, cudaMalloc(&c->xh, (size_t)cols * K * 2));
-    CK(c, cudaMalloc(&c->oh, (size_t)cols * Dq * 2));
-    CK(c, cudaMalloc(&c->ah, (size_t)cols * I * 2));
+    // activation planes of the chained step: fragment order reserves all 8
+    // column tiles (32 sequences) of every k-pair, whatever max_batch is
+    const int pcols = 64;
+    CK(c, cudaMalloc(&c->xh, (size_t)pcols * K * 2));
+    CK(c, cudaMalloc(&c->oh, (size_t)pcols * Dq * 2));
+    CK(c, cudaMalloc(&c->ah, (size_t)pcols * I * 2));
     CK(c, cudaMalloc(&c->logits, (size_t)B * d.vocab * 4));
-    CK(c, cudaMemsetAsync(c->xh, 0, (size_t)cols * K * 2, c->stream));
-    CK(c, cudaMemsetAsync(c->oh, 0, (size_t)cols * Dq * 2, c->stream));
-    CK(c, cudaMemsetAsync(c->ah, 0, (size_t)cols * I * 2, c->stream));
+    CK(c, cudaMemsetAsync(c->xh, 0, (size_t)pcols * K * 2, c->stream));
+    CK(c, cudaMemsetAsync(c->oh, 0, (size_t)pcols * Dq * 2, c->stream));
+    CK(c, cudaMemsetAsync(c->ah, 0, (size_t)pcols * I * 2, c->stream));
     CK(c, cudaMemsetAsync(c->keys, 0, B * 8, c->stream));
     CK(c, cudaMemsetAsync(c->counter, 0, 4, c->stream));
     CK(c, cudaMemsetAsync(c->status, 0, 4, c->stream));
@@ -447,36 +450,36 @@ void enqueue_step(q3i8_ctx* c, int B, bool want_logits) {
     const int ks_resid = B > 4 ? 4 : 1;
 
     launch_embed(c->tokens, B, c->embed.raw, c->embed.scale, H, c->x, st);
-    launch_rmsnorm(c->x, nullptr, B, H, c->layers[0].attn_norm, d.rms_eps, nullptr, c->xh, st);
+    launch_rmsnorm(c->x, nullptr, B, H, c->layers[0].attn_norm, d.rms_eps, nullptr, c->xh, st, 1);
     for (int l = 0; l < d.n_layers; ++l) {
         const DevLayer& L = c->layers[l];
         GemvArgs a{};
         a.B = B;
-        a.w = L.qkv.frag, a.scale = L.qkv.scale, a.rows = L.qkv.rows, a.K = H, a.xh = c->xh;
+        a.w = L.qkv.frag, a.scale = L.qkv.scale, a.rows = L.qkv.rows, a.K = H, a.xh = c->xh, a.xfrag = 1;
         a.y = c->qkv, a.ldy = L.qkv.rows;
         launch_gemv(a, kStore, gemv_grid(a.rows, kStore, c->num_sms), st);
         launch_qk_rope_append(c->qkv, B, nh, nkv, hd, c->seq_ids, c->pos, L.q_norm, L.k_norm, d.rms_eps, c->rope,
                               c->qr, c->kc + l * layer_kv, c->vc + l * layer_kv, c->cap, st);
         launch_attention(c->qr, c->kc + l * layer_kv, c->vc + l * layer_kv, c->seq_ids, c->pos, 1, B, nh, nkv, hd,
-                         c->cap, splits, c->part, nullptr, c->oh, Dq, c->status, st);
+                         c->cap, splits, c->part, nullptr, c->oh, Dq, c->status, st, 1);
         a = GemvArgs{};
         a.B = B;
-        a.w = L.o.frag, a.scale = L.o.scale, a.rows = L.o.rows, a.K = Dq, a.xh = c->oh;
+        a.w = L.o.frag, a.scale = L.o.scale, a.rows = L.o.rows, a.K = Dq, a.xh = c->oh, a.xfrag = 1;
         a.y = c->x, a.ldy = H, a.ksplit = ks_resid;
         launch_gemv(a, kResid, gemv_grid(a.rows, kResid, c->num_sms) * ks_resid, st);
-        launch_rmsnorm(c->x, nullptr, B, H, L.ffn_norm, d.rms_eps, nullptr, c->xh, st);
+        launch_rmsnorm(c->x, nullptr, B, H, L.ffn_norm, d.rms_eps, nullptr, c->xh, st, 1);
         a = GemvArgs{};
         a.B = B;
-        a.w = L.gu.frag, a.scale = L.gu.scale, a.rows = L.gu.rows, a.K = H, a.xh = c->xh;
-        a.yh = c->ah, a.ldyh = I;
+        a.w = L.gu.frag, a.scale = L.gu.scale, a.rows = L.gu.rows, a.K = H, a.xh = c->xh, a.xfrag = 1;
+        a.yh = c->ah, a.ldyh = I, a.yfrag = 1;
         launch_gemv(a, kSiluGate, gemv_grid(a.rows, kSiluGate, c->num_sms), st);
         a = GemvArgs{};
         a.B = B;
-        a.w = L.down.frag, a.scale = L.down.scale, a.rows = L.down.rows, a.K = I, a.xh = c->ah;
+        a.w = L.down.frag, a.scale = L.down.scale, a.rows = L.down.rows, a.K = I, a.xh = c->ah, a.xfrag = 1;
         a.y = c->x, a.ldy = H, a.ksplit = ks_resid;
         launch_gemv(a, kResid, gemv_grid(a.rows, kResid, c->num_sms) * ks_resid, st);
         const float* g_next = (l + 1 < d.n_layers) ? c->layers[l + 1].attn_norm : c->final_norm;
-        launch_rmsnorm(c->x, nullptr, B, H, g_next, d.rms_eps, nullptr, c->xh, st);
+        launch_rmsnorm(c->x, nullptr, B, H, g_next, d.rms_eps, nullptr, c->xh, st, 1);
     }
     enqueue_lm_head(c, B, true, want_logits ? c->logits : nullptr);
 }
@@ -485,6 +488,7 @@ void enqueue_lm_head(q3i8_ctx* c, int B, bool advance_pos, float* logits) {
     GemvArgs a{};
     a.B = B;
     a.w = c->embed.frag, a.scale = c->embed.scale, a.rows = c->embed.rows, a.K = c->d.hidden, a.xh = c->xh;
+    a.xfrag = 1;  // the final RMSNorm writes fragment-ordered planes
     a.keys = c->keys, a.counter = c->counter, a.tokens = c->tokens, a.out_ids = c->out_ids, a.step = c->step;
     a.out_cap = c->out_cap, a.pos = c->pos, a.advance_pos = advance_pos ? 1 : 0;
     a.valid_rows = c->embed.valid_rows, a.logits = logits;
@@ -730,7 +734,7 @@ static int run_prefill(q3i8_ctx* c, int B, const int32_t* d_ids, const int32_t* 
         (void)Dkv;
     }
     if (tc_rc) return fail(c, Q3_ERR_CUDA, "prefill: tensor-core GEMM could not be set up (%d)", tc_rc);
-    launch_rmsnorm(c->pf_x, c->pf_last, B, H, c->final_norm, d.rms_eps, nullptr, c->xh, st);
+    launch_rmsnorm(c->pf_x, c->pf_last, B, H, c->final_norm, d.rms_eps, nullptr, c->xh, st, 1);
     enqueue_lm_head(c, B, false, d_logits);
     CK(c, cudaGetLastError());
     c->launches += prefill_launches(c, M);

@@ -68,11 +68,17 @@ __global__ void __launch_bounds__(256) gemv_kernel(GemvArgs a) {
             const int k0 = p * 32 + 2 * t;
 #pragma unroll
             for (int n = 0; n < NT; ++n) {
-                const __half* xr = a.xh + (size_t)(8 * n + g) * a.K + k0;
-                uint32_t b0 = *reinterpret_cast<const uint32_t*>(xr);
-                uint32_t b1 = *reinterpret_cast<const uint32_t*>(xr + 8);
-                uint32_t b2 = *reinterpret_cast<const uint32_t*>(xr + 16);
-                uint32_t b3 = *reinterpret_cast<const uint32_t*>(xr + 24);
+                uint32_t b0, b1, b2, b3;
+                if (a.xfrag) {
+                    const uint4 bw = *reinterpret_cast<const uint4*>(a.xh + ((((size_t)p * 8 + n) * 32 + lane) << 3));
+                    b0 = bw.x, b1 = bw.y, b2 = bw.z, b3 = bw.w;
+                } else {
+                    const __half* xr = a.xh + (size_t)(8 * n + g) * a.K + k0;
+                    b0 = *reinterpret_cast<const uint32_t*>(xr);
+                    b1 = *reinterpret_cast<const uint32_t*>(xr + 8);
+                    b2 = *reinterpret_cast<const uint32_t*>(xr + 16);
+                    b3 = *reinterpret_cast<const uint32_t*>(xr + 24);
+                }
                 mma_f16_16816(acc[n], A0, b0, b1);
                 mma_f16_16816(acc[n], A1, b2, b3);
             }
@@ -101,8 +107,8 @@ __global__ void __launch_bounds__(256) gemv_kernel(GemvArgs a) {
                     const int idx = tile * 8 + gg;
                     __half hi, lo;
                     split_f16(v, hi, lo);
-                    a.yh[(size_t)(2 * b) * a.ldyh + idx] = hi;
-                    a.yh[(size_t)(2 * b + 1) * a.ldyh + idx] = lo;
+                    a.yh[plane_index(2 * b, idx, a.ldyh, a.yfrag)] = hi;
+                    a.yh[plane_index(2 * b + 1, idx, a.ldyh, a.yfrag)] = lo;
                 }
             }
         } else {
@@ -202,7 +208,7 @@ void launch_embed(const int32_t* ids, int n, const int8_t* E, const float* sE, i
 // rows (xn, [n][H]) and/or f16 hi/lo planes (xh, columns 2i and 2i+1).
 // =====================================================================
 __global__ void rmsnorm_kernel(const float* x, const int32_t* rows, int H, const float* g, float eps, float* xn,
-                               __half* xh) {
+                               __half* xh, int frag) {
     __shared__ float part[32];
     __shared__ float s_inv;
     const int i = blockIdx.x;
@@ -226,15 +232,15 @@ __global__ void rmsnorm_kernel(const float* x, const int32_t* rows, int H, const
         if (xh) {
             __half hi, lo;
             split_f16(v, hi, lo);
-            xh[(size_t)(2 * i) * H + k] = hi;
-            xh[(size_t)(2 * i + 1) * H + k] = lo;
+            xh[plane_index(2 * i, k, H, frag)] = hi;
+            xh[plane_index(2 * i + 1, k, H, frag)] = lo;
         }
     }
 }
 
 void launch_rmsnorm(const float* x, const int32_t* rows, int n, int H, const float* g, float eps, float* xn,
-                    __half* xh, cudaStream_t st) {
-    if (n > 0) rmsnorm_kernel<<<n, 256, 0, st>>>(x, rows, H, g, eps, xn, xh);
+                    __half* xh, cudaStream_t st, int frag) {
+    if (n > 0) rmsnorm_kernel<<<n, 256, 0, st>>>(x, rows, H, g, eps, xn, xh, frag);
 }
 
 // =====================================================================
@@ -494,7 +500,8 @@ __global__ void __launch_bounds__(128) attn_split_kernel(const float* q, const _
 
 // out[r][h][:] = sum_s acc_s e^{m_s - M} / sum_s l_s e^{m_s - M}
 template <int HD>
-__global__ void attn_merge_kernel(const float* part, int nh, int splits, float* out, __half* outh, int ldh) {
+__global__ void attn_merge_kernel(const float* part, int nh, int splits, float* out, __half* outh, int ldh,
+                                  int frag) {
     const int rh = blockIdx.x;  // r * nh + h
     const int d = threadIdx.x;
     const float* p = part + (size_t)rh * splits * (HD + 2);
@@ -514,8 +521,8 @@ __global__ void attn_merge_kernel(const float* part, int nh, int splits, float* 
     if (outh) {
         __half hi, lo;
         split_f16(o, hi, lo);
-        outh[(size_t)(2 * r) * ldh + h * HD + d] = hi;
-        outh[(size_t)(2 * r + 1) * ldh + h * HD + d] = lo;
+        outh[plane_index(2 * r, h * HD + d, ldh, frag)] = hi;
+        outh[plane_index(2 * r + 1, h * HD + d, ldh, frag)] = lo;
     }
 }
 
@@ -538,13 +545,14 @@ static void launch_attn_t(const float* q, const __nv_bfloat16* k, const __nv_bfl
 
 int launch_attention(const float* q, const __nv_bfloat16* k, const __nv_bfloat16* v, const int32_t* row_seq,
                      const int32_t* row_len, int len_add, int R, int nh, int nkv, int hd, int cap, int splits,
-                     float* part, float* out, __half* outh, int ldh, int32_t* status, cudaStream_t st) {
+                     float* part, float* out, __half* outh, int ldh, int32_t* status, cudaStream_t st,
+                     int frag) {
     if (R <= 0) return 0;
     const int group = nh / nkv;
 #define Q3_ATTN_CASE(HDV, GV)                                                                         \
     if (hd == HDV && group == GV) {                                                                   \
         launch_attn_t<HDV, GV>(q, k, v, row_seq, row_len, len_add, R, nh, nkv, cap, splits, part, status, st); \
-        attn_merge_kernel<HDV><<<R * nh, HDV, 0, st>>>(part, nh, splits, out, outh, ldh);              \
+        attn_merge_kernel<HDV><<<R * nh, HDV, 0, st>>>(part, nh, splits, out, outh, ldh, frag);        \
         return 0;                                                                                     \
     }
     Q3_ATTN_CASE(128, 1)

@@ -44,7 +44,23 @@ struct GemvArgs {
     int valid_rows;            // rows >= valid_rows (padding) take no part in the argmax
     float* logits;             // optional [B][valid_rows]
     int ksplit;                // kResid only: K split over this many CTAs per tile, summed by atomicAdd (0 = 1)
+    int xfrag;                 // xh is in fragment order (plane_index), else plain [8*NT][K] planes
+    int yfrag;                 // kSiluGate: yh in fragment order
 };
+
+// Activation planes hold column c = 2b + part (part 0 = f16 hi, 1 = lo of
+// sequence b) over K.  Plain order: c * K + k.  Fragment order: the B
+// operand registers of the m16n8k16 MMA, so that a lane's four words for
+// one k-pair (32 k) and one 8-column tile are one 16-byte load:
+// word ((p * 8 + c / 8) * 32 + lane) * 4 + w, lane = 4 (c % 8) + (k % 8) / 2,
+// w = 2 ((k / 16) % 2) + (k / 8) % 2, p = k / 32; half k % 2 of the word.
+// Room for 8 column tiles (32 sequences), as the plain layout.
+__host__ __device__ inline size_t plane_index(int col, int k, int K, int frag) {
+    if (!frag) return (size_t)col * K + k;
+    const size_t word = (((size_t)(k >> 5) * 8 + (col >> 3)) * 32 + ((col & 7) * 4 + ((k & 7) >> 1))) * 4 +
+                        (((k >> 4) & 1) * 2 + ((k >> 3) & 1));
+    return word * 2 + (k & 1);
+}
 
 void launch_gemv(const GemvArgs& a, int mode, int grid, cudaStream_t st);
 int gemv_grid(int rows, int mode, int num_sms);
@@ -53,7 +69,7 @@ void launch_embed(const int32_t* ids, int n, const int8_t* E, const float* sE, i
 
 // RMSNorm of rows (row map optional) -> fp32 rows and/or f16 hi/lo planes.
 void launch_rmsnorm(const float* x, const int32_t* rows, int n, int H, const float* g, float eps, float* xn,
-                    __half* xh, cudaStream_t st);
+                    __half* xh, cudaStream_t st, int frag = 0);
 
 void launch_qk_rope_append(const float* qkv, int R, int nh, int nkv, int hd, const int32_t* row_seq,
                            const int32_t* row_pos, const float* q_norm, const float* k_norm, float eps,
@@ -64,7 +80,8 @@ size_t attn_part_bytes(int R, int nh, int hd, int splits);
 // Attends positions 0 .. row_len[r] + len_add - 1 of sequence row_seq[r].
 int launch_attention(const float* q, const __nv_bfloat16* k, const __nv_bfloat16* v, const int32_t* row_seq,
                      const int32_t* row_len, int len_add, int R, int nh, int nkv, int hd, int cap, int splits,
-                     float* part, float* out, __half* outh, int ldh, int32_t* status, cudaStream_t st);
+                     float* part, float* out, __half* outh, int ldh, int32_t* status, cudaStream_t st,
+                     int frag = 0);
 
 // Causal prefill attention on tensor cores (GROUP == 2, hd == 128): blocks
 // of 32 prompt positions of one sequence, {sequence, first position, flat
