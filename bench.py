@@ -257,6 +257,32 @@ def batched_sweep(q3, dev, hbm_peak, batches=(8, 16, 32)):
     return out
 
 
+def long_jobs(q3, dev, hbm_peak, names=("1.7b-b1-p256-n1024", "0.6b-b1-p4096-n2048")):
+    """One whole job of each B = 1 long workload (after a prefill-only warm-up): prefill tok/s, decode tok/s,
+    mean step time and the decode step's HBM roofline fraction, with the weight / KV split of its bytes."""
+    import torch
+
+    out = {}
+    for name in names:
+        wl = synth.WORKLOADS[name]
+        ml = synth.make_model(wl.shape, wl.weight_seed)
+        pl = synth.prompts(wl)
+        lens = np.array([len(p) for p in pl], np.int32)
+        dec = q3.Decoder(ml, max_batch=len(pl), max_ctx=wl.max_ctx)
+        d_ids = torch.from_numpy(np.concatenate(pl).astype(np.int32)).to(dev)
+        d_out = torch.empty((len(pl), wl.new_tokens), dtype=torch.int32, device=dev)
+        dec.decode_device(d_ids, lens, 2, d_out)
+        st = dec.decode_device(d_ids, lens, wl.new_tokens, d_out)
+        wbytes = wl.shape.weight_bytes()
+        sb = float(np.mean([dec.step_bytes(lens + i) for i in range(0, wl.new_tokens - 1, 16)]))
+        gbs = sb / (st["step_us"] * 1e-6) / 1e9
+        out[name] = {"prefill_tok_s": st["prefill_tokens_per_sec"], "decode_tok_s": st["decode_tokens_per_sec"],
+                     "step_us": st["step_us"], "step_bytes_mean": sb, "weight_bytes": wbytes,
+                     "kv_bytes_mean": sb - wbytes, "achieved_gbs": gbs, "frac": gbs / hbm_peak}
+        dec.close()
+    return out
+
+
 def run_gpu(args, w):
     import torch
 
@@ -315,6 +341,7 @@ def run_gpu(args, w):
 
     # the batched decode workloads (B = 8 / 16 / 32), outside the timed region
     batched = batched_sweep(q3, dev, hbm_peak) if (rank == 0 and not args.no_batched and w.batch == 1) else None
+    longer = long_jobs(q3, dev, hbm_peak) if (rank == 0 and not args.no_batched and w.batch == 1) else None
 
     # e2e through the public API with host buffers
     out_e2e = None
@@ -361,6 +388,7 @@ def run_gpu(args, w):
             "e2e": {"value": e2e_val, "unit": "tok/s", "h2d_bytes_per_step": int(flat.nbytes + 8 * flat.size + 12 * B),
                     "d2h_bytes_per_step": int(n_tok * 4), "ids_match_device_run": same},
             "batched_decode": batched,
+            "long_jobs": longer,
             "gpu_launches": int(launches),
             "wall_s": wall,
             "clocks": clocks,
@@ -382,7 +410,8 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS))
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--no-batched", action="store_true", help="skip the B = 8 / 16 / 32 decode jobs")
+    ap.add_argument("--no-batched", action="store_true",
+                    help="skip the extra jobs (B = 8 / 16 / 32 decode, the 1.7B and long-context jobs)")
     ap.add_argument("--new-tokens", type=int, default=None,
                     help="override the workload's generated tokens per sequence (e.g. to profile its prefill)")
     args = ap.parse_args()

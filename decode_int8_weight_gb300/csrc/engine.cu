@@ -431,7 +431,7 @@ extern "C" void q3i8_destroy(q3i8_ctx* c) {
 // ------------------------------------------------------------------ the decode step
 
 int decode_splits(const q3i8_ctx* c, int B) {
-    int s = (2 * c->num_sms + B * c->d.n_kv_heads - 1) / (B * c->d.n_kv_heads);
+    int s = (8 * c->num_sms + B * c->d.n_kv_heads - 1) / (B * c->d.n_kv_heads);
     s = std::min(s, c->cap / kChunkPos);
     s = std::min(s, c->dec_splits_max);
     return std::max(s, 1);
