@@ -79,7 +79,7 @@ typedef struct q3i8_dims {
     int32_t vocab;              /* V (tied embedding rows) */
     float rope_theta;           /* 1e6 for Qwen3 */
     float rms_eps;              /* 1e-6 for Qwen3 */
-    int32_t max_batch;          /* most sequences per call, 1..64 */
+    int32_t max_batch;          /* most sequences per call, 1..32 */
     int32_t max_ctx;            /* initial per-sequence KV capacity in positions
                                    (0 means 512); raised automatically up to
                                    65,536 when a call needs more */
