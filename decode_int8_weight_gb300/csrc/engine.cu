@@ -458,10 +458,9 @@ void enqueue_step(q3i8_ctx* c, int B, bool want_logits) {
         a.w = L.qkv.frag, a.scale = L.qkv.scale, a.rows = L.qkv.rows, a.K = H, a.xh = c->xh, a.xfrag = 1;
         a.y = c->qkv, a.ldy = L.qkv.rows;
         launch_gemv(a, kStore, gemv_grid(a.rows, kStore, c->num_sms), st);
-        launch_qk_rope_append(c->qkv, B, nh, nkv, hd, c->seq_ids, c->pos, L.q_norm, L.k_norm, d.rms_eps, c->rope,
-                              c->qr, c->kc + l * layer_kv, c->vc + l * layer_kv, c->cap, st);
-        launch_attention(c->qr, c->kc + l * layer_kv, c->vc + l * layer_kv, c->seq_ids, c->pos, 1, B, nh, nkv, hd,
-                         c->cap, splits, c->part, nullptr, c->oh, Dq, c->status, st, 1);
+        launch_attention_decode(c->qkv, L.q_norm, L.k_norm, d.rms_eps, c->rope, c->kc + l * layer_kv,
+                                c->vc + l * layer_kv, c->seq_ids, c->pos, B, nh, nkv, hd, c->cap, splits, c->part,
+                                c->oh, Dq, c->status, st, 1);
         a = GemvArgs{};
         a.B = B;
         a.w = L.o.frag, a.scale = L.o.scale, a.rows = L.o.rows, a.K = Dq, a.xh = c->oh, a.xfrag = 1;
@@ -613,7 +612,7 @@ static int enqueue_decode_step(q3i8_ctx* c, int B, bool want_logits) {
     return Q3_OK;
 }
 
-int step_launches(const q3i8_ctx* c, int B) { return persistent_for(c, B) ? 1 : 2 + c->d.n_layers * 9 + 1; }
+int step_launches(const q3i8_ctx* c, int B) { return persistent_for(c, B) ? 1 : 2 + c->d.n_layers * 8 + 1; }
 // Kernels of one prefill over M prompt rows: embed; per layer 2 RMSNorms, the
 // QK-norm/RoPE/append, attention split + merge and the 4 projections (one
 // tensor-core GEMM each, or one GEMV per chunk of kPrefillChunk rows); final

@@ -336,44 +336,19 @@ struct AttnSmem {
     uint64_t bar[2];
 };
 
+// The chunk loop shared by the decode attention kernels: positions
+// [start, end) of one (sequence, kv head) in chunks of kChunk, staged two
+// at a time by bulk copies; each warp folds its 16 positions of a chunk into
+// its own online-softmax state (m, l, acc) for the GROUP query heads.
+// False when a bounded wait gave up (the status is set, copies drained).
 template <int HD, int GROUP>
-__global__ void __launch_bounds__(128) attn_split_kernel(const float* q, const __nv_bfloat16* kc,
-                                                         const __nv_bfloat16* vc, const int32_t* row_seq,
-                                                         const int32_t* row_len, int len_add, int nh, int nkv,
-                                                         int cap, int splits, float* part, int32_t* status) {
-    constexpr int D = HD / 32;  // dims per lane
-    extern __shared__ __align__(128) unsigned char smem_raw[];
-    AttnSmem<HD>& sm = *reinterpret_cast<AttnSmem<HD>*>(smem_raw);
-    __shared__ float wm[4][GROUP], wl[4][GROUP];
-    __shared__ float wacc[4][GROUP][HD];
-
-    const int sp = blockIdx.x, g = blockIdx.y, r = blockIdx.z;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int len = row_len[r] + len_add, seq = row_seq[r];
-    int per = (len + splits - 1) / splits;
-    per = (per + kChunk - 1) / kChunk * kChunk;
-    const int start = sp * per;
-    const int end = min(len, start + per);
-    float* outp = part + ((size_t)r * nh + (size_t)g * GROUP) * splits * (HD + 2);
-    if (start >= end) {
-        for (int i = threadIdx.x; i < GROUP * (HD + 2); i += blockDim.x) {
-            const int h = i / (HD + 2), e = i % (HD + 2);
-            outp[((size_t)h * splits + sp) * (HD + 2) + e] = (e == HD) ? -INFINITY : 0.f;
-        }
-        return;
-    }
-    const int nchunks = (end - start + kChunk - 1) / kChunk;
-    const size_t head_base = ((size_t)seq * nkv + g) * cap * HD;
-    const __nv_bfloat16* kb = kc + head_base + (size_t)start * HD;
-    const __nv_bfloat16* vb = vc + head_base + (size_t)start * HD;
+Q3_DEV bool attn_chunks(AttnSmem<HD>& sm, const __nv_bfloat16* kb, const __nv_bfloat16* vb, int start, int end,
+                            const float (&qr)[GROUP][HD / 32], float scale, float (&m)[GROUP], float (&l)[GROUP],
+                            float (&acc)[GROUP][HD / 32], int32_t* status) {
+    constexpr int D = HD / 32;
     constexpr uint32_t kBytes = kChunk * HD * 2;
-
-    if (threadIdx.x == 0) {
-        mbar_init(&sm.bar[0], 1);
-        mbar_init(&sm.bar[1], 1);
-        fence_mbar_init();
-    }
-    __syncthreads();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nchunks = end > start ? (end - start + kChunk - 1) / kChunk : 0;
     if (threadIdx.x == 0) {
         for (int c = 0; c < 2 && c < nchunks; ++c) {
             mbar_arrive_expect_tx(&sm.bar[c], 2 * kBytes);
@@ -381,22 +356,6 @@ __global__ void __launch_bounds__(128) attn_split_kernel(const float* q, const _
             bulk_g2s(sm.v[c], vb + (size_t)c * kChunk * HD, kBytes, &sm.bar[c]);
         }
     }
-
-    float qr[GROUP][D];
-#pragma unroll
-    for (int h = 0; h < GROUP; ++h)
-#pragma unroll
-        for (int d = 0; d < D; ++d) qr[h][d] = q[((size_t)r * nh + g * GROUP + h) * HD + lane * D + d];
-    const float scale = 1.0f / sqrtf((float)HD);
-    float m[GROUP], l[GROUP], acc[GROUP][D];
-#pragma unroll
-    for (int h = 0; h < GROUP; ++h) {
-        m[h] = -INFINITY;
-        l[h] = 0.f;
-#pragma unroll
-        for (int d = 0; d < D; ++d) acc[h][d] = 0.f;
-    }
-
     bool ok = true;
     for (int c = 0; c < nchunks; ++c) {
         const int s = c & 1;
@@ -458,16 +417,22 @@ __global__ void __launch_bounds__(128) attn_split_kernel(const float* q, const _
             bulk_g2s(sm.v[s], vb + (size_t)(c + 2) * kChunk * HD, kBytes, &sm.bar[s]);
         }
     }
-    if (!ok) {
-        // a bounded wait gave up: record it, give the other copy a bounded
-        // chance to land, and leave without writing results
-        if (threadIdx.x == 0) {
-            set_status(status, kStatusTimeout);
-            for (int s = 0; s < 2; ++s) mbar_wait_bounded(&sm.bar[s], 0);
-        }
-        return;
+    if (!ok && threadIdx.x == 0) {
+        // a bounded wait gave up: record it and give the other copy a bounded chance to land
+        set_status(status, kStatusTimeout);
+        for (int s = 0; s < 2; ++s) mbar_wait_bounded(&sm.bar[s], 0);
     }
-    // merge the four warps' online-softmax states
+    return ok;
+}
+
+// Merge the four warps' online-softmax states and write this split's
+// partial state {acc[HD], m, l} per query head.
+template <int HD, int GROUP>
+Q3_DEV void attn_write_partial(const float (&m)[GROUP], const float (&l)[GROUP], const float (&acc)[GROUP][HD / 32],
+                                   float (&wm)[4][GROUP], float (&wl)[4][GROUP], float (&wacc)[4][GROUP][HD],
+                                   float* outp, int splits, int sp) {
+    constexpr int D = HD / 32;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (lane == 0)
         for (int h = 0; h < GROUP; ++h) {
             wm[warp][h] = m[h];
@@ -496,6 +461,184 @@ __global__ void __launch_bounds__(128) attn_split_kernel(const float* q, const _
             o[HD + 1] = L;
         }
     }
+}
+
+// Split s of row r attends positions [start, end) of its sequence with
+// queries that are already normed and rotated.
+template <int HD, int GROUP>
+__global__ void __launch_bounds__(128) attn_split_kernel(const float* q, const __nv_bfloat16* kc,
+                                                         const __nv_bfloat16* vc, const int32_t* row_seq,
+                                                         const int32_t* row_len, int len_add, int nh, int nkv,
+                                                         int cap, int splits, float* part, int32_t* status) {
+    constexpr int D = HD / 32;  // dims per lane
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    AttnSmem<HD>& sm = *reinterpret_cast<AttnSmem<HD>*>(smem_raw);
+    __shared__ float wm[4][GROUP], wl[4][GROUP];
+    __shared__ float wacc[4][GROUP][HD];
+
+    const int sp = blockIdx.x, g = blockIdx.y, r = blockIdx.z;
+    const int lane = threadIdx.x & 31;
+    const int len = row_len[r] + len_add, seq = row_seq[r];
+    int per = (len + splits - 1) / splits;
+    per = (per + kChunk - 1) / kChunk * kChunk;
+    const int start = sp * per;
+    const int end = min(len, start + per);
+    float* outp = part + ((size_t)r * nh + (size_t)g * GROUP) * splits * (HD + 2);
+    if (start >= end) {
+        for (int i = threadIdx.x; i < GROUP * (HD + 2); i += blockDim.x) {
+            const int h = i / (HD + 2), e = i % (HD + 2);
+            outp[((size_t)h * splits + sp) * (HD + 2) + e] = (e == HD) ? -INFINITY : 0.f;
+        }
+        return;
+    }
+    const size_t head_base = ((size_t)seq * nkv + g) * cap * HD;
+    if (threadIdx.x == 0) {
+        mbar_init(&sm.bar[0], 1);
+        mbar_init(&sm.bar[1], 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    float qr[GROUP][D];
+#pragma unroll
+    for (int h = 0; h < GROUP; ++h)
+#pragma unroll
+        for (int d = 0; d < D; ++d) qr[h][d] = q[((size_t)r * nh + g * GROUP + h) * HD + lane * D + d];
+    const float scale = 1.0f / sqrtf((float)HD);
+    float m[GROUP], l[GROUP], acc[GROUP][D];
+#pragma unroll
+    for (int h = 0; h < GROUP; ++h) {
+        m[h] = -INFINITY;
+        l[h] = 0.f;
+#pragma unroll
+        for (int d = 0; d < D; ++d) acc[h][d] = 0.f;
+    }
+    if (!attn_chunks<HD, GROUP>(sm, kc + head_base + (size_t)start * HD, vc + head_base + (size_t)start * HD, start,
+                                end, qr, scale, m, l, acc, status))
+        return;
+    attn_write_partial<HD, GROUP>(m, l, acc, wm, wl, wacc, outp, splits, sp);
+}
+
+// Decode step with the QK-RMSNorm, RoPE and KV append folded in: row r's new
+// position p = row_pos[r] is appended (bf16, by the split that owns p) and
+// attended from registers, so the cache reads cover positions < p only.
+template <int HD, int GROUP>
+__global__ void __launch_bounds__(128) attn_decode_kernel(const float* qkv, const float* q_norm, const float* k_norm,
+                                                          float eps, const float2* rope_cs, __nv_bfloat16* kc,
+                                                          __nv_bfloat16* vc, const int32_t* row_seq,
+                                                          const int32_t* row_pos, int nh, int nkv, int cap,
+                                                          int splits, float* part, int32_t* status) {
+    constexpr int D = HD / 32;
+    constexpr int E = HD / 32;
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    AttnSmem<HD>& sm = *reinterpret_cast<AttnSmem<HD>*>(smem_raw);
+    __shared__ float wm[4][GROUP], wl[4][GROUP];
+    __shared__ float wacc[4][GROUP][HD];
+    __shared__ float qs[GROUP][HD], kp[HD], vp[HD];
+
+    const int sp = blockIdx.x, g = blockIdx.y, r = blockIdx.z;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int pos = row_pos[r], seq = row_seq[r];
+    const int len = pos + 1;
+    int per = (len + splits - 1) / splits;
+    per = (per + kChunk - 1) / kChunk * kChunk;
+    const int start = sp * per;
+    const int end = min(len, start + per);
+    float* outp = part + ((size_t)r * nh + (size_t)g * GROUP) * splits * (HD + 2);
+    if (start >= end) {
+        for (int i = threadIdx.x; i < GROUP * (HD + 2); i += blockDim.x) {
+            const int h = i / (HD + 2), e = i % (HD + 2);
+            outp[((size_t)h * splits + sp) * (HD + 2) + e] = (e == HD) ? -INFINITY : 0.f;
+        }
+        return;
+    }
+    const bool owns_p = pos >= start && pos < end;
+    const size_t head_base = ((size_t)seq * nkv + g) * cap * HD;
+    if (threadIdx.x == 0) {
+        mbar_init(&sm.bar[0], 1);
+        mbar_init(&sm.bar[1], 1);
+        fence_mbar_init();
+    }
+    // the group's queries (and, in the owning split, the new K and V): one
+    // warp per head, lane l holding elements l + 32j
+    const float* row = qkv + (size_t)r * (nh + 2 * nkv) * HD;
+    const float2* cs = rope_cs + (size_t)pos * (HD / 2);
+    for (int h = warp; h < GROUP + (owns_p ? 2 : 0); h += 4) {
+        const bool is_v = h == GROUP + 1;
+        const float* src = h < GROUP ? row + (size_t)(g * GROUP + h) * HD
+                                     : row + (size_t)((is_v ? nh + nkv : nh) + g) * HD;
+        float v[E];
+#pragma unroll
+        for (int j = 0; j < E; ++j) v[j] = src[lane + 32 * j];
+        if (!is_v) {
+            const float* gain = h < GROUP ? q_norm : k_norm;
+            float ss = 0.f;
+#pragma unroll
+            for (int j = 0; j < E; ++j) ss += v[j] * v[j];
+            ss = warp_sum(ss);
+            const float inv = 1.0f / sqrtf(ss / (float)HD + eps);
+#pragma unroll
+            for (int j = 0; j < E; ++j) v[j] = __fmul_rn(__fmul_rn(v[j], inv), gain[lane + 32 * j]);
+#pragma unroll
+            for (int j = 0; j < E / 2; ++j) {
+                const float2 c = cs[lane + 32 * j];
+                const float a0 = v[j], b0 = v[j + E / 2];
+                v[j] = __fsub_rn(__fmul_rn(a0, c.x), __fmul_rn(b0, c.y));
+                v[j + E / 2] = __fadd_rn(__fmul_rn(b0, c.x), __fmul_rn(a0, c.y));
+            }
+        }
+        if (h < GROUP) {
+#pragma unroll
+            for (int j = 0; j < E; ++j) qs[h][lane + 32 * j] = v[j];
+        } else {
+            __nv_bfloat16* dst = (is_v ? vc : kc) + head_base + (size_t)pos * HD;
+            float* keep = is_v ? vp : kp;
+#pragma unroll
+            for (int j = 0; j < E; ++j) {
+                const __nv_bfloat16 b = __float2bfloat16_rn(v[j]);
+                dst[lane + 32 * j] = b;
+                keep[lane + 32 * j] = __bfloat162float(b);
+            }
+        }
+    }
+    __syncthreads();
+
+    float qr[GROUP][D];
+#pragma unroll
+    for (int h = 0; h < GROUP; ++h)
+#pragma unroll
+        for (int d = 0; d < D; ++d) qr[h][d] = qs[h][lane * D + d];
+    const float scale = 1.0f / sqrtf((float)HD);
+    float m[GROUP], l[GROUP], acc[GROUP][D];
+#pragma unroll
+    for (int h = 0; h < GROUP; ++h) {
+        m[h] = -INFINITY;
+        l[h] = 0.f;
+#pragma unroll
+        for (int d = 0; d < D; ++d) acc[h][d] = 0.f;
+    }
+    const int cend = owns_p ? pos : end;  // cached positions only
+    if (!attn_chunks<HD, GROUP>(sm, kc + head_base + (size_t)start * HD, vc + head_base + (size_t)start * HD, start,
+                                cend, qr, scale, m, l, acc, status))
+        return;
+    if (owns_p && warp == 0) {
+        // position p from the rounded values kept in shared memory
+#pragma unroll
+        for (int h = 0; h < GROUP; ++h) {
+            float dot = 0.f;
+#pragma unroll
+            for (int d = 0; d < D; ++d) dot += qr[h][d] * kp[lane * D + d];
+            const float sc = warp_sum(dot) * scale;
+            const float mn = fmaxf(m[h], sc);
+            const float corr = (m[h] == -INFINITY) ? 0.f : expf(m[h] - mn);
+            const float pe = expf(sc - mn);
+            l[h] = l[h] * corr + pe;
+#pragma unroll
+            for (int d = 0; d < D; ++d) acc[h][d] = acc[h][d] * corr + pe * vp[lane * D + d];
+            m[h] = mn;
+        }
+    }
+    attn_write_partial<HD, GROUP>(m, l, acc, wm, wl, wacc, outp, splits, sp);
 }
 
 // out[r][h][:] = sum_s acc_s e^{m_s - M} / sum_s l_s e^{m_s - M}
@@ -565,6 +708,47 @@ int launch_attention(const float* q, const __nv_bfloat16* k, const __nv_bfloat16
     Q3_ATTN_CASE(64, 8)
 #undef Q3_ATTN_CASE
     return -1;  // unsupported head_dim / group
+}
+
+template <int HD, int GROUP>
+static void launch_attn_decode_t(const float* qkv, const float* q_norm, const float* k_norm, float eps,
+                                 const float2* rope_cs, __nv_bfloat16* kc, __nv_bfloat16* vc, const int32_t* row_seq,
+                                 const int32_t* row_pos, int R, int nh, int nkv, int cap, int splits, float* part,
+                                 int32_t* status, cudaStream_t st) {
+    static bool attr_set = false;
+    const int smem = (int)sizeof(AttnSmem<HD>);
+    if (!attr_set) {
+        cudaFuncSetAttribute(attn_decode_kernel<HD, GROUP>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        attr_set = true;
+    }
+    dim3 grid(splits, nkv, R);
+    attn_decode_kernel<HD, GROUP><<<grid, 128, smem, st>>>(qkv, q_norm, k_norm, eps, rope_cs, kc, vc, row_seq, row_pos,
+                                                           nh, nkv, cap, splits, part, status);
+}
+
+int launch_attention_decode(const float* qkv, const float* q_norm, const float* k_norm, float eps,
+                            const float2* rope_cs, __nv_bfloat16* kc, __nv_bfloat16* vc, const int32_t* row_seq,
+                            const int32_t* row_pos, int R, int nh, int nkv, int hd, int cap, int splits, float* part,
+                            __half* outh, int ldh, int32_t* status, cudaStream_t st, int frag) {
+    if (R <= 0) return 0;
+    const int group = nh / nkv;
+#define Q3_ATTN_CASE(HDV, GV)                                                                                      \
+    if (hd == HDV && group == GV) {                                                                                \
+        launch_attn_decode_t<HDV, GV>(qkv, q_norm, k_norm, eps, rope_cs, kc, vc, row_seq, row_pos, R, nh, nkv, cap, \
+                                      splits, part, status, st);                                                   \
+        attn_merge_kernel<HDV><<<R * nh, HDV, 0, st>>>(part, nh, splits, nullptr, outh, ldh, frag);                \
+        return 0;                                                                                                  \
+    }
+    Q3_ATTN_CASE(128, 1)
+    Q3_ATTN_CASE(128, 2)
+    Q3_ATTN_CASE(128, 4)
+    Q3_ATTN_CASE(128, 8)
+    Q3_ATTN_CASE(64, 1)
+    Q3_ATTN_CASE(64, 2)
+    Q3_ATTN_CASE(64, 4)
+    Q3_ATTN_CASE(64, 8)
+#undef Q3_ATTN_CASE
+    return -1;
 }
 
 

@@ -83,6 +83,15 @@ int launch_attention(const float* q, const __nv_bfloat16* k, const __nv_bfloat16
                      float* part, float* out, __half* outh, int ldh, int32_t* status, cudaStream_t st,
                      int frag = 0);
 
+// One decode step's attention with the QK-RMSNorm, RoPE and bf16 KV append
+// folded in: qkv [R][(nh + 2 nkv) hd] fp32 as projected, row_pos[r] the new
+// position (appended, then attended with positions 0..row_pos[r]); output
+// hi/lo f16 planes (outh, ldh, frag as launch_attention).
+int launch_attention_decode(const float* qkv, const float* q_norm, const float* k_norm, float eps,
+                            const float2* rope_cs, __nv_bfloat16* kc, __nv_bfloat16* vc, const int32_t* row_seq,
+                            const int32_t* row_pos, int R, int nh, int nkv, int hd, int cap, int splits, float* part,
+                            __half* outh, int ldh, int32_t* status, cudaStream_t st, int frag);
+
 // Causal prefill attention on tensor cores (GROUP == 2, hd == 128): blocks
 // of 32 prompt positions of one sequence, {sequence, first position, flat
 // row of the sequence's position 0, length}, built by attn_prefill_blocks
