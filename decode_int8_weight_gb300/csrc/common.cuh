@@ -151,6 +151,15 @@ Q3_DEV uint2 lds64(uint32_t a) {
     return r;
 }
 
+// ------------------------------------------------------------- programmatic dependent launch
+// A kernel launched with programmatic stream serialization may start while
+// the previous kernel in the stream is still running.  It lets its own
+// successor be scheduled at once (pdl_launch_dependents) and waits until
+// every kernel it depends on has completed and its writes are visible
+// (pdl_wait) before touching memory.  Both are no-ops for a plain launch.
+Q3_DEV void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+Q3_DEV void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ------------------------------------------------------------- misc
 Q3_DEV float warp_sum(float v) {
 #pragma unroll

@@ -36,6 +36,8 @@ size_t packed_offset(int row, int k, int K) {
 // =====================================================================
 template <int NT, int MODE>
 __global__ void __launch_bounds__(256) gemv_kernel(GemvArgs a) {
+    pdl_launch_dependents();
+    pdl_wait();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, t = lane & 3;
     const int n_tiles = a.rows >> 4;
@@ -164,13 +166,29 @@ __global__ void __launch_bounds__(256) gemv_kernel(GemvArgs a) {
     }
 }
 
+// Launch with programmatic stream serialization (see pdl_wait).
+template <typename... KArgs, typename... Args>
+static void launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 template <int NT>
 static void launch_gemv_nt(const GemvArgs& a, int mode, int grid, cudaStream_t st) {
     switch (mode) {
-        case kStore: gemv_kernel<NT, kStore><<<grid, 256, 0, st>>>(a); break;
-        case kResid: gemv_kernel<NT, kResid><<<grid, 256, 0, st>>>(a); break;
-        case kSiluGate: gemv_kernel<NT, kSiluGate><<<grid, 256, 0, st>>>(a); break;
-        default: gemv_kernel<NT, kArgmax><<<grid, 256, 0, st>>>(a); break;
+        case kStore: launch_pdl(gemv_kernel<NT, kStore>, grid, 256, 0, st, a); break;
+        case kResid: launch_pdl(gemv_kernel<NT, kResid>, grid, 256, 0, st, a); break;
+        case kSiluGate: launch_pdl(gemv_kernel<NT, kSiluGate>, grid, 256, 0, st, a); break;
+        default: launch_pdl(gemv_kernel<NT, kArgmax>, grid, 256, 0, st, a); break;
     }
 }
 
@@ -192,6 +210,8 @@ int gemv_grid(int rows, int mode, int num_sms) {
 // Embedding gather from the tied int8 table: x = float(q[tok]) * s[tok].
 // =====================================================================
 __global__ void embed_kernel(const int32_t* ids, const int8_t* E, const float* sE, int H, float* x) {
+    pdl_launch_dependents();
+    pdl_wait();
     const int r = blockIdx.x;
     const int tok = ids[r];
     const float s = sE[tok];
@@ -200,7 +220,7 @@ __global__ void embed_kernel(const int32_t* ids, const int8_t* E, const float* s
 }
 
 void launch_embed(const int32_t* ids, int n, const int8_t* E, const float* sE, int H, float* x, cudaStream_t st) {
-    if (n > 0) embed_kernel<<<n, 256, 0, st>>>(ids, E, sE, H, x);
+    if (n > 0) launch_pdl(embed_kernel, n, 256, 0, st, ids, E, sE, H, x);
 }
 
 // =====================================================================
@@ -209,6 +229,8 @@ void launch_embed(const int32_t* ids, int n, const int8_t* E, const float* sE, i
 // =====================================================================
 __global__ void rmsnorm_kernel(const float* x, const int32_t* rows, int H, const float* g, float eps, float* xn,
                                __half* xh, int frag) {
+    pdl_launch_dependents();
+    pdl_wait();
     __shared__ float part[32];
     __shared__ float s_inv;
     const int i = blockIdx.x;
@@ -240,7 +262,7 @@ __global__ void rmsnorm_kernel(const float* x, const int32_t* rows, int H, const
 
 void launch_rmsnorm(const float* x, const int32_t* rows, int n, int H, const float* g, float eps, float* xn,
                     __half* xh, cudaStream_t st, int frag) {
-    if (n > 0) rmsnorm_kernel<<<n, 256, 0, st>>>(x, rows, H, g, eps, xn, xh, frag);
+    if (n > 0) launch_pdl(rmsnorm_kernel, n, 256, 0, st, x, rows, H, g, eps, xn, xh, frag);
 }
 
 // =====================================================================
@@ -528,6 +550,8 @@ __global__ void __launch_bounds__(128) attn_decode_kernel(const float* qkv, cons
                                                           __nv_bfloat16* vc, const int32_t* row_seq,
                                                           const int32_t* row_pos, int nh, int nkv, int cap,
                                                           int splits, float* part, int32_t* status) {
+    pdl_launch_dependents();
+    pdl_wait();
     constexpr int D = HD / 32;
     constexpr int E = HD / 32;
     extern __shared__ __align__(128) unsigned char smem_raw[];
@@ -645,6 +669,8 @@ __global__ void __launch_bounds__(128) attn_decode_kernel(const float* qkv, cons
 template <int HD>
 __global__ void attn_merge_kernel(const float* part, int nh, int splits, float* out, __half* outh, int ldh,
                                   int frag) {
+    pdl_launch_dependents();
+    pdl_wait();
     const int rh = blockIdx.x;  // r * nh + h
     const int d = threadIdx.x;
     const float* p = part + (size_t)rh * splits * (HD + 2);
@@ -722,8 +748,8 @@ static void launch_attn_decode_t(const float* qkv, const float* q_norm, const fl
         attr_set = true;
     }
     dim3 grid(splits, nkv, R);
-    attn_decode_kernel<HD, GROUP><<<grid, 128, smem, st>>>(qkv, q_norm, k_norm, eps, rope_cs, kc, vc, row_seq, row_pos,
-                                                           nh, nkv, cap, splits, part, status);
+    launch_pdl(attn_decode_kernel<HD, GROUP>, grid, 128, smem, st, qkv, q_norm, k_norm, eps, rope_cs, kc, vc, row_seq,
+               row_pos, nh, nkv, cap, splits, part, status);
 }
 
 int launch_attention_decode(const float* qkv, const float* q_norm, const float* k_norm, float eps,
@@ -736,7 +762,7 @@ int launch_attention_decode(const float* qkv, const float* q_norm, const float* 
     if (hd == HDV && group == GV) {                                                                                \
         launch_attn_decode_t<HDV, GV>(qkv, q_norm, k_norm, eps, rope_cs, kc, vc, row_seq, row_pos, R, nh, nkv, cap, \
                                       splits, part, status, st);                                                   \
-        attn_merge_kernel<HDV><<<R * nh, HDV, 0, st>>>(part, nh, splits, nullptr, outh, ldh, frag);                \
+        launch_pdl(attn_merge_kernel<HDV>, R * nh, HDV, 0, st, part, nh, splits, (float*)nullptr, outh, ldh, frag); \
         return 0;                                                                                                  \
     }
     Q3_ATTN_CASE(128, 1)
