@@ -34,16 +34,16 @@ sys.path.insert(0, ROOT)
 
 import synth  # noqa: E402
 
-# DRAM bytes (read + write) of one decode-step launch, from an ncu capture of
-# the persistent step kernel (profiles/persistent_step_0.6b-b1-p32-n128.md).
-# A figure holds only for the kernel sources it was taken on, identified by
+# DRAM bytes (read + write) of one decode step (the graph's kernels summed),
+# from an ncu capture (profiles/chained_step_0.6b-b1-p32-n128.md).  A figure
+# holds only for the sources it was taken on, identified by
 # kernel_source_id(); for any other build the roofline reports null.
-NCU_TRAFFIC = {("eb5ac27c3e230ed5", "0.6b-b1-p32-n128", 1): 610_962_432}
+NCU_TRAFFIC = {("aef8b9c30d82e33a", "0.6b-b1-p32-n128", 1): 615_049_216}
 
 
 def kernel_source_id() -> str:
     h = hashlib.sha256()
-    for f in ("persistent.cu", "persistent.h", "common.cuh"):
+    for f in ("kernels.cu", "kernels.h", "common.cuh", "engine.cu"):
         with open(os.path.join(ROOT, "decode_int8_weight_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]

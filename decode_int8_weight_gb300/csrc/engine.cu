@@ -544,11 +544,12 @@ int persistent_setup(q3i8_ctx* c) {
     const uint32_t one = 1;
     CK(c, cudaMemcpy(c->p_epoch, &one, 4, cudaMemcpyHostToDevice));
     c->use_persistent = true;
-    // B <= 4 stages each phase's whole input in shared memory and is the
-    // measured winner; at B >= 8 the chained kernels are faster (the
-    // persistent path then reads its operands from the flagged words)
-    c->p_max_batch = 4;
-    if (const char* mb = getenv("Q3I8_PERSISTENT_MAX_BATCH")) c->p_max_batch = std::max(1, atoi(mb));
+    // Measured on GB300 (0.6B shape): the chained kernels with programmatic
+    // dependent launch decode faster at every batch (B = 1: 1.01 vs 1.09 ms
+    // per step; B = 8: 1.0 vs 2.0 ms), so by default no batch takes the
+    // persistent kernel; Q3I8_PERSISTENT_MAX_BATCH selects it up to that B.
+    c->p_max_batch = 0;
+    if (const char* mb = getenv("Q3I8_PERSISTENT_MAX_BATCH")) c->p_max_batch = std::max(0, atoi(mb));
     return Q3_OK;
 }
 

@@ -67,7 +67,7 @@ struct q3i8_ctx {
 
     // persistent decode step (one cooperative kernel per step)
     bool use_persistent = false;
-    int p_max_batch = 4;  // largest B decoded by the persistent kernel; larger B take the chained kernels
+    int p_max_batch = 0;  // largest B decoded by the persistent kernel; larger B take the chained kernels
     int p_grid = 0, p_ns = 0, p_kmax = 0, p_optin = 0;
     const uint8_t** d_mats = nullptr;     // device [L*4]
     const float** d_gains = nullptr;      // device [L*4]

@@ -113,6 +113,26 @@ def test_0p6b_b8_ragged(pkg):
     _teacher_forced_check(pkg, "0.6b-b8-p16to256-n128", steps=24)
 
 
+def test_0p6b_b1_persistent_kernel(pkg, monkeypatch):
+    # the persistent step kernel (staged operands, B <= 4) on the full job
+    monkeypatch.setenv("Q3I8_PERSISTENT_MAX_BATCH", "4")
+    worst, _ = _teacher_forced_check(pkg, "0.6b-b1-p32-n128")
+    print("persistent 0.6b b1 max |dlogit|", worst)
+
+
+def test_tiny_persistent_kernel_deterministic(pkg, monkeypatch):
+    monkeypatch.setenv("Q3I8_PERSISTENT_MAX_BATCH", "4")
+    _teacher_forced_check(pkg, "tiny-b1-p8-n16")
+    w = synth.WORKLOADS["tiny-b1-p8-n16"]
+    m, _ = model_for(w.name)
+    dec = pkg.Decoder(m, max_batch=1, max_ctx=w.max_ctx)
+    p = synth.prompts(w)
+    a, _, _ = dec.decode(p, 16)
+    b, _, _ = dec.decode(p, 16)
+    assert np.array_equal(a, b)
+    dec.close()
+
+
 def test_0p6b_b8_persistent_operands_from_words(pkg, monkeypatch):
     # B > 4 decodes with the chained kernels by default; this keeps the
     # persistent kernel's wide-batch path (operands read from the flagged
