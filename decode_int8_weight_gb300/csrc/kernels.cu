@@ -665,27 +665,43 @@ __global__ void __launch_bounds__(128) attn_decode_kernel(const float* qkv, cons
     attn_write_partial<HD, GROUP>(m, l, acc, wm, wl, wacc, outp, splits, sp);
 }
 
-// out[r][h][:] = sum_s acc_s e^{m_s - M} / sum_s l_s e^{m_s - M}
+// out[r][h][:] = sum_s acc_s e^{m_s - M} / sum_s l_s e^{m_s - M} over the
+// row's non-empty splits (the split kernels' range rule); the split weights
+// are computed once per block by warp 0, then every thread sums its column.
 template <int HD>
-__global__ void attn_merge_kernel(const float* part, int nh, int splits, float* out, __half* outh, int ldh,
-                                  int frag) {
+__global__ void attn_merge_kernel(const float* part, int nh, int splits, const int32_t* row_len, int len_add,
+                                  float* out, __half* outh, int ldh, int frag) {
     pdl_launch_dependents();
     pdl_wait();
+    __shared__ float sm_m[64], sm_f[64];
+    __shared__ float s_l;
     const int rh = blockIdx.x;  // r * nh + h
     const int d = threadIdx.x;
-    const float* p = part + (size_t)rh * splits * (HD + 2);
-    float M = -INFINITY;
-    for (int s = 0; s < splits; ++s) M = fmaxf(M, p[(size_t)s * (HD + 2) + HD]);
-    float L = 0.f, A = 0.f;
-    for (int s = 0; s < splits; ++s) {
-        const float ms = p[(size_t)s * (HD + 2) + HD];
-        if (ms == -INFINITY) continue;
-        const float f = expf(ms - M);
-        L += p[(size_t)s * (HD + 2) + HD + 1] * f;
-        A += p[(size_t)s * (HD + 2) + d] * f;
-    }
-    const float o = A / L;
     const int r = rh / nh, h = rh % nh;
+    const int len = row_len[r] + len_add;
+    int per = (len + splits - 1) / splits;
+    per = (per + kChunk - 1) / kChunk * kChunk;
+    const int nne = min(splits, (len + per - 1) / per);
+    const float* p = part + (size_t)rh * splits * (HD + 2);
+    if (d < 32) {
+        // lane j holds splits j and j + 32
+        const float m0 = d < nne ? p[(size_t)d * (HD + 2) + HD] : -INFINITY;
+        const float m1 = d + 32 < nne ? p[(size_t)(d + 32) * (HD + 2) + HD] : -INFINITY;
+        const float M = warp_max(fmaxf(m0, m1));
+        const float f0 = m0 == -INFINITY ? 0.f : expf(m0 - M);
+        const float f1 = m1 == -INFINITY ? 0.f : expf(m1 - M);
+        const float l0 = f0 != 0.f ? p[(size_t)d * (HD + 2) + HD + 1] * f0 : 0.f;
+        const float l1 = f1 != 0.f ? p[(size_t)(d + 32) * (HD + 2) + HD + 1] * f1 : 0.f;
+        const float L = warp_sum(l0 + l1);
+        if (d < nne) sm_m[d] = m0, sm_f[d] = f0;
+        if (d + 32 < nne) sm_m[d + 32] = m1, sm_f[d + 32] = f1;
+        if (d == 0) s_l = L;
+    }
+    __syncthreads();
+    float A = 0.f;
+    for (int s2 = 0; s2 < nne; ++s2)
+        if (sm_m[s2] != -INFINITY) A += p[(size_t)s2 * (HD + 2) + d] * sm_f[s2];
+    const float o = A / s_l;
     if (out) out[(size_t)rh * HD + d] = o;
     if (outh) {
         __half hi, lo;
@@ -721,7 +737,8 @@ int launch_attention(const float* q, const __nv_bfloat16* k, const __nv_bfloat16
 #define Q3_ATTN_CASE(HDV, GV)                                                                         \
     if (hd == HDV && group == GV) {                                                                   \
         launch_attn_t<HDV, GV>(q, k, v, row_seq, row_len, len_add, R, nh, nkv, cap, splits, part, status, st); \
-        attn_merge_kernel<HDV><<<R * nh, HDV, 0, st>>>(part, nh, splits, out, outh, ldh, frag);        \
+        attn_merge_kernel<HDV><<<R * nh, HDV, 0, st>>>(part, nh, splits, row_len, len_add, out, outh, ldh, \
+                                                       frag);                                                 \
         return 0;                                                                                     \
     }
     Q3_ATTN_CASE(128, 1)
@@ -762,7 +779,8 @@ int launch_attention_decode(const float* qkv, const float* q_norm, const float* 
     if (hd == HDV && group == GV) {                                                                                \
         launch_attn_decode_t<HDV, GV>(qkv, q_norm, k_norm, eps, rope_cs, kc, vc, row_seq, row_pos, R, nh, nkv, cap, \
                                       splits, part, status, st);                                                   \
-        launch_pdl(attn_merge_kernel<HDV>, R * nh, HDV, 0, st, part, nh, splits, (float*)nullptr, outh, ldh, frag); \
+        launch_pdl(attn_merge_kernel<HDV>, R * nh, HDV, 0, st, part, nh, splits, row_pos, 1, (float*)nullptr,   \
+                   outh, ldh, frag);                                                                               \
         return 0;                                                                                                  \
     }
     Q3_ATTN_CASE(128, 1)
