@@ -49,6 +49,8 @@ struct q3i8_ctx {
     int32_t *tokens = nullptr, *pos = nullptr, *seq_ids = nullptr, *step = nullptr, *status = nullptr;
     unsigned long long* keys = nullptr;
     unsigned int* counter = nullptr;
+    float* kpart = nullptr;            // split-K parts of the residual GEMVs
+    unsigned int* tile_cnt = nullptr;  // their per-tile arrival counters
     int32_t* out_ids = nullptr;  // [bmax][out_cap]
     int out_cap = 0;
 
@@ -102,6 +104,7 @@ int step_launches(const q3i8_ctx* c, int B);
 int persistent_setup(q3i8_ctx* c);
 int persistent_reset(q3i8_ctx* c);
 cudaError_t enqueue_persistent(q3i8_ctx* c, int B, float* logits, unsigned long long* trace = nullptr);
+constexpr int kResidSplit = 4;    // K parts per tile of the decode step's residual GEMVs (O, down)
 constexpr int kPrefillChunk = 32;  // prompt rows per weight sweep of a prefill projection on the GEMV
 // prefills longer than this many rows run their projections on the tcgen05 GEMM
 int prefill_launches(const q3i8_ctx* c, int M);

@@ -113,6 +113,35 @@ __global__ void __launch_bounds__(256) gemv_kernel(GemvArgs a) {
                     a.yh[plane_index(2 * b + 1, idx, a.ldyh, a.yfrag)] = lo;
                 }
             }
+        } else if (MODE == kResid && ks > 1 && a.kpart) {
+            // split K: park this part's sums; the tile's last part to finish adds
+            // all parts in order, so the result does not depend on timing
+            float* kp = a.kpart + ((size_t)tile * ks + part) * (NT * 64);
+            for (int i = threadIdx.x; i < NT * 64; i += blockDim.x) {
+                const int n = i >> 6, ln = (i & 63) >> 1, half = i & 1;
+                float sum = 0.f;
+#pragma unroll
+                for (int w = 0; w < 8; ++w) sum += red[w][n][ln][half];
+                kp[i] = sum;
+            }
+            __threadfence();
+            __syncthreads();
+            if (threadIdx.x == 0) is_last = (atomicAdd(a.tile_cnt + tile, 1u) == (unsigned)(ks - 1));
+            __syncthreads();
+            if (is_last) {
+                __threadfence();
+                for (int i = threadIdx.x; i < NT * 64; i += blockDim.x) {
+                    const int n = i >> 6, ln = (i & 63) >> 1, half = i & 1, gg = ln >> 2, b = 4 * n + (ln & 3);
+                    float sum = 0.f;
+                    for (int q = 0; q < ks; ++q) sum += __ldcg(a.kpart + ((size_t)tile * ks + q) * (NT * 64) + i);
+                    if (b < a.B) {
+                        const int row = tile * 16 + gg + 8 * half;
+                        float* p = a.y + (size_t)b * a.ldy + row;
+                        *p = *p + a.scale[row] * sum;
+                    }
+                }
+                if (threadIdx.x == 0) a.tile_cnt[tile] = 0u;
+            }
         } else {
             for (int i = threadIdx.x; i < NT * 64; i += blockDim.x) {
                 const int n = i >> 6, ln = (i & 63) >> 1, half = i & 1, gg = ln >> 2, b = 4 * n + (ln & 3);
@@ -126,7 +155,7 @@ __global__ void __launch_bounds__(256) gemv_kernel(GemvArgs a) {
                         a.y[(size_t)b * a.ldy + row] = v;
                     } else if (MODE == kResid) {
                         float* p = a.y + (size_t)b * a.ldy + row;
-                        if (ks > 1) atomicAdd(p, v);
+                        if (ks > 1) atomicAdd(p, v);  // split K without kpart: parts meet in atomic adds
                         else *p = *p + v;
                     } else {
                         if (row < a.valid_rows) {

@@ -43,7 +43,12 @@ struct GemvArgs {
     int advance_pos;
     int valid_rows;            // rows >= valid_rows (padding) take no part in the argmax
     float* logits;             // optional [B][valid_rows]
-    int ksplit;                // kResid only: K split over this many CTAs per tile, summed by atomicAdd (0 = 1)
+    int ksplit;                // kResid only: K split over this many CTAs per tile (0 = 1).  With kpart the
+                               // parts are parked in kpart [tiles][ksplit][4 NT 16] and the last CTA of a
+                               // tile (tile_cnt [tiles], zero between launches, left zero) adds them in
+                               // order; without, each part atomically adds its share to y
+    float* kpart;
+    unsigned int* tile_cnt;
     int xfrag;                 // xh is in fragment order (plane_index), else plain [8*NT][K] planes
     int yfrag;                 // kSiluGate: yh in fragment order
 };
