@@ -385,7 +385,6 @@ int init_state(q3i8_ctx* c) {
     CK(c, cudaMalloc(&c->status, 4));
     CK(c, cudaMalloc(&c->x, (size_t)B * H * 4));
     CK(c, cudaMalloc(&c->qkv, (size_t)B * (Dq + 2 * Dkv) * 4));
-    CK(c, cudaMalloc(&c->qr, (size_t)B * Dq * 4));
     c->dec_splits_max = 64;
     CK(c, cudaMalloc(&c->part, attn_part_bytes(B, d.n_heads, d.head_dim, c->dec_splits_max)));
     const int K = std::max(std::max(H, I), Dq);
@@ -419,7 +418,7 @@ extern "C" void q3i8_destroy(q3i8_ctx* c) {
         cudaFree(L.attn_norm), cudaFree(L.ffn_norm), cudaFree(L.q_norm), cudaFree(L.k_norm);
     }
     void* ptrs[] = {c->final_norm, c->kc, c->vc, c->rope, c->tokens, c->pos, c->seq_ids, c->step, c->keys,
-                    c->counter, c->kpart, c->tile_cnt, c->status, c->x, c->qkv, c->qr, c->part, c->xh, c->oh, c->ah, c->logits,
+                    c->counter, c->kpart, c->tile_cnt, c->status, c->x, c->qkv, c->part, c->xh, c->oh, c->ah, c->logits,
                     c->out_ids, c->pf_x, c->pf_qkv, c->pf_q, c->pf_xh, c->pf_oh, c->pf_ah, c->pf_blocks,
                     c->pf_part, c->pf_ids, c->pf_seq, c->pf_pos, c->pf_last, c->d_mats, c->d_gains,
                     c->p_epoch, c->p_keys, c->p_exit, c->p_attn_cnt, c->p_abort, c->p_diag, c->p_ll, c->p_part, c->p_trace};

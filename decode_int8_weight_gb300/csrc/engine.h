@@ -55,7 +55,7 @@ struct q3i8_ctx {
     int out_cap = 0;
 
     // decode activations
-    float *x = nullptr, *qkv = nullptr, *qr = nullptr, *part = nullptr, *logits = nullptr;
+    float *x = nullptr, *qkv = nullptr, *part = nullptr, *logits = nullptr;
     __half *xh = nullptr, *oh = nullptr, *ah = nullptr;
     int dec_splits_max = 64;
 
