@@ -277,7 +277,10 @@ __global__ void rmsnorm_kernel(const float* x, const int32_t* rows, int H, const
     }
     __syncthreads();
     const float inv = s_inv;
-    for (int k = threadIdx.x; k < H; k += blockDim.x) {
+    // a row may be spread over gridDim.y CTAs: each computes the whole sum
+    // (same order) and writes its slice
+    const int k_lo = (int)((long long)H * blockIdx.y / gridDim.y), k_hi = (int)((long long)H * (blockIdx.y + 1) / gridDim.y);
+    for (int k = k_lo + threadIdx.x; k < k_hi; k += blockDim.x) {
         const float v = __fmul_rn(__fmul_rn(xr[k], inv), g[k]);
         if (xn) xn[(size_t)i * H + k] = v;
         if (xh) {
@@ -291,7 +294,9 @@ __global__ void rmsnorm_kernel(const float* x, const int32_t* rows, int H, const
 
 void launch_rmsnorm(const float* x, const int32_t* rows, int n, int H, const float* g, float eps, float* xn,
                     __half* xh, cudaStream_t st, int frag) {
-    if (n > 0) launch_pdl(rmsnorm_kernel, n, 256, 0, st, x, rows, H, g, eps, xn, xh, frag);
+    // few rows (decode): spread each row's writes over up to 8 CTAs, about 64 CTAs in all
+    const int parts = std::max(1, std::min(std::min(8, H / 256), 64 / n));
+    if (n > 0) launch_pdl(rmsnorm_kernel, dim3(n, parts), 256, 0, st, x, rows, H, g, eps, xn, xh, frag);
 }
 
 // =====================================================================
