@@ -63,6 +63,17 @@ def peaks():
         return 6800.0, "fallback"
 
 
+def bf16_sustained_tflops() -> float:
+    """Measured sustained dense bf16 throughput (the prefill's tensor roofline); the profiling fallback else."""
+    try:
+        return float(json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))["bf16_tflops_sustained"])
+    except Exception:
+        return 1700.0
+
+
+BF16_SUSTAINED_TFLOPS = bf16_sustained_tflops()
+
+
 # ---------------------------------------------------------------- clocks sampling
 
 class ClockSampler:
@@ -276,7 +287,14 @@ def long_jobs(q3, dev, hbm_peak, names=("1.7b-b1-p256-n1024", "0.6b-b1-p4096-n20
         wbytes = wl.shape.weight_bytes()
         sb = float(np.mean([dec.step_bytes(lens + i) for i in range(0, wl.new_tokens - 1, 16)]))
         gbs = sb / (st["step_us"] * 1e-6) / 1e9
-        out[name] = {"prefill_tok_s": st["prefill_tokens_per_sec"], "decode_tok_s": st["decode_tokens_per_sec"],
+        # prefill work: the projections (2 flops per weight per token, lm_head excluded) and causal attention
+        sh, M = wl.shape, int(lens.sum())
+        proj = 2.0 * sh.n_layers * ((sh.dq + 2 * sh.dkv) * sh.hidden + sh.hidden * sh.dq + 3 * sh.intermediate * sh.hidden)
+        attn = 4.0 * sh.n_heads * sh.head_dim * float((lens.astype(np.float64) ** 2).sum()) / 2 * sh.n_layers
+        pf_tflops = (proj * M + attn) / (st["prefill_ms"] * 1e-3) / 1e12 if st["prefill_ms"] > 0 else 0.0
+        out[name] = {"prefill_tok_s": st["prefill_tokens_per_sec"], "prefill_tflops": pf_tflops,
+                     "prefill_frac_bf16_sustained": pf_tflops / BF16_SUSTAINED_TFLOPS,
+                     "decode_tok_s": st["decode_tokens_per_sec"],
                      "step_us": st["step_us"], "step_bytes_mean": sb, "weight_bytes": wbytes,
                      "kv_bytes_mean": sb - wbytes, "achieved_gbs": gbs, "frac": gbs / hbm_peak}
         dec.close()
