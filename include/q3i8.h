@@ -150,8 +150,8 @@ int q3i8_init(const q3i8_dims* dims, const q3i8_mat* embed, const q3i8_layer* la
  *                  and including the first eos_id when eos_id >= 0.
  *   stats          optional timings (NULL to skip).
  * Resets the KV cache, prefills every prompt, runs max_new_tokens-1 decode
- * steps (each one replay of a captured CUDA graph) and copies the ids back
- * once at the end.  Context sizing: max(512, longest prompt + new tokens),
+ * steps (each one replay of a captured CUDA graph of the step's kernels) and
+ * copies the ids back once at the end.  Context sizing: max(512, longest prompt + new tokens),
  * raised automatically up to 65,536 positions ("Model-agnostic LLM
  * inference", section "Long context"). */
 int q3i8_decode(q3i8_ctx* ctx, int32_t B, const int32_t* const* prompt_ids, const int32_t* prompt_lens,
@@ -196,8 +196,10 @@ int64_t q3i8_launch_count(const q3i8_ctx* ctx);
  * logits) with %globaltimer stamps recorded at every phase boundary of the
  * persistent step kernel, and copy them to the HOST array stamps
  * [grid][stride] (nanoseconds).  *grid and *stride receive the shape.  Needs a
- * prior q3i8_prefill; returns Q3_ERR_STATE when the context decodes with the
- * chained kernels or when cap is too small. */
+ * prior q3i8_prefill; returns Q3_ERR_STATE when the batch decodes with the
+ * chained kernels (the default; the environment variable
+ * Q3I8_PERSISTENT_MAX_BATCH=B, read at q3i8_init, selects the persistent
+ * kernel up to B sequences) or when cap is too small. */
 int q3i8_trace_step(q3i8_ctx* ctx, const int32_t* tokens, uint64_t* stamps, size_t cap, int32_t* grid,
                     int32_t* stride);
 
