@@ -38,7 +38,7 @@ STATUS = {0: "ok", 1: "unsupported_architecture", 2: "invalid_arguments", 3: "co
 EXPORTS = ["q3i8_validate_dims", "q3i8_init", "q3i8_decode", "q3i8_decode_device", "q3i8_prefill",
            "q3i8_step_logits", "q3i8_read_kv", "q3i8_step_bytes", "q3i8_step_launches", "q3i8_launch_count", "q3i8_last_error",
            "q3i8_status_name", "q3i8_destroy", "q3i8_trace_step", "q3i8_op_gemm_i8", "q3i8_op_attention_workspace", "q3i8_op_attention",
-           "q3i8_op_attention_static"]
+           "q3i8_op_attention_static", "q3i8_op_wait_probe"]
 
 
 class Q3Error(RuntimeError):
@@ -112,6 +112,7 @@ def lib():
             L.q3i8_op_attention_workspace.argtypes = [i32, i32, i32, i32]
             L.q3i8_op_attention.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, vp, vp, sz, vp, vp]
             L.q3i8_op_attention_static.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, vp, vp, vp]
+            L.q3i8_op_wait_probe.argtypes = [i32, i32, vp, vp, vp]
             _lib = L
     return _lib
 
@@ -298,4 +299,15 @@ def op_attention_static(q, k, v, row_seq, row_len, n_kv_heads: int, splits: int,
     rc = lib().q3i8_op_attention_static(_tptr(q), _tptr(k), _tptr(v), _tptr(row_seq), _tptr(row_len), R, nh,
                                         n_kv_heads, hd, cap, splits, _tptr(out), _tptr(status),
                                         ctypes.c_void_p(stream) if stream else None)
+    _check(rc, None)
+
+
+def op_wait_probe(arrive: bool, limit: int, status, elapsed_ns=None, stream=None):
+    """Run the library's bounded mbarrier wait on a phase that completes only
+    when ``arrive`` is set, with at most ``limit`` polls (negative: the
+    kernels' own limit).  ``status`` is a device int32 tensor, ``elapsed_ns``
+    an optional device int64 tensor.  Raises Q3Error (code Q3_ERR_TIMEOUT)
+    when the wait ran out (see q3i8_op_wait_probe)."""
+    rc = lib().q3i8_op_wait_probe(1 if arrive else 0, int(limit), _tptr(status), _tptr(elapsed_ns),
+                                  ctypes.c_void_p(stream) if stream else None)
     _check(rc, None)

@@ -9,10 +9,12 @@
 
 namespace q3 {
 
-// Spin limit of every bounded device wait (iterations of a try_wait/poll
-// loop with a short sleep): well above any legitimate wait (~seconds), far
-// below a watchdog.  After it a kernel records Q3 status 7 and returns.
+// Limits of every bounded device wait: a poll count (iterations of a
+// try_wait/poll loop with a short sleep) and a wall time, whichever runs out
+// first.  Both sit far above any legitimate wait (microseconds).  After one
+// runs out a kernel records Q3 status 7 and returns.
 constexpr uint32_t kSpinLimit = 1u << 22;
+constexpr uint64_t kWaitWallNs = 1000000000ull;
 constexpr int kStatusTimeout = 7;
 
 // ------------------------------------------------------------- conversions
@@ -108,10 +110,24 @@ Q3_DEV bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Bounded wait on an mbarrier phase; false if the limit ran out.
-Q3_DEV bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
-    for (uint32_t i = 0; i < kSpinLimit; ++i) {
+Q3_DEV uint64_t globaltimer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Bounded wait on an mbarrier phase: at most `limit` polls and about
+// kWaitWallNs of wall time (read every 256 polls); false if either ran out
+// (limit 0 gives up at once).
+Q3_DEV bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, uint32_t limit = kSpinLimit) {
+    uint64_t t0 = 0;
+    for (uint32_t i = 0; i < limit; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 255) == 255) {
+            const uint64_t now = globaltimer_ns();
+            if (t0 == 0) t0 = now;
+            else if (now - t0 > kWaitWallNs) return false;
+        }
         if (i > 64) __nanosleep(64);
     }
     return false;

@@ -270,6 +270,23 @@ int q3i8_op_attention_static(const float* q, const uint16_t* k, const uint16_t* 
                              const int32_t* row_len, int32_t R, int32_t n_heads, int32_t n_kv_heads, int32_t hd,
                              int32_t cap, int32_t splits, float* out, int32_t* d_status, void* cuda_stream);
 
+/* Check of the device-side time-out path.  The pages have no counterpart of
+ * this call; it exists so that the give-up branch of the library's bounded
+ * waits can be run on a GPU without faulting or hanging it.
+ *
+ * Launches one warp that waits on phase 0 of a shared-memory mbarrier
+ * through the same bounded wait the attention and prefill kernels use: at
+ * most `limit` polls (limit < 0: the kernels' own 2^22; limit 0: give up
+ * without polling) and at most about one second of wall time, whichever
+ * runs out first.  The phase completes only when `arrive` is non-zero.
+ *   d_status     device int32, required; zeroed by the call, then set to
+ *                Q3_ERR_TIMEOUT by each thread whose wait gave up.
+ *   d_elapsed_ns device uint64 (may be NULL): wall time of thread 0's wait.
+ * Synchronises `cuda_stream`.  Returns Q3_OK when the wait saw the phase,
+ * Q3_ERR_TIMEOUT when it ran out (the context stays usable), Q3_ERR_CUDA on
+ * a launch or copy error. */
+int q3i8_op_wait_probe(int32_t arrive, int32_t limit, int32_t* d_status, uint64_t* d_elapsed_ns, void* cuda_stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -98,3 +98,9 @@ def test_init_rejects_bad_shape_before_touching_the_device(pkg):
     with pytest.raises(pkg.Q3Error) as e:
         pkg.Decoder(m, max_batch=1)
     assert e.value.status == "unsupported_architecture" and "GQA" in str(e.value)
+
+
+def test_wait_probe_rejects_missing_status_before_touching_the_device(pkg):
+    with pytest.raises(pkg.Q3Error) as e:
+        pkg.op_wait_probe(False, 0, None)
+    assert e.value.status == "invalid_arguments" and "d_status" in str(e.value)
