@@ -143,6 +143,12 @@ Q3_DEV void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) 
         : "memory");
 }
 
+// Ask L2 to fetch [p, p + bytes) from global memory; nothing is returned to
+// the SM (p 16-byte aligned, bytes a multiple of 16).
+Q3_DEV void prefetch_l2_bulk(const void* p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
 // ------------------------------------------------------------- shared-memory loads
 // Explicit shared-space loads (32-bit shared addresses), so that hot loops
 // never go through generic addressing.

@@ -34,14 +34,32 @@ size_t packed_offset(int row, int k, int K) {
 // The 8 warps' partial sums meet in shared memory; the epilogue applies the
 // row scale and the mode's fusion.
 // =====================================================================
+// Work items of one CTA whose weights it asks L2 for before waiting on the
+// previous kernel.
+constexpr int kGemvPrefetchItems = 2;
+
 template <int NT, int MODE>
 __global__ void __launch_bounds__(256) gemv_kernel(GemvArgs a) {
     pdl_launch_dependents();
-    pdl_wait();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, t = lane & 3;
     const int n_tiles = a.rows >> 4;
     const int kpairs = a.K >> 5;
+    const int ks = (MODE == kResid && a.ksplit > 1) ? a.ksplit : 1;
+    // The weights do not depend on the previous kernel: start moving this
+    // CTA's first items into L2 (4 KB requests spread over the threads)
+    // while that kernel finishes.
+    for (int j = 0; j < kGemvPrefetchItems; ++j) {
+        const int item = blockIdx.x + j * gridDim.x;
+        if (item >= n_tiles * ks) break;
+        const int tile = item / ks, part = item - tile * ks;
+        const int p_lo = (int)((long long)kpairs * part / ks), p_hi = (int)((long long)kpairs * (part + 1) / ks);
+        const uint8_t* base = a.w + (size_t)tile * (kTileHeader + 16 * (size_t)a.K) + kTileHeader + (size_t)p_lo * 512;
+        const uint32_t bytes = (uint32_t)(p_hi - p_lo) * 512u;
+        for (uint32_t off = threadIdx.x * 4096u; off < bytes; off += blockDim.x * 4096u)
+            prefetch_l2_bulk(base + off, bytes - off < 4096u ? bytes - off : 4096u);
+    }
+    pdl_wait();
     __shared__ float red[8][NT][32][2];
     __shared__ unsigned long long best[4 * NT];
     __shared__ int is_last;
@@ -51,7 +69,6 @@ __global__ void __launch_bounds__(256) gemv_kernel(GemvArgs a) {
         __syncthreads();
     }
     // work item = (tile, K part); residual tiles may be split over ks CTAs
-    const int ks = (MODE == kResid && a.ksplit > 1) ? a.ksplit : 1;
     for (int item = blockIdx.x; item < n_tiles * ks; item += gridDim.x) {
         const int tile = item / ks, part = item - tile * ks;
         const int p_lo = (int)((long long)kpairs * part / ks), p_hi = (int)((long long)kpairs * (part + 1) / ks);
@@ -575,6 +592,10 @@ __global__ void __launch_bounds__(128) attn_split_kernel(const float* q, const _
     attn_write_partial<HD, GROUP>(m, l, acc, wm, wl, wacc, outp, splits, sp);
 }
 
+// Whether the decode attention asks L2 for its cached K/V before waiting on
+// the previous kernel.
+constexpr bool kAttnPrefetch = true;
+
 // Decode step with the QK-RMSNorm, RoPE and KV append folded in: row r's new
 // position p = row_pos[r] is appended (bf16, by the split that owns p) and
 // attended from registers, so the cache reads cover positions < p only.
@@ -585,6 +606,25 @@ __global__ void __launch_bounds__(128) attn_decode_kernel(const float* qkv, cons
                                                           const int32_t* row_pos, int nh, int nkv, int cap,
                                                           int splits, float* part, int32_t* status) {
     pdl_launch_dependents();
+    if (kAttnPrefetch) {
+        // The cached positions this split reads were written by earlier
+        // steps: start moving them into L2 while the previous kernel
+        // finishes (only a hint, so the position read here may be early).
+        const int r = blockIdx.z, sp = blockIdx.x, g = blockIdx.y;
+        const int pos = min(row_pos[r], cap - 1);
+        int per = (pos + splits) / splits;
+        per = (per + kChunk - 1) / kChunk * kChunk;
+        const int lo = sp * per, hi = min(pos, lo + per);
+        if (pos >= 0 && lo < hi) {
+            const size_t base = (((size_t)row_seq[r] * nkv + g) * cap + lo) * HD;
+            const uint32_t bytes = (uint32_t)(hi - lo) * HD * 2u;
+            for (uint32_t off = threadIdx.x * 4096u; off < bytes; off += blockDim.x * 4096u) {
+                const uint32_t n = bytes - off < 4096u ? bytes - off : 4096u;
+                prefetch_l2_bulk(reinterpret_cast<const uint8_t*>(kc + base) + off, n);
+                prefetch_l2_bulk(reinterpret_cast<const uint8_t*>(vc + base) + off, n);
+            }
+        }
+    }
     pdl_wait();
     constexpr int D = HD / 32;
     constexpr int E = HD / 32;
