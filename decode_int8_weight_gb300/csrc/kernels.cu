@@ -499,11 +499,15 @@ Q3_DEV bool attn_chunks(AttnSmem<HD>& sm, const __nv_bfloat16* kb, const __nv_bf
 }
 
 // Merge the four warps' online-softmax states and write this split's
-// partial state {acc[HD], m, l} per query head.
+// partial state {acc[HD], m, l} per query head; or, when outh is given (the
+// only split of its row), the attention output acc / l itself as hi/lo f16
+// planes, row r, query heads h0.. (the merge kernel's arithmetic for one
+// split, whose weight e^0 is exactly 1).
 template <int HD, int GROUP>
 Q3_DEV void attn_write_partial(const float (&m)[GROUP], const float (&l)[GROUP], const float (&acc)[GROUP][HD / 32],
                                    float (&wm)[4][GROUP], float (&wl)[4][GROUP], float (&wacc)[4][GROUP][HD],
-                                   float* outp, int splits, int sp) {
+                                   float* outp, int splits, int sp, __half* outh = nullptr, int ldh = 0,
+                                   int frag = 0, int r = 0, int h0 = 0) {
     constexpr int D = HD / 32;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (lane == 0)
@@ -526,6 +530,13 @@ Q3_DEV void attn_write_partial(const float (&m)[GROUP], const float (&l)[GROUP],
             const float f = expf(wm[w][h] - M);
             L += wl[w][h] * f;
             A += wacc[w][h][d] * f;
+        }
+        if (outh) {
+            __half hi, lo;
+            split_f16(A / L, hi, lo);
+            outh[plane_index(2 * r, (h0 + h) * HD + d, ldh, frag)] = hi;
+            outh[plane_index(2 * r + 1, (h0 + h) * HD + d, ldh, frag)] = lo;
+            continue;
         }
         float* o = outp + ((size_t)h * splits + sp) * (HD + 2);
         o[d] = A;
@@ -604,7 +615,8 @@ __global__ void __launch_bounds__(128) attn_decode_kernel(const float* qkv, cons
                                                           float eps, const float2* rope_cs, __nv_bfloat16* kc,
                                                           __nv_bfloat16* vc, const int32_t* row_seq,
                                                           const int32_t* row_pos, int nh, int nkv, int cap,
-                                                          int splits, float* part, int32_t* status) {
+                                                          int splits, float* part, __half* outh, int ldh, int frag,
+                                                          int32_t* status) {
     pdl_launch_dependents();
     if (kAttnPrefetch) {
         // The cached positions this split reads were written by earlier
@@ -736,7 +748,7 @@ __global__ void __launch_bounds__(128) attn_decode_kernel(const float* qkv, cons
             m[h] = mn;
         }
     }
-    attn_write_partial<HD, GROUP>(m, l, acc, wm, wl, wacc, outp, splits, sp);
+    attn_write_partial<HD, GROUP>(m, l, acc, wm, wl, wacc, outp, splits, sp, outh, ldh, frag, r, g * GROUP);
 }
 
 // out[r][h][:] = sum_s acc_s e^{m_s - M} / sum_s l_s e^{m_s - M} over the
@@ -831,7 +843,7 @@ template <int HD, int GROUP>
 static void launch_attn_decode_t(const float* qkv, const float* q_norm, const float* k_norm, float eps,
                                  const float2* rope_cs, __nv_bfloat16* kc, __nv_bfloat16* vc, const int32_t* row_seq,
                                  const int32_t* row_pos, int R, int nh, int nkv, int cap, int splits, float* part,
-                                 int32_t* status, cudaStream_t st) {
+                                 __half* outh, int ldh, int frag, int32_t* status, cudaStream_t st) {
     static bool attr_set = false;
     const int smem = (int)sizeof(AttnSmem<HD>);
     if (!attr_set) {
@@ -840,7 +852,7 @@ static void launch_attn_decode_t(const float* qkv, const float* q_norm, const fl
     }
     dim3 grid(splits, nkv, R);
     launch_pdl(attn_decode_kernel<HD, GROUP>, grid, 128, smem, st, qkv, q_norm, k_norm, eps, rope_cs, kc, vc, row_seq,
-               row_pos, nh, nkv, cap, splits, part, status);
+               row_pos, nh, nkv, cap, splits, part, outh, ldh, frag, status);
 }
 
 int launch_attention_decode(const float* qkv, const float* q_norm, const float* k_norm, float eps,
@@ -852,9 +864,10 @@ int launch_attention_decode(const float* qkv, const float* q_norm, const float* 
 #define Q3_ATTN_CASE(HDV, GV)                                                                                      \
     if (hd == HDV && group == GV) {                                                                                \
         launch_attn_decode_t<HDV, GV>(qkv, q_norm, k_norm, eps, rope_cs, kc, vc, row_seq, row_pos, R, nh, nkv, cap, \
-                                      splits, part, status, st);                                                   \
-        launch_pdl(attn_merge_kernel<HDV>, R * nh, HDV, 0, st, part, nh, splits, row_pos, 1, (float*)nullptr,   \
-                   outh, ldh, frag);                                                                               \
+                                      splits, part, splits == 1 ? outh : nullptr, ldh, frag, status, st);          \
+        if (splits > 1)                                                                                            \
+            launch_pdl(attn_merge_kernel<HDV>, R * nh, HDV, 0, st, part, nh, splits, row_pos, 1, (float*)nullptr, \
+                       outh, ldh, frag);                                                                           \
         return 0;                                                                                                  \
     }
     Q3_ATTN_CASE(128, 1)

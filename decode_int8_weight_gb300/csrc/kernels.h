@@ -91,7 +91,8 @@ int launch_attention(const float* q, const __nv_bfloat16* k, const __nv_bfloat16
 // One decode step's attention with the QK-RMSNorm, RoPE and bf16 KV append
 // folded in: qkv [R][(nh + 2 nkv) hd] fp32 as projected, row_pos[r] the new
 // position (appended, then attended with positions 0..row_pos[r]); output
-// hi/lo f16 planes (outh, ldh, frag as launch_attention).
+// hi/lo f16 planes (outh, ldh, frag as launch_attention).  With splits == 1
+// the attention kernel writes the output itself and no merge is launched.
 int launch_attention_decode(const float* qkv, const float* q_norm, const float* k_norm, float eps,
                             const float2* rope_cs, __nv_bfloat16* kc, __nv_bfloat16* vc, const int32_t* row_seq,
                             const int32_t* row_pos, int R, int nh, int nkv, int hd, int cap, int splits, float* part,

@@ -38,12 +38,12 @@ def model_for(name, random_gains=False):
     return _models[key]
 
 
-def _teacher_forced_check(pkg, name, B=None, random_gains=False, steps=None):
+def _teacher_forced_check(pkg, name, B=None, random_gains=False, steps=None, max_ctx=None):
     w = synth.WORKLOADS[name]
     m, orc = model_for(name, random_gains)
     prompts = synth.prompts(w, B)
     n_new = steps or w.new_tokens
-    dec = pkg.Decoder(m, max_batch=len(prompts), max_ctx=w.max_ctx)
+    dec = pkg.Decoder(m, max_batch=len(prompts), max_ctx=max_ctx or w.max_ctx)
     ids, counts, stats = dec.decode(prompts, n_new)
     assert np.all(counts == n_new)
     # teacher-forced GPU logits along the GPU's own tokens
@@ -66,6 +66,13 @@ def _teacher_forced_check(pkg, name, B=None, random_gains=False, steps=None):
 
 def test_tiny_b1_greedy_and_logits(pkg):
     worst, _ = _teacher_forced_check(pkg, "tiny-b1-p8-n16")
+    assert worst < 1e-3
+
+
+def test_tiny_one_attention_split(pkg):
+    # a 64-position context is one KV chunk, so the decode attention runs one
+    # split per kv head and writes its output itself, with no merge launch
+    worst, _ = _teacher_forced_check(pkg, "tiny-b1-p8-n16", B=3, max_ctx=64)
     assert worst < 1e-3
 
 
