@@ -34,9 +34,22 @@ size_t packed_offset(int row, int k, int K) {
 // The 8 warps' partial sums meet in shared memory; the epilogue applies the
 // row scale and the mode's fusion.
 // =====================================================================
-// Work items of one CTA whose weights it asks L2 for before waiting on the
-// previous kernel.
+// Work items of one CTA whose weights it asks L2 for ahead of use: the
+// first ones before waiting on the previous kernel, then each item's
+// successor this far ahead.
 constexpr int kGemvPrefetchItems = 2;
+constexpr bool kGemvRollingPrefetch = true;
+
+// Ask L2 for the weight bytes of work item `item` (4 KB requests spread over
+// the CTA's threads).
+Q3_DEV void gemv_prefetch_item(const GemvArgs& a, int item, int ks, int kpairs) {
+    const int tile = item / ks, part = item - tile * ks;
+    const int p_lo = (int)((long long)kpairs * part / ks), p_hi = (int)((long long)kpairs * (part + 1) / ks);
+    const uint8_t* base = a.w + (size_t)tile * (kTileHeader + 16 * (size_t)a.K) + kTileHeader + (size_t)p_lo * 512;
+    const uint32_t bytes = (uint32_t)(p_hi - p_lo) * 512u;
+    for (uint32_t off = threadIdx.x * 4096u; off < bytes; off += blockDim.x * 4096u)
+        prefetch_l2_bulk(base + off, bytes - off < 4096u ? bytes - off : 4096u);
+}
 
 template <int NT, int MODE>
 __global__ void __launch_bounds__(256) gemv_kernel(GemvArgs a) {
@@ -47,17 +60,11 @@ __global__ void __launch_bounds__(256) gemv_kernel(GemvArgs a) {
     const int kpairs = a.K >> 5;
     const int ks = (MODE == kResid && a.ksplit > 1) ? a.ksplit : 1;
     // The weights do not depend on the previous kernel: start moving this
-    // CTA's first items into L2 (4 KB requests spread over the threads)
-    // while that kernel finishes.
+    // CTA's first items into L2 while that kernel finishes.
     for (int j = 0; j < kGemvPrefetchItems; ++j) {
         const int item = blockIdx.x + j * gridDim.x;
         if (item >= n_tiles * ks) break;
-        const int tile = item / ks, part = item - tile * ks;
-        const int p_lo = (int)((long long)kpairs * part / ks), p_hi = (int)((long long)kpairs * (part + 1) / ks);
-        const uint8_t* base = a.w + (size_t)tile * (kTileHeader + 16 * (size_t)a.K) + kTileHeader + (size_t)p_lo * 512;
-        const uint32_t bytes = (uint32_t)(p_hi - p_lo) * 512u;
-        for (uint32_t off = threadIdx.x * 4096u; off < bytes; off += blockDim.x * 4096u)
-            prefetch_l2_bulk(base + off, bytes - off < 4096u ? bytes - off : 4096u);
+        gemv_prefetch_item(a, item, ks, kpairs);
     }
     pdl_wait();
     __shared__ float red[8][NT][32][2];
@@ -70,6 +77,10 @@ __global__ void __launch_bounds__(256) gemv_kernel(GemvArgs a) {
     }
     // work item = (tile, K part); residual tiles may be split over ks CTAs
     for (int item = blockIdx.x; item < n_tiles * ks; item += gridDim.x) {
+        if (kGemvRollingPrefetch) {
+            const long long ahead = item + (long long)kGemvPrefetchItems * gridDim.x;
+            if (ahead < (long long)n_tiles * ks) gemv_prefetch_item(a, (int)ahead, ks, kpairs);
+        }
         const int tile = item / ks, part = item - tile * ks;
         const int p_lo = (int)((long long)kpairs * part / ks), p_hi = (int)((long long)kpairs * (part + 1) / ks);
         float acc[NT][4];
