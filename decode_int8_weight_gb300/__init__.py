@@ -38,7 +38,11 @@ STATUS = {0: "ok", 1: "unsupported_architecture", 2: "invalid_arguments", 3: "co
 EXPORTS = ["q3i8_validate_dims", "q3i8_init", "q3i8_decode", "q3i8_decode_device", "q3i8_prefill",
            "q3i8_step_logits", "q3i8_read_kv", "q3i8_step_bytes", "q3i8_step_launches", "q3i8_launch_count", "q3i8_last_error",
            "q3i8_status_name", "q3i8_destroy", "q3i8_trace_step", "q3i8_op_gemm_i8", "q3i8_op_attention_workspace", "q3i8_op_attention",
-           "q3i8_op_attention_static", "q3i8_op_wait_probe"]
+           "q3i8_op_attention_static", "q3i8_op_wait_probe", "q3i8_cache_payload_bytes", "q3i8_cache_write",
+           "q3i8_cache_open", "q3i8_cache_tables", "q3i8_cache_close"]
+
+# q3i8_cache_open gate results
+CACHE_GATE = {0: "valid", 1: "absent", 2: "bad_magic", 3: "dims", 4: "manifest", 5: "length"}
 
 
 class Q3Error(RuntimeError):
@@ -113,6 +117,14 @@ def lib():
             L.q3i8_op_attention.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, vp, vp, sz, vp, vp]
             L.q3i8_op_attention_static.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, vp, vp, vp]
             L.q3i8_op_wait_probe.argtypes = [i32, i32, vp, vp, vp]
+            L.q3i8_cache_payload_bytes.restype = ctypes.c_uint64
+            L.q3i8_cache_payload_bytes.argtypes = [ctypes.POINTER(Dims)]
+            L.q3i8_cache_write.argtypes = [ctypes.c_char_p, ctypes.POINTER(Dims), ctypes.POINTER(Mat),
+                                           ctypes.POINTER(Layer), vp, ctypes.c_char_p, sz]
+            L.q3i8_cache_open.argtypes = [ctypes.c_char_p, ctypes.POINTER(Dims), ctypes.c_char_p, sz,
+                                          ctypes.POINTER(vp), ctypes.POINTER(i32)]
+            L.q3i8_cache_tables.argtypes = [vp, ctypes.POINTER(Mat), ctypes.POINTER(Layer), ctypes.POINTER(vp)]
+            L.q3i8_cache_close.argtypes = [vp]
             _lib = L
     return _lib
 
@@ -145,6 +157,31 @@ def _tptr(t):
     return ctypes.c_void_p(t.data_ptr()) if t is not None else None
 
 
+def _host_tables(model):
+    """q3i8_init's host argument tables for a model (synth.Model layout).
+    Returns (embed Mat, Layer array, final_norm address, arrays to keep alive)."""
+    keep = []
+
+    def mat(m):
+        q = np.ascontiguousarray(m.q, np.int8)
+        s = np.ascontiguousarray(m.s, np.float32)
+        keep.extend([q, s])
+        return Mat(q.ctypes.data, s.ctypes.data)
+
+    def vec(a):
+        a = np.ascontiguousarray(a, np.float32)
+        keep.append(a)
+        return a.ctypes.data
+
+    layers = (Layer * model.shape.n_layers)()
+    for i, ly in enumerate(model.layers):
+        layers[i] = Layer(mat(ly.wq), mat(ly.wk), mat(ly.wv), mat(ly.wo), mat(ly.wg), mat(ly.wu), mat(ly.wd),
+                          vec(ly.attn_norm), vec(ly.ffn_norm), vec(ly.q_norm), vec(ly.k_norm))
+    emb = mat(model.embed)
+    fin = vec(model.final_norm)
+    return emb, layers, fin, keep
+
+
 class Decoder:
     """One q3i8 context: weights resident on the current CUDA device."""
 
@@ -153,25 +190,7 @@ class Decoder:
         self.shape = sh
         self.max_batch = max_batch
         dims = make_dims(sh, max_batch, max_ctx)
-        keep = []
-
-        def mat(m):
-            q = np.ascontiguousarray(m.q, np.int8)
-            s = np.ascontiguousarray(m.s, np.float32)
-            keep.extend([q, s])
-            return Mat(q.ctypes.data, s.ctypes.data)
-
-        def vec(a):
-            a = np.ascontiguousarray(a, np.float32)
-            keep.append(a)
-            return a.ctypes.data
-
-        layers = (Layer * sh.n_layers)()
-        for i, ly in enumerate(model.layers):
-            layers[i] = Layer(mat(ly.wq), mat(ly.wk), mat(ly.wv), mat(ly.wo), mat(ly.wg), mat(ly.wu), mat(ly.wd),
-                              vec(ly.attn_norm), vec(ly.ffn_norm), vec(ly.q_norm), vec(ly.k_norm))
-        emb = mat(model.embed)
-        fin = vec(model.final_norm)
+        emb, layers, fin, keep = _host_tables(model)
         h = ctypes.c_void_p()
         rc = lib().q3i8_init(ctypes.byref(dims), ctypes.byref(emb), layers, ctypes.c_void_p(fin),
                              ctypes.c_void_p(stream) if stream else None, ctypes.byref(h))
@@ -311,3 +330,99 @@ def op_wait_probe(arrive: bool, limit: int, status, elapsed_ns=None, stream=None
     rc = lib().q3i8_op_wait_probe(1 if arrive else 0, int(limit), _tptr(status), _tptr(elapsed_ns),
                                   ctypes.c_void_p(stream) if stream else None)
     _check(rc, None)
+
+
+# ------------------------------------------------------------ quantized load cache
+
+class _CMat:
+    def __init__(self, q, s):
+        self.q, self.s = q, s
+
+
+class _CLayer:
+    pass
+
+
+class CachedModel:
+    """A model (synth.Model layout) whose arrays are views of an open cache's
+    bytes (q3i8_cache_open); the cache stays open while this object lives."""
+
+    def __init__(self, shape, handle):
+        self.shape = shape
+        self._h = handle
+        L = lib()
+        n = shape.n_layers
+        emb, layers, fin = Mat(), (Layer * n)(), ctypes.c_void_p()
+        _check(L.q3i8_cache_tables(handle, ctypes.byref(emb), layers, ctypes.byref(fin)), None)
+        H, I, hd = shape.hidden, shape.intermediate, shape.head_dim
+        Dq, Dkv = shape.n_heads * hd, shape.n_kv_heads * hd
+
+        def arr(addr, ctype, shp):
+            return np.ctypeslib.as_array(ctypes.cast(addr, ctypes.POINTER(ctype)), shape=shp)
+
+        def mat(m, rows, cols):
+            return _CMat(arr(m.w, ctypes.c_int8, (rows, cols)), arr(m.scale, ctypes.c_float, (rows,)))
+
+        self.embed = mat(emb, shape.vocab, H)
+        self.final_norm = arr(fin.value, ctypes.c_float, (H,))
+        self.layers = []
+        for ly in layers:
+            c = _CLayer()
+            c.wq, c.wk, c.wv = mat(ly.q, Dq, H), mat(ly.k, Dkv, H), mat(ly.v, Dkv, H)
+            c.wo = mat(ly.o, H, Dq)
+            c.wg, c.wu, c.wd = mat(ly.gate, I, H), mat(ly.up, I, H), mat(ly.down, H, I)
+            c.attn_norm, c.ffn_norm = arr(ly.attn_norm, ctypes.c_float, (H,)), arr(ly.ffn_norm, ctypes.c_float, (H,))
+            c.q_norm, c.k_norm = arr(ly.q_norm, ctypes.c_float, (hd,)), arr(ly.k_norm, ctypes.c_float, (hd,))
+            self.layers.append(c)
+
+    def close(self):
+        if getattr(self, "_h", None):
+            lib().q3i8_cache_close(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def cache_payload_bytes(shape) -> int:
+    d = make_dims(shape, 1)
+    return int(lib().q3i8_cache_payload_bytes(ctypes.byref(d)))
+
+
+def cache_write(path: str, model, manifest: bytes = b""):
+    """Write the model's post-quantization arrays to a cache file (q3i8_cache_write)."""
+    d = make_dims(model.shape, 1)
+    emb, layers, fin, keep = _host_tables(model)
+    rc = lib().q3i8_cache_write(os.fsencode(path), ctypes.byref(d), ctypes.byref(emb), layers,
+                                ctypes.c_void_p(fin), manifest, len(manifest))
+    _check(rc, None)
+    del keep
+
+
+def cache_open(path: str, shape, manifest: bytes = b""):
+    """(CachedModel or None, gate name): the cache at path if it passes the
+    gate for this shape and manifest (q3i8_cache_open)."""
+    d = make_dims(shape, 1)
+    h, gate = ctypes.c_void_p(), ctypes.c_int32(-1)
+    rc = lib().q3i8_cache_open(os.fsencode(path), ctypes.byref(d), manifest, len(manifest), ctypes.byref(h),
+                               ctypes.byref(gate))
+    _check(rc, None)
+    if gate.value != 0:
+        return None, CACHE_GATE[gate.value]
+    return CachedModel(shape, h), "valid"
+
+
+def load_cached(path: str, shape, manifest: bytes, build):
+    """The page's flow: restore the cache when it passes the gate, otherwise
+    call build() (the full path: convert and quantize), write a fresh cache
+    and return the built model.  Returns (model, gate name of the cache that
+    was found)."""
+    model, gate = cache_open(path, shape, manifest)
+    if model is not None:
+        return model, gate
+    model = build()
+    cache_write(path, model, manifest)
+    return model, gate

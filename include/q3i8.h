@@ -287,6 +287,53 @@ int q3i8_op_attention_static(const float* q, const uint16_t* k, const uint16_t* 
  * a launch or copy error. */
 int q3i8_op_wait_probe(int32_t arrive, int32_t limit, int32_t* d_status, uint64_t* d_elapsed_ns, void* cuda_stream);
 
+/* ------------------------------------------------------ quantized load cache
+ * "Model-agnostic LLM inference", section "The quantized load cache": the
+ * post-quantization bytes q3i8_init takes (int8 weights, fp32 per-row scales,
+ * fp32 norm gains; about one byte per parameter: 598,230,528 bytes for the
+ * Qwen3-0.6B shape) in one file, behind a validity gate of magic + dims +
+ * SHA-256 of a caller-chosen manifest (the checkpoint's identity, e.g. its
+ * manifest file) + exact length.  A cache that fails the gate is not used:
+ * the caller takes its full path and writes a fresh cache.  Decoding from a
+ * cache's tables gives byte-identical results, since q3i8_init receives the
+ * same bytes.  Payload corruption that keeps the length is not detected (the
+ * gate hashes the manifest, not the payload).  Host only; no GPU call. */
+typedef struct q3i8_cache q3i8_cache;
+
+/* q3i8_cache_open's gate result */
+#define Q3I8_CACHE_VALID 0     /* the cache matches: use it */
+#define Q3I8_CACHE_ABSENT 1    /* no readable file at the path */
+#define Q3I8_CACHE_BAD_MAGIC 2 /* not a cache file, or another format version */
+#define Q3I8_CACHE_DIMS 3      /* written for other dims */
+#define Q3I8_CACHE_MANIFEST 4  /* written for another manifest (checkpoint) */
+#define Q3I8_CACHE_LENGTH 5    /* truncated or extended */
+
+/* Payload bytes of a cache for these dims (0 for NULL). */
+uint64_t q3i8_cache_payload_bytes(const q3i8_dims* dims);
+
+/* Write a cache of the given host arrays (the arguments q3i8_init takes) to
+ * `path`: written beside it and renamed into place, so a reader never sees
+ * a partial file.  manifest may be NULL when manifest_len is 0.  Returns
+ * Q3_ERR_UNSUPPORTED_ARCH for dims the gates of q3i8_validate_dims reject,
+ * Q3_ERR_INVALID_ARGUMENTS for a NULL pointer or a failed write. */
+int q3i8_cache_write(const char* path, const q3i8_dims* dims, const q3i8_mat* embed, const q3i8_layer* layers,
+                     const float* final_norm, const void* manifest, size_t manifest_len);
+
+/* Check the cache at `path` against dims (max_batch and max_ctx are not part
+ * of the gate) and the manifest.  *gate receives a Q3I8_CACHE_* code; only
+ * for Q3I8_CACHE_VALID is *out set, to a handle owning the file's bytes
+ * (free with q3i8_cache_close).  A failed gate returns Q3_OK; errors are
+ * NULL arguments (Q3_ERR_INVALID_ARGUMENTS), unsupported dims
+ * (Q3_ERR_UNSUPPORTED_ARCH) and host memory (Q3_ERR_OOM). */
+int q3i8_cache_open(const char* path, const q3i8_dims* dims, const void* manifest, size_t manifest_len,
+                    q3i8_cache** out, int32_t* gate);
+
+/* The cache's arrays as q3i8_init arguments: embed, layers[n_layers] and
+ * final_norm point into the handle's memory, valid until q3i8_cache_close. */
+int q3i8_cache_tables(const q3i8_cache* cache, q3i8_mat* embed, q3i8_layer* layers, const float** final_norm);
+
+void q3i8_cache_close(q3i8_cache* cache);
+
 #ifdef __cplusplus
 }
 #endif
