@@ -2,7 +2,7 @@
 "The quantized load cache": cached and cold calls give byte-identical greedy
 sequences).  A context initialised from a cache's tables decodes the same
 ids and the same prefill logits, bit for bit, as one initialised from the
-model's own arrays."""
+model's own arrays.  Collected after the parity tests."""
 import numpy as np
 import pytest
 
