@@ -18,6 +18,9 @@ gcc and marshals numpy arrays through ctypes.  What each function follows:
 * ``Oracle.forward``: prefill builds the KV cache from the whole prompt and a
   decode step adds one token ("LLM inference overview", sections "Results"
   and "Workload characteristics"); both are the same causal pass here.
+* ``sampling``: the sampling chain of "Model-agnostic LLM inference",
+  section "Sampling" (penalties, temperature, top-k, min-p, top-p, seeded
+  draw), in float64 numpy; see its module docstring for the readings.
 """
 from __future__ import annotations
 
