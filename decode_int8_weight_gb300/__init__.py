@@ -39,7 +39,9 @@ EXPORTS = ["q3i8_validate_dims", "q3i8_init", "q3i8_decode", "q3i8_decode_device
            "q3i8_step_logits", "q3i8_read_kv", "q3i8_step_bytes", "q3i8_step_launches", "q3i8_launch_count", "q3i8_last_error",
            "q3i8_status_name", "q3i8_destroy", "q3i8_trace_step", "q3i8_op_gemm_i8", "q3i8_op_attention_workspace", "q3i8_op_attention",
            "q3i8_op_attention_static", "q3i8_op_wait_probe", "q3i8_cache_payload_bytes", "q3i8_cache_write",
-           "q3i8_cache_open", "q3i8_cache_tables", "q3i8_cache_close"]
+           "q3i8_cache_open", "q3i8_cache_tables", "q3i8_cache_close", "q3i8_sched_new", "q3i8_sched_destroy",
+           "q3i8_sched_submit", "q3i8_sched_plan", "q3i8_sched_complete_prefill", "q3i8_sched_complete_step",
+           "q3i8_sched_idle", "q3i8_sched_result"]
 
 # q3i8_cache_open gate results
 CACHE_GATE = {0: "valid", 1: "absent", 2: "bad_magic", 3: "dims", 4: "manifest", 5: "length"}
@@ -125,6 +127,15 @@ def lib():
                                           ctypes.POINTER(vp), ctypes.POINTER(i32)]
             L.q3i8_cache_tables.argtypes = [vp, ctypes.POINTER(Mat), ctypes.POINTER(Layer), ctypes.POINTER(vp)]
             L.q3i8_cache_close.argtypes = [vp]
+            L.q3i8_sched_new.argtypes = [i32, i32, ctypes.POINTER(vp)]
+            L.q3i8_sched_destroy.argtypes = [vp]
+            L.q3i8_sched_submit.argtypes = [vp, vp, i32, i32, i32, ctypes.POINTER(i32)]
+            L.q3i8_sched_plan.argtypes = [vp, ctypes.POINTER(i32), vp, vp, ctypes.POINTER(i32), vp, vp, vp, vp]
+            L.q3i8_sched_complete_prefill.argtypes = [vp, i32, vp, vp]
+            L.q3i8_sched_complete_step.argtypes = [vp, i32, vp]
+            L.q3i8_sched_idle.restype = i32
+            L.q3i8_sched_idle.argtypes = [vp]
+            L.q3i8_sched_result.argtypes = [vp, i32, vp, i32, ctypes.POINTER(i32), ctypes.POINTER(i32)]
             _lib = L
     return _lib
 
@@ -426,3 +437,67 @@ def load_cached(path: str, shape, manifest: bytes, build):
     model = build()
     cache_write(path, model, manifest)
     return model, gate
+
+
+# ------------------------------------------------------------ continuous batching
+
+class Scheduler:
+    """Host scheduler of a continuous batch (q3i8_sched_*): FIFO admission
+    into free KV slots between steps, retirement at max_new_tokens or eos."""
+
+    def __init__(self, max_batch: int, max_ctx: int):
+        self.max_batch = max_batch
+        h = ctypes.c_void_p()
+        _check(lib().q3i8_sched_new(max_batch, max_ctx, ctypes.byref(h)), None)
+        self._h = h
+
+    def close(self):
+        if getattr(self, "_h", None):
+            lib().q3i8_sched_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def submit(self, prompt, max_new_tokens: int, eos_id: int = -1) -> int:
+        p = np.ascontiguousarray(prompt, np.int32)
+        rid = ctypes.c_int32()
+        _check(lib().q3i8_sched_submit(self._h, _p(p), p.size, max_new_tokens, eos_id, ctypes.byref(rid)), None)
+        return rid.value
+
+    def plan(self):
+        """(admissions [(request, slot)], rows [(request, slot, position, token)])."""
+        n = self.max_batch
+        na, nr = ctypes.c_int32(), ctypes.c_int32()
+        ar, asl = np.zeros(n, np.int32), np.zeros(n, np.int32)
+        rr, rs, rp, rt = (np.zeros(n, np.int32) for _ in range(4))
+        _check(lib().q3i8_sched_plan(self._h, ctypes.byref(na), _p(ar), _p(asl), ctypes.byref(nr), _p(rr), _p(rs),
+                                     _p(rp), _p(rt)), None)
+        adm = [(int(ar[i]), int(asl[i])) for i in range(na.value)]
+        rows = [(int(rr[i]), int(rs[i]), int(rp[i]), int(rt[i])) for i in range(nr.value)]
+        return adm, rows
+
+    def complete_prefill(self, request_ids, first_tokens):
+        r = np.ascontiguousarray(request_ids, np.int32)
+        t = np.ascontiguousarray(first_tokens, np.int32)
+        assert r.size == t.size
+        _check(lib().q3i8_sched_complete_prefill(self._h, r.size, _p(r), _p(t)), None)
+
+    def complete_step(self, tokens):
+        t = np.ascontiguousarray(tokens, np.int32)
+        _check(lib().q3i8_sched_complete_step(self._h, t.size, _p(t)), None)
+
+    def idle(self) -> bool:
+        return bool(lib().q3i8_sched_idle(self._h))
+
+    def result(self, request_id: int):
+        """(tokens generated so far, finished)."""
+        n, done = ctypes.c_int32(), ctypes.c_int32()
+        _check(lib().q3i8_sched_result(self._h, request_id, None, 0, ctypes.byref(n), ctypes.byref(done)), None)
+        out = np.zeros(max(n.value, 1), np.int32)
+        _check(lib().q3i8_sched_result(self._h, request_id, _p(out), n.value, ctypes.byref(n), ctypes.byref(done)),
+               None)
+        return out[:n.value], bool(done.value)

@@ -334,6 +334,58 @@ int q3i8_cache_tables(const q3i8_cache* cache, q3i8_mat* embed, q3i8_layer* laye
 
 void q3i8_cache_close(q3i8_cache* cache);
 
+/* --------------------------------------------------- continuous batching
+ * Host-side scheduler of a continuous batch ("LLM inference overview",
+ * section "Workload characteristics": one weight sweep per step serves every
+ * sequence in flight; each row of a decode step carries its own sequence
+ * slot and position).  Requests wait in a FIFO queue, take the lowest free
+ * KV slot between steps, and free it when they finish (max_new_tokens
+ * tokens, or eos_id, which is kept).  Host only; no GPU call.
+ *
+ * One step of the caller's loop:
+ *   q3i8_sched_plan            admissions (request, slot) and decode rows
+ *                              (request, slot, position, input token);
+ *   prefill each admission     into its slot, then
+ *   q3i8_sched_complete_prefill with each admission's first token;
+ *   decode the rows            then q3i8_sched_complete_step with each
+ *                              row's next token, in row order.
+ * A sequence occupies prompt_len + max_new_tokens - 1 positions of its slot. */
+typedef struct q3i8_sched q3i8_sched;
+
+/* max_batch slots of max_ctx positions each. */
+int q3i8_sched_new(int32_t max_batch, int32_t max_ctx, q3i8_sched** out);
+void q3i8_sched_destroy(q3i8_sched* sched);
+
+/* Queue a request (the prompt is copied).  Q3_ERR_INVALID_ARGUMENTS for an
+ * empty prompt or max_new_tokens < 1, Q3_ERR_CONTEXT when it cannot fit a
+ * slot.  *request_id numbers requests from 0 in submission order. */
+int q3i8_sched_submit(q3i8_sched* sched, const int32_t* prompt, int32_t prompt_len, int32_t max_new_tokens,
+                      int32_t eos_id, int32_t* request_id);
+
+/* Plan the next step.  Arrays hold max_batch entries.  Rows are the
+ * sequences in flight in slot order (position = prompt_len + generated - 1,
+ * token = the last generated token); admissions are queued requests placed
+ * in free slots, which join the rows after their prefill.  Q3_ERR_STATE if
+ * the previous plan's prefill or step has not been completed. */
+int q3i8_sched_plan(q3i8_sched* sched, int32_t* n_admit, int32_t* admit_request, int32_t* admit_slot,
+                    int32_t* n_rows, int32_t* row_request, int32_t* row_slot, int32_t* row_pos,
+                    int32_t* row_token);
+
+/* Report the first generated token of admitted requests (any order). */
+int q3i8_sched_complete_prefill(q3i8_sched* sched, int32_t n, const int32_t* request_ids,
+                                const int32_t* first_tokens);
+
+/* Report the next token of each row of the last plan, in row order. */
+int q3i8_sched_complete_step(q3i8_sched* sched, int32_t n_rows, const int32_t* tokens);
+
+/* 1 when nothing is queued, in flight or awaiting a report. */
+int32_t q3i8_sched_idle(const q3i8_sched* sched);
+
+/* A request's generated tokens so far (up to cap written), their count and
+ * whether it has finished. */
+int q3i8_sched_result(const q3i8_sched* sched, int32_t request_id, int32_t* tokens, int32_t cap, int32_t* n_tokens,
+                      int32_t* done);
+
 #ifdef __cplusplus
 }
 #endif
