@@ -26,6 +26,11 @@
  *
  * Threading: a context is bound to one device and one CUDA stream and is not
  * thread-safe; use one context per host thread.
+ *
+ * Groups of calls: the decode context (q3i8_init .. q3i8_destroy); single
+ * kernels on caller memory for isolated checks (q3i8_op_*); the quantized
+ * load cache (q3i8_cache_*, host only); the continuous-batching scheduler
+ * (q3i8_sched_*, host only).
  */
 #ifndef Q3I8_H
 #define Q3I8_H
