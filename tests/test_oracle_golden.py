@@ -32,3 +32,26 @@ def test_tiny_oracle_matches_frozen_fixture():
         if g["top1_minus_top2"][i] <= 1e-4:
             break
         assert gen[i] == frozen[i], f"step {i}"
+
+
+SAMPLING = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden", "tiny_sampling.json")
+
+
+def test_sampling_oracle_matches_frozen_fixture():
+    # the sampling chain ("Model-agnostic LLM inference", section "Sampling")
+    # still draws the frozen tokens, with the frozen draws and intervals
+    from oracle import sampling
+
+    g = json.load(open(SAMPLING))
+    w = synth.WORKLOADS[g["workload"]]
+    orc = oracle.Oracle(synth.make_model(w.shape, w.weight_seed), nthreads=2)
+    prompt = synth.prompts(w)[0]
+    assert [int(t) for t in prompt] == g["prompt"]
+    for case in g["cases"]:
+        p = sampling.Params(**case["params"])
+        us = [sampling.uniform(g["seed"], 0, i) for i in range(len(case["tokens"]))]
+        assert us == case["u"]
+        for (lo, hi), u in zip(case["interval"], us):
+            assert lo <= u < hi
+        toks = sampling.decode(orc, prompt, len(case["tokens"]), p, g["seed"])
+        assert toks.tolist() == case["tokens"], case["params"]
