@@ -272,13 +272,7 @@ int launch_attn_prefill(const float* q, const __nv_bfloat16* kc, const __nv_bflo
                         int nblocks, int nh, int nkv, int hd, int cap, __half* outh, int ldh, cudaStream_t st) {
     if (nblocks <= 0) return 0;
     if (!attn_prefill_supported(nh, nkv, hd) || cap % kKT) return -1;
-    static bool attr_done = false;
-    if (!attr_done) {
-        if (cudaFuncSetAttribute(attn_prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPfSmem) !=
-            cudaSuccess)
-            return -2;
-        attr_done = true;
-    }
+    if (allow_max_dynamic_smem((const void*)attn_prefill_kernel) != cudaSuccess) return -2;
     attn_prefill_kernel<<<dim3(nblocks, nkv), kPfThreads, kPfSmem, st>>>(q, kc, vc, blocks, nh, nkv, cap, outh, ldh);
     return 0;
 }

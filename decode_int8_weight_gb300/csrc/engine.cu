@@ -314,6 +314,7 @@ extern "C" int q3i8_init(const q3i8_dims* dims, const q3i8_mat* embed, const q3i
     if (rc == Q3_OK) rc = ensure_capacity(c, c->cap_request);
     if (rc == Q3_OK) rc = ensure_out(c, 256);
     if (rc == Q3_OK) rc = persistent_setup(c);
+    if (rc == Q3_OK) rc = step_setup(c);
     if (rc == Q3_OK && cudaStreamSynchronize(c->stream) != cudaSuccess) rc = fail(c, Q3_ERR_CUDA, "init sync failed");
     if (rc != Q3_OK) {
         g_tls_error = c->err;
@@ -421,7 +422,8 @@ extern "C" void q3i8_destroy(q3i8_ctx* c) {
                     c->counter, c->kpart, c->tile_cnt, c->status, c->x, c->qkv, c->part, c->xh, c->oh, c->ah, c->logits,
                     c->out_ids, c->pf_x, c->pf_qkv, c->pf_q, c->pf_xh, c->pf_oh, c->pf_ah, c->pf_blocks,
                     c->pf_part, c->pf_ids, c->pf_seq, c->pf_pos, c->pf_last, c->d_mats, c->d_gains,
-                    c->p_epoch, c->p_keys, c->p_exit, c->p_attn_cnt, c->p_abort, c->p_diag, c->p_ll, c->p_part, c->p_trace};
+                    c->p_epoch, c->p_keys, c->p_exit, c->p_attn_cnt, c->p_abort, c->p_diag, c->p_ll, c->p_part, c->p_trace,
+                    c->xa, c->xf};
     for (void* p : ptrs) cudaFree(p);
     if (c->ev0) cudaEventDestroy(c->ev0);
     if (c->ev1) cudaEventDestroy(c->ev1);
@@ -444,7 +446,7 @@ int decode_splits(const q3i8_ctx* c, int B) {
 }
 
 // Enqueue one decode step for B sequences: tokens[b] at positions pos[b].
-void enqueue_step(q3i8_ctx* c, int B, bool want_logits) {
+int enqueue_step(q3i8_ctx* c, int B, bool want_logits) {
     const q3i8_dims& d = c->d;
     const int H = d.hidden, I = d.intermediate, hd = d.head_dim, nh = d.n_heads, nkv = d.n_kv_heads;
     const int Dq = nh * hd;
@@ -467,9 +469,10 @@ void enqueue_step(q3i8_ctx* c, int B, bool want_logits) {
         a.w = L.qkv.frag, a.scale = L.qkv.scale, a.rows = L.qkv.rows, a.K = H, a.xh = c->xh, a.xfrag = 1;
         a.y = c->qkv, a.ldy = L.qkv.rows;
         launch_gemv(a, kStore, gemv_grid(a.rows, kStore, c->num_sms), st);
-        launch_attention_decode(c->qkv, L.q_norm, L.k_norm, d.rms_eps, c->rope, c->kc + l * layer_kv,
-                                c->vc + l * layer_kv, c->seq_ids, c->pos, B, nh, nkv, hd, c->cap, splits, c->part,
-                                c->oh, Dq, c->status, st, 1);
+        if (launch_attention_decode(c->qkv, L.q_norm, L.k_norm, d.rms_eps, c->rope, c->kc + l * layer_kv,
+                                    c->vc + l * layer_kv, c->seq_ids, c->pos, B, nh, nkv, hd, c->cap, splits, c->part,
+                                    c->oh, Dq, c->status, st, 1))
+            return fail(c, Q3_ERR_CUDA, "decode attention could not be launched");
         a = GemvArgs{};
         a.B = B;
         a.w = L.o.frag, a.scale = L.o.scale, a.rows = L.o.rows, a.K = Dq, a.xh = c->oh, a.xfrag = 1;
@@ -490,6 +493,7 @@ void enqueue_step(q3i8_ctx* c, int B, bool want_logits) {
         launch_rmsnorm(c->x, nullptr, B, H, g_next, d.rms_eps, nullptr, c->xh, st, 1);
     }
     enqueue_lm_head(c, B, true, want_logits ? c->logits : nullptr);
+    return Q3_OK;
 }
 
 void enqueue_lm_head(q3i8_ctx* c, int B, bool advance_pos, float* logits) {
@@ -501,6 +505,93 @@ void enqueue_lm_head(q3i8_ctx* c, int B, bool advance_pos, float* logits) {
     a.out_cap = c->out_cap, a.pos = c->pos, a.advance_pos = advance_pos ? 1 : 0;
     a.valid_rows = c->embed.valid_rows, a.logits = logits;
     launch_gemv(a, kArgmax, gemv_grid(a.rows, kArgmax, c->num_sms), c->stream);
+}
+
+// ------------------------------------------------------------------ small-batch step (step.cu)
+
+static StepShape step_shape(const q3i8_ctx* c) {
+    const q3i8_dims& d = c->d;
+    return StepShape{d.hidden, d.intermediate, d.n_heads, d.n_kv_heads, d.head_dim, c->embed.rows};
+}
+
+// Chooses the launch geometry of the small-batch step and allocates its
+// fixed-point residual accumulators.  Q3I8_DECODE_PATH=chained keeps every
+// batch on the chained kernels.
+int step_setup(q3i8_ctx* c) {
+    const char* env = getenv("Q3I8_DECODE_PATH");
+    if (env && strcmp(env, "chained") == 0) return Q3_OK;
+    int optin = 0;
+    CK(c, cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, c->dev));
+    StepPlan p;
+    if (!step_plan(step_shape(c), c->num_sms, optin, &p)) return Q3_OK;
+    if (!step_prepare_device(step_shape(c), p))
+        return fail(c, Q3_ERR_CUDA, "decode step kernels: shared-memory opt-in refused");
+    if (attn_block_max_clusters(c->d.hidden, c->d.head_dim, p.kv_stages) < 1) return Q3_OK;
+    const size_t n = (size_t)c->bmax * c->d.hidden;
+    CK(c, cudaMalloc(&c->xa, n * sizeof(long long)));
+    CK(c, cudaMalloc(&c->xf, n * sizeof(long long)));
+    CK(c, cudaMemsetAsync(c->xa, 0, n * sizeof(long long), c->stream));
+    CK(c, cudaMemsetAsync(c->xf, 0, n * sizeof(long long), c->stream));
+    c->splan = p;
+    c->use_step = true;
+    c->step_max_batch = kStepMaxBatch;
+    if (const char* mb = getenv("Q3I8_STEP_MAX_BATCH")) c->step_max_batch = std::max(0, std::min(kStepMaxBatch, atoi(mb)));
+    return Q3_OK;
+}
+
+// Clears the residual accumulators after a step that did not finish.
+static void step_reset(q3i8_ctx* c) {
+    if (!c->use_step) return;
+    const size_t n = (size_t)c->bmax * c->d.hidden * sizeof(long long);
+    cudaMemsetAsync(c->xa, 0, n, c->stream);
+    cudaMemsetAsync(c->xf, 0, n, c->stream);
+}
+
+// One decode step for B <= kStepMaxBatch sequences: per layer the attention
+// block, gate/up and down kernels, then the lm_head.
+int enqueue_step_fused(q3i8_ctx* c, int B, bool want_logits) {
+    const q3i8_dims& d = c->d;
+    const int H = d.hidden, I = d.intermediate, hd = d.head_dim;
+    const size_t layer_kv = (size_t)c->bmax * d.n_kv_heads * c->cap * hd;
+    const StepPlan& p = c->splan;
+    cudaStream_t st = c->stream;
+    for (int l = 0; l < d.n_layers; ++l) {
+        const DevLayer& L = c->layers[l];
+        AttnBlockArgs a{};
+        a.B = B, a.H = H, a.nh = d.n_heads, a.nkv = d.n_kv_heads, a.cap = c->cap, a.kv_stages = p.kv_stages;
+        a.eps = d.rms_eps;
+        a.wqkv = L.qkv.frag, a.wo = L.o.frag, a.o_scale = L.o.scale;
+        a.attn_norm = L.attn_norm, a.q_norm = L.q_norm, a.k_norm = L.k_norm, a.rope = c->rope;
+        a.kc = c->kc + l * layer_kv, a.vc = c->vc + l * layer_kv;
+        a.seq_ids = c->seq_ids, a.pos = c->pos, a.pos_early = l > 0 ? 1 : 0;
+        a.xin = l > 0 ? c->xf : nullptr;
+        a.tokens = c->tokens, a.emb = c->embed.raw, a.emb_scale = c->embed.scale;
+        a.xa = c->xa, a.status = c->status;
+        cudaError_t e = launch_attn_block(a, hd, st);
+        if (e != cudaSuccess) return fail(c, Q3_ERR_CUDA, "attention block launch: %s", cudaGetErrorString(e));
+        FfnGateArgs gargs{};
+        gargs.B = B, gargs.H = H, gargs.I = I, gargs.tpc = p.gate_tpc, gargs.eps = d.rms_eps;
+        gargs.wgu = L.gu.frag, gargs.ffn_norm = L.ffn_norm, gargs.xa = c->xa, gargs.xf = c->xf, gargs.ah = c->ah;
+        gargs.status = c->status;
+        e = launch_ffn_gate(gargs, p.gate_grid, st);
+        if (e != cudaSuccess) return fail(c, Q3_ERR_CUDA, "gate/up launch: %s", cudaGetErrorString(e));
+        FfnDownArgs dargs{};
+        dargs.B = B, dargs.H = H, dargs.I = I, dargs.ks = p.down_ks;
+        dargs.wd = L.down.frag, dargs.d_scale = L.down.scale, dargs.ah = c->ah, dargs.xa = c->xa, dargs.xf = c->xf;
+        dargs.status = c->status;
+        e = launch_ffn_down(dargs, p.down_grid, st);
+        if (e != cudaSuccess) return fail(c, Q3_ERR_CUDA, "down launch: %s", cudaGetErrorString(e));
+    }
+    LmHeadArgs m{};
+    m.B = B, m.H = H, m.rows = c->embed.rows, m.valid_rows = c->embed.valid_rows, m.stages = p.lm_stages;
+    m.eps = d.rms_eps;
+    m.w = c->embed.frag, m.final_norm = c->final_norm, m.xf = c->xf;
+    m.keys = c->keys, m.counter = c->counter, m.tokens = c->tokens, m.out_ids = c->out_ids, m.step = c->step;
+    m.out_cap = c->out_cap, m.pos = c->pos, m.advance_pos = 1, m.logits = want_logits ? c->logits : nullptr;
+    m.status = c->status;
+    cudaError_t e = launch_lm_head(m, p.lm_grid, st);
+    if (e != cudaSuccess) return fail(c, Q3_ERR_CUDA, "lm_head launch: %s", cudaGetErrorString(e));
+    return Q3_OK;
 }
 
 // ------------------------------------------------------------------ persistent step
@@ -612,18 +703,21 @@ cudaError_t enqueue_persistent(q3i8_ctx* c, int B, float* logits, unsigned long 
 // shape allows it, else the chained kernels.
 static bool persistent_for(const q3i8_ctx* c, int B) { return c->use_persistent && B <= c->p_max_batch; }
 
+static bool fused_for(const q3i8_ctx* c, int B) { return c->use_step && B <= c->step_max_batch; }
+
 static int enqueue_decode_step(q3i8_ctx* c, int B, bool want_logits) {
     if (persistent_for(c, B)) {
         cudaError_t e = enqueue_persistent(c, B, want_logits ? c->logits : nullptr);
         if (e != cudaSuccess) return fail(c, Q3_ERR_CUDA, "persistent step launch: %s", cudaGetErrorString(e));
         return Q3_OK;
     }
-    enqueue_step(c, B, want_logits);
-    return Q3_OK;
+    if (fused_for(c, B)) return enqueue_step_fused(c, B, want_logits);
+    return enqueue_step(c, B, want_logits);
 }
 
 int step_launches(const q3i8_ctx* c, int B) {
     if (persistent_for(c, B)) return 1;
+    if (fused_for(c, B)) return 3 * c->d.n_layers + 1;
     return 2 + c->d.n_layers * (decode_splits(c, B) == 1 ? 7 : 8) + 1;
 }
 // Kernels of one prefill over M prompt rows: embed; per layer 2 RMSNorms, the
@@ -768,6 +862,8 @@ static int check_status(q3i8_ctx* c) {
             cudaMemcpy(dg, c->p_diag, sizeof dg, cudaMemcpyDeviceToHost);
             persistent_reset(c);
         }
+        step_reset(c);
+        cudaStreamSynchronize(c->stream);
         return fail(c, Q3_ERR_TIMEOUT,
                     "a bounded device wait gave up (status %d; site %d cta %d warp %d layer %d phase %d aux %d)", st,
                     dg[0], dg[1], dg[2], dg[3], dg[4], dg[5]);

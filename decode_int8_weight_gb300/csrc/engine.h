@@ -9,6 +9,7 @@
 #include <vector>
 
 #include "../../include/q3i8.h"
+#include "step.h"
 
 namespace q3 {
 constexpr int kMaxBatch = 32;      // GEMV activation operand: 4 sequences per 8-column MMA tile, 8 tiles
@@ -83,6 +84,12 @@ struct q3i8_ctx {
     float* p_part = nullptr;
     size_t p_ll_bytes = 0;
 
+    // small-batch decode step (step.cu): three kernels per layer
+    bool use_step = false;
+    int step_max_batch = 0;  // largest B decoded by it; larger B take the chained kernels
+    q3::StepPlan splan;
+    long long *xa = nullptr, *xf = nullptr;  // residual stream accumulators [bmax][H], value * 2^32
+
     std::map<int, cudaGraphExec_t> graphs;  // decode step graph per batch size
     cudaEvent_t ev0 = nullptr, ev1 = nullptr, ev2 = nullptr;
 
@@ -98,7 +105,9 @@ int init_state(q3i8_ctx* c);
 int ensure_capacity(q3i8_ctx* c, int need_ctx);
 void drop_graphs(q3i8_ctx* c);
 int decode_splits(const q3i8_ctx* c, int B);
-void enqueue_step(q3i8_ctx* c, int B, bool want_logits);
+int enqueue_step(q3i8_ctx* c, int B, bool want_logits);
+int step_setup(q3i8_ctx* c);
+int enqueue_step_fused(q3i8_ctx* c, int B, bool want_logits);
 void enqueue_lm_head(q3i8_ctx* c, int B, bool advance_pos, float* logits);
 int step_launches(const q3i8_ctx* c, int B);
 int persistent_setup(q3i8_ctx* c);

@@ -811,18 +811,15 @@ __global__ void attn_merge_kernel(const float* part, int nh, int splits, const i
 size_t attn_part_bytes(int R, int nh, int hd, int splits) { return (size_t)R * nh * splits * (hd + 2) * sizeof(float); }
 
 template <int HD, int GROUP>
-static void launch_attn_t(const float* q, const __nv_bfloat16* k, const __nv_bfloat16* v, const int32_t* row_seq,
+static bool launch_attn_t(const float* q, const __nv_bfloat16* k, const __nv_bfloat16* v, const int32_t* row_seq,
                           const int32_t* row_len, int len_add, int R, int nh, int nkv, int cap, int splits,
                           float* part, int32_t* status, cudaStream_t st) {
-    static bool attr_set = false;
     const int smem = (int)sizeof(AttnSmem<HD>);
-    if (!attr_set) {
-        cudaFuncSetAttribute(attn_split_kernel<HD, GROUP>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        attr_set = true;
-    }
+    if (allow_max_dynamic_smem((const void*)attn_split_kernel<HD, GROUP>) != cudaSuccess) return false;
     dim3 grid(splits, nkv, R);
     attn_split_kernel<HD, GROUP><<<grid, 128, smem, st>>>(q, k, v, row_seq, row_len, len_add, nh, nkv, cap, splits,
                                                           part, status);
+    return true;
 }
 
 int launch_attention(const float* q, const __nv_bfloat16* k, const __nv_bfloat16* v, const int32_t* row_seq,
@@ -833,7 +830,9 @@ int launch_attention(const float* q, const __nv_bfloat16* k, const __nv_bfloat16
     const int group = nh / nkv;
 #define Q3_ATTN_CASE(HDV, GV)                                                                         \
     if (hd == HDV && group == GV) {                                                                   \
-        launch_attn_t<HDV, GV>(q, k, v, row_seq, row_len, len_add, R, nh, nkv, cap, splits, part, status, st); \
+        if (!launch_attn_t<HDV, GV>(q, k, v, row_seq, row_len, len_add, R, nh, nkv, cap, splits, part, status, \
+                                    st))                                                              \
+            return -2;                                                                                \
         attn_merge_kernel<HDV><<<R * nh, HDV, 0, st>>>(part, nh, splits, row_len, len_add, out, outh, ldh, \
                                                        frag);                                                 \
         return 0;                                                                                     \
@@ -851,19 +850,16 @@ int launch_attention(const float* q, const __nv_bfloat16* k, const __nv_bfloat16
 }
 
 template <int HD, int GROUP>
-static void launch_attn_decode_t(const float* qkv, const float* q_norm, const float* k_norm, float eps,
+static bool launch_attn_decode_t(const float* qkv, const float* q_norm, const float* k_norm, float eps,
                                  const float2* rope_cs, __nv_bfloat16* kc, __nv_bfloat16* vc, const int32_t* row_seq,
                                  const int32_t* row_pos, int R, int nh, int nkv, int cap, int splits, float* part,
                                  __half* outh, int ldh, int frag, int32_t* status, cudaStream_t st) {
-    static bool attr_set = false;
     const int smem = (int)sizeof(AttnSmem<HD>);
-    if (!attr_set) {
-        cudaFuncSetAttribute(attn_decode_kernel<HD, GROUP>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        attr_set = true;
-    }
+    if (allow_max_dynamic_smem((const void*)attn_decode_kernel<HD, GROUP>) != cudaSuccess) return false;
     dim3 grid(splits, nkv, R);
     launch_pdl(attn_decode_kernel<HD, GROUP>, grid, 128, smem, st, qkv, q_norm, k_norm, eps, rope_cs, kc, vc, row_seq,
                row_pos, nh, nkv, cap, splits, part, outh, ldh, frag, status);
+    return true;
 }
 
 int launch_attention_decode(const float* qkv, const float* q_norm, const float* k_norm, float eps,
@@ -874,8 +870,9 @@ int launch_attention_decode(const float* qkv, const float* q_norm, const float* 
     const int group = nh / nkv;
 #define Q3_ATTN_CASE(HDV, GV)                                                                                      \
     if (hd == HDV && group == GV) {                                                                                \
-        launch_attn_decode_t<HDV, GV>(qkv, q_norm, k_norm, eps, rope_cs, kc, vc, row_seq, row_pos, R, nh, nkv, cap, \
-                                      splits, part, splits == 1 ? outh : nullptr, ldh, frag, status, st);          \
+        if (!launch_attn_decode_t<HDV, GV>(qkv, q_norm, k_norm, eps, rope_cs, kc, vc, row_seq, row_pos, R, nh, nkv,  \
+                                           cap, splits, part, splits == 1 ? outh : nullptr, ldh, frag, status, st)) \
+            return -2;                                                                                             \
         if (splits > 1)                                                                                            \
             launch_pdl(attn_merge_kernel<HDV>, R * nh, HDV, 0, st, part, nh, splits, row_pos, 1, (float*)nullptr, \
                        outh, ldh, frag);                                                                           \

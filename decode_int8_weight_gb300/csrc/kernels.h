@@ -67,6 +67,10 @@ __host__ __device__ inline size_t plane_index(int col, int k, int K, int frag) {
     return word * 2 + (k & 1);
 }
 
+// Opts kernel fn in to the device's largest dynamic shared memory on the
+// current device, once per (kernel, device); thread-safe.
+cudaError_t allow_max_dynamic_smem(const void* fn);
+
 void launch_gemv(const GemvArgs& a, int mode, int grid, cudaStream_t st);
 int gemv_grid(int rows, int mode, int num_sms);
 

@@ -1,0 +1,1128 @@
+// Small-batch decode step: three kernels per layer plus the lm_head sweep (sm_103a).
+//
+// The decoder block is the Qwen3 family's ("Model-agnostic LLM inference",
+// section "Supported models"): RMSNorm -> QKV -> per-head RMSNorm on Q and
+// K -> RoPE -> bf16 KV append -> grouped-query attention -> O + residual ->
+// RMSNorm -> SiLU-gated FFN + residual; then the final RMSNorm and the tied
+// lm_head with the greedy argmax ("Run local LLM decode", section
+// "Limitations").  Single-stream decode streams every weight once per step
+// ("LLM inference overview", section "Workload characteristics"), so each
+// kernel moves its weights into shared memory before it waits on the
+// previous kernel: after the wait only the activations are loaded.
+//
+// Every kernel is launched with programmatic dependent launch.  A kernel
+// lets its successor start only after its own wait has returned, so when a
+// kernel's prologue runs, every kernel two or more places before it in the
+// stream has completed: the prologues read only constant data (weights,
+// scales) and, from the second layer on, the positions and the cached K/V
+// of earlier steps.
+#include <algorithm>
+
+#include <cooperative_groups.h>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "step.h"
+
+namespace cg = cooperative_groups;
+
+namespace q3 {
+namespace {
+
+constexpr int kThreads = 256;  // 8 warps
+constexpr int kWarps = 8;
+constexpr int kLmThreads = 288;  // lm_head: 8 consumer warps + 1 producer warp
+constexpr int kGateTmax = 4;     // gate/up tiles per CTA (most)
+constexpr int kDownKpw = 12;     // down k-pairs per warp (most)
+
+// ------------------------------------------------------------- fixed point
+// The residual stream between kernels is value * 2^32 in a signed 64-bit
+// integer (resolution 2.3e-10, range +-2.1e9).  Partial sums of a split
+// projection are converted once and meet in integer atomic adds, which give
+// the same bits in any order.
+constexpr float kFixOne = 4294967296.0f;
+constexpr float kFixUnit = 2.3283064365386963e-10f;
+
+// Both conversions go through 32-bit halves: the 64-bit integer <-> float
+// conversions are much slower on this part, and these give the same results
+// (round to nearest even into the fixed point; correctly rounded back).
+Q3_DEV long long fix_of(float v) {
+    const float f = v * kFixOne;
+    const float a = fabsf(f);
+    const uint32_t hi = __float2uint_rz(a * kFixUnit);
+    const float rem = a - (float)hi * kFixOne;  // exact: a multiple of ulp(a) below 2^32
+    const unsigned long long m = ((unsigned long long)hi << 32) + __float2uint_rn(rem);
+    return f < 0.f ? -(long long)m : (long long)m;
+}
+Q3_DEV float float_of_fix(long long x) {
+    const bool neg = x < 0;
+    const unsigned long long m = neg ? (unsigned long long)(-(x + 1)) + 1ull : (unsigned long long)x;
+    const float v = __uint2float_rn((uint32_t)(m >> 32)) + __uint2float_rn((uint32_t)m) * kFixUnit;
+    return neg ? -v : v;
+}
+Q3_DEV void red_add_fix(long long* p, long long v) {
+    asm volatile("red.relaxed.gpu.global.add.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+// ------------------------------------------------------------- clusters
+Q3_DEV int cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return (int)r;
+}
+Q3_DEV void cluster_arrive() { asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory"); }
+Q3_DEV void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
+template <typename T>
+Q3_DEV const T* peer(const T* p, int rank) {
+    return cg::this_cluster().map_shared_rank(p, rank);
+}
+
+// ------------------------------------------------------------- operands
+// Index of the f16 half for column col (0..7) and k within one 8-column tile
+// of a fragment-ordered B operand (the m16n8k16 B registers of lane
+// 4 col + (k % 8) / 2, word 2 ((k / 16) % 2) + (k / 8) % 2, half k % 2).
+Q3_DEV int frag_half(int col, int k) {
+    const int lanef = col * 4 + ((k & 7) >> 1);
+    const int w = ((k >> 4) & 1) * 2 + ((k >> 3) & 1);
+    return (((k >> 5) * 32 + lanef) * 4 + w) * 2 + (k & 1);
+}
+
+Q3_DEV uint32_t pack_half2(__half a, __half b) {
+    return (uint32_t)__half_as_ushort(a) | ((uint32_t)__half_as_ushort(b) << 16);
+}
+
+// 32-bit word of the fragment-ordered B operand (one 8-column tile) that
+// holds column col, k and k + 1 (k even).
+Q3_DEV int frag_word(int col, int k) {
+    return (((k >> 5) * 32 + col * 4 + ((k & 7) >> 1)) * 4) + ((k >> 4) & 1) * 2 + ((k >> 3) & 1);
+}
+
+// RMSNorm of up to 4 rows into the fragment-ordered B operand of one 8-column
+// MMA tile: column 2b holds f16(v) and column 2b + 1 holds f16(v - f16(v)) of
+// v = (x[b][k] * inv_rms[b]) * gain[k].  Columns of rows b >= B are left
+// as they are: each output column of an MMA depends only on its own operand
+// column, so those outputs are simply never read.  x is read from the
+// fixed-point stream xin ([B][H]) or, with xin null, is the embedding row of
+// token tok[b] (emb, emb_scale); gain is in shared memory.  Thread t owns
+// k = 4t .. 4t + 3; every thread of the block takes part in the barriers.
+// H <= 4 * 256.
+Q3_DEV void norm_operand(uint4* xop, const long long* xin, const int* tok, const int8_t* emb, const float* emb_scale,
+                         int B, int H, const float* gain, float eps, float* s_red) {
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const bool own = tid < kThreads && 4 * tid < H;
+    const int k0 = 4 * tid;
+    float x[kStepMaxBatch][4];
+    float ss[kStepMaxBatch];
+#pragma unroll
+    for (int b = 0; b < kStepMaxBatch; ++b) {
+        ss[b] = 0.f;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) x[b][j] = 0.f;
+        if (own && b < B) {
+            if (xin) {
+                const longlong2 v0 = __ldcg(reinterpret_cast<const longlong2*>(xin + (size_t)b * H + k0));
+                const longlong2 v1 = __ldcg(reinterpret_cast<const longlong2*>(xin + (size_t)b * H + k0 + 2));
+                x[b][0] = float_of_fix(v0.x), x[b][1] = float_of_fix(v0.y);
+                x[b][2] = float_of_fix(v1.x), x[b][3] = float_of_fix(v1.y);
+            } else {
+                const int t = tok[b];
+                const char4 e = *reinterpret_cast<const char4*>(emb + (size_t)t * H + k0);
+                const float es = emb_scale[t];
+                x[b][0] = (float)e.x * es, x[b][1] = (float)e.y * es, x[b][2] = (float)e.z * es, x[b][3] = (float)e.w * es;
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) ss[b] += x[b][j] * x[b][j];
+        }
+    }
+#pragma unroll
+    for (int b = 0; b < kStepMaxBatch; ++b)
+        if (b < B) {
+            ss[b] = warp_sum(ss[b]);
+            if (lane == 0 && warp < kWarps) s_red[warp * 4 + b] = ss[b];
+        }
+    __syncthreads();
+    if (own) {
+        const float4 g = *reinterpret_cast<const float4*>(gain + k0);
+        const float gg[4] = {g.x, g.y, g.z, g.w};
+        uint32_t* xw = reinterpret_cast<uint32_t*>(xop);
+#pragma unroll
+        for (int b = 0; b < kStepMaxBatch; ++b) {
+            if (b >= B) break;
+            float t = 0.f;
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) t += s_red[w * 4 + b];
+            const float inv = 1.0f / sqrtf(t / (float)H + eps);
+            __half hi[4], lo[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) split_f16(__fmul_rn(__fmul_rn(x[b][j], inv), gg[j]), hi[j], lo[j]);
+            xw[frag_word(2 * b, k0)] = pack_half2(hi[0], hi[1]);
+            xw[frag_word(2 * b, k0 + 2)] = pack_half2(hi[2], hi[3]);
+            xw[frag_word(2 * b + 1, k0)] = pack_half2(lo[0], lo[1]);
+            xw[frag_word(2 * b + 1, k0 + 2)] = pack_half2(lo[2], lo[3]);
+        }
+    }
+    __syncthreads();
+}
+
+// Two m16n8k16 MMAs from one 16-byte lane chunk of a tile blob (rows g, g+8;
+// two 16-wide k-steps) and the lane's four B words.
+Q3_DEV void mma_pair(float (&c0)[4], float (&c1)[4], const uint4& wv, const uint4& bv) {
+    uint32_t A0[4], A1[4];
+    u8x4_to_f16x2x2(wv.x, A0[0], A0[1]);
+    u8x4_to_f16x2x2(wv.y, A0[2], A0[3]);
+    u8x4_to_f16x2x2(wv.z, A1[0], A1[1]);
+    u8x4_to_f16x2x2(wv.w, A1[2], A1[3]);
+    mma_f16_16816(c0, A0, bv.x, bv.y);
+    mma_f16_16816(c1, A1, bv.z, bv.w);
+}
+
+// acc[t] += tile t (t < nt) of the tile blobs at w (shared memory, K =
+// 32 kpairs) times the operand, over this warp's k-pairs (warp, warp + 8, ...).
+template <int TMAX>
+Q3_DEV void mma_tiles(float (&acc)[TMAX][4], const unsigned char* w, uint32_t blob, int nt, const uint4* xop,
+                      int kpairs) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    float acc2[TMAX][4];
+#pragma unroll
+    for (int t = 0; t < TMAX; ++t)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc[t][i] = acc2[t][i] = 0.f;
+    for (int p = warp; p < kpairs; p += kWarps) {
+        const uint4 bv = xop[p * 32 + lane];
+#pragma unroll
+        for (int t = 0; t < TMAX; ++t) {
+            if (t < nt) {
+                const uint4 wv =
+                    *reinterpret_cast<const uint4*>(w + (size_t)t * blob + kTileHeader + (size_t)p * 512 + lane * 16);
+                mma_pair(acc[t], acc2[t], wv, bv);
+            }
+        }
+    }
+#pragma unroll
+    for (int t = 0; t < TMAX; ++t)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc[t][i] += acc2[t][i];
+}
+
+// Bounded wait shared by a whole block: every thread waits, and the block
+// agrees on the outcome (true when any thread's wait gave up).
+Q3_DEV bool block_wait_failed(uint64_t* bar, uint32_t parity) {
+    const bool ok = mbar_wait_bounded(bar, parity);
+    return __syncthreads_or(!ok) != 0;
+}
+
+}  // namespace
+
+// ===================================================================== layouts
+struct AttnBlockLayout {
+    uint32_t wq, wo, red, xop, qkv, qn, kn, vn, ring, wst, part, oop, osc, gain, qkg, rope, resid, misc, bars, total;
+};
+
+__host__ __device__ inline uint32_t take_smem(uint32_t& off, size_t bytes) {
+    const uint32_t o = off;
+    off = (uint32_t)((off + bytes + 127) & ~(size_t)127);
+    return o;
+}
+
+// The QKV weight region is dead once the QKV rows are reduced: the per-head
+// vectors, softmax states and the O operand reuse it.  The partial sums of
+// the QKV reduction reuse the operand region.
+__host__ __device__ inline AttnBlockLayout attn_block_layout(int H, int hd, int kv_stages) {
+    AttnBlockLayout L{};
+    uint32_t off = 0;
+    const int T = 3 * hd / 16, tmax = (T + kClusterCtas - 1) / kClusterCtas;
+    {
+        uint32_t w = 0;
+        L.qn = take_smem(w, (size_t)kStepMaxBatch * hd * 4);
+        L.kn = take_smem(w, (size_t)kStepMaxBatch * hd * 4);
+        L.vn = take_smem(w, (size_t)kStepMaxBatch * hd * 4);
+        L.wst = take_smem(w, (size_t)kWarps * kStepMaxBatch * hd * 4);  // warp states, then the parked parts
+        L.part = take_smem(w, (size_t)kStepMaxBatch * (hd + 4) * 4);  // 16-byte aligned states
+        L.oop = take_smem(w, (size_t)(hd / 32) * 512);
+        const size_t wq_bytes = (size_t)tmax * tile_blob_bytes(H);
+        L.wq = take_smem(off, wq_bytes > w ? wq_bytes : w);
+        L.qn += L.wq, L.kn += L.wq, L.vn += L.wq, L.wst += L.wq, L.part += L.wq, L.oop += L.wq;
+    }
+    L.wo = take_smem(off, (size_t)(H / kClusterCtas / 16) * (hd / 32) * 512);
+    {
+        const size_t xop_bytes = (size_t)(H / 32) * 512, red_bytes = (size_t)tmax * kWarps * 32 * 16;
+        L.xop = take_smem(off, xop_bytes > red_bytes ? xop_bytes : red_bytes);
+        L.red = L.xop;
+    }
+    L.qkv = take_smem(off, (size_t)tmax * 16 * kStepMaxBatch * 4);
+    L.ring = take_smem(off, (size_t)kv_stages * 2 * kStepKvChunk * hd * 2);
+    L.osc = take_smem(off, (size_t)(H / kClusterCtas) * 4);
+    L.gain = take_smem(off, (size_t)H * 4);
+    L.qkg = take_smem(off, (size_t)2 * hd * 4);
+    L.rope = take_smem(off, (size_t)kStepMaxBatch * (hd / 2) * 8);
+    L.resid = take_smem(off, (size_t)kStepMaxBatch * (H / kClusterCtas) * 8);
+    L.misc = take_smem(off, 256);
+    L.bars = take_smem(off, (size_t)(2 + kv_stages) * 8);
+    L.total = off;
+    return L;
+}
+
+struct GateLayout {
+    uint32_t w, xop, red, gain, misc, bar, total;
+};
+__host__ __device__ inline GateLayout gate_layout(int H, int tpc) {
+    GateLayout L{};
+    uint32_t off = 0;
+    L.w = take_smem(off, (size_t)tpc * tile_blob_bytes(H));
+    {
+        const size_t xop_bytes = (size_t)(H / 32) * 512, red_bytes = (size_t)tpc * kWarps * 32 * 16;
+        L.xop = take_smem(off, xop_bytes > red_bytes ? xop_bytes : red_bytes);  // the partial sums reuse it
+        L.red = L.xop;
+    }
+    L.gain = take_smem(off, (size_t)H * 4);
+    L.misc = take_smem(off, 256);
+    L.bar = take_smem(off, 8);
+    L.total = off;
+    return L;
+}
+
+struct DownLayout {
+    uint32_t w, red, misc, bar, total;
+};
+__host__ __device__ inline DownLayout down_layout(int I, int ks) {
+    DownLayout L{};
+    uint32_t off = 0;
+    const int kp = I / 32, per = (kp + ks - 1) / ks;
+    L.w = take_smem(off, (size_t)per * 512);
+    L.red = take_smem(off, (size_t)kWarps * 32 * 16);
+    L.misc = take_smem(off, 128);
+    L.bar = take_smem(off, 8);
+    L.total = off;
+    return L;
+}
+
+struct LmLayout {
+    uint32_t ring, xop, gain, best, misc, bars, total;
+};
+__host__ __device__ inline LmLayout lm_layout(int H, int stages) {
+    LmLayout L{};
+    uint32_t off = 0;
+    L.ring = take_smem(off, (size_t)stages * tile_blob_bytes(H));
+    L.xop = take_smem(off, (size_t)(H / 32) * 512);
+    L.gain = take_smem(off, (size_t)H * 4);
+    L.best = take_smem(off, (size_t)kWarps * 4 * 8);
+    L.misc = take_smem(off, 256);
+    L.bars = take_smem(off, (size_t)2 * stages * 8);
+    L.total = off;
+    return L;
+}
+
+// ===================================================================== attention block
+// Cluster c (8 CTAs) serves query head h = c of kv group g = h / (nh / nkv).
+//  1. RMSNorm of the residual stream (every CTA, from the fixed-point rows).
+//  2. The cluster's QKV rows (head h of Wq, group g of Wk and Wv: 3 hd rows
+//     in 16-row tiles) are split over the 8 CTAs; each CTA multiplies its
+//     tiles, already in shared memory, by the normed rows.
+//  3. Every CTA gathers the 3 hd values per sequence from its peers' shared
+//     memory, applies the per-head RMSNorm of q and k and RoPE at the
+//     sequence's position, and rounds k and v to bf16.  CTA 7 of the group's
+//     first cluster appends them to the cache.
+//  4. The cached positions 0..p-1 of each sequence are split over the 8 CTAs
+//     (16-position chunks staged by bulk copies); CTA 7 also attends the new
+//     position p from the rounded values it holds.  Each CTA keeps an online
+//     softmax state (m, l, acc) per sequence.
+//  5. Every CTA merges the 8 states (distributed shared memory) into the
+//     head's output o and multiplies its H/8 rows of Wo[:, head h] by it; the
+//     rows are added to the fixed-point residual stream (cluster 0 also adds
+//     the stream's input).
+// Before the wait the CTA starts the bulk copies of its QKV tiles and O
+// slice and copies the gains, row scales and (from the second layer on,
+// where the positions are final) the RoPE rows into shared memory and
+// starts its K/V stages; after the wait the only global reads are the
+// residual rows (and, in the first layer, the tokens and their embedding).
+template <int HD>
+__global__ void __launch_bounds__(kThreads, 2) attn_block_kernel(const AttnBlockArgs a) {
+    constexpr int D = HD / 32;  // contiguous dims per lane (attention)
+    constexpr int E = HD / 32;  // elements l + 32 j per lane (QK-norm, RoPE)
+    constexpr int TH = HD / 16;
+    constexpr int T = 3 * TH;
+    constexpr int TMAX = (T + kClusterCtas - 1) / kClusterCtas;
+    constexpr int PS = HD + 4;  // floats per softmax state {acc[HD], m, l, pad}: 16-byte aligned rows
+    extern __shared__ __align__(128) unsigned char smem[];
+    const AttnBlockLayout L = attn_block_layout(a.H, HD, a.kv_stages);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int r = cluster_rank();
+    const int h = blockIdx.x / kClusterCtas;
+    const int G = a.nh / a.nkv, g = h / G;
+    const int H = a.H, B = a.B, S = a.kv_stages;
+    const int Dq = a.nh * HD, Dkv = a.nkv * HD;
+    const int t0 = r * T / kClusterCtas, t1 = (r + 1) * T / kClusterCtas, nt = t1 - t0;
+    const uint32_t blob = (uint32_t)tile_blob_bytes(H);
+    const int ro = H / kClusterCtas, otiles = ro / 16;
+    const uint32_t oseg = (HD / 32) * 512;
+    const uint32_t oblob = (uint32_t)tile_blob_bytes(Dq);
+    const bool appender = (h % G == 0) && (r == kClusterCtas - 1);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bars);  // 0 QKV weights, 1 O slice, 2.. K/V stages
+    int* s_pos = reinterpret_cast<int*>(smem + L.misc);
+    int* s_seq = s_pos + 4;
+    int* s_tok = s_seq + 4;
+    int* s_last = s_tok + 4;               // [S] last item issued into each stage (-1: none)
+    float* s_inv = reinterpret_cast<float*>(s_last + 8);
+    float* s_red = s_inv + 4;              // [8][4]
+    float* osc = reinterpret_cast<float*>(smem + L.osc);
+    float* s_gain = reinterpret_cast<float*>(smem + L.gain);
+    float* s_qg = reinterpret_cast<float*>(smem + L.qkg);
+    float* s_kg = s_qg + HD;
+    float2* s_rope = reinterpret_cast<float2*>(smem + L.rope);
+    long long* s_res = reinterpret_cast<long long*>(smem + L.resid);
+    uint4* xop = reinterpret_cast<uint4*>(smem + L.xop);
+    float* qkv = reinterpret_cast<float*>(smem + L.qkv);
+    float* qn = reinterpret_cast<float*>(smem + L.qn);
+    float* kn = reinterpret_cast<float*>(smem + L.kn);
+    float* vn = reinterpret_cast<float*>(smem + L.vn);
+    float* wst = reinterpret_cast<float*>(smem + L.wst);
+    float* part = reinterpret_cast<float*>(smem + L.part);
+    uint4* oop = reinterpret_cast<uint4*>(smem + L.oop);
+    __nv_bfloat16* ring = reinterpret_cast<__nv_bfloat16*>(smem + L.ring);
+
+    auto gtile = [&](int t) -> int {
+        if (t < TH) return h * TH + t;
+        if (t < 2 * TH) return Dq / 16 + g * TH + (t - TH);
+        return (Dq + Dkv) / 16 + g * TH + (t - 2 * TH);
+    };
+    auto o_src = [&](int i) -> const uint8_t* {
+        return a.wo + (size_t)(r * otiles + i) * oblob + kTileHeader + (size_t)h * oseg;
+    };
+    auto split_lo = [&](int b) { return r * s_pos[b] / kClusterCtas; };
+    auto split_hi = [&](int b) { return (r + 1) * s_pos[b] / kClusterCtas; };
+    auto nchunks = [&](int b) { return (split_hi(b) - split_lo(b) + kStepKvChunk - 1) / kStepKvChunk; };
+    auto count_items = [&]() {
+        int n = 0;
+        for (int b = 0; b < B; ++b) n += nchunks(b);
+        return n;
+    };
+    auto issue_kv = [&](int i) {  // thread 0 only
+        int b = 0, c = i;
+        while (c >= nchunks(b)) c -= nchunks(b), ++b;
+        const int lo = split_lo(b) + c * kStepKvChunk;
+        const int cnt = min(kStepKvChunk, split_hi(b) - lo);
+        const size_t base = (((size_t)s_seq[b] * a.nkv + g) * a.cap + lo) * HD;
+        const uint32_t bytes = (uint32_t)cnt * HD * 2u;
+        const int s = i % S;
+        __nv_bfloat16* dk = ring + (size_t)s * 2 * kStepKvChunk * HD;
+        mbar_arrive_expect_tx(&bars[2 + s], 2 * bytes);
+        bulk_g2s(dk, a.kc + base, bytes, &bars[2 + s]);
+        bulk_g2s(dk + kStepKvChunk * HD, a.vc + base, bytes, &bars[2 + s]);
+        s_last[s] = i;
+    };
+    // positions known: RoPE rows into shared memory; the first K/V stages
+    auto position_work = [&]() {
+        for (int i = tid; i < B * (HD / 2); i += kThreads) {
+            const int b = i / (HD / 2), j = i - b * (HD / 2);
+            s_rope[i] = a.rope[(size_t)s_pos[b] * (HD / 2) + j];
+        }
+        if (tid == 0) {
+            const int n = count_items();
+            for (int i = 0; i < S && i < n; ++i) issue_kv(i);
+        }
+    };
+
+    // ---- prologue: constant data and, from the second layer on, the positions
+    if (tid == 0) {
+        for (int i = 0; i < 2 + S; ++i) mbar_init(&bars[i], 1);
+        fence_mbar_init();
+        for (int i = 0; i < S; ++i) s_last[i] = -1;
+    }
+    if (a.pos_early && tid < B) {
+        s_pos[tid] = a.pos[tid];
+        s_seq[tid] = a.seq_ids[tid];
+    }
+    __syncthreads();
+    if (tid == 0) {
+        mbar_arrive_expect_tx(&bars[0], (uint32_t)nt * blob);
+        for (int t = t0; t < t1; ++t)
+            bulk_g2s(smem + L.wq + (size_t)(t - t0) * blob, a.wqkv + (size_t)gtile(t) * blob, blob, &bars[0]);
+        mbar_arrive_expect_tx(&bars[1], (uint32_t)otiles * oseg);
+        for (int i = 0; i < otiles; ++i) bulk_g2s(smem + L.wo + (size_t)i * oseg, o_src(i), oseg, &bars[1]);
+    }
+    for (int i = tid; i < ro; i += kThreads) osc[i] = a.o_scale[r * ro + i];
+    for (int i = tid; i < H; i += kThreads) s_gain[i] = a.attn_norm[i];
+    for (int i = tid; i < HD; i += kThreads) s_qg[i] = a.q_norm[i], s_kg[i] = a.k_norm[i];
+    if (a.pos_early) position_work();
+    pdl_wait();
+    pdl_launch_dependents();
+
+    // ---- after the wait: positions and tokens (first layer), residual rows
+    if (!a.pos_early) {
+        if (tid < B) {
+            s_pos[tid] = a.pos[tid];
+            s_seq[tid] = a.seq_ids[tid];
+            if (!a.xin) s_tok[tid] = a.tokens[tid];
+        }
+        __syncthreads();
+        position_work();
+    }
+    if (h == 0)  // this cluster adds the stream's input to its rows
+        for (int i = tid; i < B * ro; i += kThreads) {
+            const int b = i / ro, R = r * ro + (i - b * ro);
+            s_res[i] = a.xin ? __ldcg(a.xin + (size_t)b * H + R)
+                             : fix_of((float)a.emb[(size_t)s_tok[b] * H + R] * a.emb_scale[s_tok[b]]);
+        }
+    const int n_items = count_items();
+
+    // ---- 1. RMSNorm operand, 2. this CTA's QKV rows
+    norm_operand(xop, a.xin, s_tok, a.emb, a.emb_scale, B, H, s_gain, a.eps, s_red);
+    bool bad = block_wait_failed(&bars[0], 0);
+    {
+        float acc[TMAX][4];
+        mma_tiles<TMAX>(acc, smem + L.wq, blob, bad ? 0 : nt, xop, H / 32);
+        __syncthreads();  // every warp is done with the operand (the partial sums reuse it)
+        float4* red = reinterpret_cast<float4*>(smem + L.red);
+#pragma unroll
+        for (int t = 0; t < TMAX; ++t)
+            if (t < nt) red[(t * kWarps + warp) * 32 + lane] = make_float4(acc[t][0], acc[t][1], acc[t][2], acc[t][3]);
+        __syncthreads();
+        if (tid < nt * 32) {
+            const int t = tid >> 5, ln = tid & 31, gg = ln >> 2, tq = ln & 3;
+            float s0 = 0.f, s1 = 0.f;
+            for (int w = 0; w < kWarps; ++w) {
+                const float4 v = red[(t * kWarps + w) * 32 + ln];
+                s0 += v.x + v.y;
+                s1 += v.z + v.w;
+            }
+            const float* sc = reinterpret_cast<const float*>(smem + L.wq + (size_t)t * blob);
+            qkv[(t * 16 + gg) * 4 + tq] = sc[gg] * s0;
+            qkv[(t * 16 + gg + 8) * 4 + tq] = sc[gg + 8] * s1;
+        }
+    }
+    cluster_arrive();
+    cluster_wait();  // every CTA's QKV rows are visible in the cluster
+
+    // ---- 3. gather q, k, v from the peers; QK-RMSNorm, RoPE, bf16 rounding
+    // warp b < B: query of sequence b; warp 4 + b: key and value of sequence b
+    // (lane l holds elements l + 32 j, so both members of a RoPE pair sit in
+    // one lane)
+    if ((warp & 3) < B) {
+        const int b = warp & 3;
+        const bool is_q = warp < 4;
+        auto fetch = [&](int j) -> float {  // row j of the cluster's 3 hd rows, sequence b
+            const int t = j >> 4;
+            const int owner = (kClusterCtas * t + kClusterCtas - 1) / T;
+            const int ot0 = owner * T / kClusterCtas;
+            return peer(qkv, owner)[((t - ot0) * 16 + (j & 15)) * 4 + b];
+        };
+        float v[E], vv[E];
+#pragma unroll
+        for (int j = 0; j < E; ++j) {
+            v[j] = fetch((is_q ? 0 : HD) + lane + 32 * j);
+            vv[j] = is_q ? 0.f : fetch(2 * HD + lane + 32 * j);
+        }
+        const float* gain = is_q ? s_qg : s_kg;
+        const float2* cs = s_rope + b * (HD / 2);
+        float ss = 0.f;
+#pragma unroll
+        for (int j = 0; j < E; ++j) ss += v[j] * v[j];
+        ss = warp_sum(ss);
+        const float inv = 1.0f / sqrtf(ss / (float)HD + a.eps);
+#pragma unroll
+        for (int j = 0; j < E; ++j) v[j] = __fmul_rn(__fmul_rn(v[j], inv), gain[lane + 32 * j]);
+#pragma unroll
+        for (int j = 0; j < E / 2; ++j) {
+            const float2 c = cs[lane + 32 * j];
+            const float a0 = v[j], b0 = v[j + E / 2];
+            v[j] = __fsub_rn(__fmul_rn(a0, c.x), __fmul_rn(b0, c.y));
+            v[j + E / 2] = __fadd_rn(__fmul_rn(b0, c.x), __fmul_rn(a0, c.y));
+        }
+        float* vec = (is_q ? qn : kn) + b * HD;
+        if (is_q) {
+#pragma unroll
+            for (int j = 0; j < E; ++j) vec[lane + 32 * j] = v[j];
+        } else {
+#pragma unroll
+            for (int j = 0; j < E; ++j) {
+                vec[lane + 32 * j] = __bfloat162float(__float2bfloat16_rn(v[j]));
+                vn[b * HD + lane + 32 * j] = __bfloat162float(__float2bfloat16_rn(vv[j]));
+            }
+        }
+    }
+    __syncthreads();
+
+    // ---- 4. attention over this CTA's split of every sequence
+    const float scale = 1.0f / sqrtf((float)HD);
+    int item = 0;
+    for (int b = 0; b < B; ++b) {
+        float q[D], acc[D];
+        float m = -INFINITY, l = 0.f;
+#pragma unroll
+        for (int d = 0; d < D; ++d) q[d] = qn[b * HD + lane * D + d], acc[d] = 0.f;
+        const int lo = split_lo(b), hi = split_hi(b), nch = nchunks(b);
+        for (int c = 0; c < nch; ++c, ++item) {
+            const int s = item % S;
+            const bool ok = bad || mbar_wait_bounded(&bars[2 + s], (uint32_t)(item / S) & 1u);
+            const int cnt = min(kStepKvChunk, hi - lo - c * kStepKvChunk);
+            const __nv_bfloat16* ks = ring + (size_t)s * 2 * kStepKvChunk * HD;
+            const __nv_bfloat16* vs = ks + kStepKvChunk * HD;
+            float sc[kStepKvChunk / kWarps];
+#pragma unroll
+            for (int i = 0; i < kStepKvChunk / kWarps; ++i) {
+                const int j = warp + kWarps * i;
+                float dot = 0.f;
+                if (j < cnt && ok && !bad) {
+                    const __nv_bfloat16* kr = ks + (size_t)j * HD + lane * D;
+#pragma unroll
+                    for (int d = 0; d < D; ++d) dot += q[d] * __bfloat162float(kr[d]);
+                }
+                dot = warp_sum(dot);
+                sc[i] = (j < cnt) ? dot * scale : -INFINITY;
+            }
+            float cm = sc[0];
+#pragma unroll
+            for (int i = 1; i < kStepKvChunk / kWarps; ++i) cm = fmaxf(cm, sc[i]);
+            const float mn = fmaxf(m, cm);
+            if (mn != -INFINITY) {
+                const float corr = (m == -INFINITY) ? 0.f : expf(m - mn);
+                l *= corr;
+#pragma unroll
+                for (int d = 0; d < D; ++d) acc[d] *= corr;
+#pragma unroll
+                for (int i = 0; i < kStepKvChunk / kWarps; ++i) {
+                    if (sc[i] == -INFINITY) continue;
+                    const float p = expf(sc[i] - mn);
+                    l += p;
+                    const __nv_bfloat16* vr = vs + (size_t)(warp + kWarps * i) * HD + lane * D;
+#pragma unroll
+                    for (int d = 0; d < D; ++d) acc[d] += p * __bfloat162float(vr[d]);
+                }
+                m = mn;
+            }
+            bad = __syncthreads_or(!ok) != 0 || bad;  // every warp is done with stage s
+            if (tid == 0 && !bad && item + S < n_items) issue_kv(item + S);
+        }
+        if (r == kClusterCtas - 1 && warp == 0) {
+            // the new position, from the rounded values in shared memory
+            float dot = 0.f;
+#pragma unroll
+            for (int d = 0; d < D; ++d) dot += q[d] * kn[b * HD + lane * D + d];
+            const float sc = warp_sum(dot) * scale;
+            const float mn = fmaxf(m, sc);
+            const float corr = (m == -INFINITY) ? 0.f : expf(m - mn);
+            const float pe = expf(sc - mn);
+            l = l * corr + pe;
+#pragma unroll
+            for (int d = 0; d < D; ++d) acc[d] = acc[d] * corr + pe * vn[b * HD + lane * D + d];
+            m = mn;
+        }
+        // merge the 8 warps' states into this CTA's state for sequence b
+        float* ws = wst + warp * (HD + 2);
+        if (lane == 0) ws[HD] = m, ws[HD + 1] = l;
+#pragma unroll
+        for (int d = 0; d < D; ++d) ws[lane * D + d] = acc[d];
+        __syncthreads();
+        for (int d = tid; d < HD; d += kThreads) {
+            float M = -INFINITY;
+            for (int w = 0; w < kWarps; ++w) M = fmaxf(M, wst[w * (HD + 2) + HD]);
+            float Ls = 0.f, A = 0.f;
+            if (M != -INFINITY)
+                for (int w = 0; w < kWarps; ++w) {
+                    const float mw = wst[w * (HD + 2) + HD];
+                    if (mw == -INFINITY) continue;
+                    const float f = expf(mw - M);
+                    Ls += wst[w * (HD + 2) + HD + 1] * f;
+                    A += wst[w * (HD + 2) + d] * f;
+                }
+            float* pb = part + b * PS;
+            pb[d] = A;
+            if (d == 0) pb[HD] = M, pb[HD + 1] = Ls;
+        }
+        __syncthreads();
+    }
+
+    // ---- 5. merge the cluster's states; this CTA's rows of Wo[:, head h]
+    cluster_arrive();
+    cluster_wait();  // every CTA's states are visible in the cluster
+    // warp w reads CTA w's state of every sequence (one batch of 16-byte
+    // loads), scales it by its softmax weight and parks it; then each output
+    // element sums the 8 parked parts
+    {
+        float* s_m = reinterpret_cast<float*>(smem + L.qkv);  // [8][4] m, then [8][4] l (the QKV rows are done)
+        float* s_l = s_m + kClusterCtas * 4;
+        float4 av[kStepMaxBatch];
+        const float* pp = peer(part, warp);
+        constexpr int V = HD / 4;  // float4 per state
+#pragma unroll
+        for (int b = 0; b < kStepMaxBatch; ++b)
+            if (b < B && lane < V) av[b] = *reinterpret_cast<const float4*>(pp + b * PS + lane * 4);
+        if (lane < B) {
+            s_m[warp * 4 + lane] = pp[lane * PS + HD];
+            s_l[warp * 4 + lane] = pp[lane * PS + HD + 1];
+        }
+        __syncthreads();
+        float* contrib = wst;  // [8][4][HD] (the warps' attention states are done)
+#pragma unroll
+        for (int b = 0; b < kStepMaxBatch; ++b) {
+            if (b >= B) break;
+            float M = -INFINITY;
+#pragma unroll
+            for (int w = 0; w < kClusterCtas; ++w) M = fmaxf(M, s_m[w * 4 + b]);
+            float Ls = 0.f;
+#pragma unroll
+            for (int w = 0; w < kClusterCtas; ++w) {
+                const float mw = s_m[w * 4 + b];
+                if (mw != -INFINITY) Ls += s_l[w * 4 + b] * expf(mw - M);
+            }
+            const float mine = s_m[warp * 4 + b];
+            const float f = (mine == -INFINITY) ? 0.f : expf(mine - M) / Ls;
+            if (lane < V) {
+                const float4 x = av[b];
+                *reinterpret_cast<float4*>(contrib + (warp * kStepMaxBatch + b) * HD + lane * 4) =
+                    make_float4(x.x * f, x.y * f, x.z * f, x.w * f);
+            }
+        }
+        __syncthreads();
+        __half* ooph = reinterpret_cast<__half*>(oop);
+        for (int i = tid; i < B * HD; i += kThreads) {
+            const int b = i / HD, d = i - b * HD;
+            float o = 0.f;
+#pragma unroll
+            for (int w = 0; w < kClusterCtas; ++w) o += contrib[(w * kStepMaxBatch + b) * HD + d];
+            __half hi, lo;
+            split_f16(o, hi, lo);
+            ooph[frag_half(2 * b, d)] = hi;
+            ooph[frag_half(2 * b + 1, d)] = lo;
+        }
+    }
+    cluster_arrive();  // done with the peers' shared memory (waited for before leaving)
+    bad = block_wait_failed(&bars[1], 0) || bad;
+    if (warp < otiles && !bad) {
+        const unsigned char* wt = smem + L.wo + (size_t)warp * oseg;
+        float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int p = 0; p < HD / 32; ++p) {
+            const uint4 wv = *reinterpret_cast<const uint4*>(wt + p * 512 + lane * 16);
+            mma_pair(c0, c1, wv, oop[p * 32 + lane]);
+        }
+        const int gg = lane >> 2, tq = lane & 3;
+        if (tq < B) {
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                const int rl = warp * 16 + gg + 8 * half;
+                const int R = r * ro + rl;
+                const float s = half ? (c0[2] + c0[3] + c1[2] + c1[3]) : (c0[0] + c0[1] + c1[0] + c1[1]);
+                long long f = fix_of(osc[rl] * s);
+                if (h == 0) f += s_res[tq * ro + rl];
+                red_add_fix(a.xa + (size_t)tq * H + R, f);
+            }
+        }
+    }
+    if (appender)
+        for (int i = tid; i < B * HD; i += kThreads) {
+            const int b = i / HD, d = i - b * HD;
+            const size_t slot = (((size_t)s_seq[b] * a.nkv + g) * a.cap + s_pos[b]) * HD + d;
+            a.kc[slot] = __float2bfloat16_rn(kn[i]);
+            a.vc[slot] = __float2bfloat16_rn(vn[i]);
+        }
+    if (bad && tid == 0) {
+        set_status(a.status, kStatusTimeout);
+        // let every copy this CTA started land before its shared memory goes away
+        mbar_wait_bounded(&bars[0], 0);
+        mbar_wait_bounded(&bars[1], 0);
+        for (int s = 0; s < S; ++s)
+            if (s_last[s] >= 0) mbar_wait_bounded(&bars[2 + s], (uint32_t)(s_last[s] / S) & 1u);
+    }
+    cluster_wait();  // no CTA leaves while a peer may still read its shared memory
+}
+
+// ===================================================================== gate/up
+// CTA c takes tpc consecutive 16-row gate/up tiles (8 gate rows and the
+// same 8 up units each), already in shared memory, and writes the hi/lo
+// planes of a = silu(gate) * up for its 8 tpc units.  It also clears its
+// share of the next residual accumulator.
+__global__ void __launch_bounds__(kThreads, 2) ffn_gate_kernel(const FfnGateArgs a) {
+    extern __shared__ __align__(128) unsigned char smem[];
+    const GateLayout L = gate_layout(a.H, a.tpc);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int H = a.H, B = a.B;
+    const int tiles = 2 * a.I / 16;
+    const int tb = blockIdx.x * a.tpc, nt = min(a.tpc, tiles - tb);
+    const uint32_t blob = (uint32_t)tile_blob_bytes(H);
+    uint64_t* bar = reinterpret_cast<uint64_t*>(smem + L.bar);
+    float* s_inv = reinterpret_cast<float*>(smem + L.misc);
+    float* s_red = s_inv + 4;
+    uint4* xop = reinterpret_cast<uint4*>(smem + L.xop);
+    if (tid == 0) {
+        mbar_init(bar, 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (tid == 0 && nt > 0) {
+        mbar_arrive_expect_tx(bar, (uint32_t)nt * blob);
+        bulk_g2s(smem + L.w, a.wgu + (size_t)tb * blob, (uint32_t)nt * blob, bar);
+    }
+    float* s_gain = reinterpret_cast<float*>(smem + L.gain);
+    for (int i = tid; i < H; i += kThreads) s_gain[i] = a.ffn_norm[i];
+    pdl_wait();
+    pdl_launch_dependents();
+    {
+        const int n = B * H, per = (n + gridDim.x - 1) / gridDim.x;
+        const int z0 = blockIdx.x * per, z1 = min(n, z0 + per);
+        for (int i = z0 + tid; i < z1; i += kThreads) a.xf[i] = 0;
+    }
+    norm_operand(xop, a.xa, nullptr, nullptr, nullptr, B, H, s_gain, a.eps, s_red);
+    const bool bad = nt > 0 && block_wait_failed(bar, 0);
+    float acc[kGateTmax][4];
+    mma_tiles<kGateTmax>(acc, smem + L.w, blob, bad ? 0 : nt, xop, H / 32);
+    __syncthreads();  // every warp is done with the operand (the partial sums reuse it)
+    float4* red = reinterpret_cast<float4*>(smem + L.red);
+#pragma unroll
+    for (int t = 0; t < kGateTmax; ++t)
+        if (t < nt) red[(t * kWarps + warp) * 32 + lane] = make_float4(acc[t][0], acc[t][1], acc[t][2], acc[t][3]);
+    __syncthreads();
+    for (int i = tid; i < nt * 32; i += kThreads) {
+        const int t = i >> 5, ln = i & 31, gg = ln >> 2, tq = ln & 3;
+        if (tq >= B) continue;
+        float s0 = 0.f, s1 = 0.f;
+        for (int w = 0; w < kWarps; ++w) {
+            const float4 v = red[(t * kWarps + w) * 32 + ln];
+            s0 += v.x + v.y;
+            s1 += v.z + v.w;
+        }
+        const float* sc = reinterpret_cast<const float*>(smem + L.w + (size_t)t * blob);
+        const float gate = sc[gg] * s0, up = sc[gg + 8] * s1;
+        const float v = (gate / (1.0f + expf(-gate))) * up;
+        const int unit = (tb + t) * 8 + gg;
+        __half hi, lo;
+        split_f16(v, hi, lo);
+        a.ah[plane_index(2 * tq, unit, a.I, 1)] = hi;
+        a.ah[plane_index(2 * tq + 1, unit, a.I, 1)] = lo;
+    }
+    if (bad && tid == 0) {
+        set_status(a.status, kStatusTimeout);
+        mbar_wait_bounded(bar, 0);
+    }
+}
+
+// ===================================================================== down
+// CTA (tile, part) multiplies its k-pair range of one 16-row down tile
+// (shared memory) by the activation planes, then adds the rows to the
+// fixed-point residual stream; part 0 also carries the stream's input
+// over and clears it for the next layer.
+__global__ void __launch_bounds__(kThreads, 2) ffn_down_kernel(const FfnDownArgs a) {
+    extern __shared__ __align__(128) unsigned char smem[];
+    const DownLayout L = down_layout(a.I, a.ks);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int tile = blockIdx.x / a.ks, part = blockIdx.x - tile * a.ks;
+    const int kp = a.I / 32;
+    const int p_lo = kp * part / a.ks, p_hi = kp * (part + 1) / a.ks;
+    uint64_t* bar = reinterpret_cast<uint64_t*>(smem + L.bar);
+    float* s_sc = reinterpret_cast<float*>(smem + L.misc);
+    if (tid == 0) {
+        mbar_init(bar, 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (tid == 0) {
+        const uint32_t bytes = (uint32_t)(p_hi - p_lo) * 512u;
+        mbar_arrive_expect_tx(bar, bytes);
+        bulk_g2s(smem + L.w, a.wd + (size_t)tile * tile_blob_bytes(a.I) + kTileHeader + (size_t)p_lo * 512, bytes,
+                 bar);
+    }
+    if (tid < 16) s_sc[tid] = a.d_scale[tile * 16 + tid];
+    pdl_wait();
+    pdl_launch_dependents();
+    // this warp's activation words first (independent loads), then the MMAs
+    uint4 bw[kDownKpw];
+    const uint4* ap = reinterpret_cast<const uint4*>(a.ah);
+#pragma unroll
+    for (int j = 0; j < kDownKpw; ++j) {
+        const int p = p_lo + warp + kWarps * j;
+        if (p < p_hi) bw[j] = __ldcg(ap + ((size_t)p * 8) * 32 + lane);
+    }
+    const bool bad = block_wait_failed(bar, 0);
+    float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
+    if (!bad) {
+#pragma unroll
+        for (int j = 0; j < kDownKpw; ++j) {
+            const int p = p_lo + warp + kWarps * j;
+            if (p < p_hi) {
+                const uint4 wv = *reinterpret_cast<const uint4*>(smem + L.w + (size_t)(p - p_lo) * 512 + lane * 16);
+                mma_pair(c0, c1, wv, bw[j]);
+            }
+        }
+    }
+    float4* red = reinterpret_cast<float4*>(smem + L.red);
+    red[warp * 32 + lane] = make_float4(c0[0] + c1[0], c0[1] + c1[1], c0[2] + c1[2], c0[3] + c1[3]);
+    __syncthreads();
+    if (tid < 32) {
+        const int gg = tid >> 2, tq = tid & 3;
+        if (tq < a.B) {
+            float s0 = 0.f, s1 = 0.f;
+            for (int w = 0; w < kWarps; ++w) {
+                const float4 v = red[w * 32 + tid];
+                s0 += v.x + v.y;
+                s1 += v.z + v.w;
+            }
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                const int row = tile * 16 + gg + 8 * half;
+                long long f = fix_of(s_sc[gg + 8 * half] * (half ? s1 : s0));
+                if (part == 0) {
+                    long long* xr = a.xa + (size_t)tq * a.H + row;
+                    f += __ldcg(xr);
+                    *xr = 0;
+                }
+                red_add_fix(a.xf + (size_t)tq * a.H + row, f);
+            }
+        }
+    }
+    if (bad && tid == 0) {
+        set_status(a.status, kStatusTimeout);
+        mbar_wait_bounded(bar, 0);
+    }
+}
+
+// ===================================================================== lm_head
+// The tied embedding table swept once: a producer warp streams the CTA's
+// range of 16-row tiles into a ring of shared-memory stages (the first
+// stages before the wait), and 8 consumer warps each take whole tiles
+// (tile j -> warp j % 8) against the final-RMSNorm operand.  Each lane
+// keeps the best (value, lowest index) key of its sequence; block, then
+// grid atomicMax; the last CTA publishes the tokens.
+__global__ void __launch_bounds__(kLmThreads, 2) lm_head_kernel(const LmHeadArgs a) {
+    extern __shared__ __align__(128) unsigned char smem[];
+    const LmLayout L = lm_layout(a.H, a.stages);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int S = a.stages, H = a.H, B = a.B;
+    const int ntiles = a.rows / 16;
+    const int j0 = (int)((long long)ntiles * blockIdx.x / gridDim.x);
+    const int n = (int)((long long)ntiles * (blockIdx.x + 1) / gridDim.x) - j0;
+    const uint32_t blob = (uint32_t)tile_blob_bytes(H);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bars);
+    uint64_t* empty = full + S;
+    unsigned long long* wbest = reinterpret_cast<unsigned long long*>(smem + L.best);
+    float* s_inv = reinterpret_cast<float*>(smem + L.misc);
+    float* s_red = s_inv + 4;
+    int* s_abort = reinterpret_cast<int*>(s_red + 32);
+    int* s_last = s_abort + 1;
+    uint4* xop = reinterpret_cast<uint4*>(smem + L.xop);
+    const bool producer = warp == kWarps && lane == 0;
+    if (tid == 0) {
+        for (int s = 0; s < S; ++s) mbar_init(&full[s], 1), mbar_init(&empty[s], 1);
+        fence_mbar_init();
+        *s_abort = 0;
+        *s_last = 0;
+    }
+    __syncthreads();
+    int issued = 0;
+    auto issue = [&](int j) {
+        const int s = j % S;
+        mbar_arrive_expect_tx(&full[s], blob);
+        bulk_g2s(smem + L.ring + (size_t)s * blob, a.w + (size_t)(j0 + j) * blob, blob, &full[s]);
+    };
+    if (producer)
+        for (; issued < S && issued < n; ++issued) issue(issued);
+    float* s_gain = reinterpret_cast<float*>(smem + L.gain);
+    for (int i = tid; i < H; i += kLmThreads) s_gain[i] = a.final_norm[i];
+    pdl_wait();
+    pdl_launch_dependents();
+    norm_operand(xop, a.xf, nullptr, nullptr, nullptr, B, H, s_gain, a.eps, s_red);
+
+    if (producer) {
+        for (; issued < n; ++issued) {
+            const int s = issued % S;
+            if (*reinterpret_cast<volatile int*>(s_abort) ||
+                !mbar_wait_bounded(&empty[s], (uint32_t)(issued / S - 1) & 1u)) {
+                *reinterpret_cast<volatile int*>(s_abort) = 1;
+                break;
+            }
+            issue(issued);
+        }
+        *s_last = issued;
+    }
+    unsigned long long best = 0ull;
+    if (warp < kWarps) {
+        const int kpairs = H / 32;
+        const int gg = lane >> 2, tq = lane & 3;
+        for (int j = warp; j < n; j += kWarps) {
+            const int s = j % S;
+            if (*reinterpret_cast<volatile int*>(s_abort)) break;
+            if (!mbar_wait_bounded(&full[s], (uint32_t)(j / S) & 1u)) {
+                *reinterpret_cast<volatile int*>(s_abort) = 1;
+                break;
+            }
+            const unsigned char* wt = smem + L.ring + (size_t)s * blob;
+            float c[4][4];
+#pragma unroll
+            for (int x = 0; x < 4; ++x) c[x][0] = c[x][1] = c[x][2] = c[x][3] = 0.f;
+            for (int p = 0; p < kpairs; p += 2) {
+                const uint4 w0 = *reinterpret_cast<const uint4*>(wt + kTileHeader + (size_t)p * 512 + lane * 16);
+                const uint4 w1 = *reinterpret_cast<const uint4*>(wt + kTileHeader + (size_t)(p + 1) * 512 + lane * 16);
+                mma_pair(c[0], c[1], w0, xop[p * 32 + lane]);
+                mma_pair(c[2], c[3], w1, xop[(p + 1) * 32 + lane]);
+            }
+            const float* sc = reinterpret_cast<const float*>(wt);
+            const float sc0 = sc[gg], sc1 = sc[gg + 8];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[s]);
+            const float v0 = sc0 * (c[0][0] + c[0][1] + c[1][0] + c[1][1] + c[2][0] + c[2][1] + c[3][0] + c[3][1]);
+            const float v1 = sc1 * (c[0][2] + c[0][3] + c[1][2] + c[1][3] + c[2][2] + c[2][3] + c[3][2] + c[3][3]);
+            const int row0 = (j0 + j) * 16 + gg, row1 = row0 + 8;
+            if (tq < B) {
+                if (row0 < a.valid_rows) {
+                    if (a.logits) a.logits[(size_t)tq * a.valid_rows + row0] = v0;
+                    const unsigned long long k0 = argmax_key(v0, (uint32_t)row0);
+                    best = k0 > best ? k0 : best;
+                }
+                if (row1 < a.valid_rows) {
+                    if (a.logits) a.logits[(size_t)tq * a.valid_rows + row1] = v1;
+                    const unsigned long long k1 = argmax_key(v1, (uint32_t)row1);
+                    best = k1 > best ? k1 : best;
+                }
+            }
+        }
+#pragma unroll
+        for (int o = 4; o < 32; o <<= 1) {
+            const unsigned long long other = __shfl_xor_sync(0xffffffffu, best, o);
+            best = other > best ? other : best;
+        }
+        if (lane < 4) wbest[warp * 4 + lane] = best;
+    }
+    __syncthreads();
+    __shared__ int is_last;
+    if (tid < B) {
+        unsigned long long k = 0ull;
+        for (int w = 0; w < kWarps; ++w) k = wbest[w * 4 + tid] > k ? wbest[w * 4 + tid] : k;
+        atomicMax(&a.keys[tid], k);
+    }
+    if (*reinterpret_cast<volatile int*>(s_abort) && tid == 0) {
+        set_status(a.status, kStatusTimeout);
+        for (int s = 0; s < S; ++s) {
+            // the last tile issued into stage s, if any
+            const int last = *s_last - 1 - ((*s_last - 1 - s) % S + S) % S;
+            if (last >= 0 && last < *s_last) mbar_wait_bounded(&full[s], (uint32_t)(last / S) & 1u);
+        }
+    }
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) is_last = (atomicAdd(a.counter, 1u) == gridDim.x - 1);
+    __syncthreads();
+    if (is_last) {
+        __threadfence();
+        const int step = *reinterpret_cast<volatile int32_t*>(a.step);
+        if (tid < B) {
+            const unsigned long long k = atomicExch(&a.keys[tid], 0ull);
+            const int tok = (int)argmax_key_index(k);
+            a.tokens[tid] = tok;
+            if (step < a.out_cap) a.out_ids[(size_t)tid * a.out_cap + step] = tok;
+            if (a.advance_pos) a.pos[tid] += 1;
+        }
+        __syncthreads();
+        if (tid == 0) {
+            *a.step = step + 1;
+            *a.counter = 0u;
+        }
+    }
+}
+
+// ===================================================================== host side
+size_t attn_block_smem(int H, int hd, int kv_stages) { return attn_block_layout(H, hd, kv_stages).total; }
+size_t ffn_gate_smem(int H, int tpc) { return gate_layout(H, tpc).total; }
+size_t ffn_down_smem(int I, int ks) { return down_layout(I, ks).total; }
+size_t lm_head_smem(int H, int stages) { return lm_layout(H, stages).total; }
+
+bool step_plan(const StepShape& s, int num_sms, int smem_optin, StepPlan* p) {
+    if (s.hd != 64 && s.hd != 128) return false;
+    if (s.nkv < 1 || s.nh % s.nkv) return false;
+    if (s.H % 128 || s.H > 1024 || s.I % 32 || s.vocab_rows % 16) return false;
+    StepPlan q;
+    q.kv_stages = p->kv_stages < 1 ? 2 : p->kv_stages;
+    if (attn_block_smem(s.H, s.hd, q.kv_stages) > (size_t)smem_optin) return false;
+    const int gtiles = 2 * s.I / 16;
+    q.gate_tpc = std::min(kGateTmax, std::max(1, (gtiles + num_sms - 1) / num_sms));
+    while (q.gate_tpc > 1 && ffn_gate_smem(s.H, q.gate_tpc) > (size_t)smem_optin) --q.gate_tpc;
+    if (ffn_gate_smem(s.H, q.gate_tpc) > (size_t)smem_optin) return false;
+    q.gate_grid = (gtiles + q.gate_tpc - 1) / q.gate_tpc;
+    const int dtiles = s.H / 16, kp = s.I / 32;
+    q.down_ks = std::max(1, std::min(8, num_sms / dtiles));
+    while ((kp + q.down_ks - 1) / q.down_ks > kDownKpw * kWarps) ++q.down_ks;
+    if (q.down_ks > kp) return false;
+    q.down_grid = dtiles * q.down_ks;
+    q.lm_stages = 8;
+    while (q.lm_stages > 2 && lm_head_smem(s.H, q.lm_stages) > (size_t)smem_optin) --q.lm_stages;
+    if (lm_head_smem(s.H, q.lm_stages) > (size_t)smem_optin) return false;
+    q.lm_grid = std::min(num_sms, s.vocab_rows / 16);
+    *p = q;
+    return true;
+}
+
+bool step_prepare_device(const StepShape& s, const StepPlan& p) {
+    (void)s;
+    (void)p;
+    const void* fns[] = {(const void*)attn_block_kernel<64>, (const void*)attn_block_kernel<128>,
+                         (const void*)ffn_gate_kernel, (const void*)ffn_down_kernel, (const void*)lm_head_kernel};
+    for (const void* f : fns)
+        if (allow_max_dynamic_smem(f) != cudaSuccess) return false;
+    return true;
+}
+
+template <typename... KArgs, typename... Args>
+static cudaError_t launch_ex(void (*kern)(KArgs...), int grid, int block, size_t smem, int cluster, cudaStream_t st,
+                             Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(block);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute at[2];
+    int na = 0;
+    at[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+    if (cluster > 1) {
+        at[na].id = cudaLaunchAttributeClusterDimension;
+        at[na].val.clusterDim.x = cluster;
+        at[na].val.clusterDim.y = 1;
+        at[na].val.clusterDim.z = 1;
+        ++na;
+    }
+    cfg.attrs = at;
+    cfg.numAttrs = na;
+    return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
+cudaError_t launch_attn_block(const AttnBlockArgs& a, int hd, cudaStream_t st) {
+    const size_t smem = attn_block_smem(a.H, hd, a.kv_stages);
+    const int grid = a.nh * kClusterCtas;
+    if (hd == 128) return launch_ex(attn_block_kernel<128>, grid, kThreads, smem, kClusterCtas, st, a);
+    if (hd == 64) return launch_ex(attn_block_kernel<64>, grid, kThreads, smem, kClusterCtas, st, a);
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_ffn_gate(const FfnGateArgs& a, int grid, cudaStream_t st) {
+    return launch_ex(ffn_gate_kernel, grid, kThreads, ffn_gate_smem(a.H, a.tpc), 1, st, a);
+}
+
+cudaError_t launch_ffn_down(const FfnDownArgs& a, int grid, cudaStream_t st) {
+    return launch_ex(ffn_down_kernel, grid, kThreads, ffn_down_smem(a.I, a.ks), 1, st, a);
+}
+
+cudaError_t launch_lm_head(const LmHeadArgs& a, int grid, cudaStream_t st) {
+    return launch_ex(lm_head_kernel, grid, kLmThreads, lm_head_smem(a.H, a.stages), 1, st, a);
+}
+
+int attn_block_max_clusters(int H, int hd, int kv_stages) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(kClusterCtas);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = attn_block_smem(H, hd, kv_stages);
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = kClusterCtas;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    int n = 0;
+    const void* f = hd == 128 ? (const void*)attn_block_kernel<128> : (const void*)attn_block_kernel<64>;
+    if (cudaOccupancyMaxActiveClusters(&n, f, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    return n;
+}
+
+}  // namespace q3

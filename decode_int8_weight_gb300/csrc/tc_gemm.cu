@@ -325,13 +325,7 @@ int launch_tc_gemm(const __half* a_planes, const int8_t* w, const float* scale, 
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return -3;
     }
-    static bool attr_done = false;
-    if (!attr_done) {
-        if (cudaFuncSetAttribute(tc_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes) !=
-            cudaSuccess)
-            return -4;
-        attr_done = true;
-    }
+    if (allow_max_dynamic_smem((const void*)tc_gemm_kernel) != cudaSuccess) return -4;
     TcArgs g{scale, M, N, K, mode, y, ldy, yh, ldyh, status};
     const dim3 grid(N / kBN, (M + kBM - 1) / kBM);
     tc_gemm_kernel<<<grid, kTcThreads, kSmemBytes, st>>>(ta, tb, g);
