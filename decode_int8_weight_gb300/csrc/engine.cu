@@ -460,7 +460,7 @@ int enqueue_step(q3i8_ctx* c, int B, bool want_logits) {
     const int ks_resid = kResidSplit;
     float* kpart = B <= 4 ? c->kpart : nullptr;
 
-    launch_embed(c->tokens, B, c->embed.raw, c->embed.scale, H, c->x, st);
+    launch_embed(c->tokens, B, c->embed.raw, c->embed.scale, H, d.vocab, c->x, c->status, st);
     launch_rmsnorm(c->x, nullptr, B, H, c->layers[0].attn_norm, d.rms_eps, nullptr, c->xh, st, 1);
     for (int l = 0; l < d.n_layers; ++l) {
         const DevLayer& L = c->layers[l];
@@ -524,10 +524,11 @@ int step_setup(q3i8_ctx* c) {
     CK(c, cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, c->dev));
     StepPlan p;
     if (!step_plan(step_shape(c), c->num_sms, optin, &p)) return Q3_OK;
-    if (!step_prepare_device(step_shape(c), p))
-        return fail(c, Q3_ERR_CUDA, "decode step kernels: shared-memory opt-in refused");
-    if (attn_block_max_clusters(c->d.hidden, c->d.head_dim, p.kv_stages) < 1) return Q3_OK;
-    const size_t n = (size_t)c->bmax * c->d.hidden;
+    if (!step_prepare_device()) return fail(c, Q3_ERR_CUDA, "decode step kernels: shared-memory opt-in refused");
+    if (attn_block_max_clusters(c->d.hidden, c->d.head_dim, p.kv_stages) < 1 ||
+        ffn_block_max_clusters(c->d.hidden) < 1)
+        return Q3_OK;
+    const size_t n = 2 * (size_t)c->bmax * c->d.hidden;  // two buffers each
     CK(c, cudaMalloc(&c->xa, n * sizeof(long long)));
     CK(c, cudaMalloc(&c->xf, n * sizeof(long long)));
     CK(c, cudaMemsetAsync(c->xa, 0, n * sizeof(long long), c->stream));
@@ -542,50 +543,56 @@ int step_setup(q3i8_ctx* c) {
 // Clears the residual accumulators after a step that did not finish.
 static void step_reset(q3i8_ctx* c) {
     if (!c->use_step) return;
-    const size_t n = (size_t)c->bmax * c->d.hidden * sizeof(long long);
+    const size_t n = 2 * (size_t)c->bmax * c->d.hidden * sizeof(long long);
     cudaMemsetAsync(c->xa, 0, n, c->stream);
     cudaMemsetAsync(c->xf, 0, n, c->stream);
 }
 
 // One decode step for B <= kStepMaxBatch sequences: per layer the attention
-// block, gate/up and down kernels, then the lm_head.
+// block and the FFN block, then the lm_head.  Layer l accumulates the
+// attention block's output in xa[l % 2] and the FFN block's in xf[l % 2];
+// a buffer is cleared by a kernel that runs after its last reader and
+// before its next writer: the attention block of layer l clears xf[l % 2]
+// and xa[(l + 1) % 2], the lm_head clears xa[0] for the next step.
 int enqueue_step_fused(q3i8_ctx* c, int B, bool want_logits) {
     const q3i8_dims& d = c->d;
-    const int H = d.hidden, I = d.intermediate, hd = d.head_dim;
+    const int H = d.hidden, I = d.intermediate, hd = d.head_dim, nl = d.n_layers;
     const size_t layer_kv = (size_t)c->bmax * d.n_kv_heads * c->cap * hd;
+    const size_t nbuf = (size_t)c->bmax * H;
     const StepPlan& p = c->splan;
     cudaStream_t st = c->stream;
-    for (int l = 0; l < d.n_layers; ++l) {
+    for (int l = 0; l < nl; ++l) {
         const DevLayer& L = c->layers[l];
+        long long* xa = c->xa + (l % 2) * nbuf;
+        long long* xf = c->xf + (l % 2) * nbuf;
         AttnBlockArgs a{};
         a.B = B, a.H = H, a.nh = d.n_heads, a.nkv = d.n_kv_heads, a.cap = c->cap, a.kv_stages = p.kv_stages;
+        a.vocab = d.vocab;
         a.eps = d.rms_eps;
-        a.wqkv = L.qkv.frag, a.wo = L.o.frag, a.o_scale = L.o.scale;
+        a.wqkv = L.qkv.frag, a.qkv_scale = L.qkv.scale, a.wo = L.o.frag, a.o_scale = L.o.scale;
         a.attn_norm = L.attn_norm, a.q_norm = L.q_norm, a.k_norm = L.k_norm, a.rope = c->rope;
         a.kc = c->kc + l * layer_kv, a.vc = c->vc + l * layer_kv;
         a.seq_ids = c->seq_ids, a.pos = c->pos, a.pos_early = l > 0 ? 1 : 0;
-        a.xin = l > 0 ? c->xf : nullptr;
+        a.xin = l > 0 ? c->xf + ((l - 1) % 2) * nbuf : nullptr;
         a.tokens = c->tokens, a.emb = c->embed.raw, a.emb_scale = c->embed.scale;
-        a.xa = c->xa, a.status = c->status;
+        a.xa = xa;
+        a.clear0 = xf;
+        a.clear1 = l + 1 < nl ? c->xa + ((l + 1) % 2) * nbuf : nullptr;
+        a.status = c->status;
         cudaError_t e = launch_attn_block(a, hd, st);
         if (e != cudaSuccess) return fail(c, Q3_ERR_CUDA, "attention block launch: %s", cudaGetErrorString(e));
-        FfnGateArgs gargs{};
-        gargs.B = B, gargs.H = H, gargs.I = I, gargs.tpc = p.gate_tpc, gargs.eps = d.rms_eps;
-        gargs.wgu = L.gu.frag, gargs.ffn_norm = L.ffn_norm, gargs.xa = c->xa, gargs.xf = c->xf, gargs.ah = c->ah;
-        gargs.status = c->status;
-        e = launch_ffn_gate(gargs, p.gate_grid, st);
-        if (e != cudaSuccess) return fail(c, Q3_ERR_CUDA, "gate/up launch: %s", cudaGetErrorString(e));
-        FfnDownArgs dargs{};
-        dargs.B = B, dargs.H = H, dargs.I = I, dargs.ks = p.down_ks;
-        dargs.wd = L.down.frag, dargs.d_scale = L.down.scale, dargs.ah = c->ah, dargs.xa = c->xa, dargs.xf = c->xf;
-        dargs.status = c->status;
-        e = launch_ffn_down(dargs, p.down_grid, st);
-        if (e != cudaSuccess) return fail(c, Q3_ERR_CUDA, "down launch: %s", cudaGetErrorString(e));
+        FfnBlockArgs f{};
+        f.B = B, f.H = H, f.I = I, f.eps = d.rms_eps;
+        f.wgu = L.gu.frag, f.gu_scale = L.gu.scale, f.wd = L.down.frag, f.d_scale = L.down.scale;
+        f.ffn_norm = L.ffn_norm, f.xa = xa, f.xf = xf, f.status = c->status;
+        e = launch_ffn_block(f, p.ffn_grid, st);
+        if (e != cudaSuccess) return fail(c, Q3_ERR_CUDA, "FFN block launch: %s", cudaGetErrorString(e));
     }
     LmHeadArgs m{};
     m.B = B, m.H = H, m.rows = c->embed.rows, m.valid_rows = c->embed.valid_rows, m.stages = p.lm_stages;
     m.eps = d.rms_eps;
-    m.w = c->embed.frag, m.final_norm = c->final_norm, m.xf = c->xf;
+    m.w = c->embed.frag, m.final_norm = c->final_norm, m.xf = c->xf + ((nl - 1) % 2) * nbuf;
+    m.clear = c->xa;
     m.keys = c->keys, m.counter = c->counter, m.tokens = c->tokens, m.out_ids = c->out_ids, m.step = c->step;
     m.out_cap = c->out_cap, m.pos = c->pos, m.advance_pos = 1, m.logits = want_logits ? c->logits : nullptr;
     m.status = c->status;
@@ -717,7 +724,7 @@ static int enqueue_decode_step(q3i8_ctx* c, int B, bool want_logits) {
 
 int step_launches(const q3i8_ctx* c, int B) {
     if (persistent_for(c, B)) return 1;
-    if (fused_for(c, B)) return 3 * c->d.n_layers + 1;
+    if (fused_for(c, B)) return 2 * c->d.n_layers + 1;
     return 2 + c->d.n_layers * (decode_splits(c, B) == 1 ? 7 : 8) + 1;
 }
 // Kernels of one prefill over M prompt rows: embed; per layer 2 RMSNorms, the
@@ -818,7 +825,7 @@ static int run_prefill(q3i8_ctx* c, int B, const int32_t* d_ids, const int32_t* 
         CK(c, cudaMemcpyAsync(c->pf_blocks, blk.data(), (size_t)nblk * sizeof(int4), cudaMemcpyHostToDevice, st));
         CK(c, cudaStreamSynchronize(st));  // blk is a host temporary
     }
-    launch_embed(d_ids, M, c->embed.raw, c->embed.scale, H, c->pf_x, st);
+    launch_embed(d_ids, M, c->embed.raw, c->embed.scale, H, d.vocab, c->pf_x, c->status, st);
     for (int l = 0; l < d.n_layers; ++l) {
         const DevLayer& L = c->layers[l];
         launch_rmsnorm(c->pf_x, nullptr, M, H, L.attn_norm, d.rms_eps, nullptr, c->pf_xh, st);
@@ -864,6 +871,8 @@ static int check_status(q3i8_ctx* c) {
         }
         step_reset(c);
         cudaStreamSynchronize(c->stream);
+        if (st == kStatusBadToken)
+            return fail(c, Q3_ERR_INVALID_ARGUMENTS, "a token id outside [0, %d) reached the device", c->d.vocab);
         return fail(c, Q3_ERR_TIMEOUT,
                     "a bounded device wait gave up (status %d; site %d cta %d warp %d layer %d phase %d aux %d)", st,
                     dg[0], dg[1], dg[2], dg[3], dg[4], dg[5]);

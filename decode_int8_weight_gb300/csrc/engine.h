@@ -84,11 +84,11 @@ struct q3i8_ctx {
     float* p_part = nullptr;
     size_t p_ll_bytes = 0;
 
-    // small-batch decode step (step.cu): three kernels per layer
+    // small-batch decode step (step.cu): two cluster kernels per layer
     bool use_step = false;
     int step_max_batch = 0;  // largest B decoded by it; larger B take the chained kernels
     q3::StepPlan splan;
-    long long *xa = nullptr, *xf = nullptr;  // residual stream accumulators [bmax][H], value * 2^32
+    long long *xa = nullptr, *xf = nullptr;  // residual stream accumulators [2][bmax][H], value * 2^32
 
     std::map<int, cudaGraphExec_t> graphs;  // decode step graph per batch size
     cudaEvent_t ev0 = nullptr, ev1 = nullptr, ev2 = nullptr;

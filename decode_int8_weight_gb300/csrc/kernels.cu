@@ -266,18 +266,27 @@ int gemv_grid(int rows, int mode, int num_sms) {
 // =====================================================================
 // Embedding gather from the tied int8 table: x = float(q[tok]) * s[tok].
 // =====================================================================
-__global__ void embed_kernel(const int32_t* ids, const int8_t* E, const float* sE, int H, float* x) {
+// An id outside [0, vocab) is never dereferenced: its row is filled with
+// zeros and the status word records it (the call reports invalid arguments).
+__global__ void embed_kernel(const int32_t* ids, const int8_t* E, const float* sE, int H, int vocab, float* x,
+                             int32_t* status) {
     pdl_launch_dependents();
     pdl_wait();
     const int r = blockIdx.x;
     const int tok = ids[r];
+    if (tok < 0 || tok >= vocab) {
+        if (threadIdx.x == 0) set_status(status, kStatusBadToken);
+        for (int i = threadIdx.x; i < H; i += blockDim.x) x[(size_t)r * H + i] = 0.f;
+        return;
+    }
     const float s = sE[tok];
     const int8_t* row = E + (size_t)tok * H;
     for (int i = threadIdx.x; i < H; i += blockDim.x) x[(size_t)r * H + i] = (float)row[i] * s;
 }
 
-void launch_embed(const int32_t* ids, int n, const int8_t* E, const float* sE, int H, float* x, cudaStream_t st) {
-    if (n > 0) launch_pdl(embed_kernel, n, 256, 0, st, ids, E, sE, H, x);
+void launch_embed(const int32_t* ids, int n, const int8_t* E, const float* sE, int H, int vocab, float* x,
+                  int32_t* status, cudaStream_t st) {
+    if (n > 0) launch_pdl(embed_kernel, n, 256, 0, st, ids, E, sE, H, vocab, x, status);
 }
 
 // =====================================================================

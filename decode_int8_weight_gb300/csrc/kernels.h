@@ -17,6 +17,10 @@ namespace q3 {
 // registers of an m16n8k16 tensor-core MMA, so one 16-byte load feeds two
 // MMAs, and a tile is one contiguous run of bytes for a bulk copy.
 constexpr int kTileHeader = 128;
+
+// Status word value for a token id outside [0, vocab) met on the device
+// (the call reports invalid arguments).
+constexpr int kStatusBadToken = 8;
 size_t packed_offset(int row, int k, int K);  // byte offset of W[row][k] in the blob sequence
 __host__ __device__ inline size_t tile_blob_bytes(int K) { return kTileHeader + 16 * (size_t)K; }
 
@@ -74,7 +78,9 @@ cudaError_t allow_max_dynamic_smem(const void* fn);
 void launch_gemv(const GemvArgs& a, int mode, int grid, cudaStream_t st);
 int gemv_grid(int rows, int mode, int num_sms);
 
-void launch_embed(const int32_t* ids, int n, const int8_t* E, const float* sE, int H, float* x, cudaStream_t st);
+// x[r] = float(E[ids[r]]) * sE[ids[r]]; an id outside [0, vocab) gives a zero row and status kStatusBadToken.
+void launch_embed(const int32_t* ids, int n, const int8_t* E, const float* sE, int H, int vocab, float* x,
+                  int32_t* status, cudaStream_t st);
 
 // RMSNorm of rows (row map optional) -> fp32 rows and/or f16 hi/lo planes.
 void launch_rmsnorm(const float* x, const int32_t* rows, int n, int H, const float* g, float eps, float* xn,

@@ -1,4 +1,4 @@
-// Small-batch decode step: three kernels per layer plus the lm_head sweep (sm_103a).
+// Small-batch decode step: two cluster kernels per layer plus the lm_head sweep (sm_103a).
 //
 // The decoder block is the Qwen3 family's ("Model-agnostic LLM inference",
 // section "Supported models"): RMSNorm -> QKV -> per-head RMSNorm on Q and
@@ -31,9 +31,7 @@ namespace {
 
 constexpr int kThreads = 256;  // 8 warps
 constexpr int kWarps = 8;
-constexpr int kLmThreads = 288;  // lm_head: 8 consumer warps + 1 producer warp
-constexpr int kGateTmax = 4;     // gate/up tiles per CTA (most)
-constexpr int kDownKpw = 12;     // down k-pairs per warp (most)
+constexpr int kLmThreads = 288;  // lm_head: up to 8 consumer warps + 1 producer warp
 
 // ------------------------------------------------------------- fixed point
 // The residual stream between kernels is value * 2^32 in a signed 64-bit
@@ -176,34 +174,6 @@ Q3_DEV void mma_pair(float (&c0)[4], float (&c1)[4], const uint4& wv, const uint
     mma_f16_16816(c1, A1, bv.z, bv.w);
 }
 
-// acc[t] += tile t (t < nt) of the tile blobs at w (shared memory, K =
-// 32 kpairs) times the operand, over this warp's k-pairs (warp, warp + 8, ...).
-template <int TMAX>
-Q3_DEV void mma_tiles(float (&acc)[TMAX][4], const unsigned char* w, uint32_t blob, int nt, const uint4* xop,
-                      int kpairs) {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    float acc2[TMAX][4];
-#pragma unroll
-    for (int t = 0; t < TMAX; ++t)
-#pragma unroll
-        for (int i = 0; i < 4; ++i) acc[t][i] = acc2[t][i] = 0.f;
-    for (int p = warp; p < kpairs; p += kWarps) {
-        const uint4 bv = xop[p * 32 + lane];
-#pragma unroll
-        for (int t = 0; t < TMAX; ++t) {
-            if (t < nt) {
-                const uint4 wv =
-                    *reinterpret_cast<const uint4*>(w + (size_t)t * blob + kTileHeader + (size_t)p * 512 + lane * 16);
-                mma_pair(acc[t], acc2[t], wv, bv);
-            }
-        }
-    }
-#pragma unroll
-    for (int t = 0; t < TMAX; ++t)
-#pragma unroll
-        for (int i = 0; i < 4; ++i) acc[t][i] += acc2[t][i];
-}
-
 // Bounded wait shared by a whole block: every thread waits, and the block
 // agrees on the outcome (true when any thread's wait gave up).
 Q3_DEV bool block_wait_failed(uint64_t* bar, uint32_t parity) {
@@ -211,48 +181,144 @@ Q3_DEV bool block_wait_failed(uint64_t* bar, uint32_t parity) {
     return __syncthreads_or(!ok) != 0;
 }
 
+// The operand of one K slice.  Columns 2b and 2b + 1 hold f16(v) and
+// f16(v - f16(v)) of v = gain[k] * x[b][k] for the slice's local k = 0 ..
+// 32 nkp - 1 (global k = kbase + local); the RMSNorm's 1 / rms is a factor of
+// the whole row and is applied to the finished dot products instead.
+// s_ss[b] receives the slice's sum of squares of x[b].  x comes from the
+// fixed-point stream xin ([B][H]) or, with xin null, is the embedding row of
+// token tok[b].  Thread t < 8 nkp B owns 4 consecutive k of sequence
+// t / (8 nkp); 8 nkp <= 32, so a sequence's threads share one warp.
+Q3_DEV void slice_operand(uint4* xop, float* s_ss, const long long* xin, const int* tok, const int8_t* emb,
+                          const float* emb_scale, int B, int H, int kbase, int nkp, const float* s_gain) {
+    const int t = threadIdx.x;
+    const int per_b = 8 * nkp;
+    const bool own = t < B * per_b;
+    const int b = own ? t / per_b : 0;
+    const int kl = 4 * (t - b * per_b);
+    float x[4] = {0.f, 0.f, 0.f, 0.f};
+    if (own) {
+        const int k = kbase + kl;
+        if (xin) {
+            const longlong2 v0 = __ldcg(reinterpret_cast<const longlong2*>(xin + (size_t)b * H + k));
+            const longlong2 v1 = __ldcg(reinterpret_cast<const longlong2*>(xin + (size_t)b * H + k + 2));
+            x[0] = float_of_fix(v0.x), x[1] = float_of_fix(v0.y), x[2] = float_of_fix(v1.x), x[3] = float_of_fix(v1.y);
+        } else {
+            const int tk = tok[b];
+            const char4 e = *reinterpret_cast<const char4*>(emb + (size_t)tk * H + k);
+            const float es = emb_scale[tk];
+            x[0] = (float)e.x * es, x[1] = (float)e.y * es, x[2] = (float)e.z * es, x[3] = (float)e.w * es;
+        }
+    }
+    float ss = x[0] * x[0] + x[1] * x[1] + x[2] * x[2] + x[3] * x[3];
+    // sum over the per_b threads of this sequence (an aligned group inside one warp)
+    for (int o = 1; o < per_b; o <<= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    if (own) {
+        if (kl == 0) s_ss[b] = ss;
+        const float4 g = *reinterpret_cast<const float4*>(s_gain + kl);
+        const float gg[4] = {g.x, g.y, g.z, g.w};
+        __half hi[4], lo[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) split_f16(__fmul_rn(gg[j], x[j]), hi[j], lo[j]);
+        uint32_t* xw = reinterpret_cast<uint32_t*>(xop);
+        xw[frag_word(2 * b, kl)] = pack_half2(hi[0], hi[1]);
+        xw[frag_word(2 * b, kl + 2)] = pack_half2(hi[2], hi[3]);
+        xw[frag_word(2 * b + 1, kl)] = pack_half2(lo[0], lo[1]);
+        xw[frag_word(2 * b + 1, kl + 2)] = pack_half2(lo[2], lo[3]);
+    }
+}
+
+// Partial sums of a cluster's tiles over this CTA's K slice: warp w takes
+// tiles w, w + 8, ... (< nt) of the slice blobs at w_slices (nkp k-pairs,
+// 512 bytes each, per tile) against the slice operand, and writes row
+// 16 t + g (and + 8) of sequence column q to out[q * ld + row], q = 0..3
+// (the columns of absent sequences hold whatever their operand columns gave).
+template <int TPW>
+Q3_DEV void cluster_tiles_mma(const unsigned char* w_slices, int nt, int nkp, const uint4* xop, float* out, int ld) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane >> 2, q = lane & 3;
+    float c0[TPW][4], c1[TPW][4];
+#pragma unroll
+    for (int i = 0; i < TPW; ++i)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) c0[i][e] = c1[i][e] = 0.f;
+    for (int p = 0; p < nkp; ++p) {
+        const uint4 bv = xop[p * 32 + lane];
+#pragma unroll
+        for (int i = 0; i < TPW; ++i) {
+            const int t = warp + kWarps * i;
+            if (t < nt) {
+                const uint4 wv = *reinterpret_cast<const uint4*>(w_slices + ((size_t)t * nkp + p) * 512 + lane * 16);
+                mma_pair(c0[i], c1[i], wv, bv);
+            }
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < TPW; ++i) {
+        const int t = warp + kWarps * i;
+        if (t < nt) {
+            out[q * ld + t * 16 + g] = c0[i][0] + c0[i][1] + c1[i][0] + c1[i][1];
+            out[q * ld + t * 16 + g + 8] = c0[i][2] + c0[i][3] + c1[i][2] + c1[i][3];
+        }
+    }
+}
+
+// 1 / rms of sequence b from the cluster's partial sums of squares (peers
+// in rank order, so every CTA gets the same bits).
+Q3_DEV float cluster_inv_rms(const float* s_ss, int b, int H, float eps) {
+    float t = 0.f;
+#pragma unroll
+    for (int r = 0; r < kClusterCtas; ++r) t += peer(s_ss, r)[b];
+    return 1.0f / sqrtf(t / (float)H + eps);
+}
+
+// Clears this CTA's share of a [n] accumulator (fire-and-forget stores).
+Q3_DEV void clear_share(long long* p, int n) {
+    if (!p) return;
+    const int per = (n + gridDim.x - 1) / gridDim.x;
+    const int z0 = blockIdx.x * per, z1 = min(n, z0 + per);
+    for (int i = z0 + (int)threadIdx.x; i < z1; i += blockDim.x) p[i] = 0;
+}
+
 }  // namespace
 
 // ===================================================================== layouts
-struct AttnBlockLayout {
-    uint32_t wq, wo, red, xop, qkv, qn, kn, vn, ring, wst, part, oop, osc, gain, qkg, rope, resid, misc, bars, total;
-};
-
 __host__ __device__ inline uint32_t take_smem(uint32_t& off, size_t bytes) {
     const uint32_t o = off;
     off = (uint32_t)((off + bytes + 127) & ~(size_t)127);
     return o;
 }
 
-// The QKV weight region is dead once the QKV rows are reduced: the per-head
-// vectors, softmax states and the O operand reuse it.  The partial sums of
-// the QKV reduction reuse the operand region.
+struct AttnBlockLayout {
+    uint32_t wq, qn, kn, vn, wst, part, oop, wo, xop, pqkv, ss, ring, sc, osc, gain, qkg, rope, resid, misc, bars, total;
+};
+
+// The QKV weight slices are dead once the partial sums are written: the
+// per-head vectors, the softmax states and the O operand reuse that region.
 __host__ __device__ inline AttnBlockLayout attn_block_layout(int H, int hd, int kv_stages) {
     AttnBlockLayout L{};
     uint32_t off = 0;
-    const int T = 3 * hd / 16, tmax = (T + kClusterCtas - 1) / kClusterCtas;
+    const int T = 3 * hd / 16, nkp = H / 32 / kClusterCtas;
     {
         uint32_t w = 0;
         L.qn = take_smem(w, (size_t)kStepMaxBatch * hd * 4);
         L.kn = take_smem(w, (size_t)kStepMaxBatch * hd * 4);
         L.vn = take_smem(w, (size_t)kStepMaxBatch * hd * 4);
         L.wst = take_smem(w, (size_t)kWarps * kStepMaxBatch * hd * 4);  // warp states, then the parked parts
-        L.part = take_smem(w, (size_t)kStepMaxBatch * (hd + 4) * 4);  // 16-byte aligned states
+        L.part = take_smem(w, (size_t)kStepMaxBatch * (hd + 4) * 4);    // 16-byte aligned states
         L.oop = take_smem(w, (size_t)(hd / 32) * 512);
-        const size_t wq_bytes = (size_t)tmax * tile_blob_bytes(H);
+        const size_t wq_bytes = (size_t)T * nkp * 512;
         L.wq = take_smem(off, wq_bytes > w ? wq_bytes : w);
         L.qn += L.wq, L.kn += L.wq, L.vn += L.wq, L.wst += L.wq, L.part += L.wq, L.oop += L.wq;
     }
     L.wo = take_smem(off, (size_t)(H / kClusterCtas / 16) * (hd / 32) * 512);
-    {
-        const size_t xop_bytes = (size_t)(H / 32) * 512, red_bytes = (size_t)tmax * kWarps * 32 * 16;
-        L.xop = take_smem(off, xop_bytes > red_bytes ? xop_bytes : red_bytes);
-        L.red = L.xop;
-    }
-    L.qkv = take_smem(off, (size_t)tmax * 16 * kStepMaxBatch * 4);
+    L.xop = take_smem(off, (size_t)nkp * 512);
+    L.pqkv = take_smem(off, (size_t)kStepMaxBatch * 3 * hd * 4);
+    L.ss = take_smem(off, (size_t)kStepMaxBatch * 4);
     L.ring = take_smem(off, (size_t)kv_stages * 2 * kStepKvChunk * hd * 2);
+    L.sc = take_smem(off, (size_t)3 * hd * 4);
     L.osc = take_smem(off, (size_t)(H / kClusterCtas) * 4);
-    L.gain = take_smem(off, (size_t)H * 4);
+    L.gain = take_smem(off, (size_t)nkp * 32 * 4);
     L.qkg = take_smem(off, (size_t)2 * hd * 4);
     L.rope = take_smem(off, (size_t)kStepMaxBatch * (hd / 2) * 8);
     L.resid = take_smem(off, (size_t)kStepMaxBatch * (H / kClusterCtas) * 8);
@@ -262,36 +328,25 @@ __host__ __device__ inline AttnBlockLayout attn_block_layout(int H, int hd, int 
     return L;
 }
 
-struct GateLayout {
-    uint32_t w, xop, red, gain, misc, bar, total;
+struct FfnLayout {
+    uint32_t wgu, wd, xop, pgu, ss, dop, sgu, sd, gain, resid, misc, bars, total;
 };
-__host__ __device__ inline GateLayout gate_layout(int H, int tpc) {
-    GateLayout L{};
+__host__ __device__ inline FfnLayout ffn_layout(int H) {
+    FfnLayout L{};
     uint32_t off = 0;
-    L.w = take_smem(off, (size_t)tpc * tile_blob_bytes(H));
-    {
-        const size_t xop_bytes = (size_t)(H / 32) * 512, red_bytes = (size_t)tpc * kWarps * 32 * 16;
-        L.xop = take_smem(off, xop_bytes > red_bytes ? xop_bytes : red_bytes);  // the partial sums reuse it
-        L.red = L.xop;
-    }
-    L.gain = take_smem(off, (size_t)H * 4);
-    L.misc = take_smem(off, 256);
-    L.bar = take_smem(off, 8);
-    L.total = off;
-    return L;
-}
-
-struct DownLayout {
-    uint32_t w, red, misc, bar, total;
-};
-__host__ __device__ inline DownLayout down_layout(int I, int ks) {
-    DownLayout L{};
-    uint32_t off = 0;
-    const int kp = I / 32, per = (kp + ks - 1) / ks;
-    L.w = take_smem(off, (size_t)per * 512);
-    L.red = take_smem(off, (size_t)kWarps * 32 * 16);
-    L.misc = take_smem(off, 128);
-    L.bar = take_smem(off, 8);
+    const int nkp = H / 32 / kClusterCtas, dt = H / kClusterCtas / 16;
+    L.wgu = take_smem(off, (size_t)(2 * kFfnUnits / 16) * nkp * 512);
+    L.wd = take_smem(off, (size_t)dt * (kFfnUnits / 32) * 512);
+    L.xop = take_smem(off, (size_t)nkp * 512);
+    L.pgu = take_smem(off, (size_t)kStepMaxBatch * 2 * kFfnUnits * 4);
+    L.ss = take_smem(off, (size_t)kStepMaxBatch * 4);
+    L.dop = take_smem(off, (size_t)(kFfnUnits / 32) * 512);
+    L.sgu = take_smem(off, (size_t)2 * kFfnUnits * 4);
+    L.sd = take_smem(off, (size_t)(H / kClusterCtas) * 4);
+    L.gain = take_smem(off, (size_t)nkp * 32 * 4);
+    L.resid = take_smem(off, (size_t)kStepMaxBatch * (H / kClusterCtas) * 8);
+    L.misc = take_smem(off, 64);
+    L.bars = take_smem(off, 2 * 8);
     L.total = off;
     return L;
 }
@@ -313,36 +368,37 @@ __host__ __device__ inline LmLayout lm_layout(int H, int stages) {
 }
 
 // ===================================================================== attention block
-// Cluster c (8 CTAs) serves query head h = c of kv group g = h / (nh / nkv).
-//  1. RMSNorm of the residual stream (every CTA, from the fixed-point rows).
-//  2. The cluster's QKV rows (head h of Wq, group g of Wk and Wv: 3 hd rows
-//     in 16-row tiles) are split over the 8 CTAs; each CTA multiplies its
-//     tiles, already in shared memory, by the normed rows.
-//  3. Every CTA gathers the 3 hd values per sequence from its peers' shared
-//     memory, applies the per-head RMSNorm of q and k and RoPE at the
-//     sequence's position, and rounds k and v to bf16.  CTA 7 of the group's
-//     first cluster appends them to the cache.
-//  4. The cached positions 0..p-1 of each sequence are split over the 8 CTAs
+// Cluster h (8 CTAs) serves query head h of kv group g = h / (nh / nkv).
+//  1. The cluster's QKV rows (head h of Wq, group g of Wk and Wv: 3 hd rows
+//     in 16-row tiles) are multiplied by the residual stream, K split over the
+//     8 CTAs: CTA r holds the k-pairs [r KP / 8, (r + 1) KP / 8) of every
+//     tile in shared memory and warp w the tiles w, w + 8, ...; the RMSNorm
+//     gain is folded into the operand and 1 / rms into the result.
+//  2. Every CTA sums the 8 partial rows (distributed shared memory) for the
+//     vectors it needs, applies the row scales, 1 / rms, the per-head RMSNorm
+//     of q and k and RoPE at the sequence's position, and rounds k and v to
+//     bf16.  CTA 7 of the group's first cluster appends them to the cache
+//     (at the very end, so that no barrier waits for those stores).
+//  3. The cached positions 0..p-1 of each sequence are split over the 8 CTAs
 //     (16-position chunks staged by bulk copies); CTA 7 also attends the new
-//     position p from the rounded values it holds.  Each CTA keeps an online
-//     softmax state (m, l, acc) per sequence.
-//  5. Every CTA merges the 8 states (distributed shared memory) into the
-//     head's output o and multiplies its H/8 rows of Wo[:, head h] by it; the
-//     rows are added to the fixed-point residual stream (cluster 0 also adds
-//     the stream's input).
-// Before the wait the CTA starts the bulk copies of its QKV tiles and O
-// slice and copies the gains, row scales and (from the second layer on,
-// where the positions are final) the RoPE rows into shared memory and
-// starts its K/V stages; after the wait the only global reads are the
-// residual rows (and, in the first layer, the tokens and their embedding).
+//     position p from the rounded values.  Each CTA keeps an online softmax
+//     state (m, l, acc) per sequence.
+//  4. Every CTA merges the 8 states into the head's output o and multiplies
+//     its H / 8 rows of Wo[:, head h] by it; the rows are added to the
+//     fixed-point residual stream (cluster 0 also adds the stream's input).
+// Before the wait the CTA starts the bulk copies of its weight slices and O
+// rows and copies the gains, row scales and (from the second layer on,
+// where the positions are final) the RoPE rows into shared memory and starts
+// its K/V stages; after the wait the only global reads are its slice of the
+// residual rows (in the first layer: the tokens and their embedding).
 template <int HD>
 __global__ void __launch_bounds__(kThreads, 2) attn_block_kernel(const AttnBlockArgs a) {
-    constexpr int D = HD / 32;  // contiguous dims per lane (attention)
-    constexpr int E = HD / 32;  // elements l + 32 j per lane (QK-norm, RoPE)
+    constexpr int D = HD / 32;  // elements per lane of a head vector (lane l: D l .. D l + D - 1)
     constexpr int TH = HD / 16;
     constexpr int T = 3 * TH;
-    constexpr int TMAX = (T + kClusterCtas - 1) / kClusterCtas;
+    constexpr int TPW = (T + kWarps - 1) / kWarps;
     constexpr int PS = HD + 4;  // floats per softmax state {acc[HD], m, l, pad}: 16-byte aligned rows
+    constexpr int R3 = 3 * HD;  // rows of the cluster
     extern __shared__ __align__(128) unsigned char smem[];
     const AttnBlockLayout L = attn_block_layout(a.H, HD, a.kv_stages);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -351,19 +407,18 @@ __global__ void __launch_bounds__(kThreads, 2) attn_block_kernel(const AttnBlock
     const int G = a.nh / a.nkv, g = h / G;
     const int H = a.H, B = a.B, S = a.kv_stages;
     const int Dq = a.nh * HD, Dkv = a.nkv * HD;
-    const int t0 = r * T / kClusterCtas, t1 = (r + 1) * T / kClusterCtas, nt = t1 - t0;
+    const int nkp = H / 32 / kClusterCtas, kp0 = r * nkp;
     const uint32_t blob = (uint32_t)tile_blob_bytes(H);
     const int ro = H / kClusterCtas, otiles = ro / 16;
     const uint32_t oseg = (HD / 32) * 512;
     const uint32_t oblob = (uint32_t)tile_blob_bytes(Dq);
     const bool appender = (h % G == 0) && (r == kClusterCtas - 1);
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bars);  // 0 QKV weights, 1 O slice, 2.. K/V stages
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bars);  // 0 QKV slices, 1 O rows, 2.. K/V stages
     int* s_pos = reinterpret_cast<int*>(smem + L.misc);
     int* s_seq = s_pos + 4;
     int* s_tok = s_seq + 4;
-    int* s_last = s_tok + 4;               // [S] last item issued into each stage (-1: none)
-    float* s_inv = reinterpret_cast<float*>(s_last + 8);
-    float* s_red = s_inv + 4;              // [8][4]
+    int* s_last = s_tok + 4;  // [S] last item issued into each stage (-1: none)
+    float* s_sc = reinterpret_cast<float*>(smem + L.sc);
     float* osc = reinterpret_cast<float*>(smem + L.osc);
     float* s_gain = reinterpret_cast<float*>(smem + L.gain);
     float* s_qg = reinterpret_cast<float*>(smem + L.qkg);
@@ -371,7 +426,8 @@ __global__ void __launch_bounds__(kThreads, 2) attn_block_kernel(const AttnBlock
     float2* s_rope = reinterpret_cast<float2*>(smem + L.rope);
     long long* s_res = reinterpret_cast<long long*>(smem + L.resid);
     uint4* xop = reinterpret_cast<uint4*>(smem + L.xop);
-    float* qkv = reinterpret_cast<float*>(smem + L.qkv);
+    float* pqkv = reinterpret_cast<float*>(smem + L.pqkv);
+    float* s_ss = reinterpret_cast<float*>(smem + L.ss);
     float* qn = reinterpret_cast<float*>(smem + L.qn);
     float* kn = reinterpret_cast<float*>(smem + L.kn);
     float* vn = reinterpret_cast<float*>(smem + L.vn);
@@ -380,10 +436,10 @@ __global__ void __launch_bounds__(kThreads, 2) attn_block_kernel(const AttnBlock
     uint4* oop = reinterpret_cast<uint4*>(smem + L.oop);
     __nv_bfloat16* ring = reinterpret_cast<__nv_bfloat16*>(smem + L.ring);
 
-    auto gtile = [&](int t) -> int {
-        if (t < TH) return h * TH + t;
-        if (t < 2 * TH) return Dq / 16 + g * TH + (t - TH);
-        return (Dq + Dkv) / 16 + g * TH + (t - 2 * TH);
+    auto grow = [&](int j) -> int {  // global QKV row of cluster row j
+        if (j < HD) return h * HD + j;
+        if (j < 2 * HD) return Dq + g * HD + (j - HD);
+        return Dq + Dkv + g * HD + (j - 2 * HD);
     };
     auto o_src = [&](int i) -> const uint8_t* {
         return a.wo + (size_t)(r * otiles + i) * oblob + kTileHeader + (size_t)h * oseg;
@@ -434,25 +490,34 @@ __global__ void __launch_bounds__(kThreads, 2) attn_block_kernel(const AttnBlock
     }
     __syncthreads();
     if (tid == 0) {
-        mbar_arrive_expect_tx(&bars[0], (uint32_t)nt * blob);
-        for (int t = t0; t < t1; ++t)
-            bulk_g2s(smem + L.wq + (size_t)(t - t0) * blob, a.wqkv + (size_t)gtile(t) * blob, blob, &bars[0]);
+        mbar_arrive_expect_tx(&bars[0], (uint32_t)(T * nkp * 512));
+        for (int t = 0; t < T; ++t)
+            bulk_g2s(smem + L.wq + (size_t)t * nkp * 512,
+                     a.wqkv + (size_t)(grow(t * 16) / 16) * blob + kTileHeader + (size_t)kp0 * 512,
+                     (uint32_t)nkp * 512, &bars[0]);
         mbar_arrive_expect_tx(&bars[1], (uint32_t)otiles * oseg);
         for (int i = 0; i < otiles; ++i) bulk_g2s(smem + L.wo + (size_t)i * oseg, o_src(i), oseg, &bars[1]);
     }
+    for (int i = tid; i < R3; i += kThreads) s_sc[i] = a.qkv_scale[grow(i)];
     for (int i = tid; i < ro; i += kThreads) osc[i] = a.o_scale[r * ro + i];
-    for (int i = tid; i < H; i += kThreads) s_gain[i] = a.attn_norm[i];
+    for (int i = tid; i < nkp * 32; i += kThreads) s_gain[i] = a.attn_norm[kp0 * 32 + i];
     for (int i = tid; i < HD; i += kThreads) s_qg[i] = a.q_norm[i], s_kg[i] = a.k_norm[i];
     if (a.pos_early) position_work();
     pdl_wait();
     pdl_launch_dependents();
 
-    // ---- after the wait: positions and tokens (first layer), residual rows
+    // ---- after the wait: positions and tokens (first layer), residual rows, accumulators to clear
     if (!a.pos_early) {
         if (tid < B) {
             s_pos[tid] = a.pos[tid];
             s_seq[tid] = a.seq_ids[tid];
-            if (!a.xin) s_tok[tid] = a.tokens[tid];
+            if (!a.xin) {
+                // a token outside the table is never dereferenced: it reads row 0 and the call reports it
+                const int t = a.tokens[tid];
+                const bool okt = t >= 0 && t < a.vocab;
+                if (!okt) set_status(a.status, kStatusBadToken);
+                s_tok[tid] = okt ? t : 0;
+            }
         }
         __syncthreads();
         position_work();
@@ -463,86 +528,74 @@ __global__ void __launch_bounds__(kThreads, 2) attn_block_kernel(const AttnBlock
             s_res[i] = a.xin ? __ldcg(a.xin + (size_t)b * H + R)
                              : fix_of((float)a.emb[(size_t)s_tok[b] * H + R] * a.emb_scale[s_tok[b]]);
         }
+    clear_share(a.clear0, B * H);
+    clear_share(a.clear1, B * H);
     const int n_items = count_items();
 
-    // ---- 1. RMSNorm operand, 2. this CTA's QKV rows
-    norm_operand(xop, a.xin, s_tok, a.emb, a.emb_scale, B, H, s_gain, a.eps, s_red);
+    // ---- 1. this CTA's K slice of the cluster's QKV rows
+    slice_operand(xop, s_ss, a.xin, s_tok, a.emb, a.emb_scale, B, H, kp0 * 32, nkp, s_gain);
     bool bad = block_wait_failed(&bars[0], 0);
-    {
-        float acc[TMAX][4];
-        mma_tiles<TMAX>(acc, smem + L.wq, blob, bad ? 0 : nt, xop, H / 32);
-        __syncthreads();  // every warp is done with the operand (the partial sums reuse it)
-        float4* red = reinterpret_cast<float4*>(smem + L.red);
-#pragma unroll
-        for (int t = 0; t < TMAX; ++t)
-            if (t < nt) red[(t * kWarps + warp) * 32 + lane] = make_float4(acc[t][0], acc[t][1], acc[t][2], acc[t][3]);
-        __syncthreads();
-        if (tid < nt * 32) {
-            const int t = tid >> 5, ln = tid & 31, gg = ln >> 2, tq = ln & 3;
-            float s0 = 0.f, s1 = 0.f;
-            for (int w = 0; w < kWarps; ++w) {
-                const float4 v = red[(t * kWarps + w) * 32 + ln];
-                s0 += v.x + v.y;
-                s1 += v.z + v.w;
-            }
-            const float* sc = reinterpret_cast<const float*>(smem + L.wq + (size_t)t * blob);
-            qkv[(t * 16 + gg) * 4 + tq] = sc[gg] * s0;
-            qkv[(t * 16 + gg + 8) * 4 + tq] = sc[gg + 8] * s1;
-        }
-    }
+    if (!bad) cluster_tiles_mma<TPW>(smem + L.wq, T, nkp, xop, pqkv, R3);
     cluster_arrive();
-    cluster_wait();  // every CTA's QKV rows are visible in the cluster
+    cluster_wait();  // every CTA's partial rows are visible in the cluster
 
-    // ---- 3. gather q, k, v from the peers; QK-RMSNorm, RoPE, bf16 rounding
-    // warp b < B: query of sequence b; warp 4 + b: key and value of sequence b
-    // (lane l holds elements l + 32 j, so both members of a RoPE pair sit in
-    // one lane)
+    // ---- 2. q, k, v of each sequence: partial rows summed, scaled, normed, rotated
+    // warp b < B: query of sequence b; warp 4 + b: key and value of sequence b.
+    // Lane l holds elements D l .. D l + D - 1; the RoPE partner of element i
+    // (i + hd / 2 or i - hd / 2) sits in lane l ^ 16.
     if ((warp & 3) < B) {
         const int b = warp & 3;
         const bool is_q = warp < 4;
-        auto fetch = [&](int j) -> float {  // row j of the cluster's 3 hd rows, sequence b
-            const int t = j >> 4;
-            const int owner = (kClusterCtas * t + kClusterCtas - 1) / T;
-            const int ot0 = owner * T / kClusterCtas;
-            return peer(qkv, owner)[((t - ot0) * 16 + (j & 15)) * 4 + b];
-        };
-        float v[E], vv[E];
+        const float inv = cluster_inv_rms(s_ss, b, H, a.eps);
+        auto rows = [&](int j0, float (&v)[D]) {  // v = scale * inv * sum over the peers, rows j0 + D l ..
 #pragma unroll
-        for (int j = 0; j < E; ++j) {
-            v[j] = fetch((is_q ? 0 : HD) + lane + 32 * j);
-            vv[j] = is_q ? 0.f : fetch(2 * HD + lane + 32 * j);
-        }
+            for (int m = 0; m < D; ++m) v[m] = 0.f;
+#pragma unroll
+            for (int rr = 0; rr < kClusterCtas; ++rr) {
+                const float* pp = peer(pqkv, rr) + b * R3 + j0 + D * lane;
+                if constexpr (D == 4) {
+                    const float4 x = *reinterpret_cast<const float4*>(pp);
+                    v[0] += x.x, v[1] += x.y, v[2] += x.z, v[3] += x.w;
+                } else {
+                    const float2 x = *reinterpret_cast<const float2*>(pp);
+                    v[0] += x.x, v[1] += x.y;
+                }
+            }
+#pragma unroll
+            for (int m = 0; m < D; ++m) v[m] = s_sc[j0 + D * lane + m] * inv * v[m];
+        };
+        float v[D], vv[D];
+        rows(is_q ? 0 : HD, v);
+        if (!is_q) rows(2 * HD, vv);
         const float* gain = is_q ? s_qg : s_kg;
-        const float2* cs = s_rope + b * (HD / 2);
         float ss = 0.f;
 #pragma unroll
-        for (int j = 0; j < E; ++j) ss += v[j] * v[j];
+        for (int m = 0; m < D; ++m) ss += v[m] * v[m];
         ss = warp_sum(ss);
-        const float inv = 1.0f / sqrtf(ss / (float)HD + a.eps);
+        const float hinv = 1.0f / sqrtf(ss / (float)HD + a.eps);
 #pragma unroll
-        for (int j = 0; j < E; ++j) v[j] = __fmul_rn(__fmul_rn(v[j], inv), gain[lane + 32 * j]);
+        for (int m = 0; m < D; ++m) v[m] = __fmul_rn(__fmul_rn(v[m], hinv), gain[D * lane + m]);
+        const float2* cs = s_rope + b * (HD / 2) + D * (lane & 15);
 #pragma unroll
-        for (int j = 0; j < E / 2; ++j) {
-            const float2 c = cs[lane + 32 * j];
-            const float a0 = v[j], b0 = v[j + E / 2];
-            v[j] = __fsub_rn(__fmul_rn(a0, c.x), __fmul_rn(b0, c.y));
-            v[j + E / 2] = __fadd_rn(__fmul_rn(b0, c.x), __fmul_rn(a0, c.y));
+        for (int m = 0; m < D; ++m) {
+            const float pv = __shfl_xor_sync(0xffffffffu, v[m], 16);
+            const float2 c = cs[m];
+            v[m] = lane < 16 ? __fsub_rn(__fmul_rn(v[m], c.x), __fmul_rn(pv, c.y))
+                             : __fadd_rn(__fmul_rn(v[m], c.x), __fmul_rn(pv, c.y));
         }
-        float* vec = (is_q ? qn : kn) + b * HD;
-        if (is_q) {
 #pragma unroll
-            for (int j = 0; j < E; ++j) vec[lane + 32 * j] = v[j];
-        } else {
-#pragma unroll
-            for (int j = 0; j < E; ++j) {
-                vec[lane + 32 * j] = __bfloat162float(__float2bfloat16_rn(v[j]));
-                vn[b * HD + lane + 32 * j] = __bfloat162float(__float2bfloat16_rn(vv[j]));
+        for (int m = 0; m < D; ++m) {
+            if (is_q) {
+                qn[b * HD + D * lane + m] = v[m];
+            } else {
+                kn[b * HD + D * lane + m] = __bfloat162float(__float2bfloat16_rn(v[m]));
+                vn[b * HD + D * lane + m] = __bfloat162float(__float2bfloat16_rn(vv[m]));
             }
         }
     }
     __syncthreads();
 
-    // ---- 4. attention over this CTA's split of every sequence
+    // ---- 3. attention over this CTA's split of every sequence
     const float scale = 1.0f / sqrtf((float)HD);
     int item = 0;
     for (int b = 0; b < B; ++b) {
@@ -608,22 +661,22 @@ __global__ void __launch_bounds__(kThreads, 2) attn_block_kernel(const AttnBlock
             m = mn;
         }
         // merge the 8 warps' states into this CTA's state for sequence b
-        float* ws = wst + warp * (HD + 2);
+        float* ws = wst + warp * PS;
         if (lane == 0) ws[HD] = m, ws[HD + 1] = l;
 #pragma unroll
         for (int d = 0; d < D; ++d) ws[lane * D + d] = acc[d];
         __syncthreads();
         for (int d = tid; d < HD; d += kThreads) {
             float M = -INFINITY;
-            for (int w = 0; w < kWarps; ++w) M = fmaxf(M, wst[w * (HD + 2) + HD]);
+            for (int w = 0; w < kWarps; ++w) M = fmaxf(M, wst[w * PS + HD]);
             float Ls = 0.f, A = 0.f;
             if (M != -INFINITY)
                 for (int w = 0; w < kWarps; ++w) {
-                    const float mw = wst[w * (HD + 2) + HD];
+                    const float mw = wst[w * PS + HD];
                     if (mw == -INFINITY) continue;
                     const float f = expf(mw - M);
-                    Ls += wst[w * (HD + 2) + HD + 1] * f;
-                    A += wst[w * (HD + 2) + d] * f;
+                    Ls += wst[w * PS + HD + 1] * f;
+                    A += wst[w * PS + d] * f;
                 }
             float* pb = part + b * PS;
             pb[d] = A;
@@ -632,45 +685,28 @@ __global__ void __launch_bounds__(kThreads, 2) attn_block_kernel(const AttnBlock
         __syncthreads();
     }
 
-    // ---- 5. merge the cluster's states; this CTA's rows of Wo[:, head h]
+    // ---- 4. merge the cluster's states; this CTA's rows of Wo[:, head h]
     cluster_arrive();
     cluster_wait();  // every CTA's states are visible in the cluster
-    // warp w reads CTA w's state of every sequence (one batch of 16-byte
-    // loads), scales it by its softmax weight and parks it; then each output
-    // element sums the 8 parked parts
     {
-        float* s_m = reinterpret_cast<float*>(smem + L.qkv);  // [8][4] m, then [8][4] l (the QKV rows are done)
-        float* s_l = s_m + kClusterCtas * 4;
-        float4 av[kStepMaxBatch];
-        const float* pp = peer(part, warp);
-        constexpr int V = HD / 4;  // float4 per state
-#pragma unroll
-        for (int b = 0; b < kStepMaxBatch; ++b)
-            if (b < B && lane < V) av[b] = *reinterpret_cast<const float4*>(pp + b * PS + lane * 4);
-        if (lane < B) {
-            s_m[warp * 4 + lane] = pp[lane * PS + HD];
-            s_l[warp * 4 + lane] = pp[lane * PS + HD + 1];
-        }
-        __syncthreads();
-        float* contrib = wst;  // [8][4][HD] (the warps' attention states are done)
+        // warp w scales CTA w's state by its softmax weight (every warp
+        // derives the same weights from the 8 (m, l) pairs) and parks it;
+        // each output element then sums the 8 parked parts in rank order
+        float* contrib = wst;  // [8][4][HD] (the warps' states are merged)
+        const float* mine = peer(part, warp);
 #pragma unroll
         for (int b = 0; b < kStepMaxBatch; ++b) {
             if (b >= B) break;
-            float M = -INFINITY;
-#pragma unroll
-            for (int w = 0; w < kClusterCtas; ++w) M = fmaxf(M, s_m[w * 4 + b]);
-            float Ls = 0.f;
-#pragma unroll
-            for (int w = 0; w < kClusterCtas; ++w) {
-                const float mw = s_m[w * 4 + b];
-                if (mw != -INFINITY) Ls += s_l[w * 4 + b] * expf(mw - M);
-            }
-            const float mine = s_m[warp * 4 + b];
-            const float f = (mine == -INFINITY) ? 0.f : expf(mine - M) / Ls;
-            if (lane < V) {
-                const float4 x = av[b];
+            const float mr = lane < kClusterCtas ? peer(part, lane)[b * PS + HD] : -INFINITY;
+            const float lr = lane < kClusterCtas ? peer(part, lane)[b * PS + HD + 1] : 0.f;
+            const float M = warp_max(mr);
+            const float f = mr == -INFINITY ? 0.f : expf(mr - M);
+            const float Ls = warp_sum(lr * f);
+            const float fw = __shfl_sync(0xffffffffu, f, warp) / Ls;
+            if (lane < HD / 4) {
+                const float4 x = *reinterpret_cast<const float4*>(mine + b * PS + lane * 4);
                 *reinterpret_cast<float4*>(contrib + (warp * kStepMaxBatch + b) * HD + lane * 4) =
-                    make_float4(x.x * f, x.y * f, x.z * f, x.w * f);
+                    make_float4(x.x * fw, x.y * fw, x.z * fw, x.w * fw);
             }
         }
         __syncthreads();
@@ -727,159 +763,139 @@ __global__ void __launch_bounds__(kThreads, 2) attn_block_kernel(const AttnBlock
     cluster_wait();  // no CTA leaves while a peer may still read its shared memory
 }
 
-// ===================================================================== gate/up
-// CTA c takes tpc consecutive 16-row gate/up tiles (8 gate rows and the
-// same 8 up units each), already in shared memory, and writes the hi/lo
-// planes of a = silu(gate) * up for its 8 tpc units.  It also clears its
-// share of the next residual accumulator.
-__global__ void __launch_bounds__(kThreads, 2) ffn_gate_kernel(const FfnGateArgs a) {
+// ===================================================================== FFN block
+// Cluster c (8 CTAs) serves FFN units [192 c, 192 c + 192): their 24 gate/up
+// tiles (8 gate rows and the same 8 up units each) and k-pairs [6 c, 6 c + 6)
+// of every down row.
+//  1. Gate/up rows times the residual stream, K split over the 8 CTAs as in
+//     the attention block (RMSNorm gain in the operand, 1 / rms after).
+//  2. Every CTA sums the 8 partial rows of all 192 units and forms
+//     a = silu(gate) * up for them.
+//  3. CTA r multiplies its H / 8 down rows (over the cluster's 192 units) by
+//     a; the rows are added to the fixed-point residual stream (cluster 0
+//     also adds the stream's input).
+__global__ void __launch_bounds__(kThreads, 2) ffn_block_kernel(const FfnBlockArgs a) {
+    constexpr int T = 2 * kFfnUnits / 16;  // gate/up tiles of the cluster
+    constexpr int TPW = (T + kWarps - 1) / kWarps;
+    constexpr int R2 = 2 * kFfnUnits;      // gate/up rows of the cluster
+    constexpr int DKP = kFfnUnits / 32;    // down k-pairs of the cluster
     extern __shared__ __align__(128) unsigned char smem[];
-    const GateLayout L = gate_layout(a.H, a.tpc);
+    const FfnLayout L = ffn_layout(a.H);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int r = cluster_rank();
+    const int c = blockIdx.x / kClusterCtas;
     const int H = a.H, B = a.B;
-    const int tiles = 2 * a.I / 16;
-    const int tb = blockIdx.x * a.tpc, nt = min(a.tpc, tiles - tb);
-    const uint32_t blob = (uint32_t)tile_blob_bytes(H);
-    uint64_t* bar = reinterpret_cast<uint64_t*>(smem + L.bar);
-    float* s_inv = reinterpret_cast<float*>(smem + L.misc);
-    float* s_red = s_inv + 4;
-    uint4* xop = reinterpret_cast<uint4*>(smem + L.xop);
-    if (tid == 0) {
-        mbar_init(bar, 1);
-        fence_mbar_init();
-    }
-    __syncthreads();
-    if (tid == 0 && nt > 0) {
-        mbar_arrive_expect_tx(bar, (uint32_t)nt * blob);
-        bulk_g2s(smem + L.w, a.wgu + (size_t)tb * blob, (uint32_t)nt * blob, bar);
-    }
+    const int nkp = H / 32 / kClusterCtas, kp0 = r * nkp;
+    const int ro = H / kClusterCtas, dt = ro / 16;
+    const uint32_t blob = (uint32_t)tile_blob_bytes(H), dblob = (uint32_t)tile_blob_bytes(a.I);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bars);  // 0 gate/up slices, 1 down rows
+    float* s_sgu = reinterpret_cast<float*>(smem + L.sgu);
+    float* s_sd = reinterpret_cast<float*>(smem + L.sd);
     float* s_gain = reinterpret_cast<float*>(smem + L.gain);
-    for (int i = tid; i < H; i += kThreads) s_gain[i] = a.ffn_norm[i];
-    pdl_wait();
-    pdl_launch_dependents();
-    {
-        const int n = B * H, per = (n + gridDim.x - 1) / gridDim.x;
-        const int z0 = blockIdx.x * per, z1 = min(n, z0 + per);
-        for (int i = z0 + tid; i < z1; i += kThreads) a.xf[i] = 0;
-    }
-    norm_operand(xop, a.xa, nullptr, nullptr, nullptr, B, H, s_gain, a.eps, s_red);
-    const bool bad = nt > 0 && block_wait_failed(bar, 0);
-    float acc[kGateTmax][4];
-    mma_tiles<kGateTmax>(acc, smem + L.w, blob, bad ? 0 : nt, xop, H / 32);
-    __syncthreads();  // every warp is done with the operand (the partial sums reuse it)
-    float4* red = reinterpret_cast<float4*>(smem + L.red);
-#pragma unroll
-    for (int t = 0; t < kGateTmax; ++t)
-        if (t < nt) red[(t * kWarps + warp) * 32 + lane] = make_float4(acc[t][0], acc[t][1], acc[t][2], acc[t][3]);
-    __syncthreads();
-    for (int i = tid; i < nt * 32; i += kThreads) {
-        const int t = i >> 5, ln = i & 31, gg = ln >> 2, tq = ln & 3;
-        if (tq >= B) continue;
-        float s0 = 0.f, s1 = 0.f;
-        for (int w = 0; w < kWarps; ++w) {
-            const float4 v = red[(t * kWarps + w) * 32 + ln];
-            s0 += v.x + v.y;
-            s1 += v.z + v.w;
-        }
-        const float* sc = reinterpret_cast<const float*>(smem + L.w + (size_t)t * blob);
-        const float gate = sc[gg] * s0, up = sc[gg + 8] * s1;
-        const float v = (gate / (1.0f + expf(-gate))) * up;
-        const int unit = (tb + t) * 8 + gg;
-        __half hi, lo;
-        split_f16(v, hi, lo);
-        a.ah[plane_index(2 * tq, unit, a.I, 1)] = hi;
-        a.ah[plane_index(2 * tq + 1, unit, a.I, 1)] = lo;
-    }
-    if (bad && tid == 0) {
-        set_status(a.status, kStatusTimeout);
-        mbar_wait_bounded(bar, 0);
-    }
-}
+    long long* s_res = reinterpret_cast<long long*>(smem + L.resid);
+    float* s_inv = reinterpret_cast<float*>(smem + L.misc);
+    uint4* xop = reinterpret_cast<uint4*>(smem + L.xop);
+    float* pgu = reinterpret_cast<float*>(smem + L.pgu);
+    float* s_ss = reinterpret_cast<float*>(smem + L.ss);
+    uint4* dop = reinterpret_cast<uint4*>(smem + L.dop);
 
-// ===================================================================== down
-// CTA (tile, part) multiplies its k-pair range of one 16-row down tile
-// (shared memory) by the activation planes, then adds the rows to the
-// fixed-point residual stream; part 0 also carries the stream's input
-// over and clears it for the next layer.
-__global__ void __launch_bounds__(kThreads, 2) ffn_down_kernel(const FfnDownArgs a) {
-    extern __shared__ __align__(128) unsigned char smem[];
-    const DownLayout L = down_layout(a.I, a.ks);
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int tile = blockIdx.x / a.ks, part = blockIdx.x - tile * a.ks;
-    const int kp = a.I / 32;
-    const int p_lo = kp * part / a.ks, p_hi = kp * (part + 1) / a.ks;
-    uint64_t* bar = reinterpret_cast<uint64_t*>(smem + L.bar);
-    float* s_sc = reinterpret_cast<float*>(smem + L.misc);
     if (tid == 0) {
-        mbar_init(bar, 1);
+        mbar_init(&bars[0], 1);
+        mbar_init(&bars[1], 1);
         fence_mbar_init();
     }
     __syncthreads();
     if (tid == 0) {
-        const uint32_t bytes = (uint32_t)(p_hi - p_lo) * 512u;
-        mbar_arrive_expect_tx(bar, bytes);
-        bulk_g2s(smem + L.w, a.wd + (size_t)tile * tile_blob_bytes(a.I) + kTileHeader + (size_t)p_lo * 512, bytes,
-                 bar);
+        mbar_arrive_expect_tx(&bars[0], (uint32_t)(T * nkp * 512));
+        for (int t = 0; t < T; ++t)
+            bulk_g2s(smem + L.wgu + (size_t)t * nkp * 512,
+                     a.wgu + (size_t)(T * c + t) * blob + kTileHeader + (size_t)kp0 * 512, (uint32_t)nkp * 512,
+                     &bars[0]);
+        mbar_arrive_expect_tx(&bars[1], (uint32_t)(dt * DKP * 512));
+        for (int i = 0; i < dt; ++i)
+            bulk_g2s(smem + L.wd + (size_t)i * DKP * 512,
+                     a.wd + (size_t)(r * dt + i) * dblob + kTileHeader + (size_t)DKP * c * 512, DKP * 512,
+                     &bars[1]);
     }
-    if (tid < 16) s_sc[tid] = a.d_scale[tile * 16 + tid];
+    for (int i = tid; i < R2; i += kThreads) s_sgu[i] = a.gu_scale[(size_t)T * 16 * c + i];
+    for (int i = tid; i < ro; i += kThreads) s_sd[i] = a.d_scale[r * ro + i];
+    for (int i = tid; i < nkp * 32; i += kThreads) s_gain[i] = a.ffn_norm[kp0 * 32 + i];
     pdl_wait();
     pdl_launch_dependents();
-    // this warp's activation words first (independent loads), then the MMAs
-    uint4 bw[kDownKpw];
-    const uint4* ap = reinterpret_cast<const uint4*>(a.ah);
+
+    if (c == 0)  // this cluster adds the stream's input to its rows
+        for (int i = tid; i < B * ro; i += kThreads) {
+            const int b = i / ro;
+            s_res[i] = __ldcg(a.xa + (size_t)b * H + r * ro + (i - b * ro));
+        }
+    // ---- 1. this CTA's K slice of the cluster's gate/up rows
+    slice_operand(xop, s_ss, a.xa, nullptr, nullptr, nullptr, B, H, kp0 * 32, nkp, s_gain);
+    bool bad = block_wait_failed(&bars[0], 0);
+    if (!bad) cluster_tiles_mma<TPW>(smem + L.wgu, T, nkp, xop, pgu, R2);
+    cluster_arrive();
+    cluster_wait();  // every CTA's partial rows are visible in the cluster
+
+    // ---- 2. a = silu(gate) * up for the cluster's units, as the down operand
+    if (tid < B) s_inv[tid] = cluster_inv_rms(s_ss, tid, H, a.eps);
+    __syncthreads();
+    {
+        __half* doph = reinterpret_cast<__half*>(dop);
+        for (int i = tid; i < B * kFfnUnits; i += kThreads) {
+            const int b = i / kFfnUnits, u = i - b * kFfnUnits;
+            const int gr = (u >> 3) * 16 + (u & 7);  // gate row of unit u; its up row is gr + 8
+            float sg = 0.f, su = 0.f;
 #pragma unroll
-    for (int j = 0; j < kDownKpw; ++j) {
-        const int p = p_lo + warp + kWarps * j;
-        if (p < p_hi) bw[j] = __ldcg(ap + ((size_t)p * 8) * 32 + lane);
-    }
-    const bool bad = block_wait_failed(bar, 0);
-    float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
-    if (!bad) {
-#pragma unroll
-        for (int j = 0; j < kDownKpw; ++j) {
-            const int p = p_lo + warp + kWarps * j;
-            if (p < p_hi) {
-                const uint4 wv = *reinterpret_cast<const uint4*>(smem + L.w + (size_t)(p - p_lo) * 512 + lane * 16);
-                mma_pair(c0, c1, wv, bw[j]);
+            for (int rr = 0; rr < kClusterCtas; ++rr) {
+                const float* pp = peer(pgu, rr) + b * R2;
+                sg += pp[gr];
+                su += pp[gr + 8];
             }
+            const float gate = s_sgu[gr] * s_inv[b] * sg;
+            const float up = s_sgu[gr + 8] * s_inv[b] * su;
+            const float v = (gate / (1.0f + expf(-gate))) * up;
+            __half hi, lo;
+            split_f16(v, hi, lo);
+            doph[frag_half(2 * b, u)] = hi;
+            doph[frag_half(2 * b + 1, u)] = lo;
         }
     }
-    float4* red = reinterpret_cast<float4*>(smem + L.red);
-    red[warp * 32 + lane] = make_float4(c0[0] + c1[0], c0[1] + c1[1], c0[2] + c1[2], c0[3] + c1[3]);
-    __syncthreads();
-    if (tid < 32) {
-        const int gg = tid >> 2, tq = tid & 3;
-        if (tq < a.B) {
-            float s0 = 0.f, s1 = 0.f;
-            for (int w = 0; w < kWarps; ++w) {
-                const float4 v = red[w * 32 + tid];
-                s0 += v.x + v.y;
-                s1 += v.z + v.w;
-            }
+    cluster_arrive();  // done with the peers' shared memory (waited for before leaving)
+
+    // ---- 3. this CTA's down rows over the cluster's units
+    bad = block_wait_failed(&bars[1], 0) || bad;
+    if (warp < dt && !bad) {
+        const unsigned char* wt = smem + L.wd + (size_t)warp * DKP * 512;
+        float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int p = 0; p < DKP; ++p) {
+            const uint4 wv = *reinterpret_cast<const uint4*>(wt + p * 512 + lane * 16);
+            mma_pair(c0, c1, wv, dop[p * 32 + lane]);
+        }
+        const int gg = lane >> 2, tq = lane & 3;
+        if (tq < B) {
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
-                const int row = tile * 16 + gg + 8 * half;
-                long long f = fix_of(s_sc[gg + 8 * half] * (half ? s1 : s0));
-                if (part == 0) {
-                    long long* xr = a.xa + (size_t)tq * a.H + row;
-                    f += __ldcg(xr);
-                    *xr = 0;
-                }
-                red_add_fix(a.xf + (size_t)tq * a.H + row, f);
+                const int rl = warp * 16 + gg + 8 * half;
+                const float s = half ? (c0[2] + c0[3] + c1[2] + c1[3]) : (c0[0] + c0[1] + c1[0] + c1[1]);
+                long long f = fix_of(s_sd[rl] * s);
+                if (c == 0) f += s_res[tq * ro + rl];
+                red_add_fix(a.xf + (size_t)tq * H + r * ro + rl, f);
             }
         }
     }
     if (bad && tid == 0) {
         set_status(a.status, kStatusTimeout);
-        mbar_wait_bounded(bar, 0);
+        mbar_wait_bounded(&bars[0], 0);
+        mbar_wait_bounded(&bars[1], 0);
     }
+    cluster_wait();  // no CTA leaves while a peer may still read its shared memory
 }
 
 // ===================================================================== lm_head
 // The tied embedding table swept once: a producer warp streams the CTA's
-// range of 16-row tiles into a ring of shared-memory stages (the first
-// stages before the wait), and 8 consumer warps each take whole tiles
-// (tile j -> warp j % 8) against the final-RMSNorm operand.  Each lane
+// range of 16-row tiles into a ring of S <= 8 shared-memory stages (the
+// first stages before the wait), and consumer warp s takes the tiles of
+// stage s (tile j -> stage and warp j % S) against the final-RMSNorm operand.  Each lane
 // keeps the best (value, lowest index) key of its sequence; block, then
 // grid atomicMax; the last CTA publishes the tokens.
 __global__ void __launch_bounds__(kLmThreads, 2) lm_head_kernel(const LmHeadArgs a) {
@@ -919,6 +935,7 @@ __global__ void __launch_bounds__(kLmThreads, 2) lm_head_kernel(const LmHeadArgs
     for (int i = tid; i < H; i += kLmThreads) s_gain[i] = a.final_norm[i];
     pdl_wait();
     pdl_launch_dependents();
+    clear_share(a.clear, B * H);
     norm_operand(xop, a.xf, nullptr, nullptr, nullptr, B, H, s_gain, a.eps, s_red);
 
     if (producer) {
@@ -937,7 +954,9 @@ __global__ void __launch_bounds__(kLmThreads, 2) lm_head_kernel(const LmHeadArgs
     if (warp < kWarps) {
         const int kpairs = H / 32;
         const int gg = lane >> 2, tq = lane & 3;
-        for (int j = warp; j < n; j += kWarps) {
+        // stage s belongs to consumer warp s alone (tile j -> stage and warp j % S), so every wait on a
+        // stage's full barrier is for the phase right after the one that warp last consumed
+        for (int j = warp; warp < S && j < n; j += S) {
             const int s = j % S;
             if (*reinterpret_cast<volatile int*>(s_abort)) break;
             if (!mbar_wait_bounded(&full[s], (uint32_t)(j / S) & 1u)) {
@@ -1020,28 +1039,20 @@ __global__ void __launch_bounds__(kLmThreads, 2) lm_head_kernel(const LmHeadArgs
 
 // ===================================================================== host side
 size_t attn_block_smem(int H, int hd, int kv_stages) { return attn_block_layout(H, hd, kv_stages).total; }
-size_t ffn_gate_smem(int H, int tpc) { return gate_layout(H, tpc).total; }
-size_t ffn_down_smem(int I, int ks) { return down_layout(I, ks).total; }
+size_t ffn_block_smem(int H) { return ffn_layout(H).total; }
 size_t lm_head_smem(int H, int stages) { return lm_layout(H, stages).total; }
 
 bool step_plan(const StepShape& s, int num_sms, int smem_optin, StepPlan* p) {
     if (s.hd != 64 && s.hd != 128) return false;
     if (s.nkv < 1 || s.nh % s.nkv) return false;
-    if (s.H % 128 || s.H > 1024 || s.I % 32 || s.vocab_rows % 16) return false;
+    // K slices of whole k-pairs, at most 4 per CTA (a sequence's operand threads share one warp)
+    if (s.H % 256 || s.H > 1024 || s.I % kFfnUnits || s.vocab_rows % 16) return false;
     StepPlan q;
     q.kv_stages = p->kv_stages < 1 ? 2 : p->kv_stages;
     if (attn_block_smem(s.H, s.hd, q.kv_stages) > (size_t)smem_optin) return false;
-    const int gtiles = 2 * s.I / 16;
-    q.gate_tpc = std::min(kGateTmax, std::max(1, (gtiles + num_sms - 1) / num_sms));
-    while (q.gate_tpc > 1 && ffn_gate_smem(s.H, q.gate_tpc) > (size_t)smem_optin) --q.gate_tpc;
-    if (ffn_gate_smem(s.H, q.gate_tpc) > (size_t)smem_optin) return false;
-    q.gate_grid = (gtiles + q.gate_tpc - 1) / q.gate_tpc;
-    const int dtiles = s.H / 16, kp = s.I / 32;
-    q.down_ks = std::max(1, std::min(8, num_sms / dtiles));
-    while ((kp + q.down_ks - 1) / q.down_ks > kDownKpw * kWarps) ++q.down_ks;
-    if (q.down_ks > kp) return false;
-    q.down_grid = dtiles * q.down_ks;
-    q.lm_stages = 8;
+    if (ffn_block_smem(s.H) > (size_t)smem_optin) return false;
+    q.ffn_grid = s.I / kFfnUnits * kClusterCtas;
+    q.lm_stages = 6;
     while (q.lm_stages > 2 && lm_head_smem(s.H, q.lm_stages) > (size_t)smem_optin) --q.lm_stages;
     if (lm_head_smem(s.H, q.lm_stages) > (size_t)smem_optin) return false;
     q.lm_grid = std::min(num_sms, s.vocab_rows / 16);
@@ -1049,11 +1060,9 @@ bool step_plan(const StepShape& s, int num_sms, int smem_optin, StepPlan* p) {
     return true;
 }
 
-bool step_prepare_device(const StepShape& s, const StepPlan& p) {
-    (void)s;
-    (void)p;
+bool step_prepare_device() {
     const void* fns[] = {(const void*)attn_block_kernel<64>, (const void*)attn_block_kernel<128>,
-                         (const void*)ffn_gate_kernel, (const void*)ffn_down_kernel, (const void*)lm_head_kernel};
+                         (const void*)ffn_block_kernel, (const void*)lm_head_kernel};
     for (const void* f : fns)
         if (allow_max_dynamic_smem(f) != cudaSuccess) return false;
     return true;
@@ -1092,23 +1101,19 @@ cudaError_t launch_attn_block(const AttnBlockArgs& a, int hd, cudaStream_t st) {
     return cudaErrorInvalidValue;
 }
 
-cudaError_t launch_ffn_gate(const FfnGateArgs& a, int grid, cudaStream_t st) {
-    return launch_ex(ffn_gate_kernel, grid, kThreads, ffn_gate_smem(a.H, a.tpc), 1, st, a);
-}
-
-cudaError_t launch_ffn_down(const FfnDownArgs& a, int grid, cudaStream_t st) {
-    return launch_ex(ffn_down_kernel, grid, kThreads, ffn_down_smem(a.I, a.ks), 1, st, a);
+cudaError_t launch_ffn_block(const FfnBlockArgs& a, int grid, cudaStream_t st) {
+    return launch_ex(ffn_block_kernel, grid, kThreads, ffn_block_smem(a.H), kClusterCtas, st, a);
 }
 
 cudaError_t launch_lm_head(const LmHeadArgs& a, int grid, cudaStream_t st) {
     return launch_ex(lm_head_kernel, grid, kLmThreads, lm_head_smem(a.H, a.stages), 1, st, a);
 }
 
-int attn_block_max_clusters(int H, int hd, int kv_stages) {
+static int max_clusters(const void* f, size_t smem) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(kClusterCtas);
     cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = attn_block_smem(H, hd, kv_stages);
+    cfg.dynamicSmemBytes = smem;
     cudaLaunchAttribute at[1];
     at[0].id = cudaLaunchAttributeClusterDimension;
     at[0].val.clusterDim.x = kClusterCtas;
@@ -1117,12 +1122,18 @@ int attn_block_max_clusters(int H, int hd, int kv_stages) {
     cfg.attrs = at;
     cfg.numAttrs = 1;
     int n = 0;
-    const void* f = hd == 128 ? (const void*)attn_block_kernel<128> : (const void*)attn_block_kernel<64>;
     if (cudaOccupancyMaxActiveClusters(&n, f, &cfg) != cudaSuccess) {
         cudaGetLastError();
         return 0;
     }
     return n;
 }
+
+int attn_block_max_clusters(int H, int hd, int kv_stages) {
+    const void* f = hd == 128 ? (const void*)attn_block_kernel<128> : (const void*)attn_block_kernel<64>;
+    return max_clusters(f, attn_block_smem(H, hd, kv_stages));
+}
+
+int ffn_block_max_clusters(int H) { return max_clusters((const void*)ffn_block_kernel, ffn_block_smem(H)); }
 
 }  // namespace q3
