@@ -454,11 +454,12 @@ int enqueue_step(q3i8_ctx* c, int B, bool want_logits) {
     cudaStream_t st = c->stream;
     const int splits = decode_splits(c, B);
     // the residual projections have only hidden/16 tiles: their K is split
-    // over kResidSplit CTAs per tile.  Up to 4 sequences the parts are summed
-    // in order by the tile's last CTA (deterministic); beyond, atomic adds
-    // measured faster (B = 32: 1.80 vs 1.94 ms per step)
+    // over kResidSplit CTAs per tile, and the tile's last CTA sums the parts
+    // in order, so a step gives the same bits on every run (atomic adds
+    // measured about 7 % faster at B = 32, 1.80 vs 1.94 ms per step, but
+    // their order, and so their rounding, changes from run to run)
     const int ks_resid = kResidSplit;
-    float* kpart = B <= 4 ? c->kpart : nullptr;
+    float* kpart = c->kpart;
 
     launch_embed(c->tokens, B, c->embed.raw, c->embed.scale, H, d.vocab, c->x, c->status, st);
     launch_rmsnorm(c->x, nullptr, B, H, c->layers[0].attn_norm, d.rms_eps, nullptr, c->xh, st, 1);
@@ -536,6 +537,8 @@ int step_setup(q3i8_ctx* c) {
     c->splan = p;
     c->use_step = true;
     c->step_max_batch = kStepMaxBatch;
+    c->step_max_ctx = 2048;
+    if (const char* mc = getenv("Q3I8_STEP_MAX_CTX")) c->step_max_ctx = std::max(0, atoi(mc));
     if (const char* mb = getenv("Q3I8_STEP_MAX_BATCH")) c->step_max_batch = std::max(0, std::min(kStepMaxBatch, atoi(mb)));
     return Q3_OK;
 }
@@ -710,7 +713,13 @@ cudaError_t enqueue_persistent(q3i8_ctx* c, int B, float* logits, unsigned long 
 // shape allows it, else the chained kernels.
 static bool persistent_for(const q3i8_ctx* c, int B) { return c->use_persistent && B <= c->p_max_batch; }
 
-static bool fused_for(const q3i8_ctx* c, int B) { return c->use_step && B <= c->step_max_batch; }
+// The small-batch step serves up to step_max_batch sequences whose contexts
+// stay within step_max_ctx positions; longer contexts attend faster in the
+// chained kernels' split-KV attention (measured: 1.20 vs 1.49 ms per step at
+// 4097..6144 positions, B = 1, 0.6B shape).
+static bool fused_for(const q3i8_ctx* c, int B) {
+    return c->use_step && B <= c->step_max_batch && c->call_ctx <= c->step_max_ctx;
+}
 
 static int enqueue_decode_step(q3i8_ctx* c, int B, bool want_logits) {
     if (persistent_for(c, B)) {
@@ -743,7 +752,8 @@ int prefill_launches(const q3i8_ctx* c, int M) {
 
 // Graph of one decode step at batch B (captured on first use).
 static int get_graph(q3i8_ctx* c, int B, cudaGraphExec_t* out) {
-    auto it = c->graphs.find(B);
+    const int key = 2 * B + (fused_for(c, B) ? 1 : 0);  // one graph per batch size and step kind
+    auto it = c->graphs.find(key);
     if (it != c->graphs.end()) {
         *out = it->second;
         return Q3_OK;
@@ -761,7 +771,7 @@ static int get_graph(q3i8_ctx* c, int B, cudaGraphExec_t* out) {
     e = cudaGraphInstantiate(&ex, g, 0);
     cudaGraphDestroy(g);
     if (e != cudaSuccess) return fail(c, Q3_ERR_CUDA, "graph instantiate failed: %s", cudaGetErrorString(e));
-    c->graphs[B] = ex;
+    c->graphs[key] = ex;
     *out = ex;
     return Q3_OK;
 }
@@ -906,25 +916,58 @@ static int ensure_events(q3i8_ctx* c) {
     return Q3_OK;
 }
 
-static int decode_core(q3i8_ctx* c, int B, const int32_t* d_ids, const int32_t* lens, int max_new,
-                       q3i8_stats* stats) {
+// Prefill, then decode steps until max_new tokens per sequence exist or,
+// with eos_id >= 0, until every sequence has produced eos_id: the step graph
+// is then replayed in chunks of kEosChunk steps and the chunk's ids are read
+// back to see whether all sequences are done.  *steps_run receives the
+// number of decode steps run.
+constexpr int kEosChunk = 16;
+
+static int decode_core(q3i8_ctx* c, int B, const int32_t* d_ids, const int32_t* lens, int max_new, int need,
+                       int32_t eos_id, q3i8_stats* stats, int* steps_run = nullptr) {
     int rc = ensure_events(c);
     if (rc) return rc;
+    c->call_ctx = need;
     CK(c, cudaEventRecord(c->ev0, c->stream));
     rc = run_prefill(c, B, d_ids, lens, nullptr);
     if (rc) return rc;
     CK(c, cudaEventRecord(c->ev1, c->stream));
+    int steps = 0;
     if (max_new > 1) {
         cudaGraphExec_t g;
         rc = get_graph(c, B, &g);
         if (rc) return rc;
-        for (int i = 1; i < max_new; ++i) CK(c, cudaGraphLaunch(g, c->stream));
-        c->launches += (int64_t)(max_new - 1) * step_launches(c, B);
+        if (eos_id < 0) {
+            for (int i = 1; i < max_new; ++i) CK(c, cudaGraphLaunch(g, c->stream));
+            steps = max_new - 1;
+        } else {
+            std::vector<char> done(B, 0);
+            std::vector<int32_t> ids((size_t)B * kEosChunk);
+            int col = 0;  // next out_ids column to inspect (column 0 is the prefill's token)
+            while (true) {
+                const int ncols = std::min(kEosChunk, steps + 1 - col);
+                if (ncols > 0) {
+                    CK(c, cudaMemcpy2DAsync(ids.data(), (size_t)ncols * 4, c->out_ids + col, (size_t)c->out_cap * 4,
+                                            (size_t)ncols * 4, B, cudaMemcpyDeviceToHost, c->stream));
+                    CK(c, cudaStreamSynchronize(c->stream));
+                    for (int b = 0; b < B; ++b)
+                        for (int j = 0; j < ncols; ++j) done[b] |= ids[(size_t)b * ncols + j] == eos_id;
+                    col += ncols;
+                }
+                if (std::all_of(done.begin(), done.end(), [](char d) { return d != 0; }) || steps >= max_new - 1)
+                    break;
+                const int n = std::min(kEosChunk, max_new - 1 - steps);
+                for (int i = 0; i < n; ++i) CK(c, cudaGraphLaunch(g, c->stream));
+                steps += n;
+            }
+        }
+        c->launches += (int64_t)steps * step_launches(c, B);
     }
     CK(c, cudaEventRecord(c->ev2, c->stream));
     rc = check_status(c);
     if (rc) return rc;
-    for (int b = 0; b < B; ++b) c->seq_len[b] += max_new - 1;
+    if (steps_run) *steps_run = steps;
+    for (int b = 0; b < B; ++b) c->seq_len[b] += steps;
     if (stats) {
         float pf = 0, dc = 0;
         CK(c, cudaEventElapsedTime(&pf, c->ev0, c->ev1));
@@ -934,10 +977,10 @@ static int decode_core(q3i8_ctx* c, int B, const int32_t* d_ids, const int32_t* 
         stats->prefill_ms = pf;
         stats->decode_ms = dc;
         stats->prefill_tokens = ptoks;
-        stats->decode_steps = max_new - 1;
+        stats->decode_steps = steps;
         stats->prefill_tokens_per_sec = pf > 0 ? ptoks / (pf * 1e-3) : 0;
-        stats->decode_tokens_per_sec = (dc > 0 && max_new > 1) ? (double)B * (max_new - 1) / (dc * 1e-3) : 0;
-        stats->step_us = max_new > 1 ? dc * 1e3 / (max_new - 1) : 0;
+        stats->decode_tokens_per_sec = (dc > 0 && steps > 0) ? (double)B * steps / (dc * 1e-3) : 0;
+        stats->step_us = steps > 0 ? dc * 1e3 / steps : 0;
     }
     return Q3_OK;
 }
@@ -951,7 +994,7 @@ extern "C" int q3i8_decode_device(q3i8_ctx* c, int32_t B, const int32_t* d_promp
     if (!d_prompt_ids || !d_out_ids) return fail(c, Q3_ERR_INVALID_ARGUMENTS, "device id buffer is NULL");
     if ((rc = ensure_capacity(c, need))) return rc;
     if ((rc = ensure_out(c, max_new_tokens))) return rc;
-    if ((rc = decode_core(c, B, d_prompt_ids, prompt_lens, max_new_tokens, stats))) return rc;
+    if ((rc = decode_core(c, B, d_prompt_ids, prompt_lens, max_new_tokens, need, -1, stats))) return rc;
     CK(c, cudaMemcpy2DAsync(d_out_ids, (size_t)max_new_tokens * 4, c->out_ids, (size_t)c->out_cap * 4,
                             (size_t)max_new_tokens * 4, B, cudaMemcpyDeviceToDevice, c->stream));
     CK(c, cudaStreamSynchronize(c->stream));
@@ -981,18 +1024,21 @@ extern "C" int q3i8_decode(q3i8_ctx* c, int32_t B, const int32_t* const* prompt_
     if ((rc = ensure_out(c, max_new_tokens))) return rc;
     if ((rc = ensure_prefill(c, (int)all.size()))) return rc;
     CK(c, cudaMemcpyAsync(c->pf_ids, all.data(), all.size() * 4, cudaMemcpyHostToDevice, c->stream));
-    if ((rc = decode_core(c, B, c->pf_ids, prompt_lens, max_new_tokens, stats))) return rc;
+    int steps = 0;
+    if ((rc = decode_core(c, B, c->pf_ids, prompt_lens, max_new_tokens, need, eos_id, stats, &steps))) return rc;
+    const int made = steps + 1;  // ids produced per sequence
     CK(c, cudaMemcpy2DAsync(out_ids, (size_t)max_new_tokens * 4, c->out_ids, (size_t)c->out_cap * 4,
-                            (size_t)max_new_tokens * 4, B, cudaMemcpyDeviceToHost, c->stream));
+                            (size_t)made * 4, B, cudaMemcpyDeviceToHost, c->stream));
     CK(c, cudaStreamSynchronize(c->stream));
     for (int b = 0; b < B; ++b) {
-        int n = max_new_tokens;
+        int n = made;
         if (eos_id >= 0)
-            for (int i = 0; i < max_new_tokens; ++i)
+            for (int i = 0; i < made; ++i)
                 if (out_ids[(size_t)b * max_new_tokens + i] == eos_id) {
                     n = i + 1;
                     break;
                 }
+        for (int i = made; i < max_new_tokens; ++i) out_ids[(size_t)b * max_new_tokens + i] = -1;
         if (out_counts) out_counts[b] = n;
     }
     return Q3_OK;
@@ -1038,6 +1084,7 @@ extern "C" int q3i8_step_logits(q3i8_ctx* c, const int32_t* tokens, float* logit
         if (c->seq_len[b] + 1 > c->cap)
             return fail(c, Q3_ERR_STATE, "sequence %d is at the context capacity (%d)", b, c->cap);
     }
+    c->call_ctx = 1 + *std::max_element(c->seq_len.begin(), c->seq_len.begin() + B);
     CK(c, cudaMemcpyAsync(c->tokens, tokens, B * 4, cudaMemcpyHostToDevice, c->stream));
     if (int rc0 = enqueue_decode_step(c, B, true)) return rc0;
     c->launches += step_launches(c, B);

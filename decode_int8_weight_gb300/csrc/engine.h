@@ -87,6 +87,8 @@ struct q3i8_ctx {
     // small-batch decode step (step.cu): two cluster kernels per layer
     bool use_step = false;
     int step_max_batch = 0;  // largest B decoded by it; larger B take the chained kernels
+    int step_max_ctx = 0;    // longest context (positions) it serves; longer calls take the chained kernels
+    int call_ctx = 0;        // longest context the current call can reach
     q3::StepPlan splan;
     long long *xa = nullptr, *xf = nullptr;  // residual stream accumulators [2][bmax][H], value * 2^32
 

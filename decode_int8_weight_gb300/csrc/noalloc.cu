@@ -20,7 +20,29 @@ constexpr size_t kScratchBytes = Q3I8_OP_ATTENTION_STATIC_SCRATCH_BYTES;
 constexpr int kMaxDevices = 64;
 
 std::mutex g_scratch_mu;
-float* g_scratch_ptr[kMaxDevices];  // device address of the scratch, per device
+float* g_scratch_ptr[kMaxDevices];    // device address of the scratch, per device
+void* g_scratch_ctx[kMaxDevices];     // the context that address belongs to
+
+// The current driver context (reached through the runtime's driver entry
+// point, so the library needs no link against the driver library).  A device
+// reset or a released primary context gives the device a new context whose
+// module copy of the scratch lives elsewhere, so the address is looked up
+// again whenever the context changes.
+void* current_context() {
+    typedef int (*GetCurrentFn)(void**);
+    static GetCurrentFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<GetCurrentFn>(p);
+    });
+    void* ctx = nullptr;
+    if (fn && fn(&ctx) != 0) ctx = nullptr;
+    return ctx;
+}
 
 int report(int code, const char* fmt, long long a = 0, long long b = 0) {
     char buf[256];
@@ -35,8 +57,8 @@ int report(int code, const char* fmt, long long a = 0, long long b = 0) {
 // merge kernel reads it, so its contents never need clearing.
 static __device__ __align__(256) float g_attn_scratch[kScratchBytes / sizeof(float)];
 
-// Device address of g_attn_scratch on the current device, looked up once per
-// device with that device current.
+// Device address of g_attn_scratch on the current device, looked up with
+// that device current the first time and again whenever its context changed.
 static int scratch_on_current_device(float** out) {
     int dev = -1;
     cudaError_t e = cudaGetDevice(&dev);
@@ -44,8 +66,10 @@ static int scratch_on_current_device(float** out) {
     if (dev < 0 || dev >= kMaxDevices)
         return report(Q3_ERR_INVALID_ARGUMENTS, "op_attention_static: device %lld beyond the %lld supported", dev,
                       kMaxDevices);
+    void* ctx = current_context();  // null before the runtime made one current: then looked up below
     std::lock_guard<std::mutex> lock(g_scratch_mu);
-    if (!g_scratch_ptr[dev]) {
+    if (!g_scratch_ptr[dev] || ctx != g_scratch_ctx[dev]) {
+        g_scratch_ptr[dev] = nullptr;
         void* p = nullptr;
         e = cudaGetSymbolAddress(&p, g_attn_scratch);
         if (e != cudaSuccess || !p) {
@@ -54,6 +78,7 @@ static int scratch_on_current_device(float** out) {
             return q3_report_error(Q3_ERR_CUDA, buf);
         }
         g_scratch_ptr[dev] = (float*)p;
+        g_scratch_ctx[dev] = current_context();  // the lookup made the device's context current
     }
     *out = g_scratch_ptr[dev];
     return Q3_OK;

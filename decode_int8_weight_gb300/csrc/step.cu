@@ -163,7 +163,8 @@ Q3_DEV void norm_operand(uint4* xop, const long long* xin, const int* tok, const
 }
 
 // Two m16n8k16 MMAs from one 16-byte lane chunk of a tile blob (rows g, g+8;
-// two 16-wide k-steps) and the lane's four B words.
+// two 16-wide k-steps) and the lane's four B words; the weights are
+// converted exactly (byte permute and subtraction of the 128 offset).
 Q3_DEV void mma_pair(float (&c0)[4], float (&c1)[4], const uint4& wv, const uint4& bv) {
     uint32_t A0[4], A1[4];
     u8x4_to_f16x2x2(wv.x, A0[0], A0[1]);
@@ -211,15 +212,17 @@ Q3_DEV void slice_operand(uint4* xop, float* s_ss, const long long* xin, const i
         }
     }
     float ss = x[0] * x[0] + x[1] * x[1] + x[2] * x[2] + x[3] * x[3];
+    __half hi[4], lo[4];
+    {
+        const float4 g = own ? *reinterpret_cast<const float4*>(s_gain + kl) : make_float4(0.f, 0.f, 0.f, 0.f);
+        const float gg[4] = {g.x, g.y, g.z, g.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) split_f16(__fmul_rn(gg[j], x[j]), hi[j], lo[j]);
+    }
     // sum over the per_b threads of this sequence (an aligned group inside one warp)
     for (int o = 1; o < per_b; o <<= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
     if (own) {
         if (kl == 0) s_ss[b] = ss;
-        const float4 g = *reinterpret_cast<const float4*>(s_gain + kl);
-        const float gg[4] = {g.x, g.y, g.z, g.w};
-        __half hi[4], lo[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) split_f16(__fmul_rn(gg[j], x[j]), hi[j], lo[j]);
         uint32_t* xw = reinterpret_cast<uint32_t*>(xop);
         xw[frag_word(2 * b, kl)] = pack_half2(hi[0], hi[1]);
         xw[frag_word(2 * b, kl + 2)] = pack_half2(hi[2], hi[3]);
@@ -263,13 +266,19 @@ Q3_DEV void cluster_tiles_mma(const unsigned char* w_slices, int nt, int nkp, co
     }
 }
 
-// 1 / rms of sequence b from the cluster's partial sums of squares (peers
-// in rank order, so every CTA gets the same bits).
-Q3_DEV float cluster_inv_rms(const float* s_ss, int b, int H, float eps) {
-    float t = 0.f;
+// Sum over the 8 CTAs of a cluster of element i of a shared array, as a
+// fixed pairwise tree (every CTA gets the same bits).
+Q3_DEV float cluster_sum(const float* arr, int i) {
+    float v[kClusterCtas];
 #pragma unroll
-    for (int r = 0; r < kClusterCtas; ++r) t += peer(s_ss, r)[b];
-    return 1.0f / sqrtf(t / (float)H + eps);
+    for (int r = 0; r < kClusterCtas; ++r) v[r] = peer(arr, r)[i];
+    return ((v[0] + v[1]) + (v[2] + v[3])) + ((v[4] + v[5]) + (v[6] + v[7]));
+}
+
+// 1 / rms of sequence b from the cluster's partial sums of squares (s_ss of
+// slice_operand).
+Q3_DEV float cluster_inv_rms(const float* s_ss, int b, int H, float eps) {
+    return 1.0f / sqrtf(cluster_sum(s_ss, b) / (float)H + eps);
 }
 
 // Clears this CTA's share of a [n] accumulator (fire-and-forget stores).
@@ -361,7 +370,7 @@ __host__ __device__ inline LmLayout lm_layout(int H, int stages) {
     L.xop = take_smem(off, (size_t)(H / 32) * 512);
     L.gain = take_smem(off, (size_t)H * 4);
     L.best = take_smem(off, (size_t)kWarps * 4 * 8);
-    L.misc = take_smem(off, 256);
+    L.misc = take_smem(off, 512);
     L.bars = take_smem(off, (size_t)2 * stages * 8);
     L.total = off;
     return L;
@@ -547,22 +556,26 @@ __global__ void __launch_bounds__(kThreads, 2) attn_block_kernel(const AttnBlock
         const int b = warp & 3;
         const bool is_q = warp < 4;
         const float inv = cluster_inv_rms(s_ss, b, H, a.eps);
-        auto rows = [&](int j0, float (&v)[D]) {  // v = scale * inv * sum over the peers, rows j0 + D l ..
-#pragma unroll
-            for (int m = 0; m < D; ++m) v[m] = 0.f;
+        // v = scale * inv * (sum over the peers), rows j0 + D l .. (pairwise tree over the peers)
+        auto rows = [&](int j0, float (&v)[D]) {
+            float pr[kClusterCtas][D];
 #pragma unroll
             for (int rr = 0; rr < kClusterCtas; ++rr) {
                 const float* pp = peer(pqkv, rr) + b * R3 + j0 + D * lane;
                 if constexpr (D == 4) {
                     const float4 x = *reinterpret_cast<const float4*>(pp);
-                    v[0] += x.x, v[1] += x.y, v[2] += x.z, v[3] += x.w;
+                    pr[rr][0] = x.x, pr[rr][1] = x.y, pr[rr][2] = x.z, pr[rr][3] = x.w;
                 } else {
                     const float2 x = *reinterpret_cast<const float2*>(pp);
-                    v[0] += x.x, v[1] += x.y;
+                    pr[rr][0] = x.x, pr[rr][1] = x.y;
                 }
             }
 #pragma unroll
-            for (int m = 0; m < D; ++m) v[m] = s_sc[j0 + D * lane + m] * inv * v[m];
+            for (int m = 0; m < D; ++m) {
+                const float t = ((pr[0][m] + pr[1][m]) + (pr[2][m] + pr[3][m])) +
+                                ((pr[4][m] + pr[5][m]) + (pr[6][m] + pr[7][m]));
+                v[m] = s_sc[j0 + D * lane + m] * inv * t;
+            }
         };
         float v[D], vv[D];
         rows(is_q ? 0 : HD, v);
@@ -666,21 +679,27 @@ __global__ void __launch_bounds__(kThreads, 2) attn_block_kernel(const AttnBlock
 #pragma unroll
         for (int d = 0; d < D; ++d) ws[lane * D + d] = acc[d];
         __syncthreads();
-        for (int d = tid; d < HD; d += kThreads) {
+        // every thread derives the 8 warps' weights from their (m, l) in the
+        // same order; thread d then sums its element
+        {
+            float mw[kWarps], f[kWarps];
             float M = -INFINITY;
-            for (int w = 0; w < kWarps; ++w) M = fmaxf(M, wst[w * PS + HD]);
-            float Ls = 0.f, A = 0.f;
-            if (M != -INFINITY)
-                for (int w = 0; w < kWarps; ++w) {
-                    const float mw = wst[w * PS + HD];
-                    if (mw == -INFINITY) continue;
-                    const float f = expf(mw - M);
-                    Ls += wst[w * PS + HD + 1] * f;
-                    A += wst[w * PS + d] * f;
-                }
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) mw[w] = wst[w * PS + HD], M = fmaxf(M, mw[w]);
+            float Ls = 0.f;
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) {
+                f[w] = (mw[w] == -INFINITY) ? 0.f : expf(mw[w] - M);
+                Ls += wst[w * PS + HD + 1] * f[w];
+            }
             float* pb = part + b * PS;
-            pb[d] = A;
-            if (d == 0) pb[HD] = M, pb[HD + 1] = Ls;
+            for (int d = tid; d < HD; d += kThreads) {
+                float A = 0.f;
+#pragma unroll
+                for (int w = 0; w < kWarps; ++w) A += wst[w * PS + d] * f[w];
+                pb[d] = A;
+            }
+            if (tid == 0) pb[HD] = M, pb[HD + 1] = Ls;
         }
         __syncthreads();
     }
@@ -843,13 +862,8 @@ __global__ void __launch_bounds__(kThreads, 2) ffn_block_kernel(const FfnBlockAr
         for (int i = tid; i < B * kFfnUnits; i += kThreads) {
             const int b = i / kFfnUnits, u = i - b * kFfnUnits;
             const int gr = (u >> 3) * 16 + (u & 7);  // gate row of unit u; its up row is gr + 8
-            float sg = 0.f, su = 0.f;
-#pragma unroll
-            for (int rr = 0; rr < kClusterCtas; ++rr) {
-                const float* pp = peer(pgu, rr) + b * R2;
-                sg += pp[gr];
-                su += pp[gr + 8];
-            }
+            const float sg = cluster_sum(pgu, b * R2 + gr);
+            const float su = cluster_sum(pgu, b * R2 + gr + 8);
             const float gate = s_sgu[gr] * s_inv[b] * sg;
             const float up = s_sgu[gr + 8] * s_inv[b] * su;
             const float v = (gate / (1.0f + expf(-gate))) * up;
@@ -912,7 +926,7 @@ __global__ void __launch_bounds__(kLmThreads, 2) lm_head_kernel(const LmHeadArgs
     unsigned long long* wbest = reinterpret_cast<unsigned long long*>(smem + L.best);
     float* s_inv = reinterpret_cast<float*>(smem + L.misc);
     float* s_red = s_inv + 4;
-    int* s_abort = reinterpret_cast<int*>(s_red + 32);
+    int* s_abort = reinterpret_cast<int*>(s_red + 32);  // s_red: [8][4] sums of squares
     int* s_last = s_abort + 1;
     uint4* xop = reinterpret_cast<uint4*>(smem + L.xop);
     const bool producer = warp == kWarps && lane == 0;

@@ -152,7 +152,11 @@ int q3i8_init(const q3i8_dims* dims, const q3i8_mat* embed, const q3i8_layer* la
  *   prompt_ids[b]  pointer to prompt_lens[b] token ids of sequence b.
  *   out_ids        [B][max_new_tokens] generated ids, row b for sequence b.
  *   out_counts     [B] number of valid ids per row: max_new_tokens, or up to
- *                  and including the first eos_id when eos_id >= 0.
+ *                  and including the first eos_id when eos_id >= 0.  With
+ *                  eos_id >= 0 decoding stops once every sequence has
+ *                  produced it (checked every 16 steps); entries of out_ids
+ *                  after a row's count are not meaningful (-1 where no step
+ *                  ran).
  *   stats          optional timings (NULL to skip).
  * Resets the KV cache, prefills every prompt, runs max_new_tokens-1 decode
  * steps (each one replay of a captured CUDA graph of the step's kernels) and
@@ -267,7 +271,9 @@ int q3i8_op_attention(const float* q, const uint16_t* k, const uint16_t* v, cons
  *
  * The first call on each device (the caller's current device) looks up the
  * scratch array's device address; make that first call before any stream
- * capture begins.  Calls that overlap in time on the same device (two
+ * capture begins.  The address is looked up again when the device's context
+ * has changed since (after cudaDeviceReset, for instance), so that call too
+ * should come before any capture.  Calls that overlap in time on the same device (two
  * streams, two threads) share the scratch and race: serialise them, e.g. on
  * one stream.  Returns Q3_ERR_INVALID_ARGUMENTS (with a message naming the
  * limit) when the sizes need more scratch than the limit. */

@@ -103,11 +103,8 @@ def test_kv_cache_slots_match_oracle_bits(pkg):
     for layer in range(w.shape.n_layers):
         k, v = dec.read_kv(layer, 0, len(prompt))
         ko, vo = s.kv(layer)
-        for a, b in ((k, ko), (v, vo)):
-            # identical fp32 inputs give identical bf16 bits; otherwise at most 1 bf16 ulp
-            d = np.abs(a.astype(np.int32) - b.astype(np.int32))
-            assert d.max() <= 1, f"layer {layer}: bf16 bits differ by {d.max()}"
-            assert (d == 0).mean() > 0.97
+        _kv_bits_close(k, ko, f"layer {layer} K")
+        _kv_bits_close(v, vo, f"layer {layer} V")
     dec.close()
 
 
@@ -117,7 +114,8 @@ def test_0p6b_b1_full(pkg):
 
 
 def test_0p6b_b8_ragged(pkg):
-    _teacher_forced_check(pkg, "0.6b-b8-p16to256-n128", steps=24)
+    # every sequence of the batch over all 128 steps
+    _teacher_forced_check(pkg, "0.6b-b8-p16to256-n128")
 
 
 def test_0p6b_b1_persistent_kernel(pkg, monkeypatch):
@@ -192,4 +190,159 @@ def test_eos_counts_and_errors(pkg):
     with pytest.raises(pkg.Q3Error) as e:
         dec.step_logits(np.array([1], np.int32))
     assert e.value.status == "invalid_state"
+    dec.close()
+
+
+KV_ROW_REL = 1e-4  # fp32 error allowance of a cache element, as a fraction of its row's RMS
+
+
+def _bf16_to_f32(bits):
+    return (bits.astype(np.uint32) << 16).view(np.float32)
+
+
+def _kv_bits_close(a, b, where, min_exact=0.97, spacings=1, row_rel=KV_ROW_REL):  # noqa: D401
+    """a, b: bf16 bit patterns [n_kv, n_pos, hd] (GPU, oracle).  Every slot is
+    within one bf16 spacing (the larger of the two values' spacings, so a pair
+    on either side of a power of two counts as neighbours) or, for an element
+    much smaller than its row (a dot product that cancels), within the fp32
+    error of the row: 1e-4 of the row's RMS.  Where the fp32 inputs agree to
+    rounding (the first layer) at least 97 % of the slots are bit-exact;
+    deeper layers inherit the fp32 differences of the residual stream (about
+    1e-4 relative after one layer, growing with depth), so their slots are
+    checked within two bf16 spacings or 1e-3 of the row's RMS, with no share
+    of exact slots required."""
+    fa, fb = _bf16_to_f32(a).astype(np.float64), _bf16_to_f32(b).astype(np.float64)
+    spacing = lambda f: np.ldexp(1.0, np.frexp(np.abs(f))[1] - 8)  # bf16 spacing at |f|
+    rms = np.sqrt(np.mean(fb * fb, axis=-1, keepdims=True))
+    allowed = np.maximum(spacings * np.maximum(spacing(fa), spacing(fb)), row_rel * rms)
+    d = np.abs(fa - fb)
+    assert np.all(d <= allowed), f"{where}: a slot differs by {float((d / allowed).max()):.2f}x its allowance"
+    exact = (a == b).mean()
+    assert exact >= min_exact, f"{where}: only {exact:.3f} of the slots are bit-exact"
+
+
+def test_kv_slots_after_decode_steps_hd128(pkg):
+    # the decode step appends K and V itself (head_dim 128): read the cache
+    # back after 8 steps and compare every slot with the oracle's bits
+    w = synth.WORKLOADS["0.6b-b1-p32-n128"]
+    m, orc = model_for(w.name)
+    prompt = synth.prompts(w)[0]
+    dec = pkg.Decoder(m, max_batch=1, max_ctx=w.max_ctx)
+    ids, _, _ = dec.decode([prompt], 9)
+    n = len(prompt) + 8  # the 9th token is generated but not yet appended
+    s = orc.seq(n)
+    s.forward(np.concatenate([prompt, ids[0, :8]]))
+    for layer in (0, 1, 13, w.shape.n_layers - 1):
+        k, v = dec.read_kv(layer, 0, n)
+        ko, vo = s.kv(layer)
+        if layer == 0:
+            _kv_bits_close(k[:, len(prompt):], ko[:, len(prompt):], "layer 0 K (decode steps)")
+            _kv_bits_close(v[:, len(prompt):], vo[:, len(prompt):], "layer 0 V (decode steps)")
+            _kv_bits_close(k, ko, "layer 0 K")
+            _kv_bits_close(v, vo, "layer 0 V")
+        else:
+            # deeper layers inherit the residual stream's fp32 differences, which
+            # this random-weight network amplifies with depth; every slot must
+            # still hold its own vector: each (head, position) row within 2 % of
+            # the oracle's row (a wrong position, head or layer is off by O(1))
+            for name, a, b in (("K", k, ko), ("V", v, vo)):
+                fa, fb = _bf16_to_f32(a).astype(np.float64), _bf16_to_f32(b).astype(np.float64)
+                rel = np.linalg.norm(fa - fb, axis=-1) / np.linalg.norm(fb, axis=-1)
+                assert rel.max() < 2e-2, f"layer {layer} {name}: a row is {rel.max():.3g} away from the oracle's"
+    dec.close()
+
+
+def _tied_rows_model(base, top, bottom):
+    """Every embedding row gets the same int8 row (row 17 of base); rows in
+    `top` get twice the common scale and rows in `bottom` half of it.  Logits
+    are then s_r * c for one c, so rows of a group tie bit for bit."""
+    import copy
+
+    m = copy.deepcopy(base)
+    V = m.shape.vocab
+    q0 = base.embed.q[17].copy()
+    s0 = np.float32(base.embed.s[17])
+    m.embed.q = np.ascontiguousarray(np.tile(q0, (V, 1)))
+    sc = np.full(V, s0, np.float32)
+    sc[list(top)] = np.float32(2) * s0
+    sc[list(bottom)] = np.float32(0.5) * s0
+    m.embed.s = sc
+    return m
+
+
+def test_argmax_ties_pick_the_lowest_index(pkg):
+    # ties at row 0, at the last valid row and between rows of different CTAs
+    # of the lm_head sweep; the lowest index must win on the device as in the
+    # oracle, in the prefill's and in the decode step's argmax
+    w = synth.WORKLOADS["tiny-b1-p8-n16"]
+    base, _ = model_for(w.name)
+    V = w.shape.vocab
+    prompt = synth.prompts(w)[0]
+    for top, bottom in (([0, 1000, 3000], [7, 2500]), ([V - 1], [V - 2, 3]), ([5, 2048, V - 1], [1, V - 1 - 16])):
+        m = _tied_rows_model(base, top, bottom)
+        orc = oracle.Oracle(m)
+        dec = pkg.Decoder(m, max_batch=1, max_ctx=64)
+        ids, _, _ = dec.decode([prompt], 6)
+        z = orc.teacher_forced(np.concatenate([prompt, ids[0, :-1]]), len(prompt) - 1)
+        for i in range(6):
+            best = np.flatnonzero(z[i] == z[i].max())
+            assert len(best) >= min(len(top), len(bottom)), f"no tie at step {i}"
+            assert int(ids[0, i]) == int(best[0]), f"step {i}: gpu {int(ids[0, i])}, lowest tied index {int(best[0])}"
+        dec.close()
+
+
+def test_eos_stops_the_decode(pkg):
+    w = synth.WORKLOADS["tiny-b1-p8-n16"]
+    m, _ = model_for(w.name)
+    p = synth.prompts(w)
+    dec = pkg.Decoder(m, max_batch=1, max_ctx=512)
+    ids, _, _ = dec.decode(p, 200)
+    eos = int(ids[0, 3])
+    first = int(np.argmax(ids[0] == eos))
+    ids2, counts, stats = dec.decode(p, 200, eos_id=eos)
+    assert counts[0] == first + 1
+    assert np.array_equal(ids2[0, :first + 1], ids[0, :first + 1])
+    # the work stops within one check interval (16 steps) after the eos
+    assert stats["decode_steps"] <= first + 16, stats
+    assert np.all(ids2[0, stats["decode_steps"] + 1:] == -1)
+    dec.close()
+
+
+def test_device_ids_outside_the_vocabulary_are_rejected(pkg):
+    import torch
+
+    w = synth.WORKLOADS["tiny-b1-p8-n16"]
+    m, _ = model_for(w.name)
+    p = synth.prompts(w)[0]
+    dec = pkg.Decoder(m, max_batch=1, max_ctx=64)
+    dev = torch.device("cuda")
+    out = torch.zeros((1, 4), dtype=torch.int32, device=dev)
+    for bad in (w.shape.vocab, -1):
+        ids = torch.from_numpy(np.concatenate([p[:3], [bad], p[4:]]).astype(np.int32)).to(dev)
+        with pytest.raises(pkg.Q3Error) as e:
+            dec.decode_device(ids, np.array([len(p)], np.int32), 4, out)
+        assert e.value.status == "invalid_arguments"
+    # the context is still usable
+    good = torch.from_numpy(p.astype(np.int32)).to(dev)
+    dec.decode_device(good, np.array([len(p)], np.int32), 4, out)
+    ref, _, _ = dec.decode([p], 4)
+    assert np.array_equal(out.cpu().numpy(), ref)
+    dec.close()
+
+
+@pytest.mark.parametrize("name,B", [("0.6b-b1-p32-n128", 1), ("0.6b-b8-p16to256-n128", 4),
+                                    ("0.6b-b32-p16to256-n128", 32)])
+def test_decode_is_deterministic_run_to_run(pkg, name, B):
+    # the residual sums of split projections are ordered (fixed point or the
+    # tile's last CTA), so two runs give the same bits
+    w = synth.WORKLOADS[name]
+    m = synth.make_model(w.shape, w.weight_seed)
+    p = synth.prompts(w, B)
+    dec = pkg.Decoder(m, max_batch=B, max_ctx=w.max_ctx)
+    a, _, _ = dec.decode(p, 24)
+    b, _, _ = dec.decode(p, 24)
+    assert np.array_equal(a, b)
+    za = dec.prefill(p)
+    zb = dec.prefill(p)
+    assert np.array_equal(za, zb)
     dec.close()

@@ -1,9 +1,12 @@
 """q3i8_op_attention_static (attention with library-owned scratch, no
-allocation) against q3i8_op_attention with a caller workspace, through the
-C ABI.  Kept in its own file, collected last, so that it also runs after
-every other GPU test in the same process; it passes alone as well."""
+allocation) against q3i8_op_attention with a caller workspace and against the
+CPU oracle's attention, through the C ABI.  Kept in its own file, collected
+last, so that it also runs after every other GPU test in the same process; it
+passes alone as well."""
 import numpy as np
 import pytest
+
+import oracle
 
 pytestmark = pytest.mark.gpu
 
@@ -54,14 +57,47 @@ def _both(pkg, case, nkv, splits):
     return got.cpu().numpy(), ref.cpu().numpy()
 
 
-def test_static_scratch_matches_workspace_twice_in_a_row(pkg):
-    # two calls back to back with different sizes and inputs: the second must
-    # not see anything the first left in the scratch
-    for lens, nh, nkv, hd, splits, seed in [([700, 129, 64, 1], 16, 8, 128, 8, 11),
-                                           ([65, 300], 8, 2, 64, 3, 12)]:
-        got, ref = _both(pkg, _case(lens, nh, nkv, hd, seed), nkv, splits)
+def _vs_oracle(case, lens, got):
+    q, k, v, _, _ = case
+    qh = q.cpu().numpy()
+    kh = k.cpu().numpy().view(np.uint16)
+    vh = v.cpu().numpy().view(np.uint16)
+    for r, L in enumerate(lens):
+        np.testing.assert_allclose(got[r], oracle.attention(qh[r], kh[r], vh[r], L), rtol=RTOL, atol=ATOL)
+
+
+# (lens, n_heads, n_kv_heads, head_dim, splits, seed)
+CASES = [
+    ([700, 129, 64, 1], 16, 8, 128, 8, 11),
+    ([65, 300], 8, 2, 64, 3, 12),
+    ([5, 64, 65, 200], 8, 8, 64, 4, 13),   # GQA group 1 (one query head per kv head)
+    ([1, 33, 500], 16, 8, 128, 1, 14),     # one split: the merge takes a single state
+]
+
+
+def test_static_scratch_matches_workspace_and_oracle_twice_in_a_row(pkg):
+    # calls back to back with different sizes and inputs: a call must not see
+    # anything the one before left in the scratch
+    for lens, nh, nkv, hd, splits, seed in CASES:
+        case = _case(lens, nh, nkv, hd, seed)
+        got, ref = _both(pkg, case, nkv, splits)
         assert np.isfinite(got).all()
         np.testing.assert_allclose(got, ref, rtol=RTOL, atol=ATOL)
+        _vs_oracle(case, lens, got)
+
+
+def test_static_scratch_at_its_limit(pkg):
+    # 32 rows x 16 heads x 15 splits of 130 floats: 3,993,600 bytes of the
+    # 4 MiB scratch; contexts long enough that every split has positions
+    R, nh, nkv, hd, splits = 32, 16, 8, 128, 15
+    need = pkg.op_attention_workspace(R, nh, hd, splits)
+    assert pkg.OP_ATTENTION_STATIC_SCRATCH_BYTES - 266240 < need <= pkg.OP_ATTENTION_STATIC_SCRATCH_BYTES
+    lens = [960 - 7 * r for r in range(R)]
+    for seed in (21, 22):
+        case = _case(lens, nh, nkv, hd, seed)
+        got, ref = _both(pkg, case, nkv, splits)
+        np.testing.assert_allclose(got, ref, rtol=RTOL, atol=ATOL)
+        _vs_oracle(case, lens, got)
 
 
 def test_static_scratch_rejects_sizes_beyond_limit(pkg):
