@@ -17,7 +17,10 @@ conventional reading, written out in float64 on plain numpy arrays:
 * temperature T > 0: z / T.  T = 0 is the default greedy call: the argmax
   of the raw logits (lowest index on ties), with no step of the chain;
 * candidates in the order (z descending, token ascending); top-k keeps the
-  first k of them (k = 0: all);
+  first k of them (k = 0: all).  The order is taken on the penalised logits,
+  before the division by T: for T > 0 it is the order of z / T, and taking
+  it first keeps a float64 rounding of the quotient from merging two
+  distinct values into a tie;
 * min-p keeps candidates whose softmax probability over the current
   candidates is at least min_p times the largest;
 * top-p keeps the shortest prefix whose softmax probabilities over the
@@ -90,8 +93,9 @@ def candidates(z: np.ndarray, history, p: Params):
     min-p and top-p, in draw order, with their renormalised probabilities.
     Only for temperature > 0."""
     assert p.temperature > 0
-    v = apply_penalties(z, history, p) / p.temperature
-    order = np.lexsort((np.arange(v.size), -v))  # z descending, token ascending
+    pen = apply_penalties(z, history, p)
+    order = np.lexsort((np.arange(pen.size), -pen))  # z descending, token ascending
+    v = pen / p.temperature
     if 0 < p.top_k < v.size:
         order = order[:p.top_k]
     if p.min_p > 0:

@@ -84,6 +84,16 @@ def test_top_k_with_ties():
     assert len(S.intervals(z, [], S.Params(temperature=1.0, top_k=0))) == 4
 
 
+def test_candidate_order_is_taken_before_the_temperature():
+    # two adjacent float64 logits whose quotients by T = 1.5 round to the
+    # same value: the order stays the logits' own (the larger first), so
+    # top_k = 1 keeps token 1, not the lower index of a tie the division made
+    z = np.array([1.9563777446746826, np.nextafter(1.9563777446746826, 3.0)])
+    assert z[0] < z[1] and z[0] / 1.5 == z[1] / 1.5
+    assert list(S.intervals(z, [], S.Params(temperature=1.5, top_k=1))) == [1]
+    assert list(S.intervals(z, [], S.Params(temperature=1.5))) == [1, 0]
+
+
 def _planted(probs):
     return np.log(np.asarray(probs, np.float64))
 
