@@ -35,10 +35,11 @@ LIB_PATH = os.environ.get("Q3I8_LIB") or os.path.join(_HERE, "_build", "libq3i8.
 STATUS = {0: "ok", 1: "unsupported_architecture", 2: "invalid_arguments", 3: "context_past_ceiling",
           4: "no_device", 5: "out_of_memory", 6: "cuda_error", 7: "device_wait_timeout", 8: "invalid_state"}
 
-EXPORTS = ["q3i8_validate_dims", "q3i8_init", "q3i8_decode", "q3i8_decode_device", "q3i8_prefill",
+EXPORTS = ["q3i8_validate_dims", "q3i8_init", "q3i8_decode", "q3i8_decode_sample", "q3i8_decode_device", "q3i8_prefill",
            "q3i8_step_logits", "q3i8_read_kv", "q3i8_step_bytes", "q3i8_step_launches", "q3i8_launch_count", "q3i8_last_error",
            "q3i8_status_name", "q3i8_destroy", "q3i8_trace_step", "q3i8_op_gemm_i8", "q3i8_op_attention_workspace", "q3i8_op_attention",
-           "q3i8_op_attention_static", "q3i8_op_wait_probe", "q3i8_cache_payload_bytes", "q3i8_cache_write",
+           "q3i8_op_attention_static", "q3i8_op_sample_workspace", "q3i8_op_sample", "q3i8_op_wait_probe",
+           "q3i8_cache_payload_bytes", "q3i8_cache_write",
            "q3i8_cache_open", "q3i8_cache_tables", "q3i8_cache_close", "q3i8_sched_new", "q3i8_sched_destroy",
            "q3i8_sched_submit", "q3i8_sched_plan", "q3i8_sched_complete_prefill", "q3i8_sched_complete_step",
            "q3i8_sched_idle", "q3i8_sched_result"]
@@ -79,6 +80,20 @@ class Stats(ctypes.Structure):
         return {f: getattr(self, f) for f, _ in self._fields_}
 
 
+class Sampling(ctypes.Structure):
+    """Settings of the device sampling chain (q3i8_sampling)."""
+    _fields_ = [(n, ctypes.c_double) for n in ("temperature", "top_p", "min_p", "repeat_penalty",
+                                               "presence_penalty", "frequency_penalty")] + \
+               [("top_k", ctypes.c_int32), ("reserved", ctypes.c_int32), ("seed", ctypes.c_uint64)]
+
+
+def sampling(temperature: float, top_k: int, top_p: float = 1.0, min_p: float = 0.0, repeat_penalty: float = 1.0,
+             presence_penalty: float = 0.0, frequency_penalty: float = 0.0, seed: int = 0) -> Sampling:
+    return Sampling(temperature=temperature, top_p=top_p, min_p=min_p, repeat_penalty=repeat_penalty,
+                    presence_penalty=presence_penalty, frequency_penalty=frequency_penalty, top_k=top_k, reserved=0,
+                    seed=seed & ((1 << 64) - 1))
+
+
 _lib = None
 _lock = threading.Lock()
 
@@ -97,6 +112,11 @@ def lib():
             L.q3i8_init.argtypes = [ctypes.POINTER(Dims), ctypes.POINTER(Mat), ctypes.POINTER(Layer), vp, vp,
                                     ctypes.POINTER(vp)]
             L.q3i8_decode.argtypes = [vp, i32, ctypes.POINTER(vp), vp, i32, i32, vp, vp, ctypes.POINTER(Stats)]
+            L.q3i8_decode_sample.argtypes = [vp, i32, ctypes.POINTER(vp), vp, i32, i32, ctypes.POINTER(Sampling),
+                                             vp, vp, ctypes.POINTER(Stats)]
+            L.q3i8_op_sample_workspace.restype = sz
+            L.q3i8_op_sample_workspace.argtypes = [i32, i32]
+            L.q3i8_op_sample.argtypes = [vp, i32, i32, vp, ctypes.POINTER(Sampling), i32, vp, vp, sz, vp, vp]
             L.q3i8_decode_device.argtypes = [vp, i32, vp, vp, i32, vp, ctypes.POINTER(Stats)]
             L.q3i8_prefill.argtypes = [vp, i32, ctypes.POINTER(vp), vp, vp]
             L.q3i8_step_logits.argtypes = [vp, vp, vp]
@@ -238,6 +258,18 @@ class Decoder:
         _check(rc, self._h)
         return out, counts, st.as_dict()
 
+    def decode_sample(self, prompts, max_new_tokens: int, settings: Sampling, eos_id: int = -1):
+        """Sampled decode (host buffers; see q3i8_decode_sample).  Returns (ids, counts, stats dict)."""
+        arrs, ptrs, lens = self._prompts(prompts)
+        B = len(arrs)
+        out = np.zeros((B, max_new_tokens), np.int32)
+        counts = np.zeros(B, np.int32)
+        st = Stats()
+        rc = lib().q3i8_decode_sample(self._h, B, ptrs, _p(lens), max_new_tokens, eos_id, ctypes.byref(settings),
+                                      _p(out), _p(counts), ctypes.byref(st))
+        _check(rc, self._h)
+        return out, counts, st.as_dict()
+
     def decode_device(self, d_ids, lens, max_new_tokens: int, d_out):
         """Greedy decode on device buffers (torch int32 CUDA tensors).  Returns stats."""
         lens = np.ascontiguousarray(lens, np.int32)
@@ -313,6 +345,20 @@ def op_attention(q, k, v, row_seq, row_len, n_kv_heads: int, splits: int, out, w
                                  hd, cap, splits, _tptr(out), _tptr(workspace),
                                  workspace.numel() * workspace.element_size(), _tptr(status),
                                  ctypes.c_void_p(stream) if stream else None)
+    _check(rc, None)
+
+
+def op_sample_workspace(B: int, V: int) -> int:
+    return int(lib().q3i8_op_sample_workspace(B, V))
+
+
+def op_sample(logits, counts, settings: Sampling, step: int, tokens, workspace, status=None, stream=None):
+    """The sampling chain on one step's logits (see q3i8_op_sample): logits [B, V] fp32, counts [B, V] int32
+    (updated), tokens [B] int32, workspace uint8 of op_sample_workspace(B, V) bytes; torch CUDA tensors."""
+    B, V = logits.shape
+    rc = lib().q3i8_op_sample(_tptr(logits), B, V, _tptr(counts), ctypes.byref(settings), step, _tptr(tokens),
+                              _tptr(workspace), workspace.numel() * workspace.element_size(), _tptr(status),
+                              ctypes.c_void_p(stream) if stream else None)
     _check(rc, None)
 
 

@@ -423,7 +423,7 @@ extern "C" void q3i8_destroy(q3i8_ctx* c) {
                     c->out_ids, c->pf_x, c->pf_qkv, c->pf_q, c->pf_xh, c->pf_oh, c->pf_ah, c->pf_blocks,
                     c->pf_part, c->pf_ids, c->pf_seq, c->pf_pos, c->pf_last, c->d_mats, c->d_gains,
                     c->p_epoch, c->p_keys, c->p_exit, c->p_attn_cnt, c->p_abort, c->p_diag, c->p_ll, c->p_part, c->p_trace,
-                    c->xa, c->xf};
+                    c->xa, c->xf, c->s_params, c->s_counts, c->s_band_key, c->s_band_tok};
     for (void* p : ptrs) cudaFree(p);
     if (c->ev0) cudaEventDestroy(c->ev0);
     if (c->ev1) cudaEventDestroy(c->ev1);
@@ -721,7 +721,17 @@ static bool fused_for(const q3i8_ctx* c, int B) {
     return c->use_step && B <= c->step_max_batch && c->call_ctx <= c->step_max_ctx;
 }
 
+static int enqueue_sample(q3i8_ctx* c, int B, const int32_t* step_ptr, int step_value);
+
 static int enqueue_decode_step(q3i8_ctx* c, int B, bool want_logits) {
+    if (c->sampling) {
+        // the step writes the logits, then the chain draws the token (it
+        // overwrites the argmax the lm_head left in tokens[] / out_ids)
+        c->sampling = false;
+        const int rc = enqueue_decode_step(c, B, true);
+        c->sampling = true;
+        return rc ? rc : enqueue_sample(c, B, c->step, 0);
+    }
     if (persistent_for(c, B)) {
         cudaError_t e = enqueue_persistent(c, B, want_logits ? c->logits : nullptr);
         if (e != cudaSuccess) return fail(c, Q3_ERR_CUDA, "persistent step launch: %s", cudaGetErrorString(e));
@@ -752,7 +762,8 @@ int prefill_launches(const q3i8_ctx* c, int M) {
 
 // Graph of one decode step at batch B (captured on first use).
 static int get_graph(q3i8_ctx* c, int B, cudaGraphExec_t* out) {
-    const int key = 2 * B + (fused_for(c, B) ? 1 : 0);  // one graph per batch size and step kind
+    // one graph per batch size, step kind and token choice (argmax or sampled)
+    const int key = 4 * B + (c->sampling ? 2 : 0) + (fused_for(c, B) ? 1 : 0);
     auto it = c->graphs.find(key);
     if (it != c->graphs.end()) {
         *out = it->second;
@@ -773,6 +784,57 @@ static int get_graph(q3i8_ctx* c, int B, cudaGraphExec_t* out) {
     if (e != cudaSuccess) return fail(c, Q3_ERR_CUDA, "graph instantiate failed: %s", cudaGetErrorString(e));
     c->graphs[key] = ex;
     *out = ex;
+    return Q3_OK;
+}
+
+// ------------------------------------------------------------------ sampling
+
+// Host check of the sampling settings; *greedy is set for temperature 0.
+static int validate_sampling(q3i8_ctx* c, const q3i8_sampling* s, bool* greedy) {
+    if (!s) return fail(c, Q3_ERR_INVALID_ARGUMENTS, "sampling settings are NULL");
+    const double vals[] = {s->temperature, s->top_p, s->min_p, s->repeat_penalty, s->presence_penalty,
+                           s->frequency_penalty};
+    for (double v : vals)
+        if (!std::isfinite(v)) return fail(c, Q3_ERR_INVALID_ARGUMENTS, "sampling: a setting is not finite");
+    if (s->temperature < 0) return fail(c, Q3_ERR_INVALID_ARGUMENTS, "sampling: temperature < 0");
+    *greedy = s->temperature == 0.0;
+    if (*greedy) return Q3_OK;
+    if (s->top_k < 1 || s->top_k > kSampleMaxTopK)
+        return fail(c, Q3_ERR_INVALID_ARGUMENTS, "sampling: top_k %d outside [1, %d]", s->top_k, kSampleMaxTopK);
+    if (!(s->top_p > 0 && s->top_p <= 1)) return fail(c, Q3_ERR_INVALID_ARGUMENTS, "sampling: top_p outside (0, 1]");
+    if (!(s->min_p >= 0 && s->min_p <= 1)) return fail(c, Q3_ERR_INVALID_ARGUMENTS, "sampling: min_p outside [0, 1]");
+    if (!(s->repeat_penalty > 0)) return fail(c, Q3_ERR_INVALID_ARGUMENTS, "sampling: repeat_penalty <= 0");
+    return Q3_OK;
+}
+
+static SampleParams device_params(const q3i8_sampling& s) {
+    SampleParams p{};
+    p.temperature = s.temperature, p.top_p = s.top_p, p.min_p = s.min_p, p.repeat_penalty = s.repeat_penalty;
+    p.presence_penalty = s.presence_penalty, p.frequency_penalty = s.frequency_penalty;
+    p.top_k = s.top_k, p.seed = s.seed;
+    return p;
+}
+
+// Buffers of the sampling chain for max_batch sequences (first use only).
+static int ensure_sampling(q3i8_ctx* c) {
+    if (c->s_params) return Q3_OK;
+    const size_t V = c->d.vocab, E = sample_band_entries(c->d.vocab);
+    CK(c, cudaMalloc(&c->s_counts, (size_t)c->bmax * V * 4));
+    CK(c, cudaMalloc(&c->s_band_key, (size_t)c->bmax * E * 8));
+    CK(c, cudaMalloc(&c->s_band_tok, (size_t)c->bmax * E * 4));
+    CK(c, cudaMalloc(&c->s_params, sizeof(SampleParams)));
+    return Q3_OK;
+}
+
+// The chain over c->logits for B sequences: the draw is for generated token
+// *step_ptr - 1 (or step_value when step_ptr is NULL).
+static int enqueue_sample(q3i8_ctx* c, int B, const int32_t* step_ptr, int step_value) {
+    SampleArgs a{};
+    a.logits = c->logits, a.ldz = c->d.vocab, a.V = c->d.vocab, a.counts = c->s_counts, a.params = c->s_params;
+    a.step = step_ptr, a.step_value = step_value, a.tokens = c->tokens, a.out_ids = c->out_ids, a.out_cap = c->out_cap;
+    a.band_key = c->s_band_key, a.band_tok = c->s_band_tok, a.status = c->status;
+    cudaError_t e = launch_sample(a, B, c->stream);
+    if (e != cudaSuccess) return fail(c, Q3_ERR_CUDA, "sampling launch: %s", cudaGetErrorString(e));
     return Q3_OK;
 }
 
@@ -881,6 +943,8 @@ static int check_status(q3i8_ctx* c) {
         }
         step_reset(c);
         cudaStreamSynchronize(c->stream);
+        if (st == kStatusSampleSelect)
+            return fail(c, Q3_ERR_CUDA, "sampling: the top-k selection did not add up (internal error)");
         if (st == kStatusBadToken)
             return fail(c, Q3_ERR_INVALID_ARGUMENTS, "a token id outside [0, %d) reached the device", c->d.vocab);
         return fail(c, Q3_ERR_TIMEOUT,
@@ -929,8 +993,17 @@ static int decode_core(q3i8_ctx* c, int B, const int32_t* d_ids, const int32_t* 
     if (rc) return rc;
     c->call_ctx = need;
     CK(c, cudaEventRecord(c->ev0, c->stream));
-    rc = run_prefill(c, B, d_ids, lens, nullptr);
+    rc = run_prefill(c, B, d_ids, lens, c->sampling ? c->logits : nullptr);
     if (rc) return rc;
+    if (c->sampling) {
+        // count the prompt tokens of each sequence, then draw token 0
+        int M = 0;
+        for (int b = 0; b < B; ++b) M += lens[b];
+        CK(c, cudaMemsetAsync(c->s_counts, 0, (size_t)B * c->d.vocab * 4, c->stream));
+        CK(c, launch_count_tokens(d_ids, c->pf_seq, M, c->s_counts, c->d.vocab, c->stream));
+        if ((rc = enqueue_sample(c, B, c->step, 0))) return rc;
+        c->launches += 2;
+    }
     CK(c, cudaEventRecord(c->ev1, c->stream));
     int steps = 0;
     if (max_new > 1) {
@@ -961,7 +1034,7 @@ static int decode_core(q3i8_ctx* c, int B, const int32_t* d_ids, const int32_t* 
                 steps += n;
             }
         }
-        c->launches += (int64_t)steps * step_launches(c, B);
+        c->launches += (int64_t)steps * (step_launches(c, B) + (c->sampling ? 1 : 0));
     }
     CK(c, cudaEventRecord(c->ev2, c->stream));
     rc = check_status(c);
@@ -1001,10 +1074,10 @@ extern "C" int q3i8_decode_device(q3i8_ctx* c, int32_t B, const int32_t* d_promp
     return Q3_OK;
 }
 
-extern "C" int q3i8_decode(q3i8_ctx* c, int32_t B, const int32_t* const* prompt_ids, const int32_t* prompt_lens,
-                           int32_t max_new_tokens, int32_t eos_id, int32_t* out_ids, int32_t* out_counts,
-                           q3i8_stats* stats) {
-    if (!c) return fail(nullptr, Q3_ERR_INVALID_ARGUMENTS, "ctx is NULL");
+// Decode with host buffers (q3i8_decode, q3i8_decode_sample).
+static int decode_host(q3i8_ctx* c, int32_t B, const int32_t* const* prompt_ids, const int32_t* prompt_lens,
+                       int32_t max_new_tokens, int32_t eos_id, int32_t* out_ids, int32_t* out_counts,
+                       q3i8_stats* stats) {
     int need = 0;
     int rc = validate_prompts(c, B, prompt_lens, max_new_tokens, &need);
     if (rc) return rc;
@@ -1042,6 +1115,32 @@ extern "C" int q3i8_decode(q3i8_ctx* c, int32_t B, const int32_t* const* prompt_
         if (out_counts) out_counts[b] = n;
     }
     return Q3_OK;
+}
+
+extern "C" int q3i8_decode(q3i8_ctx* c, int32_t B, const int32_t* const* prompt_ids, const int32_t* prompt_lens,
+                           int32_t max_new_tokens, int32_t eos_id, int32_t* out_ids, int32_t* out_counts,
+                           q3i8_stats* stats) {
+    if (!c) return fail(nullptr, Q3_ERR_INVALID_ARGUMENTS, "ctx is NULL");
+    return decode_host(c, B, prompt_ids, prompt_lens, max_new_tokens, eos_id, out_ids, out_counts, stats);
+}
+
+extern "C" int q3i8_decode_sample(q3i8_ctx* c, int32_t B, const int32_t* const* prompt_ids,
+                                  const int32_t* prompt_lens, int32_t max_new_tokens, int32_t eos_id,
+                                  const q3i8_sampling* sampling, int32_t* out_ids, int32_t* out_counts,
+                                  q3i8_stats* stats) {
+    if (!c) return fail(nullptr, Q3_ERR_INVALID_ARGUMENTS, "ctx is NULL");
+    bool greedy = false;
+    int rc = validate_sampling(c, sampling, &greedy);
+    if (rc) return rc;
+    if (greedy) return decode_host(c, B, prompt_ids, prompt_lens, max_new_tokens, eos_id, out_ids, out_counts, stats);
+    if ((rc = ensure_sampling(c))) return rc;
+    const SampleParams p = device_params(*sampling);
+    CK(c, cudaMemcpyAsync(c->s_params, &p, sizeof p, cudaMemcpyHostToDevice, c->stream));
+    CK(c, cudaStreamSynchronize(c->stream));  // p is a host temporary
+    c->sampling = true;
+    rc = decode_host(c, B, prompt_ids, prompt_lens, max_new_tokens, eos_id, out_ids, out_counts, stats);
+    c->sampling = false;
+    return rc;
 }
 
 extern "C" int q3i8_prefill(q3i8_ctx* c, int32_t B, const int32_t* const* prompt_ids, const int32_t* prompt_lens,
@@ -1195,6 +1294,45 @@ extern "C" int q3i8_op_gemm_i8(const uint16_t* a_planes, const int8_t* w, const 
 extern "C" size_t q3i8_op_attention_workspace(int32_t R, int32_t n_heads, int32_t hd, int32_t splits) {
     if (R <= 0 || n_heads <= 0 || hd <= 0 || splits <= 0) return 0;
     return attn_part_bytes(R, n_heads, hd, splits);
+}
+
+// Workspace of q3i8_op_sample: the settings, then the selection scratch.
+static size_t op_sample_ws(int32_t B, int32_t V) {
+    const size_t E = sample_band_entries(V);
+    return 256 + (size_t)B * E * 8 + (size_t)B * E * 4;
+}
+
+extern "C" size_t q3i8_op_sample_workspace(int32_t B, int32_t V) {
+    return (B < 1 || V < 1) ? 0 : op_sample_ws(B, V);
+}
+
+extern "C" int q3i8_op_sample(const float* logits, int32_t B, int32_t V, int32_t* counts,
+                              const q3i8_sampling* sampling, int32_t step, int32_t* tokens, void* workspace,
+                              size_t ws_bytes, int32_t* d_status, void* cuda_stream) {
+    if (!logits || !counts || !tokens || !workspace || !sampling)
+        return fail(nullptr, Q3_ERR_INVALID_ARGUMENTS, "op_sample: NULL pointer");
+    if (B < 1 || B > (1 << 20) || V < 1 || V > (1 << 28) || step < 0)
+        return fail(nullptr, Q3_ERR_INVALID_ARGUMENTS, "op_sample: unsupported sizes");
+    bool greedy = false;
+    if (validate_sampling(nullptr, sampling, &greedy)) return Q3_ERR_INVALID_ARGUMENTS;
+    if (greedy) return fail(nullptr, Q3_ERR_INVALID_ARGUMENTS, "op_sample: temperature must be > 0");
+    if (ws_bytes < op_sample_ws(B, V) || ((uintptr_t)workspace & 15))
+        return fail(nullptr, Q3_ERR_INVALID_ARGUMENTS, "op_sample: workspace too small or misaligned");
+    cudaStream_t st = (cudaStream_t)cuda_stream;
+    const SampleParams p = device_params(*sampling);
+    unsigned char* ws = (unsigned char*)workspace;
+    cudaError_t e = cudaMemcpyAsync(ws, &p, sizeof p, cudaMemcpyHostToDevice, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);  // p is a host temporary
+    if (e != cudaSuccess) return fail(nullptr, Q3_ERR_CUDA, "op_sample: settings copy: %s", cudaGetErrorString(e));
+    const size_t E = sample_band_entries(V);
+    SampleArgs a{};
+    a.logits = logits, a.ldz = V, a.V = V, a.counts = counts, a.params = (const SampleParams*)ws;
+    a.step = nullptr, a.step_value = step, a.tokens = tokens, a.out_ids = nullptr, a.out_cap = 0;
+    a.band_key = (uint64_t*)(ws + 256), a.band_tok = (int32_t*)(ws + 256 + (size_t)B * E * 8);
+    a.status = d_status;
+    e = launch_sample(a, B, st);
+    if (e != cudaSuccess) return fail(nullptr, Q3_ERR_CUDA, "op_sample launch: %s", cudaGetErrorString(e));
+    return Q3_OK;
 }
 
 extern "C" int q3i8_op_attention(const float* q, const uint16_t* k, const uint16_t* v, const int32_t* row_seq,

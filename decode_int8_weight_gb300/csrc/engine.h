@@ -10,6 +10,7 @@
 
 #include "../../include/q3i8.h"
 #include "step.h"
+#include "sample.h"
 
 namespace q3 {
 constexpr int kMaxBatch = 32;      // GEMV activation operand: 4 sequences per 8-column MMA tile, 8 tiles
@@ -91,6 +92,13 @@ struct q3i8_ctx {
     int call_ctx = 0;        // longest context the current call can reach
     q3::StepPlan splan;
     long long *xa = nullptr, *xf = nullptr;  // residual stream accumulators [2][bmax][H], value * 2^32
+
+    // seeded sampling (sample.cu), allocated by the first sampling call
+    bool sampling = false;                 // the running call samples instead of taking the argmax
+    q3::SampleParams* s_params = nullptr;  // device copy of the call's settings
+    int32_t* s_counts = nullptr;           // [bmax][vocab] occurrences of each token per sequence
+    uint64_t* s_band_key = nullptr;        // [bmax][sample_band_entries(vocab)] selection scratch
+    int32_t* s_band_tok = nullptr;
 
     std::map<int, cudaGraphExec_t> graphs;  // decode step graph per batch size
     cudaEvent_t ev0 = nullptr, ev1 = nullptr, ev2 = nullptr;

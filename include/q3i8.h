@@ -167,6 +167,50 @@ int q3i8_decode(q3i8_ctx* ctx, int32_t B, const int32_t* const* prompt_ids, cons
                 int32_t max_new_tokens, int32_t eos_id, int32_t* out_ids, int32_t* out_counts,
                 q3i8_stats* stats);
 
+/* Settings of the sampling chain ("Model-agnostic LLM inference", section
+ * "Sampling": repetition / presence / frequency penalties -> temperature ->
+ * top-k -> min-p -> top-p -> a seeded weighted draw).  Readings of the
+ * page's names, all in float64 over the model's fp32 logits:
+ *   penalties   over the tokens already in the sequence (prompt and earlier
+ *               generated tokens), token t seen c times: a positive logit is
+ *               divided by repeat_penalty and any other multiplied by it,
+ *               then presence_penalty and c * frequency_penalty are
+ *               subtracted;
+ *   temperature divides the penalised logits; 0 selects the greedy argmax
+ *               (every other setting is then ignored);
+ *   order       candidates by penalised logit descending, token ascending;
+ *   top_k       keeps the first top_k (1 .. 4096);
+ *   min_p       keeps candidates whose softmax probability is at least
+ *               min_p times the largest ([0, 1], 0 = off);
+ *   top_p       keeps the shortest prefix whose softmax probabilities sum
+ *               to at least top_p ((0, 1], 1 = off);
+ *   draw        u = the top 24 bits of SplitMix64 output c + 1 started at
+ *               seed, c = i * 2^20 + b for generated token i of sequence b,
+ *               times 2^-24; the token is the first survivor whose
+ *               cumulative probability exceeds u.
+ * The same settings and seed give the same tokens; top_k = 1 gives the
+ * greedy tokens at any temperature. */
+typedef struct q3i8_sampling {
+    double temperature;
+    double top_p;
+    double min_p;
+    double repeat_penalty;       /* > 0; 1 = off */
+    double presence_penalty;
+    double frequency_penalty;
+    int32_t top_k;
+    int32_t reserved;            /* set to 0 */
+    uint64_t seed;
+} q3i8_sampling;
+
+/* q3i8_decode with every generated token drawn by the sampling chain on the
+ * device (the first one included), from `sampling` (HOST struct; NULL is an
+ * error; temperature 0 is exactly q3i8_decode).  Each decode step's graph
+ * ends with one sampling kernel after the lm_head.  Q3_ERR_INVALID_ARGUMENTS
+ * for a setting outside the ranges above or not finite. */
+int q3i8_decode_sample(q3i8_ctx* ctx, int32_t B, const int32_t* const* prompt_ids, const int32_t* prompt_lens,
+                       int32_t max_new_tokens, int32_t eos_id, const q3i8_sampling* sampling, int32_t* out_ids,
+                       int32_t* out_counts, q3i8_stats* stats);
+
 /* As q3i8_decode, with DEVICE buffers: d_prompt_ids holds the B prompts back
  * to back (sum of prompt_lens ids, sequence 0 first); d_out_ids receives
  * [B][max_new_tokens] ids.  prompt_lens stays a host array.  Nothing is
@@ -253,6 +297,26 @@ int q3i8_op_attention(const float* q, const uint16_t* k, const uint16_t* v, cons
                       const int32_t* row_len, int32_t R, int32_t n_heads, int32_t n_kv_heads, int32_t hd,
                       int32_t cap, int32_t splits, float* out, void* workspace, size_t ws_bytes,
                       int32_t* d_status, void* cuda_stream);
+
+/* The sampling chain of q3i8_decode_sample on one step's logits:
+ *   logits    [B][V] fp32 DEVICE; row b is sequence b.
+ *   counts    [B][V] int32 DEVICE: how often each token occurs in sequence b
+ *             so far (the penalties' history); the drawn token's count is
+ *             incremented.
+ *   sampling  HOST settings; temperature must be > 0.
+ *   step      the generated-token index i of the draw (u's counter is
+ *             i * 2^20 + b).
+ *   tokens    [B] int32 DEVICE: receives the drawn tokens.
+ *   workspace at least q3i8_op_sample_workspace(B, V) bytes, 16-byte
+ *             aligned; no initialisation needed.
+ *   d_status  device int32 (may be NULL), set non-zero if the selection is
+ *             inconsistent (an internal error).
+ * Copies the settings into the workspace and waits for that copy; the draw
+ * itself is only enqueued. */
+size_t q3i8_op_sample_workspace(int32_t B, int32_t V);
+int q3i8_op_sample(const float* logits, int32_t B, int32_t V, int32_t* counts, const q3i8_sampling* sampling,
+                   int32_t step, int32_t* tokens, void* workspace, size_t ws_bytes, int32_t* d_status,
+                   void* cuda_stream);
 
 /* Upper limit, in bytes, of the scratch q3i8_op_attention_static may use:
  * attention_workspace(R, n_heads, hd, splits) must not exceed it. */
