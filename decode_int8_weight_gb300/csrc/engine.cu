@@ -527,7 +527,7 @@ int step_setup(q3i8_ctx* c) {
     if (!step_plan(step_shape(c), c->num_sms, optin, &p)) return Q3_OK;
     if (!step_prepare_device()) return fail(c, Q3_ERR_CUDA, "decode step kernels: shared-memory opt-in refused");
     if (attn_block_max_clusters(c->d.hidden, c->d.head_dim, p.kv_stages) < 1 ||
-        ffn_block_max_clusters(c->d.hidden) < 1)
+        ffn_block_max_blocks(c->d.hidden) < 1)
         return Q3_OK;
     const size_t n = 2 * (size_t)c->bmax * c->d.hidden;  // two buffers each
     CK(c, cudaMalloc(&c->xa, n * sizeof(long long)));

@@ -1,4 +1,4 @@
-// Small-batch decode step: two cluster kernels per layer plus the lm_head sweep (sm_103a).
+// Small-batch decode step: two kernels per layer plus the lm_head sweep (sm_103a).
 //
 // The decoder block is the Qwen3 family's ("Model-agnostic LLM inference",
 // section "Supported models"): RMSNorm -> QKV -> per-head RMSNorm on Q and
@@ -175,10 +175,17 @@ Q3_DEV void mma_pair(float (&c0)[4], float (&c1)[4], const uint4& wv, const uint
     mma_f16_16816(c1, A1, bv.z, bv.w);
 }
 
+// mbar_wait_bounded with its polling loop out of line: one try inline (the
+// common case, the phase has completed or completes within the try's own
+// suspend window), the loop only when that try fails.  Keeps the kernels'
+// code, fetched once per launch, small.
+__device__ __noinline__ bool wait_slow(uint64_t* bar, uint32_t parity) { return mbar_wait_bounded(bar, parity); }
+Q3_DEV bool wait_phase(uint64_t* bar, uint32_t parity) { return mbar_try_wait(bar, parity) || wait_slow(bar, parity); }
+
 // Bounded wait shared by a whole block: every thread waits, and the block
 // agrees on the outcome (true when any thread's wait gave up).
 Q3_DEV bool block_wait_failed(uint64_t* bar, uint32_t parity) {
-    const bool ok = mbar_wait_bounded(bar, parity);
+    const bool ok = wait_phase(bar, parity);
     return __syncthreads_or(!ok) != 0;
 }
 
@@ -286,6 +293,7 @@ Q3_DEV void clear_share(long long* p, int n) {
     if (!p) return;
     const int per = (n + gridDim.x - 1) / gridDim.x;
     const int z0 = blockIdx.x * per, z1 = min(n, z0 + per);
+#pragma unroll 1
     for (int i = z0 + (int)threadIdx.x; i < z1; i += blockDim.x) p[i] = 0;
 }
 
@@ -338,23 +346,21 @@ __host__ __device__ inline AttnBlockLayout attn_block_layout(int H, int hd, int 
 }
 
 struct FfnLayout {
-    uint32_t wgu, wd, xop, pgu, ss, dop, sgu, sd, gain, resid, misc, bars, total;
+    uint32_t wgu, wd, xop, dop, sgu, sd, red, resid, bars, total;
 };
 __host__ __device__ inline FfnLayout ffn_layout(int H) {
     FfnLayout L{};
     uint32_t off = 0;
-    const int nkp = H / 32 / kClusterCtas, dt = H / kClusterCtas / 16;
-    L.wgu = take_smem(off, (size_t)(2 * kFfnUnits / 16) * nkp * 512);
-    L.wd = take_smem(off, (size_t)dt * (kFfnUnits / 32) * 512);
-    L.xop = take_smem(off, (size_t)nkp * 512);
-    L.pgu = take_smem(off, (size_t)kStepMaxBatch * 2 * kFfnUnits * 4);
-    L.ss = take_smem(off, (size_t)kStepMaxBatch * 4);
-    L.dop = take_smem(off, (size_t)(kFfnUnits / 32) * 512);
+    L.wgu = take_smem(off, (size_t)(2 * kFfnUnits / 16) * tile_blob_bytes(H));
+    L.wd = take_smem(off, (size_t)(H / 16) * 512);
+    // the operand, then the warps' partial gate/up rows
+    const size_t part = (size_t)kWarps * kStepMaxBatch * 2 * kFfnUnits * 4, xop = (size_t)(H / 32) * 512;
+    L.xop = take_smem(off, xop > part ? xop : part);
+    L.dop = take_smem(off, 512);
     L.sgu = take_smem(off, (size_t)2 * kFfnUnits * 4);
-    L.sd = take_smem(off, (size_t)(H / kClusterCtas) * 4);
-    L.gain = take_smem(off, (size_t)nkp * 32 * 4);
-    L.resid = take_smem(off, (size_t)kStepMaxBatch * (H / kClusterCtas) * 8);
-    L.misc = take_smem(off, 64);
+    L.sd = take_smem(off, (size_t)H * 4);
+    L.red = take_smem(off, (size_t)kWarps * 4 * 4);
+    L.resid = take_smem(off, (size_t)kStepMaxBatch * kFfnResidRows * 8);
     L.bars = take_smem(off, 2 * 8);
     L.total = off;
     return L;
@@ -458,6 +464,7 @@ __global__ void __launch_bounds__(kThreads, 2) attn_block_kernel(const AttnBlock
     auto nchunks = [&](int b) { return (split_hi(b) - split_lo(b) + kStepKvChunk - 1) / kStepKvChunk; };
     auto count_items = [&]() {
         int n = 0;
+        #pragma unroll 1
         for (int b = 0; b < B; ++b) n += nchunks(b);
         return n;
     };
@@ -477,20 +484,24 @@ __global__ void __launch_bounds__(kThreads, 2) attn_block_kernel(const AttnBlock
     };
     // positions known: RoPE rows into shared memory; the first K/V stages
     auto position_work = [&]() {
+        #pragma unroll 1
         for (int i = tid; i < B * (HD / 2); i += kThreads) {
             const int b = i / (HD / 2), j = i - b * (HD / 2);
             s_rope[i] = a.rope[(size_t)s_pos[b] * (HD / 2) + j];
         }
         if (tid == 0) {
             const int n = count_items();
+            #pragma unroll 1
             for (int i = 0; i < S && i < n; ++i) issue_kv(i);
         }
     };
 
     // ---- prologue: constant data and, from the second layer on, the positions
     if (tid == 0) {
+        #pragma unroll 1
         for (int i = 0; i < 2 + S; ++i) mbar_init(&bars[i], 1);
         fence_mbar_init();
+        #pragma unroll 1
         for (int i = 0; i < S; ++i) s_last[i] = -1;
     }
     if (a.pos_early && tid < B) {
@@ -500,16 +511,22 @@ __global__ void __launch_bounds__(kThreads, 2) attn_block_kernel(const AttnBlock
     __syncthreads();
     if (tid == 0) {
         mbar_arrive_expect_tx(&bars[0], (uint32_t)(T * nkp * 512));
+        #pragma unroll 1
         for (int t = 0; t < T; ++t)
             bulk_g2s(smem + L.wq + (size_t)t * nkp * 512,
                      a.wqkv + (size_t)(grow(t * 16) / 16) * blob + kTileHeader + (size_t)kp0 * 512,
                      (uint32_t)nkp * 512, &bars[0]);
         mbar_arrive_expect_tx(&bars[1], (uint32_t)otiles * oseg);
+        #pragma unroll 1
         for (int i = 0; i < otiles; ++i) bulk_g2s(smem + L.wo + (size_t)i * oseg, o_src(i), oseg, &bars[1]);
     }
+    #pragma unroll 1
     for (int i = tid; i < R3; i += kThreads) s_sc[i] = a.qkv_scale[grow(i)];
+    #pragma unroll 1
     for (int i = tid; i < ro; i += kThreads) osc[i] = a.o_scale[r * ro + i];
+    #pragma unroll 1
     for (int i = tid; i < nkp * 32; i += kThreads) s_gain[i] = a.attn_norm[kp0 * 32 + i];
+    #pragma unroll 1
     for (int i = tid; i < HD; i += kThreads) s_qg[i] = a.q_norm[i], s_kg[i] = a.k_norm[i];
     if (a.pos_early) position_work();
     pdl_wait();
@@ -532,6 +549,7 @@ __global__ void __launch_bounds__(kThreads, 2) attn_block_kernel(const AttnBlock
         position_work();
     }
     if (h == 0)  // this cluster adds the stream's input to its rows
+        #pragma unroll 1
         for (int i = tid; i < B * ro; i += kThreads) {
             const int b = i / ro, R = r * ro + (i - b * ro);
             s_res[i] = a.xin ? __ldcg(a.xin + (size_t)b * H + R)
@@ -619,7 +637,7 @@ __global__ void __launch_bounds__(kThreads, 2) attn_block_kernel(const AttnBlock
         const int lo = split_lo(b), hi = split_hi(b), nch = nchunks(b);
         for (int c = 0; c < nch; ++c, ++item) {
             const int s = item % S;
-            const bool ok = bad || mbar_wait_bounded(&bars[2 + s], (uint32_t)(item / S) & 1u);
+            const bool ok = bad || wait_phase(&bars[2 + s], (uint32_t)(item / S) & 1u);
             const int cnt = min(kStepKvChunk, hi - lo - c * kStepKvChunk);
             const __nv_bfloat16* ks = ring + (size_t)s * 2 * kStepKvChunk * HD;
             const __nv_bfloat16* vs = ks + kStepKvChunk * HD;
@@ -693,6 +711,7 @@ __global__ void __launch_bounds__(kThreads, 2) attn_block_kernel(const AttnBlock
                 Ls += wst[w * PS + HD + 1] * f[w];
             }
             float* pb = part + b * PS;
+            #pragma unroll 1
             for (int d = tid; d < HD; d += kThreads) {
                 float A = 0.f;
 #pragma unroll
@@ -730,6 +749,7 @@ __global__ void __launch_bounds__(kThreads, 2) attn_block_kernel(const AttnBlock
         }
         __syncthreads();
         __half* ooph = reinterpret_cast<__half*>(oop);
+        #pragma unroll 1
         for (int i = tid; i < B * HD; i += kThreads) {
             const int b = i / HD, d = i - b * HD;
             float o = 0.f;
@@ -765,6 +785,7 @@ __global__ void __launch_bounds__(kThreads, 2) attn_block_kernel(const AttnBlock
         }
     }
     if (appender)
+        #pragma unroll 1
         for (int i = tid; i < B * HD; i += kThreads) {
             const int b = i / HD, d = i - b * HD;
             const size_t slot = (((size_t)s_seq[b] * a.nkv + g) * a.cap + s_pos[b]) * HD + d;
@@ -774,135 +795,153 @@ __global__ void __launch_bounds__(kThreads, 2) attn_block_kernel(const AttnBlock
     if (bad && tid == 0) {
         set_status(a.status, kStatusTimeout);
         // let every copy this CTA started land before its shared memory goes away
-        mbar_wait_bounded(&bars[0], 0);
-        mbar_wait_bounded(&bars[1], 0);
+        wait_phase(&bars[0], 0);
+        wait_phase(&bars[1], 0);
+        #pragma unroll 1
         for (int s = 0; s < S; ++s)
-            if (s_last[s] >= 0) mbar_wait_bounded(&bars[2 + s], (uint32_t)(s_last[s] / S) & 1u);
+            if (s_last[s] >= 0) wait_phase(&bars[2 + s], (uint32_t)(s_last[s] / S) & 1u);
     }
     cluster_wait();  // no CTA leaves while a peer may still read its shared memory
 }
 
 // ===================================================================== FFN block
-// Cluster c (8 CTAs) serves FFN units [192 c, 192 c + 192): their 24 gate/up
-// tiles (8 gate rows and the same 8 up units each) and k-pairs [6 c, 6 c + 6)
-// of every down row.
-//  1. Gate/up rows times the residual stream, K split over the 8 CTAs as in
-//     the attention block (RMSNorm gain in the operand, 1 / rms after).
-//  2. Every CTA sums the 8 partial rows of all 192 units and forms
-//     a = silu(gate) * up for them.
-//  3. CTA r multiplies its H / 8 down rows (over the cluster's 192 units) by
-//     a; the rows are added to the fixed-point residual stream (cluster 0
-//     also adds the stream's input).
+// CTA j (no cluster) serves FFN units [32 j, 32 j + 32): their 4 gate/up
+// tiles (8 gate rows and the same 8 up units each, K = H whole) and k-pair j
+// (the same 32 units) of every down row.
+//  1. The RMSNorm-ed residual row (1 / rms and the gain in the operand) times
+//     the 64 gate/up rows; warp w takes k-pairs [w KP / 8, (w + 1) KP / 8) of
+//     all 4 tiles and the 8 warps' partial rows are summed in warp order.
+//  2. a = silu(gate) * up for the 32 units, as the down operand.
+//  3. Every down row times a (one k-pair per row tile, warp w taking tiles w,
+//     w + 8, ...); the rows are added to the fixed-point residual stream, CTA
+//     j also adding the stream's input to rows R = j (mod grid).
+// With no exchange between CTAs there is no cluster barrier on the path; the
+// price is H x B residual additions per CTA instead of H / 8 x B.
 __global__ void __launch_bounds__(kThreads, 2) ffn_block_kernel(const FfnBlockArgs a) {
-    constexpr int T = 2 * kFfnUnits / 16;  // gate/up tiles of the cluster
-    constexpr int TPW = (T + kWarps - 1) / kWarps;
-    constexpr int R2 = 2 * kFfnUnits;      // gate/up rows of the cluster
-    constexpr int DKP = kFfnUnits / 32;    // down k-pairs of the cluster
+    constexpr int T = 2 * kFfnUnits / 16;  // gate/up tiles of the CTA
+    static_assert(kStepMaxBatch * kFfnResidRows <= kThreads, "one residual input per thread");
     extern __shared__ __align__(128) unsigned char smem[];
     const FfnLayout L = ffn_layout(a.H);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int r = cluster_rank();
-    const int c = blockIdx.x / kClusterCtas;
-    const int H = a.H, B = a.B;
-    const int nkp = H / 32 / kClusterCtas, kp0 = r * nkp;
-    const int ro = H / kClusterCtas, dt = ro / 16;
+    const int j = blockIdx.x, G = gridDim.x;
+    const int H = a.H, B = a.B, KP = H / 32, kpw = KP / kWarps, dtiles = H / 16;
     const uint32_t blob = (uint32_t)tile_blob_bytes(H), dblob = (uint32_t)tile_blob_bytes(a.I);
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bars);  // 0 gate/up slices, 1 down rows
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bars);  // 0 gate/up tiles, 1 down k-pairs
     float* s_sgu = reinterpret_cast<float*>(smem + L.sgu);
     float* s_sd = reinterpret_cast<float*>(smem + L.sd);
-    float* s_gain = reinterpret_cast<float*>(smem + L.gain);
+    float* s_red = reinterpret_cast<float*>(smem + L.red);
     long long* s_res = reinterpret_cast<long long*>(smem + L.resid);
-    float* s_inv = reinterpret_cast<float*>(smem + L.misc);
     uint4* xop = reinterpret_cast<uint4*>(smem + L.xop);
-    float* pgu = reinterpret_cast<float*>(smem + L.pgu);
-    float* s_ss = reinterpret_cast<float*>(smem + L.ss);
+    float* part = reinterpret_cast<float*>(smem + L.xop);  // [warp][sequence][64 rows], after the MMAs
     uint4* dop = reinterpret_cast<uint4*>(smem + L.dop);
 
     if (tid == 0) {
         mbar_init(&bars[0], 1);
         mbar_init(&bars[1], 1);
         fence_mbar_init();
+        mbar_arrive_expect_tx(&bars[0], (uint32_t)T * blob);
+        bulk_g2s(smem + L.wgu, a.wgu + (size_t)T * j * blob, (uint32_t)T * blob, &bars[0]);
+        mbar_arrive_expect_tx(&bars[1], (uint32_t)dtiles * 512);
     }
     __syncthreads();
-    if (tid == 0) {
-        mbar_arrive_expect_tx(&bars[0], (uint32_t)(T * nkp * 512));
-        for (int t = 0; t < T; ++t)
-            bulk_g2s(smem + L.wgu + (size_t)t * nkp * 512,
-                     a.wgu + (size_t)(T * c + t) * blob + kTileHeader + (size_t)kp0 * 512, (uint32_t)nkp * 512,
-                     &bars[0]);
-        mbar_arrive_expect_tx(&bars[1], (uint32_t)(dt * DKP * 512));
-        for (int i = 0; i < dt; ++i)
-            bulk_g2s(smem + L.wd + (size_t)i * DKP * 512,
-                     a.wd + (size_t)(r * dt + i) * dblob + kTileHeader + (size_t)DKP * c * 512, DKP * 512,
+    if (warp == 0)
+#pragma unroll 1
+        for (int i = lane; i < dtiles; i += 32)
+            bulk_g2s(smem + L.wd + (size_t)i * 512, a.wd + (size_t)i * dblob + kTileHeader + (size_t)j * 512, 512,
                      &bars[1]);
-    }
-    for (int i = tid; i < R2; i += kThreads) s_sgu[i] = a.gu_scale[(size_t)T * 16 * c + i];
-    for (int i = tid; i < ro; i += kThreads) s_sd[i] = a.d_scale[r * ro + i];
-    for (int i = tid; i < nkp * 32; i += kThreads) s_gain[i] = a.ffn_norm[kp0 * 32 + i];
+#pragma unroll 1
+    for (int i = tid; i < 2 * kFfnUnits; i += kThreads) s_sgu[i] = a.gu_scale[(size_t)2 * kFfnUnits * j + i];
+#pragma unroll 1
+    for (int i = tid; i < H; i += kThreads) s_sd[i] = a.d_scale[i];
     pdl_wait();
     pdl_launch_dependents();
 
-    if (c == 0)  // this cluster adds the stream's input to its rows
-        for (int i = tid; i < B * ro; i += kThreads) {
-            const int b = i / ro;
-            s_res[i] = __ldcg(a.xa + (size_t)b * H + r * ro + (i - b * ro));
-        }
-    // ---- 1. this CTA's K slice of the cluster's gate/up rows
-    slice_operand(xop, s_ss, a.xa, nullptr, nullptr, nullptr, B, H, kp0 * 32, nkp, s_gain);
-    bool bad = block_wait_failed(&bars[0], 0);
-    if (!bad) cluster_tiles_mma<TPW>(smem + L.wgu, T, nkp, xop, pgu, R2);
-    cluster_arrive();
-    cluster_wait();  // every CTA's partial rows are visible in the cluster
+    // the stream's input at this CTA's rows R = j + i G (at most one per
+    // thread: B nres <= 4 kFfnResidRows = kThreads), loaded now and parked in
+    // shared memory after the gate/up rows
+    const int nres = j < H ? (H - 1 - j) / G + 1 : 0;
+    long long res_in = 0;
+    if (tid < B * nres) res_in = __ldcg(a.xa + (size_t)(tid / nres) * H + j + (size_t)(tid % nres) * G);
 
-    // ---- 2. a = silu(gate) * up for the cluster's units, as the down operand
-    if (tid < B) s_inv[tid] = cluster_inv_rms(s_ss, tid, H, a.eps);
-    __syncthreads();
+    // ---- 1. gate/up rows times the normalised row, K split over the warps
+    norm_operand(xop, a.xa, nullptr, nullptr, nullptr, B, H, a.ffn_norm, a.eps, s_red);
+    bool bad = block_wait_failed(&bars[0], 0);
+    float c0[T][4], c1[T][4];
+#pragma unroll
+    for (int t = 0; t < T; ++t)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) c0[t][e] = c1[t][e] = 0.f;
+    if (!bad)
+#pragma unroll 1
+        for (int p = warp * kpw; p < (warp + 1) * kpw; ++p) {
+            const uint4 bv = xop[p * 32 + lane];
+#pragma unroll
+            for (int t = 0; t < T; ++t) {
+                const uint4 wv = *reinterpret_cast<const uint4*>(smem + L.wgu + (size_t)t * blob + kTileHeader +
+                                                                 (size_t)p * 512 + lane * 16);
+                mma_pair(c0[t], c1[t], wv, bv);
+            }
+        }
+    if (tid < B * nres) s_res[(tid / nres) * kFfnResidRows + tid % nres] = res_in;
+    __syncthreads();  // every warp is done with the operand: its space takes the partial rows
     {
-        __half* doph = reinterpret_cast<__half*>(dop);
-        for (int i = tid; i < B * kFfnUnits; i += kThreads) {
-            const int b = i / kFfnUnits, u = i - b * kFfnUnits;
-            const int gr = (u >> 3) * 16 + (u & 7);  // gate row of unit u; its up row is gr + 8
-            const float sg = cluster_sum(pgu, b * R2 + gr);
-            const float su = cluster_sum(pgu, b * R2 + gr + 8);
-            const float gate = s_sgu[gr] * s_inv[b] * sg;
-            const float up = s_sgu[gr + 8] * s_inv[b] * su;
-            const float v = (gate / (1.0f + expf(-gate))) * up;
-            __half hi, lo;
-            split_f16(v, hi, lo);
-            doph[frag_half(2 * b, u)] = hi;
-            doph[frag_half(2 * b + 1, u)] = lo;
+        const int g = lane >> 2, q = lane & 3;
+        float* pw = part + (warp * kStepMaxBatch + q) * (2 * kFfnUnits);
+#pragma unroll
+        for (int t = 0; t < T; ++t) {
+            pw[t * 16 + g] = c0[t][0] + c0[t][1] + c1[t][0] + c1[t][1];
+            pw[t * 16 + g + 8] = c0[t][2] + c0[t][3] + c1[t][2] + c1[t][3];
         }
     }
-    cluster_arrive();  // done with the peers' shared memory (waited for before leaving)
+    __syncthreads();
 
-    // ---- 3. this CTA's down rows over the cluster's units
-    bad = block_wait_failed(&bars[1], 0) || bad;
-    if (warp < dt && !bad) {
-        const unsigned char* wt = smem + L.wd + (size_t)warp * DKP * 512;
-        float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
+    // ---- 2. a = silu(gate) * up for the CTA's units, as the down operand
+    if (tid < B * kFfnUnits) {
+        const int b = tid / kFfnUnits, u = tid - b * kFfnUnits;
+        const int gr = (u >> 3) * 16 + (u & 7);  // gate row of unit u; its up row is gr + 8
+        float sg = 0.f, su = 0.f;
 #pragma unroll
-        for (int p = 0; p < DKP; ++p) {
-            const uint4 wv = *reinterpret_cast<const uint4*>(wt + p * 512 + lane * 16);
-            mma_pair(c0, c1, wv, dop[p * 32 + lane]);
+        for (int w = 0; w < kWarps; ++w) {
+            sg += part[(w * kStepMaxBatch + b) * (2 * kFfnUnits) + gr];
+            su += part[(w * kStepMaxBatch + b) * (2 * kFfnUnits) + gr + 8];
         }
-        const int gg = lane >> 2, tq = lane & 3;
-        if (tq < B) {
+        const float gate = s_sgu[gr] * sg, up = s_sgu[gr + 8] * su;
+        const float v = (gate / (1.0f + expf(-gate))) * up;
+        __half hi, lo;
+        split_f16(v, hi, lo);
+        __half* doph = reinterpret_cast<__half*>(dop);
+        doph[frag_half(2 * b, u)] = hi;
+        doph[frag_half(2 * b + 1, u)] = lo;
+    }
+    __syncthreads();
+
+    // ---- 3. every down row over the CTA's units
+    bad = block_wait_failed(&bars[1], 0) || bad;
+    if (!bad) {
+        const uint4 bv = dop[lane];
+        const int g = lane >> 2, q = lane & 3;
+#pragma unroll 1
+        for (int t = warp; t < dtiles; t += kWarps) {
+            float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
+            mma_pair(d0, d1, *reinterpret_cast<const uint4*>(smem + L.wd + (size_t)t * 512 + lane * 16), bv);
+            if (q < B) {
 #pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                const int rl = warp * 16 + gg + 8 * half;
-                const float s = half ? (c0[2] + c0[3] + c1[2] + c1[3]) : (c0[0] + c0[1] + c1[0] + c1[1]);
-                long long f = fix_of(s_sd[rl] * s);
-                if (c == 0) f += s_res[tq * ro + rl];
-                red_add_fix(a.xf + (size_t)tq * H + r * ro + rl, f);
+                for (int half = 0; half < 2; ++half) {
+                    const int R = t * 16 + g + 8 * half;
+                    const float s = half ? (d0[2] + d0[3] + d1[2] + d1[3]) : (d0[0] + d0[1] + d1[0] + d1[1]);
+                    long long f = fix_of(s_sd[R] * s);
+                    if (R % G == j) f += s_res[q * kFfnResidRows + R / G];
+                    red_add_fix(a.xf + (size_t)q * H + R, f);
+                }
             }
         }
     }
     if (bad && tid == 0) {
         set_status(a.status, kStatusTimeout);
-        mbar_wait_bounded(&bars[0], 0);
-        mbar_wait_bounded(&bars[1], 0);
+        // let every copy this CTA started land before its shared memory goes away
+        wait_phase(&bars[0], 0);
+        wait_phase(&bars[1], 0);
     }
-    cluster_wait();  // no CTA leaves while a peer may still read its shared memory
 }
 
 // ===================================================================== lm_head
@@ -931,6 +970,7 @@ __global__ void __launch_bounds__(kLmThreads, 2) lm_head_kernel(const LmHeadArgs
     uint4* xop = reinterpret_cast<uint4*>(smem + L.xop);
     const bool producer = warp == kWarps && lane == 0;
     if (tid == 0) {
+        #pragma unroll 1
         for (int s = 0; s < S; ++s) mbar_init(&full[s], 1), mbar_init(&empty[s], 1);
         fence_mbar_init();
         *s_abort = 0;
@@ -944,8 +984,10 @@ __global__ void __launch_bounds__(kLmThreads, 2) lm_head_kernel(const LmHeadArgs
         bulk_g2s(smem + L.ring + (size_t)s * blob, a.w + (size_t)(j0 + j) * blob, blob, &full[s]);
     };
     if (producer)
+        #pragma unroll 1
         for (; issued < S && issued < n; ++issued) issue(issued);
     float* s_gain = reinterpret_cast<float*>(smem + L.gain);
+    #pragma unroll 1
     for (int i = tid; i < H; i += kLmThreads) s_gain[i] = a.final_norm[i];
     pdl_wait();
     pdl_launch_dependents();
@@ -953,10 +995,11 @@ __global__ void __launch_bounds__(kLmThreads, 2) lm_head_kernel(const LmHeadArgs
     norm_operand(xop, a.xf, nullptr, nullptr, nullptr, B, H, s_gain, a.eps, s_red);
 
     if (producer) {
+        #pragma unroll 1
         for (; issued < n; ++issued) {
             const int s = issued % S;
             if (*reinterpret_cast<volatile int*>(s_abort) ||
-                !mbar_wait_bounded(&empty[s], (uint32_t)(issued / S - 1) & 1u)) {
+                !wait_phase(&empty[s], (uint32_t)(issued / S - 1) & 1u)) {
                 *reinterpret_cast<volatile int*>(s_abort) = 1;
                 break;
             }
@@ -973,7 +1016,7 @@ __global__ void __launch_bounds__(kLmThreads, 2) lm_head_kernel(const LmHeadArgs
         for (int j = warp; warp < S && j < n; j += S) {
             const int s = j % S;
             if (*reinterpret_cast<volatile int*>(s_abort)) break;
-            if (!mbar_wait_bounded(&full[s], (uint32_t)(j / S) & 1u)) {
+            if (!wait_phase(&full[s], (uint32_t)(j / S) & 1u)) {
                 *reinterpret_cast<volatile int*>(s_abort) = 1;
                 break;
             }
@@ -1023,10 +1066,11 @@ __global__ void __launch_bounds__(kLmThreads, 2) lm_head_kernel(const LmHeadArgs
     }
     if (*reinterpret_cast<volatile int*>(s_abort) && tid == 0) {
         set_status(a.status, kStatusTimeout);
+        #pragma unroll 1
         for (int s = 0; s < S; ++s) {
             // the last tile issued into stage s, if any
             const int last = *s_last - 1 - ((*s_last - 1 - s) % S + S) % S;
-            if (last >= 0 && last < *s_last) mbar_wait_bounded(&full[s], (uint32_t)(last / S) & 1u);
+            if (last >= 0 && last < *s_last) wait_phase(&full[s], (uint32_t)(last / S) & 1u);
         }
     }
     __threadfence();
@@ -1061,11 +1105,12 @@ bool step_plan(const StepShape& s, int num_sms, int smem_optin, StepPlan* p) {
     if (s.nkv < 1 || s.nh % s.nkv) return false;
     // K slices of whole k-pairs, at most 4 per CTA (a sequence's operand threads share one warp)
     if (s.H % 256 || s.H > 1024 || s.I % kFfnUnits || s.vocab_rows % 16) return false;
+    if ((s.H + s.I / kFfnUnits - 1) / (s.I / kFfnUnits) > kFfnResidRows) return false;  // input rows per FFN CTA
     StepPlan q;
     q.kv_stages = p->kv_stages < 1 ? 2 : p->kv_stages;
     if (attn_block_smem(s.H, s.hd, q.kv_stages) > (size_t)smem_optin) return false;
     if (ffn_block_smem(s.H) > (size_t)smem_optin) return false;
-    q.ffn_grid = s.I / kFfnUnits * kClusterCtas;
+    q.ffn_grid = s.I / kFfnUnits;
     q.lm_stages = 6;
     while (q.lm_stages > 2 && lm_head_smem(s.H, q.lm_stages) > (size_t)smem_optin) --q.lm_stages;
     if (lm_head_smem(s.H, q.lm_stages) > (size_t)smem_optin) return false;
@@ -1116,7 +1161,7 @@ cudaError_t launch_attn_block(const AttnBlockArgs& a, int hd, cudaStream_t st) {
 }
 
 cudaError_t launch_ffn_block(const FfnBlockArgs& a, int grid, cudaStream_t st) {
-    return launch_ex(ffn_block_kernel, grid, kThreads, ffn_block_smem(a.H), kClusterCtas, st, a);
+    return launch_ex(ffn_block_kernel, grid, kThreads, ffn_block_smem(a.H), 1, st, a);
 }
 
 cudaError_t launch_lm_head(const LmHeadArgs& a, int grid, cudaStream_t st) {
@@ -1148,6 +1193,13 @@ int attn_block_max_clusters(int H, int hd, int kv_stages) {
     return max_clusters(f, attn_block_smem(H, hd, kv_stages));
 }
 
-int ffn_block_max_clusters(int H) { return max_clusters((const void*)ffn_block_kernel, ffn_block_smem(H)); }
+int ffn_block_max_blocks(int H) {
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, ffn_block_kernel, kThreads, ffn_block_smem(H)) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    return n;
+}
 
 }  // namespace q3

@@ -1,19 +1,19 @@
 // The small-batch decode step (host side of step.cu).
 //
-// One layer is two cluster kernels chained by programmatic dependent launch:
+// One layer is two kernels chained by programmatic dependent launch:
 //   attention block  (one cluster of 8 CTAs per query head):
 //       RMSNorm -> the head's Q rows and its group's K, V rows -> QK-RMSNorm,
 //       RoPE, bf16 KV append -> split attention merged inside the cluster ->
 //       this head's share of the O projection, added to the residual stream;
-//   FFN block        (one cluster of 8 CTAs per 192 FFN units):
-//       RMSNorm -> the units' gate/up rows -> SiLU(gate) * up -> the units'
-//       share of the down projection, added to the residual stream;
-// and the step ends with the lm_head sweep and its argmax.  Inside a cluster
-// the 8 CTAs split K of the cluster's rows; their partial sums (and the
-// RMSNorm's partial sums of squares) meet in distributed shared memory.  The
-// residual stream is carried between kernels in 64-bit fixed point (value *
-// 2^32), so the clusters' shares meet in integer atomic adds whose result
-// does not depend on their order.
+//   FFN block        (one CTA per 32 FFN units, no cluster):
+//       RMSNorm -> the units' gate/up rows (K whole) -> SiLU(gate) * up ->
+//       the units' k-pair of every down row, added to the residual stream;
+// and the step ends with the lm_head sweep and its argmax.  Inside an
+// attention cluster the 8 CTAs split K of the cluster's rows; their partial
+// sums (and the RMSNorm's partial sums of squares) meet in distributed
+// shared memory.  The residual stream is carried between kernels in 64-bit
+// fixed point (value * 2^32), so the CTAs' shares meet in integer atomic
+// adds whose result does not depend on their order.
 #pragma once
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -25,7 +25,8 @@ namespace q3 {
 constexpr int kStepMaxBatch = 4;  // sequences per step (one 8-column MMA tile: hi and lo of 4 sequences)
 constexpr int kClusterCtas = 8;   // CTAs per cluster
 constexpr int kStepKvChunk = 16;  // K/V positions per shared-memory stage of the attention block
-constexpr int kFfnUnits = 192;    // FFN units per cluster (24 gate/up tiles; 6 k-pairs of the down rows)
+constexpr int kFfnUnits = 32;     // FFN units per CTA of the FFN block (4 gate/up tiles; one k-pair of each down row)
+constexpr int kFfnResidRows = 64; // most residual rows an FFN CTA adds the stream's input to
 
 struct AttnBlockArgs {
     int B, H, nh, nkv, cap, kv_stages, vocab;
@@ -113,6 +114,6 @@ cudaError_t launch_lm_head(const LmHeadArgs& a, int grid, cudaStream_t st);
 // Largest number of clusters of each kernel that can be resident at once on
 // the current device (0 if none).
 int attn_block_max_clusters(int H, int hd, int kv_stages);
-int ffn_block_max_clusters(int H);
+int ffn_block_max_blocks(int H);  // FFN blocks resident per SM (0: cannot launch)
 
 }  // namespace q3
