@@ -42,7 +42,8 @@ EXPORTS = ["q3i8_validate_dims", "q3i8_init", "q3i8_decode", "q3i8_decode_sample
            "q3i8_cache_payload_bytes", "q3i8_cache_write",
            "q3i8_cache_open", "q3i8_cache_tables", "q3i8_cache_close", "q3i8_sched_new", "q3i8_sched_destroy",
            "q3i8_sched_submit", "q3i8_sched_plan", "q3i8_sched_complete_prefill", "q3i8_sched_complete_step",
-           "q3i8_sched_idle", "q3i8_sched_result"]
+           "q3i8_sched_idle", "q3i8_sched_result", "q3i8_cb_reserve", "q3i8_cb_prefill", "q3i8_cb_step",
+           "q3i8_sched_run"]
 
 # q3i8_cache_open gate results
 CACHE_GATE = {0: "valid", 1: "absent", 2: "bad_magic", 3: "dims", 4: "manifest", 5: "length"}
@@ -155,6 +156,10 @@ def lib():
             L.q3i8_sched_complete_step.argtypes = [vp, i32, vp]
             L.q3i8_sched_idle.restype = i32
             L.q3i8_sched_idle.argtypes = [vp]
+            L.q3i8_cb_reserve.argtypes = [vp, i32]
+            L.q3i8_cb_prefill.argtypes = [vp, i32, vp, ctypes.POINTER(vp), vp, vp]
+            L.q3i8_cb_step.argtypes = [vp, i32, vp, vp, vp, vp]
+            L.q3i8_sched_run.argtypes = [vp, vp, ctypes.POINTER(Stats)]
             L.q3i8_sched_result.argtypes = [vp, i32, vp, i32, ctypes.POINTER(i32), ctypes.POINTER(i32)]
             _lib = L
     return _lib
@@ -319,6 +324,31 @@ class Decoder:
 
     def launch_count(self) -> int:
         return int(lib().q3i8_launch_count(self._h))
+
+    # continuous batching on the device (q3i8_cb_*, q3i8_sched_run)
+    def cb_reserve(self, max_ctx: int):
+        _check(lib().q3i8_cb_reserve(self._h, max_ctx), self._h)
+
+    def cb_prefill(self, slots, prompts):
+        arrs, ptrs, lens = self._prompts(prompts)
+        slots = np.ascontiguousarray(slots, np.int32)
+        out = np.zeros(len(arrs), np.int32)
+        _check(lib().q3i8_cb_prefill(self._h, len(arrs), _p(slots), ptrs, _p(lens), _p(out)), self._h)
+        return out
+
+    def cb_step(self, slots, positions, tokens):
+        slots = np.ascontiguousarray(slots, np.int32)
+        positions = np.ascontiguousarray(positions, np.int32)
+        tokens = np.ascontiguousarray(tokens, np.int32)
+        out = np.zeros(slots.size, np.int32)
+        _check(lib().q3i8_cb_step(self._h, slots.size, _p(slots), _p(positions), _p(tokens), _p(out)), self._h)
+        return out
+
+    def sched_run(self, sched):
+        """Run a Scheduler to idle on this context's GPU; returns the stats dict."""
+        st = Stats()
+        _check(lib().q3i8_sched_run(self._h, sched._h, ctypes.byref(st)), self._h)
+        return st.as_dict()
 
 
 def op_gemm_i8(a_planes, w, scale, y, status=None, stream=None):

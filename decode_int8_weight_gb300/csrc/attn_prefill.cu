@@ -256,11 +256,11 @@ __global__ void __launch_bounds__(kPfThreads, 2)
 
 bool attn_prefill_supported(int nh, int nkv, int hd) { return hd == kHD && nkv > 0 && nh == 2 * nkv; }
 
-int attn_prefill_blocks(const int32_t* lens, int B, int4* out, int cap_blocks) {
+int attn_prefill_blocks(const int32_t* lens, int B, int4* out, int cap_blocks, const int32_t* slots) {
     int n = 0, row0 = 0;
     for (int b = 0; b < B; ++b) {
         for (int p = 0; p < lens[b]; p += kQRows) {
-            if (n < cap_blocks) out[n] = make_int4(b, p, row0, lens[b]);
+            if (n < cap_blocks) out[n] = make_int4(slots ? slots[b] : b, p, row0, lens[b]);
             ++n;
         }
         row0 += lens[b];

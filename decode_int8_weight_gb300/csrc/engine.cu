@@ -8,6 +8,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <chrono>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -843,7 +844,16 @@ static int enqueue_sample(q3i8_ctx* c, int B, const int32_t* step_ptr, int step_
 // Prefill B prompts given back to back in device memory; leaves the first
 // generated token of each sequence in tokens[] / out_ids[:, 0] (step = 1)
 // and pos[b] = prompt length.
-static int run_prefill(q3i8_ctx* c, int B, const int32_t* d_ids, const int32_t* lens, float* d_logits) {
+static int restore_seq_ids(q3i8_ctx* c);
+// scheduler internals (sched.cu)
+int q3_sched_slots(const q3i8_sched* s);
+int q3_sched_max_ctx(const q3i8_sched* s);
+const int32_t* q3_sched_prompt(const q3i8_sched* s, int request_id, int32_t* len);
+
+// slots: the KV cache sequence of prompt b (NULL: b itself, the plain
+// decode's layout); other sequences' cache entries are not touched.
+static int run_prefill(q3i8_ctx* c, int B, const int32_t* d_ids, const int32_t* lens, float* d_logits,
+                       const int32_t* slots = nullptr) {
     const q3i8_dims& d = c->d;
     const int H = d.hidden, I = d.intermediate, hd = d.head_dim, nh = d.n_heads, nkv = d.n_kv_heads;
     const int Dq = nh * hd, Dkv = nkv * hd;
@@ -851,10 +861,11 @@ static int run_prefill(q3i8_ctx* c, int B, const int32_t* d_ids, const int32_t* 
     for (int b = 0; b < B; ++b) M += lens[b], maxlen = std::max(maxlen, lens[b]);
     int rc = ensure_prefill(c, M);
     if (rc) return rc;
+    if (!slots && (rc = restore_seq_ids(c))) return rc;
     cudaStream_t st = c->stream;
     std::vector<int32_t> seq(M), pos(M), last(B), plen(lens, lens + B);
     for (int b = 0, r = 0; b < B; ++b) {
-        for (int t = 0; t < lens[b]; ++t, ++r) seq[r] = b, pos[r] = t;
+        for (int t = 0; t < lens[b]; ++t, ++r) seq[r] = slots ? slots[b] : b, pos[r] = t;
         last[b] = r - 1;
     }
     if (!c->pf_last) CK(c, cudaMalloc(&c->pf_last, kMaxBatch * 4));
@@ -892,7 +903,7 @@ static int run_prefill(q3i8_ctx* c, int B, const int32_t* d_ids, const int32_t* 
     const bool tc_attn = attn_prefill_supported(nh, nkv, hd);
     if (tc_attn) {
         std::vector<int4> blk(c->pf_blocks_cap);
-        nblk = attn_prefill_blocks(lens, B, blk.data(), c->pf_blocks_cap);
+        nblk = attn_prefill_blocks(lens, B, blk.data(), c->pf_blocks_cap, slots);
         if (nblk > c->pf_blocks_cap) return fail(c, Q3_ERR_STATE, "prefill: query block table too small");
         CK(c, cudaMemcpyAsync(c->pf_blocks, blk.data(), (size_t)nblk * sizeof(int4), cudaMemcpyHostToDevice, st));
         CK(c, cudaStreamSynchronize(st));  // blk is a host temporary
@@ -1192,6 +1203,151 @@ extern "C" int q3i8_step_logits(q3i8_ctx* c, const int32_t* tokens, float* logit
     int rc = check_status(c);
     if (rc) return rc;
     for (int b = 0; b < B; ++b) c->seq_len[b] += 1;
+    return Q3_OK;
+}
+
+// ------------------------------------------------------------------ continuous batching
+
+// Sequence ids of the decode rows back to 0 .. max_batch - 1 (the plain
+// calls' layout) after continuous-batching steps pointed them at slots.
+static int restore_seq_ids(q3i8_ctx* c) {
+    if (!c->seq_ids_custom) return Q3_OK;
+    std::vector<int32_t> ids(c->bmax);
+    for (int b = 0; b < c->bmax; ++b) ids[b] = b;
+    CK(c, cudaMemcpyAsync(c->seq_ids, ids.data(), c->bmax * 4, cudaMemcpyHostToDevice, c->stream));
+    CK(c, cudaStreamSynchronize(c->stream));  // ids is a host temporary
+    c->seq_ids_custom = false;
+    return Q3_OK;
+}
+
+extern "C" int q3i8_cb_reserve(q3i8_ctx* c, int32_t max_ctx) {
+    if (!c) return fail(nullptr, Q3_ERR_INVALID_ARGUMENTS, "ctx is NULL");
+    if (max_ctx < 1) return fail(c, Q3_ERR_INVALID_ARGUMENTS, "cb_reserve: max_ctx < 1");
+    int rc = ensure_capacity(c, max_ctx);
+    if (rc) return rc;
+    return ensure_out(c, 256);
+}
+
+extern "C" int q3i8_cb_prefill(q3i8_ctx* c, int32_t n, const int32_t* slots, const int32_t* const* prompt_ids,
+                               const int32_t* prompt_lens, int32_t* first_tokens) {
+    if (!c) return fail(nullptr, Q3_ERR_INVALID_ARGUMENTS, "ctx is NULL");
+    if (n < 1 || n > c->bmax) return fail(c, Q3_ERR_INVALID_ARGUMENTS, "cb_prefill: n=%d outside [1, %d]", n, c->bmax);
+    if (!slots || !prompt_ids || !prompt_lens || !first_tokens)
+        return fail(c, Q3_ERR_INVALID_ARGUMENTS, "cb_prefill: NULL argument");
+    if (!c->kc) return fail(c, Q3_ERR_STATE, "cb_prefill before q3i8_cb_reserve");
+    std::vector<char> used(c->bmax, 0);
+    std::vector<int32_t> all;
+    for (int b = 0; b < n; ++b) {
+        if (slots[b] < 0 || slots[b] >= c->bmax || used[slots[b]])
+            return fail(c, Q3_ERR_INVALID_ARGUMENTS, "cb_prefill: slot %d invalid or repeated", slots[b]);
+        used[slots[b]] = 1;
+        if (!prompt_ids[b] || prompt_lens[b] < 1)
+            return fail(c, Q3_ERR_INVALID_ARGUMENTS, "cb_prefill: prompt %d is NULL or empty", b);
+        if (prompt_lens[b] > c->cap)
+            return fail(c, Q3_ERR_CONTEXT, "cb_prefill: prompt %d (%d) exceeds the reserved %d positions", b,
+                        prompt_lens[b], c->cap);
+        for (int t = 0; t < prompt_lens[b]; ++t) {
+            const int32_t id = prompt_ids[b][t];
+            if (id < 0 || id >= c->d.vocab)
+                return fail(c, Q3_ERR_INVALID_ARGUMENTS, "cb_prefill: prompt %d position %d: id %d outside [0, %d)",
+                            b, t, id, c->d.vocab);
+            all.push_back(id);
+        }
+    }
+    int rc = ensure_prefill(c, (int)all.size());
+    if (rc) return rc;
+    CK(c, cudaMemcpyAsync(c->pf_ids, all.data(), all.size() * 4, cudaMemcpyHostToDevice, c->stream));
+    if ((rc = run_prefill(c, n, c->pf_ids, prompt_lens, nullptr, slots))) return rc;
+    c->active_B = 0;  // the step-by-step interface has no session after this
+    CK(c, cudaMemcpyAsync(first_tokens, c->tokens, n * 4, cudaMemcpyDeviceToHost, c->stream));
+    return check_status(c);
+}
+
+extern "C" int q3i8_cb_step(q3i8_ctx* c, int32_t n, const int32_t* row_slot, const int32_t* row_pos,
+                            const int32_t* row_token, int32_t* next_tokens) {
+    if (!c) return fail(nullptr, Q3_ERR_INVALID_ARGUMENTS, "ctx is NULL");
+    if (n < 1 || n > c->bmax) return fail(c, Q3_ERR_INVALID_ARGUMENTS, "cb_step: n=%d outside [1, %d]", n, c->bmax);
+    if (!row_slot || !row_pos || !row_token || !next_tokens)
+        return fail(c, Q3_ERR_INVALID_ARGUMENTS, "cb_step: NULL argument");
+    if (!c->kc) return fail(c, Q3_ERR_STATE, "cb_step before q3i8_cb_reserve");
+    std::vector<char> used(c->bmax, 0);
+    int top = 0;
+    for (int r = 0; r < n; ++r) {
+        if (row_slot[r] < 0 || row_slot[r] >= c->bmax || used[row_slot[r]])
+            return fail(c, Q3_ERR_INVALID_ARGUMENTS, "cb_step: slot %d invalid or repeated", row_slot[r]);
+        used[row_slot[r]] = 1;
+        if (row_pos[r] < 1 || row_pos[r] >= c->cap)
+            return fail(c, Q3_ERR_CONTEXT, "cb_step: row %d position %d outside [1, %d)", r, row_pos[r], c->cap);
+        if (row_token[r] < 0 || row_token[r] >= c->d.vocab)
+            return fail(c, Q3_ERR_INVALID_ARGUMENTS, "cb_step: row %d token %d outside [0, %d)", r, row_token[r],
+                        c->d.vocab);
+        top = std::max(top, row_pos[r] + 1);
+    }
+    int rc = ensure_events(c);
+    if (rc) return rc;
+    c->call_ctx = top;
+    c->seq_ids_custom = true;
+    cudaStream_t st = c->stream;
+    CK(c, cudaMemcpyAsync(c->tokens, row_token, n * 4, cudaMemcpyHostToDevice, st));
+    CK(c, cudaMemcpyAsync(c->pos, row_pos, n * 4, cudaMemcpyHostToDevice, st));
+    CK(c, cudaMemcpyAsync(c->seq_ids, row_slot, n * 4, cudaMemcpyHostToDevice, st));
+    cudaGraphExec_t g;
+    if ((rc = get_graph(c, n, &g))) return rc;
+    CK(c, cudaGraphLaunch(g, st));
+    c->launches += step_launches(c, n);
+    CK(c, cudaMemcpyAsync(next_tokens, c->tokens, n * 4, cudaMemcpyDeviceToHost, st));
+    return check_status(c);
+}
+
+extern "C" int q3i8_sched_run(q3i8_ctx* c, q3i8_sched* s, q3i8_stats* stats) {
+    if (!c) return fail(nullptr, Q3_ERR_INVALID_ARGUMENTS, "ctx is NULL");
+    if (!s) return fail(c, Q3_ERR_INVALID_ARGUMENTS, "sched_run: scheduler is NULL");
+    if (q3_sched_slots(s) > c->bmax)
+        return fail(c, Q3_ERR_INVALID_ARGUMENTS, "sched_run: %d slots exceed max_batch %d", q3_sched_slots(s), c->bmax);
+    int rc = q3i8_cb_reserve(c, q3_sched_max_ctx(s));
+    if (rc) return rc;
+    const int nb = c->bmax;
+    std::vector<int32_t> a_req(nb), a_slot(nb), r_req(nb), r_slot(nb), r_pos(nb), r_tok(nb), out(nb), lens(nb);
+    std::vector<const int32_t*> ptrs(nb);
+    int64_t prefill_tokens = 0, steps = 0, step_rows = 0;
+    double prefill_ms = 0, decode_ms = 0;
+    auto now_ms = [] { return std::chrono::duration<double, std::milli>(std::chrono::steady_clock::now().time_since_epoch()).count(); };
+    while (!q3i8_sched_idle(s)) {
+        int32_t na = 0, nr = 0;
+        if ((rc = q3i8_sched_plan(s, &na, a_req.data(), a_slot.data(), &nr, r_req.data(), r_slot.data(), r_pos.data(),
+                                  r_tok.data())))
+            return fail(c, rc, "sched_run: %s", q3i8_last_error(nullptr));
+        if (na > 0) {
+            for (int i = 0; i < na; ++i) {
+                int32_t len = 0;
+                ptrs[i] = q3_sched_prompt(s, a_req[i], &len);
+                lens[i] = len;
+                prefill_tokens += len;
+            }
+            const double t0 = now_ms();
+            if ((rc = q3i8_cb_prefill(c, na, a_slot.data(), ptrs.data(), lens.data(), out.data()))) return rc;
+            prefill_ms += now_ms() - t0;
+            if ((rc = q3i8_sched_complete_prefill(s, na, a_req.data(), out.data())))
+                return fail(c, rc, "sched_run: %s", q3i8_last_error(nullptr));
+        }
+        if (nr > 0) {
+            const double t0 = now_ms();
+            if ((rc = q3i8_cb_step(c, nr, r_slot.data(), r_pos.data(), r_tok.data(), out.data()))) return rc;
+            decode_ms += now_ms() - t0;
+            ++steps, step_rows += nr;
+            if ((rc = q3i8_sched_complete_step(s, nr, out.data())))
+                return fail(c, rc, "sched_run: %s", q3i8_last_error(nullptr));
+        }
+        if (na == 0 && nr == 0) return fail(c, Q3_ERR_STATE, "sched_run: the scheduler planned no work");
+    }
+    if (stats) {
+        *stats = q3i8_stats{};
+        stats->prefill_ms = prefill_ms, stats->decode_ms = decode_ms;
+        stats->prefill_tokens = prefill_tokens, stats->decode_steps = steps;
+        stats->prefill_tokens_per_sec = prefill_ms > 0 ? prefill_tokens / (prefill_ms * 1e-3) : 0;
+        stats->decode_tokens_per_sec = decode_ms > 0 ? step_rows / (decode_ms * 1e-3) : 0;
+        stats->step_us = steps > 0 ? decode_ms * 1e3 / steps : 0;
+    }
     return Q3_OK;
 }
 

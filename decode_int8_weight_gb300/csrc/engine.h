@@ -94,6 +94,7 @@ struct q3i8_ctx {
     long long *xa = nullptr, *xf = nullptr;  // residual stream accumulators [2][bmax][H], value * 2^32
 
     // seeded sampling (sample.cu), allocated by the first sampling call
+    bool seq_ids_custom = false;           // continuous-batching steps pointed the decode rows at other slots
     bool sampling = false;                 // the running call samples instead of taking the argmax
     q3::SampleParams* s_params = nullptr;  // device copy of the call's settings
     int32_t* s_counts = nullptr;           // [bmax][vocab] occurrences of each token per sequence

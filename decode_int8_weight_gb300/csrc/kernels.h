@@ -114,7 +114,8 @@ int launch_attention_decode(const float* qkv, const float* q_norm, const float* 
 // (returns the count; writes at most cap_blocks).  Output: hi/lo f16 planes
 // outh[(2r + part) * ldh + head * hd + d].
 bool attn_prefill_supported(int nh, int nkv, int hd);
-int attn_prefill_blocks(const int32_t* lens, int B, int4* out, int cap_blocks);
+// slots: the KV cache sequence of prompt b (NULL: b itself).
+int attn_prefill_blocks(const int32_t* lens, int B, int4* out, int cap_blocks, const int32_t* slots = nullptr);
 int launch_attn_prefill(const float* q, const __nv_bfloat16* kc, const __nv_bfloat16* vc, const int4* blocks,
                         int nblocks, int nh, int nkv, int hd, int cap, __half* outh, int ldh, cudaStream_t st);
 

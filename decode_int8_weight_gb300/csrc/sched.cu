@@ -58,6 +58,19 @@ struct q3i8_sched {
     }
 };
 
+// Accessors for the device serving loop (engine.cu).
+int q3_sched_slots(const q3i8_sched* s) { return s->max_batch; }
+int q3_sched_max_ctx(const q3i8_sched* s) { return s->max_ctx; }
+const int32_t* q3_sched_prompt(const q3i8_sched* s, int request_id, int32_t* len) {
+    if (request_id < 0 || request_id >= (int)s->reqs.size()) {
+        *len = 0;
+        return nullptr;
+    }
+    const Req& r = s->reqs[request_id];
+    *len = (int32_t)r.prompt.size();
+    return r.prompt.data();
+}
+
 extern "C" int q3i8_sched_new(int32_t max_batch, int32_t max_ctx, q3i8_sched** out) {
     if (!out) return report(Q3_ERR_INVALID_ARGUMENTS, "sched_new: NULL out");
     if (max_batch < 1 || max_ctx < 2)

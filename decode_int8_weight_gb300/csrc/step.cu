@@ -321,7 +321,7 @@ __host__ __device__ inline AttnBlockLayout attn_block_layout(int H, int hd, int 
         L.qn = take_smem(w, (size_t)kStepMaxBatch * hd * 4);
         L.kn = take_smem(w, (size_t)kStepMaxBatch * hd * 4);
         L.vn = take_smem(w, (size_t)kStepMaxBatch * hd * 4);
-        L.wst = take_smem(w, (size_t)kWarps * kStepMaxBatch * hd * 4);  // warp states, then the parked parts
+        L.wst = take_smem(w, (size_t)kWarps * kStepMaxBatch * (hd + 4) * 4);  // warp states, then the parked parts
         L.part = take_smem(w, (size_t)kStepMaxBatch * (hd + 4) * 4);    // 16-byte aligned states
         L.oop = take_smem(w, (size_t)(hd / 32) * 512);
         const size_t wq_bytes = (size_t)T * nkp * 512;
@@ -691,37 +691,36 @@ __global__ void __launch_bounds__(kThreads, 2) attn_block_kernel(const AttnBlock
             for (int d = 0; d < D; ++d) acc[d] = acc[d] * corr + pe * vn[b * HD + lane * D + d];
             m = mn;
         }
-        // merge the 8 warps' states into this CTA's state for sequence b
-        float* ws = wst + warp * PS;
+        // park this warp's state for sequence b (merged once for every sequence below)
+        float* ws = wst + (b * kWarps + warp) * PS;
         if (lane == 0) ws[HD] = m, ws[HD + 1] = l;
 #pragma unroll
         for (int d = 0; d < D; ++d) ws[lane * D + d] = acc[d];
-        __syncthreads();
-        // every thread derives the 8 warps' weights from their (m, l) in the
-        // same order; thread d then sums its element
-        {
-            float mw[kWarps], f[kWarps];
-            float M = -INFINITY;
-#pragma unroll
-            for (int w = 0; w < kWarps; ++w) mw[w] = wst[w * PS + HD], M = fmaxf(M, mw[w]);
-            float Ls = 0.f;
-#pragma unroll
-            for (int w = 0; w < kWarps; ++w) {
-                f[w] = (mw[w] == -INFINITY) ? 0.f : expf(mw[w] - M);
-                Ls += wst[w * PS + HD + 1] * f[w];
-            }
-            float* pb = part + b * PS;
-            #pragma unroll 1
-            for (int d = tid; d < HD; d += kThreads) {
-                float A = 0.f;
-#pragma unroll
-                for (int w = 0; w < kWarps; ++w) A += wst[w * PS + d] * f[w];
-                pb[d] = A;
-            }
-            if (tid == 0) pb[HD] = M, pb[HD + 1] = Ls;
-        }
-        __syncthreads();
     }
+    __syncthreads();
+    // merge the 8 warps' states of each sequence into this CTA's state: the
+    // thread of element (b, d) derives the warps' weights from their (m, l)
+    // in warp order and sums its element
+#pragma unroll 1
+    for (int i = tid; i < B * HD; i += kThreads) {
+        const int b = i / HD, d = i - b * HD;
+        const float* wb = wst + b * kWarps * PS;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) M = fmaxf(M, wb[w * PS + HD]);
+        float Ls = 0.f, A = 0.f;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) {
+            const float mw = wb[w * PS + HD];
+            const float f = (mw == -INFINITY) ? 0.f : expf(mw - M);
+            Ls += wb[w * PS + HD + 1] * f;
+            A += wb[w * PS + d] * f;
+        }
+        float* pb = part + b * PS;
+        pb[d] = A;
+        if (d == 0) pb[HD] = M, pb[HD + 1] = Ls;
+    }
+    __syncthreads();
 
     // ---- 4. merge the cluster's states; this CTA's rows of Wo[:, head h]
     cluster_arrive();

@@ -30,7 +30,7 @@
  * Groups of calls: the decode context (q3i8_init .. q3i8_destroy); single
  * kernels on caller memory for isolated checks (q3i8_op_*); the quantized
  * load cache (q3i8_cache_*, host only); the continuous-batching scheduler
- * (q3i8_sched_*, host only).
+ * (q3i8_sched_*) and its device loop (q3i8_cb_*, q3i8_sched_run).
  */
 #ifndef Q3I8_H
 #define Q3I8_H
@@ -452,6 +452,38 @@ int q3i8_sched_complete_prefill(q3i8_sched* sched, int32_t n, const int32_t* req
 
 /* Report the next token of each row of the last plan, in row order. */
 int q3i8_sched_complete_step(q3i8_sched* sched, int32_t n_rows, const int32_t* tokens);
+
+/* ---- the same loop on the device.  Slots are the context's KV sequences
+ * 0 .. max_batch - 1; the calls below keep every other slot's cache. */
+
+/* Size the KV cache for max_ctx positions per slot (growing it reallocates
+ * the cache: every slot's contents are lost, so reserve before serving). */
+int q3i8_cb_reserve(q3i8_ctx* ctx, int32_t max_ctx);
+
+/* Prefill n prompts (HOST ids) into the distinct slots[0..n) and write each
+ * one's greedy first token to first_tokens[n] (HOST).  Errors: a slot out of
+ * range or repeated, an empty or NULL prompt, an id outside the vocabulary
+ * (Q3_ERR_INVALID_ARGUMENTS); a prompt longer than the reserved positions
+ * (Q3_ERR_CONTEXT); no reserve yet (Q3_ERR_STATE). */
+int q3i8_cb_prefill(q3i8_ctx* ctx, int32_t n, const int32_t* slots, const int32_t* const* prompt_ids,
+                    const int32_t* prompt_lens, int32_t* first_tokens);
+
+/* One decode step over n rows (HOST arrays): row r appends row_token[r] at
+ * position row_pos[r] (>= 1) of slot row_slot[r] (distinct slots), attends
+ * positions 0 .. row_pos[r] of that slot and writes the greedy next token to
+ * next_tokens[r].  One replay of the step graph at batch n; the rows' slots
+ * and positions are device inputs of the graph, so any mix of slots and
+ * positions shares it. */
+int q3i8_cb_step(q3i8_ctx* ctx, int32_t n, const int32_t* row_slot, const int32_t* row_pos,
+                 const int32_t* row_token, int32_t* next_tokens);
+
+/* Drive a scheduler to idle on the device: each round plans, prefills the
+ * admissions into their slots, reports their first tokens, runs one step
+ * over the plan's rows and reports their next tokens.  Reserves the cache
+ * for the scheduler's max_ctx first; its max_batch must not exceed the
+ * context's.  stats (optional): host wall time of the prefill and step
+ * calls, prompt tokens, steps, and rows per second of decode. */
+int q3i8_sched_run(q3i8_ctx* ctx, q3i8_sched* sched, q3i8_stats* stats);
 
 /* 1 when nothing is queued, in flight or awaiting a report. */
 int32_t q3i8_sched_idle(const q3i8_sched* sched);
