@@ -35,17 +35,21 @@ sys.path.insert(0, ROOT)
 import synth  # noqa: E402
 
 # DRAM bytes (read + write) of one decode step (the graph's kernels summed),
-# from an ncu capture (profiles/chained_step_0.6b-b1-p32-n128.md).  A figure
-# holds only for the sources it was taken on, identified by
-# kernel_source_id(); for any other build the roofline reports null.
-NCU_TRAFFIC = {("9b15dfeafefa21de", "0.6b-b1-p32-n128", 1): 615_639_808}
+# from an ncu launch list of the bench workload (the decode-step summary
+# under profiles/).  A figure holds only for the sources it was taken on,
+# identified by kernel_source_id(); for any other build the roofline
+# reports null.
+NCU_TRAFFIC = {("cf8d6f0242b78085", "0.6b-b1-p32-n128", 1): 608_977_664}
 
 
 def kernel_source_id() -> str:
+    """Hash of every CUDA source and header of the library."""
     h = hashlib.sha256()
-    for f in ("kernels.cu", "kernels.h", "common.cuh", "engine.cu"):
-        with open(os.path.join(ROOT, "decode_int8_weight_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+    csrc = os.path.join(ROOT, "decode_int8_weight_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, f), "rb") as fh:
+                h.update(f.encode() + b"\0" + fh.read())
     return h.hexdigest()[:16]
 
 
