@@ -37,7 +37,8 @@ STATUS = {0: "ok", 1: "unsupported_architecture", 2: "invalid_arguments", 3: "co
 
 EXPORTS = ["q3i8_validate_dims", "q3i8_init", "q3i8_decode", "q3i8_decode_sample", "q3i8_decode_device", "q3i8_prefill",
            "q3i8_step_logits", "q3i8_read_kv", "q3i8_step_bytes", "q3i8_step_launches", "q3i8_launch_count", "q3i8_last_error",
-           "q3i8_status_name", "q3i8_destroy", "q3i8_trace_step", "q3i8_op_gemm_i8", "q3i8_op_attention_workspace", "q3i8_op_attention",
+           "q3i8_status_name", "q3i8_destroy", "q3i8_trace_step", "q3i8_op_gemm_i8", "q3i8_op_gemm_i8_splitk_workspace",
+           "q3i8_op_gemm_i8_splitk", "q3i8_op_attention_workspace", "q3i8_op_attention",
            "q3i8_op_attention_static", "q3i8_op_sample_workspace", "q3i8_op_sample", "q3i8_op_wait_probe",
            "q3i8_cache_payload_bytes", "q3i8_cache_write",
            "q3i8_cache_open", "q3i8_cache_tables", "q3i8_cache_close", "q3i8_sched_new", "q3i8_sched_destroy",
@@ -135,6 +136,9 @@ def lib():
             L.q3i8_destroy.argtypes = [vp]
             L.q3i8_trace_step.argtypes = [vp, vp, vp, sz, ctypes.POINTER(i32), ctypes.POINTER(i32)]
             L.q3i8_op_gemm_i8.argtypes = [vp, vp, vp, i32, i32, i32, vp, vp, vp]
+            L.q3i8_op_gemm_i8_splitk_workspace.restype = sz
+            L.q3i8_op_gemm_i8_splitk_workspace.argtypes = [i32, i32, i32]
+            L.q3i8_op_gemm_i8_splitk.argtypes = [vp, vp, vp, i32, i32, i32, vp, vp, sz, vp, vp]
             L.q3i8_op_attention_workspace.restype = sz
             L.q3i8_op_attention_workspace.argtypes = [i32, i32, i32, i32]
             L.q3i8_op_attention.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, vp, vp, sz, vp, vp]
@@ -359,6 +363,22 @@ def op_gemm_i8(a_planes, w, scale, y, status=None, stream=None):
     assert K2 == 2 * K
     rc = lib().q3i8_op_gemm_i8(_tptr(a_planes), _tptr(w), _tptr(scale), M, N, K, _tptr(y), _tptr(status),
                                ctypes.c_void_p(stream) if stream else None)
+    _check(rc, None)
+
+
+def op_gemm_i8_splitk_workspace(M: int, N: int, K: int) -> int:
+    return int(lib().q3i8_op_gemm_i8_splitk_workspace(M, N, K))
+
+
+def op_gemm_i8_splitk(a_planes, w, scale, y, workspace=None, status=None, stream=None):
+    """op_gemm_i8 with K split over CTAs when the shape calls for it (see q3i8_op_gemm_i8_splitk); workspace: a
+    torch CUDA tensor of at least op_gemm_i8_splitk_workspace(M, N, K) bytes, or None when that is 0."""
+    M, K2 = a_planes.shape
+    N, K = w.shape
+    assert K2 == 2 * K
+    nbytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    rc = lib().q3i8_op_gemm_i8_splitk(_tptr(a_planes), _tptr(w), _tptr(scale), M, N, K, _tptr(y), _tptr(workspace),
+                                      nbytes, _tptr(status), ctypes.c_void_p(stream) if stream else None)
     _check(rc, None)
 
 

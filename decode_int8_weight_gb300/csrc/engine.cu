@@ -424,7 +424,7 @@ extern "C" void q3i8_destroy(q3i8_ctx* c) {
                     c->out_ids, c->pf_x, c->pf_qkv, c->pf_q, c->pf_xh, c->pf_oh, c->pf_ah, c->pf_blocks,
                     c->pf_part, c->pf_ids, c->pf_seq, c->pf_pos, c->pf_last, c->d_mats, c->d_gains,
                     c->p_epoch, c->p_keys, c->p_exit, c->p_attn_cnt, c->p_abort, c->p_diag, c->p_ll, c->p_part, c->p_trace,
-                    c->xa, c->xf, c->s_params, c->s_counts, c->s_band_key, c->s_band_tok};
+                    c->xa, c->xf, c->s_params, c->s_counts, c->s_band_key, c->s_band_tok, c->pf_work};
     for (void* p : ptrs) cudaFree(p);
     if (c->ev0) cudaEventDestroy(c->ev0);
     if (c->ev1) cudaEventDestroy(c->ev1);
@@ -754,7 +754,10 @@ int step_launches(const q3i8_ctx* c, int B) {
 int prefill_launches(const q3i8_ctx* c, int M) {
     const q3i8_dims& d = c->d;
     const int chunks = (M + kPrefillChunk - 1) / kPrefillChunk;
-    auto per = [&](int N, int K) { return M > kPrefillChunk && tc_gemm_supported(N, K) ? 1 : chunks; };
+    auto per = [&](int N, int K) {
+        if (M > kPrefillChunk && tc_gemm_supported(N, K)) return tc_gemm_splits(M, N, K, c->num_sms) > 1 ? 2 : 1;
+        return chunks;
+    };
     const int H = d.hidden, I = d.intermediate, Dq = d.n_heads * d.head_dim, Dkv = d.n_kv_heads * d.head_dim;
     const int proj = per(Dq + 2 * Dkv, H) + per(H, Dq) + per(2 * I, H) + per(H, I);
     const int attn = attn_prefill_supported(d.n_heads, d.n_kv_heads, d.head_dim) ? 1 : 2;
@@ -877,13 +880,26 @@ static int run_prefill(q3i8_ctx* c, int B, const int32_t* d_ids, const int32_t* 
     CK(c, cudaMemsetAsync(c->status, 0, 4, st));
     const size_t layer_kv = (size_t)c->bmax * nkv * c->cap * hd;
 
+    // split-K workspace of the tensor-core projections (short prompts on few output tiles)
+    if (M > kPrefillChunk) {
+        size_t need = 0;
+        const int shapes[4][2] = {{Dq + 2 * Dkv, H}, {H, Dq}, {2 * I, H}, {H, I}};
+        for (const auto& sh : shapes) need = std::max(need, tc_gemm_work_bytes(M, sh[0], sh[1], c->num_sms));
+        if (need > c->pf_work_bytes) {
+            cudaFree(c->pf_work);
+            c->pf_work = nullptr, c->pf_work_bytes = 0;
+            CK(c, cudaMalloc(&c->pf_work, need));
+            c->pf_work_bytes = need;
+        }
+    }
     // One projection over all prompt rows: the tcgen05 GEMM when there is
     // more than one chunk of rows, else the decode GEMV (one weight sweep per
     // chunk of up to kPrefillChunk rows).
     int tc_rc = 0;
     auto project = [&](const DevMat& W, int K, const __half* xh, int mode, float* y, int ldy, __half* yh, int ldyh) {
         if (M > kPrefillChunk && W.raw && tc_gemm_supported(W.rows, K)) {
-            const int rc = launch_tc_gemm(xh, W.raw, W.scale, M, W.rows, K, mode, y, ldy, yh, ldyh, c->status, st);
+            const int rc = launch_tc_gemm(xh, W.raw, W.scale, M, W.rows, K, mode, y, ldy, yh, ldyh, c->status, st,
+                                          c->pf_work, c->pf_work_bytes, c->num_sms);
             if (rc == 0) return;
             tc_rc = rc;
         }
@@ -1444,6 +1460,37 @@ extern "C" int q3i8_op_gemm_i8(const uint16_t* a_planes, const int8_t* w, const 
     if (rc) return fail(nullptr, Q3_ERR_CUDA, "op_gemm_i8: tensor-core GEMM could not be set up (%d)", rc);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return fail(nullptr, Q3_ERR_CUDA, "op_gemm_i8 launch: %s", cudaGetErrorString(e));
+    return Q3_OK;
+}
+
+static int current_sms() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return 0;
+    return n;
+}
+
+extern "C" size_t q3i8_op_gemm_i8_splitk_workspace(int32_t M, int32_t N, int32_t K) {
+    if (M < 1 || !tc_gemm_supported(N, K)) return 0;
+    return tc_gemm_work_bytes(M, N, K, current_sms());
+}
+
+extern "C" int q3i8_op_gemm_i8_splitk(const uint16_t* a_planes, const int8_t* w, const float* scale, int32_t M,
+                                      int32_t N, int32_t K, float* y, void* workspace, size_t ws_bytes,
+                                      int32_t* d_status, void* cuda_stream) {
+    if (!a_planes || !w || !scale || !y) return fail(nullptr, Q3_ERR_INVALID_ARGUMENTS, "op_gemm_i8_splitk: NULL pointer");
+    if (M < 1 || !tc_gemm_supported(N, K))
+        return fail(nullptr, Q3_ERR_INVALID_ARGUMENTS, "op_gemm_i8_splitk: needs M >= 1, N %% 128 == 0, K %% 64 == 0");
+    if (((uintptr_t)a_planes & 15) || ((uintptr_t)w & 15) || ((uintptr_t)y & 15) || ((uintptr_t)workspace & 15))
+        return fail(nullptr, Q3_ERR_INVALID_ARGUMENTS, "op_gemm_i8_splitk: buffers must be 16-byte aligned");
+    const int sms = current_sms();
+    if (ws_bytes < tc_gemm_work_bytes(M, N, K, sms) || (!workspace && tc_gemm_work_bytes(M, N, K, sms)))
+        return fail(nullptr, Q3_ERR_INVALID_ARGUMENTS, "op_gemm_i8_splitk: workspace too small");
+    const int rc = launch_tc_gemm(reinterpret_cast<const __half*>(a_planes), w, scale, M, N, K, kStore, y, N, nullptr,
+                                  0, d_status, (cudaStream_t)cuda_stream, (float*)workspace, ws_bytes, sms);
+    if (rc) return fail(nullptr, Q3_ERR_CUDA, "op_gemm_i8_splitk: tensor-core GEMM could not be set up (%d)", rc);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(nullptr, Q3_ERR_CUDA, "op_gemm_i8_splitk launch: %s", cudaGetErrorString(e));
     return Q3_OK;
 }
 

@@ -68,6 +68,8 @@ struct q3i8_ctx {
     int4* pf_blocks = nullptr;  // query blocks of the tensor-core prefill attention
     int pf_blocks_cap = 0;
     int32_t *pf_ids = nullptr, *pf_seq = nullptr, *pf_pos = nullptr, *pf_last = nullptr;
+    float* pf_work = nullptr;  // split-K partial sums of the prefill projections
+    size_t pf_work_bytes = 0;
 
     // persistent decode step (one cooperative kernel per step)
     bool use_persistent = false;

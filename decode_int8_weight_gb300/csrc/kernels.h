@@ -127,6 +127,12 @@ int launch_attn_prefill(const float* q, const __nv_bfloat16* kc, const __nv_bflo
 // Returns 0 when launched, < 0 when the arguments do not fit.
 bool tc_gemm_supported(int N, int K);
 int launch_tc_gemm(const __half* a_planes, const int8_t* w, const float* scale, int M, int N, int K, int mode,
-                   float* y, int ldy, __half* yh, int ldyh, int32_t* status, cudaStream_t st);
+                   float* y, int ldy, __half* yh, int ldyh, int32_t* status, cudaStream_t st, float* work = nullptr,
+                   size_t work_bytes = 0, int num_sms = 0);
+// K splits launch_tc_gemm uses for this shape on num_sms SMs (1: none), and
+// the fp32 workspace they need (0 when none); a split GEMM is two launches
+// (the GEMM and the ordered reduction).
+int tc_gemm_splits(int M, int N, int K, int num_sms);
+size_t tc_gemm_work_bytes(int M, int N, int K, int num_sms);
 
 }  // namespace q3

@@ -11,7 +11,7 @@
 // One CTA computes a 128 x 128 output tile:
 //   warp 0     TMA producer: per stage, the hi and lo activation tiles
 //              (128 x 64 f16, 128-byte swizzle) and the int8 weight tile
-//              (128 x 64 bytes) into a 3-stage ring;
+//              (128 x 64 bytes) into a 4-stage ring;
 //   warp 1     allocates 128 TMEM columns; one thread issues the MMAs
 //              (M = 128, N = 128, K = 16 each) and commits each stage back
 //              to the producer;
@@ -31,7 +31,7 @@ namespace q3 {
 namespace {
 
 constexpr int kBM = 128, kBN = 128, kBK = 64;
-constexpr int kStages = 3;
+constexpr int kStages = 4;
 constexpr int kTcThreads = 192;
 constexpr uint32_t kATile = kBM * kBK * 2;     // 16 KB f16, one of hi / lo
 constexpr uint32_t kB16Tile = kBN * kBK * 2;   // 16 KB f16 weights (converted)
@@ -48,7 +48,43 @@ struct TcArgs {
     __half* yh;
     int ldyh;
     int32_t* status;
+    int splits;    // K split over gridDim.z CTAs (1: the CTA finishes its tile itself)
+    float* part;   // splits > 1: [splits][M][N] fp32 partial sums, unscaled
 };
+
+// The output epilogue of 16 consecutive columns n .. n + 15 of row m, from
+// their scaled fp32 values: store, add to the residual, or (a 16-row group
+// of the fused gate/up matrix: 8 gate rows, then the 8 up rows of the same
+// units) SiLU-gate into hi/lo planes.
+Q3_DEV void epilogue16(const TcArgs& g, int m, int n, const float (&v)[16]) {
+    if (g.mode == kSiluGate) {
+        const int u0 = n >> 1;
+        uint32_t hw[4], lw[4];
+#pragma unroll
+        for (int i = 0; i < 8; i += 2) {
+            const float a0 = (v[i] / (1.0f + expf(-v[i]))) * v[8 + i];
+            const float a1 = (v[i + 1] / (1.0f + expf(-v[i + 1]))) * v[9 + i];
+            __half h0, l0, h1, l1;
+            split_f16(a0, h0, l0);
+            split_f16(a1, h1, l1);
+            hw[i / 2] = (uint32_t)__half_as_ushort(h0) | ((uint32_t)__half_as_ushort(h1) << 16);
+            lw[i / 2] = (uint32_t)__half_as_ushort(l0) | ((uint32_t)__half_as_ushort(l1) << 16);
+        }
+        *reinterpret_cast<uint4*>(g.yh + (size_t)(2 * m) * g.ldyh + u0) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+        *reinterpret_cast<uint4*>(g.yh + (size_t)(2 * m + 1) * g.ldyh + u0) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+    } else {
+        float4* dst = reinterpret_cast<float4*>(g.y + (size_t)m * g.ldy + n);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            float4 o = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+            if (g.mode == kResid) {
+                const float4 p = dst[i];
+                o.x += p.x, o.y += p.y, o.z += p.z, o.w += p.w;
+            }
+            dst[i] = o;
+        }
+    }
+}
 
 // ------------------------------------------------------------------ PTX wrappers
 Q3_DEV void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
@@ -135,7 +171,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n0 = blockIdx.x * kBN, m0 = blockIdx.y * kBM;
-    const int NK = g.K / kBK;
+    // this CTA's k-tiles [kt0, kt0 + NK) of the K / kBK
+    const int KT = g.K / kBK, kt0 = (int)blockIdx.z * KT / g.splits;
+    const int NK = ((int)blockIdx.z + 1) * KT / g.splits - kt0;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
@@ -164,9 +202,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 if (kt >= kStages && !wait_or_flag(&empty[s], ((kt / kStages) - 1) & 1, g.status, abort_sm)) break;
                 const uint32_t st = base + s * kStageBytes;
                 mbar_arrive_expect_tx(&full[s], kTxBytes);
-                tma_load_2d(st, &tmA, kt * kBK, m0, smem_u32(&full[s]));                 // hi
-                tma_load_2d(st + kATile, &tmA, g.K + kt * kBK, m0, smem_u32(&full[s]));  // lo
-                tma_load_2d(st + 2 * kATile + kB16Tile, &tmB, kt * kBK, n0, smem_u32(&full[s]));
+                const int kx = (kt0 + kt) * kBK;
+                tma_load_2d(st, &tmA, kx, m0, smem_u32(&full[s]));                 // hi
+                tma_load_2d(st + kATile, &tmA, g.K + kx, m0, smem_u32(&full[s]));  // lo
+                tma_load_2d(st + 2 * kATile + kB16Tile, &tmB, kx, n0, smem_u32(&full[s]));
                 issued = kt + 1;
             }
             // every copy this thread started has landed before the CTA can end
@@ -230,37 +269,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 if (m >= g.M) continue;
                 const int n = n0 + c;
                 float v[16];
+                if (g.splits > 1) {
+                    // unscaled partial sums; the reduction scales and finishes them
+                    float4* dst = reinterpret_cast<float4*>(g.part + ((size_t)blockIdx.z * g.M + m) * g.N + n);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        dst[i] = make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]),
+                                             __uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3]));
+                    continue;
+                }
 #pragma unroll
                 for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]) * __ldg(g.scale + n + i);
-                if (g.mode == kSiluGate) {
-                    // a 16-row group of the fused matrix: 8 gate rows, then the 8 up rows of the same units
-                    const int u0 = n >> 1;
-                    uint32_t hw[4], lw[4];
-#pragma unroll
-                    for (int i = 0; i < 8; i += 2) {
-                        const float a0 = (v[i] / (1.0f + expf(-v[i]))) * v[8 + i];
-                        const float a1 = (v[i + 1] / (1.0f + expf(-v[i + 1]))) * v[9 + i];
-                        __half h0, l0, h1, l1;
-                        split_f16(a0, h0, l0);
-                        split_f16(a1, h1, l1);
-                        hw[i / 2] = (uint32_t)__half_as_ushort(h0) | ((uint32_t)__half_as_ushort(h1) << 16);
-                        lw[i / 2] = (uint32_t)__half_as_ushort(l0) | ((uint32_t)__half_as_ushort(l1) << 16);
-                    }
-                    *reinterpret_cast<uint4*>(g.yh + (size_t)(2 * m) * g.ldyh + u0) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-                    *reinterpret_cast<uint4*>(g.yh + (size_t)(2 * m + 1) * g.ldyh + u0) =
-                        make_uint4(lw[0], lw[1], lw[2], lw[3]);
-                } else {
-                    float4* dst = reinterpret_cast<float4*>(g.y + (size_t)m * g.ldy + n);
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        float4 o = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
-                        if (g.mode == kResid) {
-                            const float4 p = dst[i];
-                            o.x += p.x, o.y += p.y, o.z += p.z, o.w += p.w;
-                        }
-                        dst[i] = o;
-                    }
-                }
+                epilogue16(g, m, n, v);
             }
         }
     }
@@ -270,6 +290,30 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tc_fence_after();
         tc_dealloc(tmem, kBN);
     }
+}
+
+// Split-K: thread (m, 16-column group) sums the splits' partials in split
+// order (the result does not depend on which CTA finished first), scales
+// and runs the epilogue.
+__global__ void __launch_bounds__(256) tc_splitk_reduce(TcArgs g) {
+    const int groups = g.N / 16;
+    const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= (long long)g.M * groups) return;
+    const int m = (int)(i / groups), n = (int)(i - (long long)m * groups) * 16;
+    float v[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) v[j] = 0.f;
+    for (int z = 0; z < g.splits; ++z) {
+        const float4* src = reinterpret_cast<const float4*>(g.part + ((size_t)z * g.M + m) * g.N + n);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const float4 p = __ldcg(src + q);
+            v[4 * q] += p.x, v[4 * q + 1] += p.y, v[4 * q + 2] += p.z, v[4 * q + 3] += p.w;
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < 16; ++j) v[j] *= __ldg(g.scale + n + j);
+    epilogue16(g, m, n, v);
 }
 
 // ------------------------------------------------------------------ host side
@@ -296,8 +340,28 @@ EncodeTiledFn encoder() {
 
 bool tc_gemm_supported(int N, int K) { return N > 0 && K > 0 && N % kBN == 0 && K % kBK == 0; }
 
+// K splits of an M x N x K projection when the output tiles alone leave
+// more than half of the SMs idle: as many as fit in one wave (a second,
+// partial wave would leave most SMs idle at its end), each split keeping
+// at least 4 k-tiles.
+int tc_gemm_splits(int M, int N, int K, int num_sms) {
+    const int tiles = (M + kBM - 1) / kBM * (N / kBN);
+    if (tiles * 2 > num_sms) return 1;
+    int s = num_sms / tiles;
+    s = s < 8 ? s : 8;
+    const int cap = (K / kBK) / 4;
+    s = s < cap ? s : cap;
+    return s > 1 ? s : 1;
+}
+
+size_t tc_gemm_work_bytes(int M, int N, int K, int num_sms) {
+    const int s = tc_gemm_splits(M, N, K, num_sms);
+    return s > 1 ? (size_t)s * M * N * 4 : 0;
+}
+
 int launch_tc_gemm(const __half* a_planes, const int8_t* w, const float* scale, int M, int N, int K, int mode,
-                   float* y, int ldy, __half* yh, int ldyh, int32_t* status, cudaStream_t st) {
+                   float* y, int ldy, __half* yh, int ldyh, int32_t* status, cudaStream_t st, float* work,
+                   size_t work_bytes, int num_sms) {
     if (M <= 0) return 0;
     if (!tc_gemm_supported(N, K) || (mode != kStore && mode != kResid && mode != kSiluGate)) return -1;
     if (((uintptr_t)a_planes & 15) || ((uintptr_t)w & 15) || (mode == kSiluGate ? (ldyh % 8 != 0) : (ldy % 4 != 0)))
@@ -326,9 +390,15 @@ int launch_tc_gemm(const __half* a_planes, const int8_t* w, const float* scale, 
             return -3;
     }
     if (allow_max_dynamic_smem((const void*)tc_gemm_kernel) != cudaSuccess) return -4;
-    TcArgs g{scale, M, N, K, mode, y, ldy, yh, ldyh, status};
-    const dim3 grid(N / kBN, (M + kBM - 1) / kBM);
+    int splits = num_sms > 0 ? tc_gemm_splits(M, N, K, num_sms) : 1;
+    if (splits > 1 && (!work || work_bytes < (size_t)splits * M * N * 4 || ((uintptr_t)work & 15))) splits = 1;
+    TcArgs g{scale, M, N, K, mode, y, ldy, yh, ldyh, status, splits, work};
+    const dim3 grid(N / kBN, (M + kBM - 1) / kBM, splits);
     tc_gemm_kernel<<<grid, kTcThreads, kSmemBytes, st>>>(ta, tb, g);
+    if (splits > 1) {
+        const long long n = (long long)M * (N / 16);
+        tc_splitk_reduce<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(g);
+    }
     return 0;
 }
 

@@ -279,6 +279,20 @@ void q3i8_destroy(q3i8_ctx* ctx);
 int q3i8_op_gemm_i8(const uint16_t* a_planes, const int8_t* w, const float* scale, int32_t M, int32_t N, int32_t K,
                     float* y, int32_t* d_status, void* cuda_stream);
 
+/* q3i8_op_gemm_i8 with K split over several CTAs per output tile, as the
+ * prefill does when the output tiles alone cannot cover the GPU's SMs (a
+ * short prompt on a narrow projection).  Each split writes unscaled fp32
+ * partial sums into `workspace`; a second kernel adds them in split order
+ * (the result does not depend on which CTA finished first), scales them and
+ * stores y.  The split count follows from M, N, K and the current device's
+ * SM count; q3i8_op_gemm_i8_splitk_workspace returns the bytes it needs (0
+ * when the shape is not split, in which case workspace may be NULL).
+ * workspace is 16-byte aligned device memory, no initialisation needed. */
+size_t q3i8_op_gemm_i8_splitk_workspace(int32_t M, int32_t N, int32_t K);
+int q3i8_op_gemm_i8_splitk(const uint16_t* a_planes, const int8_t* w, const float* scale, int32_t M, int32_t N,
+                           int32_t K, float* y, void* workspace, size_t ws_bytes, int32_t* d_status,
+                           void* cuda_stream);
+
 /* Split-KV grouped-query decode attention (the attention step of the
  * "Supported models" block, one query position per row):
  *   q       [R][n_heads][hd] fp32 queries (already normed and rotated).

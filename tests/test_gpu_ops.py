@@ -121,6 +121,42 @@ def test_tc_gemm_vs_oracle(pkg, M, N, K):
     assert np.all(np.abs(got - ref) <= bound), float(np.max(np.abs(got - ref) - bound))
 
 
+@pytest.mark.parametrize("M,N,K", [(256, 2048, 6144), (256, 4096, 2048), (130, 2048, 2048), (40, 1024, 1024)])
+def test_tc_gemm_split_k_vs_oracle(pkg, M, N, K):
+    """Short prompts on narrow projections (the 1.7B shape's O / down / QKV at 256 rows, a ragged row tile):
+    K split over CTAs, partial sums added in split order by a second kernel.  Same bound as the unsplit GEMM,
+    and the result equals itself run to run."""
+    import torch
+
+    ws_bytes = pkg.op_gemm_i8_splitk_workspace(M, N, K)
+    assert ws_bytes > 0  # these shapes are split on a GB300 (152 SMs)
+    rng = np.random.default_rng(M + N + K)
+    x = (rng.standard_normal((M, K)) * 1.5).astype(np.float32)
+    hi = x.astype(np.float16)
+    lo = (x - hi.astype(np.float32)).astype(np.float16)
+    xs = hi.astype(np.float32) + lo.astype(np.float32)
+    q = rng.integers(-127, 128, (N, K), dtype=np.int8)
+    s = (rng.random(N) * 0.02 + 1e-3).astype(np.float32)
+    ref = oracle.matmul_i8(q, s, xs, nthreads=oracle.default_threads())
+    dev = torch.device("cuda")
+    planes = torch.from_numpy(np.ascontiguousarray(np.concatenate([hi, lo], axis=1)).view(np.int16)).to(dev)
+    dq, ds = torch.from_numpy(q).to(dev), torch.from_numpy(s).to(dev)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    outs = []
+    for _ in range(2):
+        y = torch.full((M, N), float("nan"), device=dev)
+        pkg.op_gemm_i8_splitk(planes, dq, ds, y, ws, st)
+        torch.cuda.synchronize()
+        outs.append(y.cpu().numpy())
+    assert int(st.item()) == 0
+    assert np.array_equal(outs[0], outs[1])
+    bound = 4 * K * 6e-8 * (s[None, :] * (np.abs(xs) @ np.abs(q.astype(np.float32)).T)) + 1e-6
+    assert np.all(np.abs(outs[0] - ref) <= bound), float(np.max(np.abs(outs[0] - ref) - bound))
+    with pytest.raises(pkg.Q3Error, match="workspace"):
+        pkg.op_gemm_i8_splitk(planes, dq, ds, torch.zeros(M, N, device=dev), ws[:16], st)
+
+
 def test_tc_gemm_rejects_bad_shapes(pkg):
     import torch
 
