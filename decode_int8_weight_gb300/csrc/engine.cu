@@ -383,6 +383,7 @@ int init_state(q3i8_ctx* c) {
     CK(c, cudaMalloc(&c->counter, 4));
     CK(c, cudaMalloc(&c->kpart, (size_t)(H / 16) * kResidSplit * 8 * 64 * sizeof(float)));
     CK(c, cudaMalloc(&c->tile_cnt, (size_t)(H / 16) * sizeof(unsigned int)));
+    CK(c, cudaMalloc(&c->ss_fold, (size_t)2 * B * sizeof(long long)));
     CK(c, cudaMemset(c->tile_cnt, 0, (size_t)(H / 16) * sizeof(unsigned int)));
     CK(c, cudaMalloc(&c->status, 4));
     CK(c, cudaMalloc(&c->x, (size_t)B * H * 4));
@@ -420,7 +421,7 @@ extern "C" void q3i8_destroy(q3i8_ctx* c) {
         cudaFree(L.attn_norm), cudaFree(L.ffn_norm), cudaFree(L.q_norm), cudaFree(L.k_norm);
     }
     void* ptrs[] = {c->final_norm, c->kc, c->vc, c->rope, c->tokens, c->pos, c->seq_ids, c->step, c->keys,
-                    c->counter, c->kpart, c->tile_cnt, c->status, c->x, c->qkv, c->part, c->xh, c->oh, c->ah, c->logits,
+                    c->counter, c->kpart, c->tile_cnt, c->ss_fold, c->status, c->x, c->qkv, c->part, c->xh, c->oh, c->ah, c->logits,
                     c->out_ids, c->pf_x, c->pf_qkv, c->pf_q, c->pf_xh, c->pf_oh, c->pf_ah, c->pf_blocks,
                     c->pf_part, c->pf_ids, c->pf_seq, c->pf_pos, c->pf_last, c->d_mats, c->d_gains,
                     c->p_epoch, c->p_keys, c->p_exit, c->p_attn_cnt, c->p_abort, c->p_diag, c->p_ll, c->p_part, c->p_trace,
@@ -462,6 +463,13 @@ int enqueue_step(q3i8_ctx* c, int B, bool want_logits) {
     const int ks_resid = kResidSplit;
     float* kpart = c->kpart;
 
+    // RMSNorm folded (except layer 0's): the residual projections write the
+    // next norm's operand planes and per-sequence sums of squares (ss_a after
+    // down, ss_b after O); the consumer projections scale by 1 / rms.  Each
+    // accumulator is zeroed by a launch between its reader and its next
+    // writer: QKV clears ss_b, gate/up clears ss_a.
+    long long* ss_a = c->ss_fold;
+    long long* ss_b = c->ss_fold + c->bmax;
     launch_embed(c->tokens, B, c->embed.raw, c->embed.scale, H, d.vocab, c->x, c->status, st);
     launch_rmsnorm(c->x, nullptr, B, H, c->layers[0].attn_norm, d.rms_eps, nullptr, c->xh, st, 1);
     for (int l = 0; l < d.n_layers; ++l) {
@@ -470,6 +478,7 @@ int enqueue_step(q3i8_ctx* c, int B, bool want_logits) {
         a.B = B;
         a.w = L.qkv.frag, a.scale = L.qkv.scale, a.rows = L.qkv.rows, a.K = H, a.xh = c->xh, a.xfrag = 1;
         a.y = c->qkv, a.ldy = L.qkv.rows;
+        a.ss_in = l > 0 ? ss_a : nullptr, a.ss_clear = ss_b, a.norm_H = H, a.eps = d.rms_eps;
         launch_gemv(a, kStore, gemv_grid(a.rows, kStore, c->num_sms), st);
         if (launch_attention_decode(c->qkv, L.q_norm, L.k_norm, d.rms_eps, c->rope, c->kc + l * layer_kv,
                                     c->vc + l * layer_kv, c->seq_ids, c->pos, B, nh, nkv, hd, c->cap, splits, c->part,
@@ -479,30 +488,32 @@ int enqueue_step(q3i8_ctx* c, int B, bool want_logits) {
         a.B = B;
         a.w = L.o.frag, a.scale = L.o.scale, a.rows = L.o.rows, a.K = Dq, a.xh = c->oh, a.xfrag = 1;
         a.y = c->x, a.ldy = H, a.ksplit = ks_resid, a.kpart = kpart, a.tile_cnt = c->tile_cnt;
+        a.norm_g = L.ffn_norm, a.norm_xh = c->xh, a.ss_out = ss_b, a.norm_H = H;
         launch_gemv(a, kResid, gemv_grid(a.rows, kResid, c->num_sms) * ks_resid, st);
-        launch_rmsnorm(c->x, nullptr, B, H, L.ffn_norm, d.rms_eps, nullptr, c->xh, st, 1);
         a = GemvArgs{};
         a.B = B;
         a.w = L.gu.frag, a.scale = L.gu.scale, a.rows = L.gu.rows, a.K = H, a.xh = c->xh, a.xfrag = 1;
         a.yh = c->ah, a.ldyh = I, a.yfrag = 1;
+        a.ss_in = ss_b, a.ss_clear = ss_a, a.norm_H = H, a.eps = d.rms_eps;
         launch_gemv(a, kSiluGate, gemv_grid(a.rows, kSiluGate, c->num_sms), st);
         a = GemvArgs{};
         a.B = B;
         a.w = L.down.frag, a.scale = L.down.scale, a.rows = L.down.rows, a.K = I, a.xh = c->ah, a.xfrag = 1;
         a.y = c->x, a.ldy = H, a.ksplit = ks_resid, a.kpart = kpart, a.tile_cnt = c->tile_cnt;
+        a.norm_g = (l + 1 < d.n_layers) ? c->layers[l + 1].attn_norm : c->final_norm;
+        a.norm_xh = c->xh, a.ss_out = ss_a, a.norm_H = H;
         launch_gemv(a, kResid, gemv_grid(a.rows, kResid, c->num_sms) * ks_resid, st);
-        const float* g_next = (l + 1 < d.n_layers) ? c->layers[l + 1].attn_norm : c->final_norm;
-        launch_rmsnorm(c->x, nullptr, B, H, g_next, d.rms_eps, nullptr, c->xh, st, 1);
     }
-    enqueue_lm_head(c, B, true, want_logits ? c->logits : nullptr);
+    enqueue_lm_head(c, B, true, want_logits ? c->logits : nullptr, ss_a);
     return Q3_OK;
 }
 
-void enqueue_lm_head(q3i8_ctx* c, int B, bool advance_pos, float* logits) {
+void enqueue_lm_head(q3i8_ctx* c, int B, bool advance_pos, float* logits, const long long* ss_in) {
     GemvArgs a{};
     a.B = B;
     a.w = c->embed.frag, a.scale = c->embed.scale, a.rows = c->embed.rows, a.K = c->d.hidden, a.xh = c->xh;
-    a.xfrag = 1;  // the final RMSNorm writes fragment-ordered planes
+    a.xfrag = 1;  // the final RMSNorm (or the last down projection) writes fragment-ordered planes
+    a.ss_in = ss_in, a.norm_H = c->d.hidden, a.eps = c->d.rms_eps;
     a.keys = c->keys, a.counter = c->counter, a.tokens = c->tokens, a.out_ids = c->out_ids, a.step = c->step;
     a.out_cap = c->out_cap, a.pos = c->pos, a.advance_pos = advance_pos ? 1 : 0;
     a.valid_rows = c->embed.valid_rows, a.logits = logits;
@@ -745,7 +756,7 @@ static int enqueue_decode_step(q3i8_ctx* c, int B, bool want_logits) {
 int step_launches(const q3i8_ctx* c, int B) {
     if (persistent_for(c, B)) return 1;
     if (fused_for(c, B)) return 2 * c->d.n_layers + 1;
-    return 2 + c->d.n_layers * (decode_splits(c, B) == 1 ? 7 : 8) + 1;
+    return 2 + c->d.n_layers * (decode_splits(c, B) == 1 ? 5 : 6) + 1;
 }
 // Kernels of one prefill over M prompt rows: embed; per layer 2 RMSNorms, the
 // QK-norm/RoPE/append, attention split + merge and the 4 projections (one

@@ -52,6 +52,7 @@ struct q3i8_ctx {
     unsigned long long* keys = nullptr;
     unsigned int* counter = nullptr;
     float* kpart = nullptr;            // split-K parts of the residual GEMVs
+    long long* ss_fold = nullptr;      // [2][bmax] folded RMSNorm sums of squares (fixed point)
     unsigned int* tile_cnt = nullptr;  // their per-tile arrival counters
     int32_t* out_ids = nullptr;  // [bmax][out_cap]
     int out_cap = 0;
@@ -121,7 +122,7 @@ int decode_splits(const q3i8_ctx* c, int B);
 int enqueue_step(q3i8_ctx* c, int B, bool want_logits);
 int step_setup(q3i8_ctx* c);
 int enqueue_step_fused(q3i8_ctx* c, int B, bool want_logits);
-void enqueue_lm_head(q3i8_ctx* c, int B, bool advance_pos, float* logits);
+void enqueue_lm_head(q3i8_ctx* c, int B, bool advance_pos, float* logits, const long long* ss_in = nullptr);
 int step_launches(const q3i8_ctx* c, int B);
 int persistent_setup(q3i8_ctx* c);
 int persistent_reset(q3i8_ctx* c);

@@ -51,6 +51,10 @@ Q3_DEV void gemv_prefetch_item(const GemvArgs& a, int item, int ks, int kpairs) 
         prefetch_l2_bulk(base + off, bytes - off < 4096u ? bytes - off : 4096u);
 }
 
+// Fixed-point sums of squares (value * 2^32) of the folded RMSNorm.
+Q3_DEV long long ss_fix(float v) { return __float2ll_rn(v * 0x1p32f); }
+Q3_DEV float ss_float(long long x) { return __ll2float_rn(x) * 0x1p-32f; }
+
 template <int NT, int MODE>
 __global__ void __launch_bounds__(256) gemv_kernel(GemvArgs a) {
     pdl_launch_dependents();
@@ -70,6 +74,13 @@ __global__ void __launch_bounds__(256) gemv_kernel(GemvArgs a) {
     __shared__ float red[8][NT][32][2];
     __shared__ unsigned long long best[4 * NT];
     __shared__ int is_last;
+    __shared__ float s_inv[4 * NT];   // folded RMSNorm: 1 / rms per sequence (1 without)
+    __shared__ float s_sq[NT * 64];   // folded RMSNorm: x^2 of the tile's rows
+    if (a.ss_clear && blockIdx.x == 0)
+        for (int b = threadIdx.x; b < a.B; b += blockDim.x) a.ss_clear[b] = 0;
+    for (int b = threadIdx.x; b < 4 * NT; b += blockDim.x)
+        s_inv[b] = (a.ss_in && b < a.B) ? 1.0f / sqrtf(ss_float(__ldcg(a.ss_in + b)) / (float)a.norm_H + a.eps) : 1.0f;
+    __syncthreads();
 
     if (MODE == kArgmax) {
         for (int i = threadIdx.x; i < 4 * NT; i += blockDim.x) best[i] = 0ull;
@@ -131,8 +142,8 @@ __global__ void __launch_bounds__(256) gemv_kernel(GemvArgs a) {
                 }
                 if (b < a.B) {
                     const int rg = tile * 16 + gg;
-                    const float gate = a.scale[rg] * s0;
-                    const float up = a.scale[rg + 8] * s1;
+                    const float gate = a.scale[rg] * s0 * s_inv[b];
+                    const float up = a.scale[rg + 8] * s1 * s_inv[b];
                     const float v = (gate / (1.0f + expf(-gate))) * up;
                     const int idx = tile * 8 + gg;
                     __half hi, lo;
@@ -162,10 +173,30 @@ __global__ void __launch_bounds__(256) gemv_kernel(GemvArgs a) {
                     const int n = i >> 6, ln = (i & 63) >> 1, half = i & 1, gg = ln >> 2, b = 4 * n + (ln & 3);
                     float sum = 0.f;
                     for (int q = 0; q < ks; ++q) sum += __ldcg(a.kpart + ((size_t)tile * ks + q) * (NT * 64) + i);
+                    float xs = 0.f;
                     if (b < a.B) {
                         const int row = tile * 16 + gg + 8 * half;
                         float* p = a.y + (size_t)b * a.ldy + row;
-                        *p = *p + a.scale[row] * sum;
+                        xs = *p + a.scale[row] * sum;
+                        *p = xs;
+                        if (a.norm_g) {
+                            __half hi, lo;
+                            split_f16(__fmul_rn(xs, a.norm_g[row]), hi, lo);
+                            a.norm_xh[plane_index(2 * b, row, a.norm_H, 1)] = hi;
+                            a.norm_xh[plane_index(2 * b + 1, row, a.norm_H, 1)] = lo;
+                        }
+                    }
+                    s_sq[i] = xs * xs;
+                }
+                if (a.norm_g) {
+                    // sequence b's 16 rows of this tile, in a fixed order
+                    __syncthreads();
+                    for (int b = threadIdx.x; b < a.B; b += blockDim.x) {
+                        const int n = b >> 2, t = b & 3;
+                        float sq = 0.f;
+                        for (int gg = 0; gg < 8; ++gg)
+                            sq += s_sq[n * 64 + (4 * gg + t) * 2] + s_sq[n * 64 + (4 * gg + t) * 2 + 1];
+                        atomicAdd(reinterpret_cast<unsigned long long*>(a.ss_out + b), (unsigned long long)ss_fix(sq));
                     }
                 }
                 if (threadIdx.x == 0) a.tile_cnt[tile] = 0u;
@@ -178,7 +209,7 @@ __global__ void __launch_bounds__(256) gemv_kernel(GemvArgs a) {
                 for (int w = 0; w < 8; ++w) sum += red[w][n][ln][half];
                 if (b < a.B) {
                     const int row = tile * 16 + gg + 8 * half;
-                    const float v = a.scale[row] * sum;
+                    const float v = a.scale[row] * sum * s_inv[b];
                     if (MODE == kStore) {
                         a.y[(size_t)b * a.ldy + row] = v;
                     } else if (MODE == kResid) {

@@ -55,6 +55,22 @@ struct GemvArgs {
     unsigned int* tile_cnt;
     int xfrag;                 // xh is in fragment order (plane_index), else plain [8*NT][K] planes
     int yfrag;                 // kSiluGate: yh in fragment order
+    // RMSNorm folded into its neighbours.  kResid (with kpart): the tile's
+    // last CTA also writes the next norm's operand planes, norm_g * x in
+    // fragment order (hi/lo), for its rows into norm_xh ([8*NT][norm_H]),
+    // and adds its rows' sum of squares of x per sequence to ss_out (64-bit
+    // fixed point, value * 2^32: the sum does not depend on the order of the
+    // adds).  kStore / kSiluGate / kArgmax: each sequence's dot products are
+    // multiplied by 1 / sqrt(ss_in / norm_H + eps) (ss_in NULL: by 1).
+    // ss_clear: accumulators [B] that CTA 0 zeroes after the wait, for a
+    // later writer.
+    const float* norm_g;
+    __half* norm_xh;
+    long long* ss_out;
+    const long long* ss_in;
+    long long* ss_clear;
+    int norm_H;
+    float eps;
 };
 
 // Activation planes hold column c = 2b + part (part 0 = f16 hi, 1 = lo of
