@@ -81,7 +81,7 @@ def _logits(rng, B, V, ties=0):
 
 
 def _histories(rng, B, V, n):
-    return [rng.integers(0, V, size=n).tolist() + rng.integers(0, 50, size=n // 4).tolist() for _ in range(B)]
+    return [rng.integers(0, V, size=n).tolist() + rng.integers(0, min(50, V), size=n // 4).tolist() for _ in range(B)]
 
 
 def _counts(hists, V):
@@ -92,10 +92,11 @@ def _counts(hists, V):
 
 
 @pytest.mark.parametrize("kw", SETTINGS, ids=lambda kw: f"T{kw['temperature']}-k{kw['top_k']}")
-@pytest.mark.parametrize("V,ties", [(151936, 0), (151936, 64), (4096, 0), (1000, 3)])
+@pytest.mark.parametrize("V,ties", [(151936, 0), (151936, 64), (4096, 0), (1000, 3), (1001, 2), (37, 0)])
 def test_op_sample_matches_oracle_chain(pkg, kw, V, ties):
     import torch
 
+    # V = 1001: rows not 16-byte aligned, the one-token-per-lane path; V = 37: fewer tokens than top_k
     rng = np.random.default_rng(V + ties + int(kw["temperature"] * 10) + kw["top_k"])
     B, seed = 3, 0xC0FFEE + V
     z = _logits(rng, B, V, ties)
