@@ -2,6 +2,7 @@
 #pragma once
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cooperative_groups.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -181,6 +182,20 @@ Q3_DEV uint2 lds64(uint32_t a) {
 // (pdl_wait) before touching memory.  Both are no-ops for a plain launch.
 Q3_DEV void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 Q3_DEV void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// ------------------------------------------------------------- clusters
+Q3_DEV int cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return (int)r;
+}
+Q3_DEV void cluster_arrive() { asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory"); }
+Q3_DEV void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
+// The same object in the shared memory of CTA `rank` of this cluster.
+template <typename T>
+Q3_DEV const T* peer(const T* p, int rank) {
+    return cooperative_groups::this_cluster().map_shared_rank(p, rank);
+}
 
 // ------------------------------------------------------------- misc
 Q3_DEV float warp_sum(float v) {

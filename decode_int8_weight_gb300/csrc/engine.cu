@@ -479,6 +479,7 @@ int enqueue_step(q3i8_ctx* c, int B, bool want_logits) {
         a.w = L.qkv.frag, a.scale = L.qkv.scale, a.rows = L.qkv.rows, a.K = H, a.xh = c->xh, a.xfrag = 1;
         a.y = c->qkv, a.ldy = L.qkv.rows;
         a.ss_in = l > 0 ? ss_a : nullptr, a.ss_clear = ss_b, a.norm_H = H, a.eps = d.rms_eps;
+        a.status = c->status;
         launch_gemv(a, kStore, gemv_grid(a.rows, kStore, c->num_sms), st);
         if (launch_attention_decode(c->qkv, L.q_norm, L.k_norm, d.rms_eps, c->rope, c->kc + l * layer_kv,
                                     c->vc + l * layer_kv, c->seq_ids, c->pos, B, nh, nkv, hd, c->cap, splits, c->part,
@@ -489,12 +490,14 @@ int enqueue_step(q3i8_ctx* c, int B, bool want_logits) {
         a.w = L.o.frag, a.scale = L.o.scale, a.rows = L.o.rows, a.K = Dq, a.xh = c->oh, a.xfrag = 1;
         a.y = c->x, a.ldy = H, a.ksplit = ks_resid, a.kpart = kpart, a.tile_cnt = c->tile_cnt;
         a.norm_g = L.ffn_norm, a.norm_xh = c->xh, a.ss_out = ss_b, a.norm_H = H;
+        a.status = c->status;
         launch_gemv(a, kResid, gemv_grid(a.rows, kResid, c->num_sms) * ks_resid, st);
         a = GemvArgs{};
         a.B = B;
         a.w = L.gu.frag, a.scale = L.gu.scale, a.rows = L.gu.rows, a.K = H, a.xh = c->xh, a.xfrag = 1;
         a.yh = c->ah, a.ldyh = I, a.yfrag = 1;
         a.ss_in = ss_b, a.ss_clear = ss_a, a.norm_H = H, a.eps = d.rms_eps;
+        a.status = c->status;
         launch_gemv(a, kSiluGate, gemv_grid(a.rows, kSiluGate, c->num_sms), st);
         a = GemvArgs{};
         a.B = B;
@@ -502,6 +505,7 @@ int enqueue_step(q3i8_ctx* c, int B, bool want_logits) {
         a.y = c->x, a.ldy = H, a.ksplit = ks_resid, a.kpart = kpart, a.tile_cnt = c->tile_cnt;
         a.norm_g = (l + 1 < d.n_layers) ? c->layers[l + 1].attn_norm : c->final_norm;
         a.norm_xh = c->xh, a.ss_out = ss_a, a.norm_H = H;
+        a.status = c->status;
         launch_gemv(a, kResid, gemv_grid(a.rows, kResid, c->num_sms) * ks_resid, st);
     }
     enqueue_lm_head(c, B, true, want_logits ? c->logits : nullptr, ss_a);

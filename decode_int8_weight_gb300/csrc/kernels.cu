@@ -254,6 +254,192 @@ __global__ void __launch_bounds__(256) gemv_kernel(GemvArgs a) {
     }
 }
 
+// =====================================================================
+// The same GEMV with the CTA's weights staged before the wait.
+//
+// One CTA per (tile, K part): its slice of the tile blob is one contiguous
+// run of k-pairs, which thread 0 bulk-copies into shared memory, and the
+// tile's row scales (and, for the residual mode, the next norm's gains) are
+// read, all before waiting on the previous kernel: that kernel's tail hides
+// the weight fetch.  After the wait the CTA reads only what the previous
+// kernels wrote (the operand planes, the sums of squares, the residual
+// rows), issued before the MMAs.  When K is split (kResid), the ks CTAs of a
+// tile form a thread-block cluster: each parks its part's sums in its shared
+// memory and CTA 0 of the cluster adds the parts in order through
+// distributed shared memory, so the result has the same bits as the parked
+// parts of gemv_kernel and needs no counter or second pass through global
+// memory.  Used for the fragment-ordered operands of the decode step; the
+// epilogues are gemv_kernel's.
+// =====================================================================
+constexpr uint32_t kGemvStageMax = 64u * 1024u;  // largest weight slice staged (bytes)
+
+template <int NT, int MODE>
+__global__ void __launch_bounds__(256, NT >= 8 ? 2 : 1) gemv_staged_kernel(GemvArgs a) {
+    pdl_launch_dependents();
+    extern __shared__ __align__(128) unsigned char wsm[];
+    __shared__ float red[8][NT][32][2];
+    __shared__ float s_part[NT * 64];  // this CTA's sums (the tile's, or its K part's)
+    __shared__ float s_sq[NT * 64];
+    __shared__ float s_inv[4 * NT];
+    __shared__ float s_scale[16], s_gain[16];
+    __shared__ __align__(8) uint64_t wbar;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int ks = (MODE == kResid && a.ksplit > 1) ? a.ksplit : 1;
+    const int tile = blockIdx.x / ks, part = blockIdx.x - tile * ks;
+    const int kpairs = a.K >> 5;
+    const int p_lo = (int)((long long)kpairs * part / ks), p_hi = (int)((long long)kpairs * (part + 1) / ks);
+    const bool lead = part == 0;  // cluster rank 0 (ks > 1) adds the parts and writes the tile
+    if (threadIdx.x == 0) {
+        mbar_init(&wbar, 1);
+        fence_mbar_init();
+        const uint32_t bytes = (uint32_t)(p_hi - p_lo) * 512u;
+        mbar_arrive_expect_tx(&wbar, bytes);
+        bulk_g2s(wsm, a.w + (size_t)tile * (kTileHeader + 16 * (size_t)a.K) + kTileHeader + (size_t)p_lo * 512, bytes,
+                 &wbar);
+    }
+    if (threadIdx.x < 16) {
+        s_scale[threadIdx.x] = a.scale[tile * 16 + threadIdx.x];
+        s_gain[threadIdx.x] = (MODE == kResid && a.norm_g) ? a.norm_g[tile * 16 + threadIdx.x] : 0.f;
+    }
+    __syncthreads();  // the barrier is initialised before anyone waits on it
+    pdl_wait();
+
+    // reads of what earlier kernels wrote, in flight during the MMAs
+    long long ss = 0;
+    if (a.ss_in && threadIdx.x < a.B) ss = __ldcg(a.ss_in + threadIdx.x);
+    constexpr int kEpi = (NT * 64 + 255) / 256;  // epilogue elements per thread
+    float yin[kEpi];
+#pragma unroll
+    for (int j = 0; j < kEpi; ++j) {
+        yin[j] = 0.f;
+        const int i = threadIdx.x + 256 * j;
+        if (MODE == kResid && lead && i < NT * 64) {
+            const int n = i >> 6, ln = (i & 63) >> 1, half = i & 1, b = 4 * n + (ln & 3);
+            if (b < a.B) yin[j] = a.y[(size_t)b * a.ldy + tile * 16 + (ln >> 2) + 8 * half];
+        }
+    }
+    if (a.ss_clear && blockIdx.x == 0)
+        for (int b = threadIdx.x; b < a.B; b += blockDim.x) a.ss_clear[b] = 0;
+
+    float acc[NT][4];
+#pragma unroll
+    for (int n = 0; n < NT; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
+    const bool ok = mbar_wait_bounded(&wbar, 0);
+    if (ok) {
+        const uint32_t wbase = smem_u32(wsm) + lane * 16;
+#pragma unroll(NT >= 4 ? 2 : 4)
+        for (int p = p_lo + warp; p < p_hi; p += 8) {
+            const uint4 wv = lds128(wbase + (uint32_t)(p - p_lo) * 512u);
+            uint32_t A0[4], A1[4];
+            u8x4_to_f16x2x2(wv.x, A0[0], A0[1]);
+            u8x4_to_f16x2x2(wv.y, A0[2], A0[3]);
+            u8x4_to_f16x2x2(wv.z, A1[0], A1[1]);
+            u8x4_to_f16x2x2(wv.w, A1[2], A1[3]);
+#pragma unroll
+            for (int n = 0; n < NT; ++n) {
+                const uint4 bw = *reinterpret_cast<const uint4*>(a.xh + ((((size_t)p * 8 + n) * 32 + lane) << 3));
+                mma_f16_16816(acc[n], A0, bw.x, bw.y);
+                mma_f16_16816(acc[n], A1, bw.z, bw.w);
+            }
+        }
+    } else {
+        set_status(a.status, kStatusTimeout);
+    }
+#pragma unroll
+    for (int n = 0; n < NT; ++n) {
+        red[warp][n][lane][0] = acc[n][0] + acc[n][1];  // row g,   sequence 4n+t (hi + lo)
+        red[warp][n][lane][1] = acc[n][2] + acc[n][3];  // row g+8, sequence 4n+t
+    }
+    if (threadIdx.x < 4 * NT)
+        s_inv[threadIdx.x] = (a.ss_in && threadIdx.x < a.B)
+                                 ? 1.0f / sqrtf(ss_float(ss) / (float)a.norm_H + a.eps)
+                                 : 1.0f;
+    __syncthreads();
+    for (int i = threadIdx.x; i < NT * 64; i += blockDim.x) {
+        const int n = i >> 6, ln = (i & 63) >> 1, half = i & 1;
+        float sum = 0.f;
+#pragma unroll
+        for (int w = 0; w < 8; ++w) sum += red[w][n][ln][half];
+        s_part[i] = sum;
+    }
+    if (MODE == kResid && ks > 1) {
+        cluster_arrive();
+        cluster_wait();  // every part is visible in the cluster
+        if (lead)
+            for (int i = threadIdx.x; i < NT * 64; i += blockDim.x) {
+                float sum = 0.f;
+                for (int q = 0; q < ks; ++q) sum += peer(s_part, q)[i];
+                s_sq[i] = sum;  // the tile's sums (s_sq is free until the epilogue below)
+            }
+        cluster_arrive();  // done with the peers' shared memory
+        cluster_wait();    // no CTA leaves while the lead may still read it
+        if (!lead) {
+            if (!ok) mbar_wait_bounded(&wbar, 0);
+            return;
+        }
+        __syncthreads();
+        for (int i = threadIdx.x; i < NT * 64; i += blockDim.x) s_part[i] = s_sq[i];
+    }
+    __syncthreads();
+
+    if (MODE == kSiluGate) {
+        // tile rows 0..7 are gate rows, 8..15 the up rows of the same 8 units
+        for (int i = threadIdx.x; i < NT * 32; i += blockDim.x) {
+            const int n = i >> 5, ln = i & 31, gg = ln >> 2, b = 4 * n + (ln & 3);
+            if (b < a.B) {
+                const float gate = s_scale[gg] * s_part[n * 64 + 2 * ln] * s_inv[b];
+                const float up = s_scale[gg + 8] * s_part[n * 64 + 2 * ln + 1] * s_inv[b];
+                const float v = (gate / (1.0f + expf(-gate))) * up;
+                const int idx = tile * 8 + gg;
+                __half hi, lo;
+                split_f16(v, hi, lo);
+                a.yh[plane_index(2 * b, idx, a.ldyh, a.yfrag)] = hi;
+                a.yh[plane_index(2 * b + 1, idx, a.ldyh, a.yfrag)] = lo;
+            }
+        }
+    } else if (MODE == kResid) {
+#pragma unroll
+        for (int j = 0; j < kEpi; ++j) {
+            const int i = threadIdx.x + 256 * j;
+            if (i >= NT * 64) break;
+            const int n = i >> 6, ln = (i & 63) >> 1, half = i & 1, gg = ln >> 2, b = 4 * n + (ln & 3);
+            float xs = 0.f;
+            if (b < a.B) {
+                const int r16 = gg + 8 * half, row = tile * 16 + r16;
+                xs = yin[j] + s_scale[r16] * s_part[i];
+                a.y[(size_t)b * a.ldy + row] = xs;
+                if (a.norm_g) {
+                    __half hi, lo;
+                    split_f16(__fmul_rn(xs, s_gain[r16]), hi, lo);
+                    a.norm_xh[plane_index(2 * b, row, a.norm_H, 1)] = hi;
+                    a.norm_xh[plane_index(2 * b + 1, row, a.norm_H, 1)] = lo;
+                }
+            }
+            s_sq[i] = xs * xs;
+        }
+        if (a.norm_g) {
+            // sequence b's 16 rows of this tile, in a fixed order
+            __syncthreads();
+            for (int b = threadIdx.x; b < a.B; b += blockDim.x) {
+                const int n = b >> 2, t = b & 3;
+                float sq = 0.f;
+                for (int gg = 0; gg < 8; ++gg)
+                    sq += s_sq[n * 64 + (4 * gg + t) * 2] + s_sq[n * 64 + (4 * gg + t) * 2 + 1];
+                atomicAdd(reinterpret_cast<unsigned long long*>(a.ss_out + b), (unsigned long long)ss_fix(sq));
+            }
+        }
+    } else {
+        for (int i = threadIdx.x; i < NT * 64; i += blockDim.x) {
+            const int n = i >> 6, ln = (i & 63) >> 1, half = i & 1, gg = ln >> 2, b = 4 * n + (ln & 3);
+            if (b < a.B) {
+                const int r16 = gg + 8 * half;
+                a.y[(size_t)b * a.ldy + tile * 16 + r16] = s_scale[r16] * s_part[i] * s_inv[b];
+            }
+        }
+    }
+    if (!ok && threadIdx.x == 0) mbar_wait_bounded(&wbar, 0);
+}
+
 // Launch with programmatic stream serialization (see pdl_wait).
 template <typename... KArgs, typename... Args>
 static void launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, Args... args) {
@@ -270,8 +456,45 @@ static void launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
     cudaLaunchKernelEx(&cfg, kern, args...);
 }
 
+// The staged kernel with ks-CTA clusters (ks > 1), programmatic stream
+// serialization and dyn bytes of dynamic shared memory.
+template <int NT, int MODE>
+static bool launch_gemv_staged(const GemvArgs& a, int grid, int ks, uint32_t dyn, cudaStream_t st) {
+    const void* fn = (const void*)gemv_staged_kernel<NT, MODE>;
+    if (allow_max_dynamic_smem(fn) != cudaSuccess) return false;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = dyn;
+    cfg.stream = st;
+    cudaLaunchAttribute at[2];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    at[1].id = cudaLaunchAttributeClusterDimension;
+    at[1].val.clusterDim.x = ks;
+    at[1].val.clusterDim.y = 1;
+    at[1].val.clusterDim.z = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = ks > 1 ? 2 : 1;
+    return cudaLaunchKernelEx(&cfg, gemv_staged_kernel<NT, MODE>, a) == cudaSuccess;
+}
+
 template <int NT>
 static void launch_gemv_nt(const GemvArgs& a, int mode, int grid, cudaStream_t st) {
+    // fragment-ordered operands with one CTA per (tile, K part) whose
+    // weight slice fits: the staged kernel
+    const int ks = (mode == kResid && a.ksplit > 1) ? a.ksplit : 1;
+    const int kpairs = a.K >> 5;
+    const uint32_t dyn = (uint32_t)((kpairs + ks - 1) / ks) * 512u;
+    if (mode != kArgmax && a.xfrag && grid == (a.rows >> 4) * ks && ks <= 8 && dyn <= kGemvStageMax) {
+        bool ok = false;
+        switch (mode) {
+            case kStore: ok = launch_gemv_staged<NT, kStore>(a, grid, ks, dyn, st); break;
+            case kResid: ok = launch_gemv_staged<NT, kResid>(a, grid, ks, dyn, st); break;
+            default: ok = launch_gemv_staged<NT, kSiluGate>(a, grid, ks, dyn, st); break;
+        }
+        if (ok) return;
+    }
     switch (mode) {
         case kStore: launch_pdl(gemv_kernel<NT, kStore>, grid, 256, 0, st, a); break;
         case kResid: launch_pdl(gemv_kernel<NT, kResid>, grid, 256, 0, st, a); break;

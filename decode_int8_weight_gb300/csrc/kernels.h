@@ -71,6 +71,7 @@ struct GemvArgs {
     long long* ss_clear;
     int norm_H;
     float eps;
+    int32_t* status;           // Q3 status word (a bounded wait that ran out), may be null
 };
 
 // Activation planes hold column c = 2b + part (part 0 = f16 hi, 1 = lo of

@@ -62,19 +62,6 @@ Q3_DEV void red_add_fix(long long* p, long long v) {
     asm volatile("red.relaxed.gpu.global.add.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
 
-// ------------------------------------------------------------- clusters
-Q3_DEV int cluster_rank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return (int)r;
-}
-Q3_DEV void cluster_arrive() { asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory"); }
-Q3_DEV void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
-template <typename T>
-Q3_DEV const T* peer(const T* p, int rank) {
-    return cg::this_cluster().map_shared_rank(p, rank);
-}
-
 // ------------------------------------------------------------- operands
 // Index of the f16 half for column col (0..7) and k within one 8-column tile
 // of a fragment-ordered B operand (the m16n8k16 B registers of lane
