@@ -385,6 +385,7 @@ int init_state(q3i8_ctx* c) {
     CK(c, cudaMalloc(&c->tile_cnt, (size_t)(H / 16) * sizeof(unsigned int)));
     CK(c, cudaMalloc(&c->ss_fold, (size_t)2 * B * sizeof(long long)));
     CK(c, cudaMemset(c->tile_cnt, 0, (size_t)(H / 16) * sizeof(unsigned int)));
+    c->attn_resident = attention_decode_blocks_per_sm(d.head_dim, d.n_heads / d.n_kv_heads) * c->num_sms;
     CK(c, cudaMalloc(&c->status, 4));
     CK(c, cudaMalloc(&c->x, (size_t)B * H * 4));
     CK(c, cudaMalloc(&c->qkv, (size_t)B * (Dq + 2 * Dkv) * 4));
@@ -436,12 +437,14 @@ extern "C" void q3i8_destroy(q3i8_ctx* c) {
 
 // ------------------------------------------------------------------ the decode step
 
-// KV splits of the decode attention.  One split (a context of one chunk)
-// writes the output itself and needs no merge launch; forcing one split on
-// longer contexts measured slower (B = 1, 512 positions: 1.007 vs 0.973 ms
-// per step; B = 8: 1.15 vs 0.93 ms), since its chunks then run in series.
+// KV splits of the decode attention: as many as fill one wave of resident
+// attention CTAs (at least one).  One split writes the output itself and
+// needs no merge launch.  Measured per step at 0.6B: B = 32, one split
+// instead of five 1.10 vs 1.17 ms; B = 8 and 16 the same as the earlier
+// rule of 8 CTAs per SM; B = 1 within 0.5 % (the context caps the count).
 int decode_splits(const q3i8_ctx* c, int B) {
-    int s = (8 * c->num_sms + B * c->d.n_kv_heads - 1) / (B * c->d.n_kv_heads);
+    const int pairs = B * c->d.n_kv_heads;
+    int s = c->attn_resident > 0 ? c->attn_resident / pairs : (8 * c->num_sms + pairs - 1) / pairs;
     s = std::min(s, c->cap / kChunkPos);
     s = std::min(s, c->dec_splits_max);
     return std::max(s, 1);

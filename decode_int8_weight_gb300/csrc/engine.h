@@ -54,6 +54,7 @@ struct q3i8_ctx {
     float* kpart = nullptr;            // split-K parts of the residual GEMVs
     long long* ss_fold = nullptr;      // [2][bmax] folded RMSNorm sums of squares (fixed point)
     unsigned int* tile_cnt = nullptr;  // their per-tile arrival counters
+    int attn_resident = 0;             // decode attention CTAs resident at once on the device
     int32_t* out_ids = nullptr;  // [bmax][out_cap]
     int out_cap = 0;
 

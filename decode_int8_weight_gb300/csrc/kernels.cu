@@ -683,18 +683,60 @@ struct AttnSmem {
     uint64_t bar[2];
 };
 
+// Lane layout of the chunk loop: a warp scores J positions at once with
+// T = 32 / J lanes per position, each lane holding DL of the head's dims in
+// pieces of P consecutive dims (16-byte pieces where DL >= 8, so that one
+// load instruction of the warp reads whole 128-byte lines of a row).  With
+// few query heads per group, several positions per warp step cut the
+// shuffle reductions per score; the per-lane query and accumulator registers
+// (GROUP * DL each) stay at 32.
+template <int HD, int GROUP>
+struct AttnLanes {
+    static constexpr int J = GROUP <= 2 ? 4 : (GROUP <= 4 ? 2 : 1);
+    static constexpr int T = 32 / J;
+    static constexpr int DL = HD / T;
+    static constexpr int P = DL < 8 ? DL : 8;
+    // head dim of element e of lane t
+    static __device__ __forceinline__ int dim(int t, int e) { return (e / P) * (T * P) + t * P + (e % P); }
+};
+
+// N consecutive bf16 (N = 2, 4 or 8; 4 N-byte aligned) -> float.
+template <int N>
+Q3_DEV void ld_bf16(const __nv_bfloat16* p, float* out) {
+    uint32_t w[N / 2];
+    if constexpr (N == 8) {
+        const uint4 r = *reinterpret_cast<const uint4*>(p);
+        w[0] = r.x, w[1] = r.y, w[2] = r.z, w[3] = r.w;
+    } else if constexpr (N == 4) {
+        const uint2 r = *reinterpret_cast<const uint2*>(p);
+        w[0] = r.x, w[1] = r.y;
+    } else {
+        w[0] = *reinterpret_cast<const uint32_t*>(p);
+    }
+#pragma unroll
+    for (int i = 0; i < N / 2; ++i) {
+        out[2 * i] = bf16_bits_to_float(w[i] & 0xffff);
+        out[2 * i + 1] = bf16_bits_to_float(w[i] >> 16);
+    }
+}
+
 // The chunk loop shared by the decode attention kernels: positions
 // [start, end) of one (sequence, kv head) in chunks of kChunk, staged two
 // at a time by bulk copies; each warp folds its 16 positions of a chunk into
-// its own online-softmax state (m, l, acc) for the GROUP query heads.
-// False when a bounded wait gave up (the status is set, copies drained).
+// its own online-softmax state (m, l, acc) for the GROUP query heads, J
+// positions per step (AttnLanes).  On return l and acc are summed over the
+// warp's position lanes: every lane holds l, and the lanes of one dim group
+// t hold that group's acc.  False when a bounded wait gave up (the status
+// is set, copies drained).
 template <int HD, int GROUP>
 Q3_DEV bool attn_chunks(AttnSmem<HD>& sm, const __nv_bfloat16* kb, const __nv_bfloat16* vb, int start, int end,
-                            const float (&qr)[GROUP][HD / 32], float scale, float (&m)[GROUP], float (&l)[GROUP],
-                            float (&acc)[GROUP][HD / 32], int32_t* status) {
-    constexpr int D = HD / 32;
+                        const float (&qr)[GROUP][AttnLanes<HD, GROUP>::DL], float scale, float (&m)[GROUP],
+                        float (&l)[GROUP], float (&acc)[GROUP][AttnLanes<HD, GROUP>::DL], int32_t* status) {
+    using Ln = AttnLanes<HD, GROUP>;
+    constexpr int J = Ln::J, T = Ln::T, DL = Ln::DL, P = Ln::P, IT = 16 / J;
     constexpr uint32_t kBytes = kChunk * HD * 2;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int j = lane / T, t = lane % T;
     const int nchunks = end > start ? (end - start + kChunk - 1) / kChunk : 0;
     if (threadIdx.x == 0) {
         for (int c = 0; c < 2 && c < nchunks; ++c) {
@@ -710,52 +752,53 @@ Q3_DEV bool attn_chunks(AttnSmem<HD>& sm, const __nv_bfloat16* kb, const __nv_bf
             ok = false;
             break;
         }
-        const int p0 = start + c * kChunk + warp * 16;
-        float sc[GROUP][16];
+        const int p0 = start + c * kChunk + warp * 16 + j;  // this lane's first position
+        float sc[GROUP][IT];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            const __nv_bfloat16* krow = sm.k[s] + (size_t)(warp * 16 + i) * HD + lane * D;
-            float kv[D];
-            if constexpr (D == 4) {
-                uint2 raw = *reinterpret_cast<const uint2*>(krow);
-                kv[0] = bf16_bits_to_float(raw.x & 0xffff);
-                kv[1] = bf16_bits_to_float(raw.x >> 16);
-                kv[2] = bf16_bits_to_float(raw.y & 0xffff);
-                kv[3] = bf16_bits_to_float(raw.y >> 16);
-            } else {
-                uint32_t raw = *reinterpret_cast<const uint32_t*>(krow);
-                kv[0] = bf16_bits_to_float(raw & 0xffff);
-                kv[1] = bf16_bits_to_float(raw >> 16);
-            }
+        for (int it = 0; it < IT; ++it) {
+            const __nv_bfloat16* krow = sm.k[s] + (size_t)(warp * 16 + it * J + j) * HD;
+            float kv[DL];
+#pragma unroll
+            for (int e = 0; e < DL; e += P) ld_bf16<P>(krow + Ln::dim(t, e), kv + e);
 #pragma unroll
             for (int h = 0; h < GROUP; ++h) {
                 float dot = 0.f;
 #pragma unroll
-                for (int d = 0; d < D; ++d) dot += qr[h][d] * kv[d];
-                dot = warp_sum(dot);
-                sc[h][i] = (p0 + i < end) ? dot * scale : -INFINITY;
+                for (int d = 0; d < DL; ++d) dot += qr[h][d] * kv[d];
+#pragma unroll
+                for (int o = 1; o < T; o <<= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
+                sc[h][it] = (p0 + it * J < end) ? dot * scale : -INFINITY;
             }
         }
+        float pr[GROUP][IT];
 #pragma unroll
         for (int h = 0; h < GROUP; ++h) {
             float cm = sc[h][0];
 #pragma unroll
-            for (int i = 1; i < 16; ++i) cm = fmaxf(cm, sc[h][i]);
-            const float mn = fmaxf(m[h], cm);
-            if (mn == -INFINITY) continue;
+            for (int it = 1; it < IT; ++it) cm = fmaxf(cm, sc[h][it]);
+#pragma unroll
+            for (int o = T; o < 32; o <<= 1) cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, o));
+            const float mn = fmaxf(m[h], cm);  // -inf only while the state is still empty
             const float corr = (m[h] == -INFINITY) ? 0.f : expf(m[h] - mn);
             l[h] *= corr;
 #pragma unroll
-            for (int d = 0; d < D; ++d) acc[h][d] *= corr;
+            for (int d = 0; d < DL; ++d) acc[h][d] *= corr;
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const float p = (sc[h][i] == -INFINITY) ? 0.f : expf(sc[h][i] - mn);
-                l[h] += p;
-                const __nv_bfloat16* vrow = sm.v[s] + (size_t)(warp * 16 + i) * HD + lane * D;
-#pragma unroll
-                for (int d = 0; d < D; ++d) acc[h][d] += p * __bfloat162float(vrow[d]);
-            }
+            for (int it = 0; it < IT; ++it) pr[h][it] = (sc[h][it] == -INFINITY) ? 0.f : expf(sc[h][it] - mn);
             m[h] = mn;
+        }
+#pragma unroll
+        for (int it = 0; it < IT; ++it) {
+            const __nv_bfloat16* vrow = sm.v[s] + (size_t)(warp * 16 + it * J + j) * HD;
+            float vv[DL];
+#pragma unroll
+            for (int e = 0; e < DL; e += P) ld_bf16<P>(vrow + Ln::dim(t, e), vv + e);
+#pragma unroll
+            for (int h = 0; h < GROUP; ++h) {
+                l[h] += pr[h][it];
+#pragma unroll
+                for (int d = 0; d < DL; ++d) acc[h][d] += pr[h][it] * vv[d];
+            }
         }
         __syncthreads();  // every warp is done with stage s
         if (threadIdx.x == 0 && c + 2 < nchunks) {
@@ -764,6 +807,15 @@ Q3_DEV bool attn_chunks(AttnSmem<HD>& sm, const __nv_bfloat16* kb, const __nv_bf
             bulk_g2s(sm.v[s], vb + (size_t)(c + 2) * kChunk * HD, kBytes, &sm.bar[s]);
         }
     }
+    // sum the position lanes (j) of l and acc
+#pragma unroll
+    for (int o = T; o < 32; o <<= 1)
+#pragma unroll
+        for (int h = 0; h < GROUP; ++h) {
+            l[h] += __shfl_xor_sync(0xffffffffu, l[h], o);
+#pragma unroll
+            for (int d = 0; d < DL; ++d) acc[h][d] += __shfl_xor_sync(0xffffffffu, acc[h][d], o);
+        }
     if (!ok && threadIdx.x == 0) {
         // a bounded wait gave up: record it and give the other copy a bounded chance to land
         set_status(status, kStatusTimeout);
@@ -778,21 +830,22 @@ Q3_DEV bool attn_chunks(AttnSmem<HD>& sm, const __nv_bfloat16* kb, const __nv_bf
 // planes, row r, query heads h0.. (the merge kernel's arithmetic for one
 // split, whose weight e^0 is exactly 1).
 template <int HD, int GROUP>
-Q3_DEV void attn_write_partial(const float (&m)[GROUP], const float (&l)[GROUP], const float (&acc)[GROUP][HD / 32],
-                                   float (&wm)[4][GROUP], float (&wl)[4][GROUP], float (&wacc)[4][GROUP][HD],
-                                   float* outp, int splits, int sp, __half* outh = nullptr, int ldh = 0,
-                                   int frag = 0, int r = 0, int h0 = 0) {
-    constexpr int D = HD / 32;
+Q3_DEV void attn_write_partial(const float (&m)[GROUP], const float (&l)[GROUP],
+                               const float (&acc)[GROUP][AttnLanes<HD, GROUP>::DL], float (&wm)[4][GROUP],
+                               float (&wl)[4][GROUP], float (&wacc)[4][GROUP][HD], float* outp, int splits, int sp,
+                               __half* outh = nullptr, int ldh = 0, int frag = 0, int r = 0, int h0 = 0) {
+    using Ln = AttnLanes<HD, GROUP>;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (lane == 0)
         for (int h = 0; h < GROUP; ++h) {
             wm[warp][h] = m[h];
             wl[warp][h] = l[h];
         }
+    if (lane < Ln::T)  // position lane 0 of each dim group
 #pragma unroll
-    for (int h = 0; h < GROUP; ++h)
+        for (int h = 0; h < GROUP; ++h)
 #pragma unroll
-        for (int d = 0; d < D; ++d) wacc[warp][h][lane * D + d] = acc[h][d];
+            for (int e = 0; e < Ln::DL; ++e) wacc[warp][h][Ln::dim(lane, e)] = acc[h][e];
     __syncthreads();
     for (int i = threadIdx.x; i < GROUP * HD; i += blockDim.x) {
         const int h = i / HD, d = i % HD;
@@ -828,7 +881,6 @@ __global__ void __launch_bounds__(128) attn_split_kernel(const float* q, const _
                                                          const __nv_bfloat16* vc, const int32_t* row_seq,
                                                          const int32_t* row_len, int len_add, int nh, int nkv,
                                                          int cap, int splits, float* part, int32_t* status) {
-    constexpr int D = HD / 32;  // dims per lane
     extern __shared__ __align__(128) unsigned char smem_raw[];
     AttnSmem<HD>& sm = *reinterpret_cast<AttnSmem<HD>*>(smem_raw);
     __shared__ float wm[4][GROUP], wl[4][GROUP];
@@ -857,11 +909,14 @@ __global__ void __launch_bounds__(128) attn_split_kernel(const float* q, const _
     }
     __syncthreads();
 
+    using Ln = AttnLanes<HD, GROUP>;
+    constexpr int D = Ln::DL;
+    const int t = lane % Ln::T;
     float qr[GROUP][D];
 #pragma unroll
     for (int h = 0; h < GROUP; ++h)
 #pragma unroll
-        for (int d = 0; d < D; ++d) qr[h][d] = q[((size_t)r * nh + g * GROUP + h) * HD + lane * D + d];
+        for (int d = 0; d < D; ++d) qr[h][d] = q[((size_t)r * nh + g * GROUP + h) * HD + Ln::dim(t, d)];
     const float scale = 1.0f / sqrtf((float)HD);
     float m[GROUP], l[GROUP], acc[GROUP][D];
 #pragma unroll
@@ -912,7 +967,8 @@ __global__ void __launch_bounds__(128) attn_decode_kernel(const float* qkv, cons
         }
     }
     pdl_wait();
-    constexpr int D = HD / 32;
+    using Ln = AttnLanes<HD, GROUP>;
+    constexpr int D = Ln::DL;
     constexpr int E = HD / 32;
     extern __shared__ __align__(128) unsigned char smem_raw[];
     AttnSmem<HD>& sm = *reinterpret_cast<AttnSmem<HD>*>(smem_raw);
@@ -987,11 +1043,12 @@ __global__ void __launch_bounds__(128) attn_decode_kernel(const float* qkv, cons
     }
     __syncthreads();
 
+    const int t = lane % Ln::T;
     float qr[GROUP][D];
 #pragma unroll
     for (int h = 0; h < GROUP; ++h)
 #pragma unroll
-        for (int d = 0; d < D; ++d) qr[h][d] = qs[h][lane * D + d];
+        for (int d = 0; d < D; ++d) qr[h][d] = qs[h][Ln::dim(t, d)];
     const float scale = 1.0f / sqrtf((float)HD);
     float m[GROUP], l[GROUP], acc[GROUP][D];
 #pragma unroll
@@ -1006,19 +1063,22 @@ __global__ void __launch_bounds__(128) attn_decode_kernel(const float* qkv, cons
                                 cend, qr, scale, m, l, acc, status))
         return;
     if (owns_p && warp == 0) {
-        // position p from the rounded values kept in shared memory
+        // position p from the rounded values kept in shared memory (every
+        // position lane of a dim group holds the same state)
 #pragma unroll
         for (int h = 0; h < GROUP; ++h) {
             float dot = 0.f;
 #pragma unroll
-            for (int d = 0; d < D; ++d) dot += qr[h][d] * kp[lane * D + d];
-            const float sc = warp_sum(dot) * scale;
+            for (int d = 0; d < D; ++d) dot += qr[h][d] * kp[Ln::dim(t, d)];
+#pragma unroll
+            for (int o = 1; o < Ln::T; o <<= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
+            const float sc = dot * scale;
             const float mn = fmaxf(m[h], sc);
             const float corr = (m[h] == -INFINITY) ? 0.f : expf(m[h] - mn);
             const float pe = expf(sc - mn);
             l[h] = l[h] * corr + pe;
 #pragma unroll
-            for (int d = 0; d < D; ++d) acc[h][d] = acc[h][d] * corr + pe * vp[lane * D + d];
+            for (int d = 0; d < D; ++d) acc[h][d] = acc[h][d] * corr + pe * vp[Ln::dim(t, d)];
             m[h] = mn;
         }
     }
@@ -1123,6 +1183,31 @@ static bool launch_attn_decode_t(const float* qkv, const float* q_norm, const fl
     launch_pdl(attn_decode_kernel<HD, GROUP>, grid, 128, smem, st, qkv, q_norm, k_norm, eps, rope_cs, kc, vc, row_seq,
                row_pos, nh, nkv, cap, splits, part, outh, ldh, frag, status);
     return true;
+}
+
+template <int HD, int GROUP>
+static int attn_decode_occupancy() {
+    if (allow_max_dynamic_smem((const void*)attn_decode_kernel<HD, GROUP>) != cudaSuccess) return 0;
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attn_decode_kernel<HD, GROUP>, 128,
+                                                      sizeof(AttnSmem<HD>)) != cudaSuccess)
+        return 0;
+    return n;
+}
+
+int attention_decode_blocks_per_sm(int hd, int group) {
+#define Q3_ATTN_CASE(HDV, GV) \
+    if (hd == HDV && group == GV) return attn_decode_occupancy<HDV, GV>();
+    Q3_ATTN_CASE(128, 1)
+    Q3_ATTN_CASE(128, 2)
+    Q3_ATTN_CASE(128, 4)
+    Q3_ATTN_CASE(128, 8)
+    Q3_ATTN_CASE(64, 1)
+    Q3_ATTN_CASE(64, 2)
+    Q3_ATTN_CASE(64, 4)
+    Q3_ATTN_CASE(64, 8)
+#undef Q3_ATTN_CASE
+    return 0;
 }
 
 int launch_attention_decode(const float* qkv, const float* q_norm, const float* k_norm, float eps,

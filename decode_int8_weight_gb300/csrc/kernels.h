@@ -120,6 +120,10 @@ int launch_attention(const float* q, const __nv_bfloat16* k, const __nv_bfloat16
 // position (appended, then attended with positions 0..row_pos[r]); output
 // hi/lo f16 planes (outh, ldh, frag as launch_attention).  With splits == 1
 // the attention kernel writes the output itself and no merge is launched.
+// Decode attention CTAs (head_dim hd, group nh / nkv) resident per SM of the
+// current device (0 if the shape is not built or the query failed).
+int attention_decode_blocks_per_sm(int hd, int group);
+
 int launch_attention_decode(const float* qkv, const float* q_norm, const float* k_norm, float eps,
                             const float2* rope_cs, __nv_bfloat16* kc, __nv_bfloat16* vc, const int32_t* row_seq,
                             const int32_t* row_pos, int R, int nh, int nkv, int hd, int cap, int splits, float* part,
