@@ -6,6 +6,8 @@
 // -> O + residual -> RMSNorm -> SiLU-gated FFN + residual, then a final
 // RMSNorm and the tied lm_head with a fused argmax ("Run local LLM decode",
 // section "Limitations": every token is the argmax at its step).
+#include <algorithm>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -335,12 +337,15 @@ __global__ void __launch_bounds__(256, NT >= 8 ? 2 : 1) gemv_staged_kernel(GemvA
             u8x4_to_f16x2x2(wv.y, A0[2], A0[3]);
             u8x4_to_f16x2x2(wv.z, A1[0], A1[1]);
             u8x4_to_f16x2x2(wv.w, A1[2], A1[3]);
+            // all tiles' first k-steps, then their second ones: no MMA waits on the one before it
+            uint4 bw[NT];
 #pragma unroll
-            for (int n = 0; n < NT; ++n) {
-                const uint4 bw = *reinterpret_cast<const uint4*>(a.xh + ((((size_t)p * 8 + n) * 32 + lane) << 3));
-                mma_f16_16816(acc[n], A0, bw.x, bw.y);
-                mma_f16_16816(acc[n], A1, bw.z, bw.w);
-            }
+            for (int n = 0; n < NT; ++n)
+                bw[n] = *reinterpret_cast<const uint4*>(a.xh + ((((size_t)p * 8 + n) * 32 + lane) << 3));
+#pragma unroll
+            for (int n = 0; n < NT; ++n) mma_f16_16816(acc[n], A0, bw[n].x, bw[n].y);
+#pragma unroll
+            for (int n = 0; n < NT; ++n) mma_f16_16816(acc[n], A1, bw[n].z, bw[n].w);
         }
     } else {
         set_status(a.status, kStatusTimeout);
@@ -440,6 +445,159 @@ __global__ void __launch_bounds__(256, NT >= 8 ? 2 : 1) gemv_staged_kernel(GemvA
     if (!ok && threadIdx.x == 0) mbar_wait_bounded(&wbar, 0);
 }
 
+// =====================================================================
+// The lm_head sweep with its argmax for B > 4 (several column tiles).
+//
+// gemv_kernel splits K over the warps of a CTA, so every weight tile makes
+// each warp read its share of all NT activation tiles again from L2 (8x the
+// weight bytes at NT = 8).  Here the activation planes (NT column tiles of
+// every k-pair, fragment order) are bulk-copied into shared memory once per
+// CTA, and each warp takes whole weight tiles (all of K) in turn: it streams
+// a tile's bytes from global memory in batches of kHeadBatch k-pairs (asking
+// L2 for its next tile meanwhile) and keeps the running argmax key of each
+// of its lanes' sequences in registers.  No partial sums cross warps.  The
+// keys meet in shared memory, then in global memory; the last CTA publishes
+// the tokens as gemv_kernel does.  The dot products are summed over K in
+// k-pair order by one warp.
+// =====================================================================
+constexpr int kHeadBatch = 4;  // k-pairs of weights in flight per warp
+
+Q3_DEV void prefetch_tile_l2(const uint8_t* tile_base, uint32_t bytes, int lane) {
+    for (uint32_t off = (uint32_t)lane * 4096u; off < bytes; off += 32u * 4096u)
+        prefetch_l2_bulk(tile_base + off, bytes - off < 4096u ? bytes - off : 4096u);
+}
+
+template <int NT>
+__global__ void __launch_bounds__(256) lm_head_wide_kernel(GemvArgs a) {
+    pdl_launch_dependents();
+    extern __shared__ __align__(128) unsigned char xs[];  // [kpairs][NT][32 lanes][16 B]
+    __shared__ __align__(8) uint64_t xbar;
+    __shared__ unsigned long long best[4 * NT];
+    __shared__ float s_inv[4 * NT];
+    __shared__ int is_last;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+    const int n_tiles = a.rows >> 4, kpairs = a.K >> 5;
+    const int nw = gridDim.x * 8;
+    const size_t blob = kTileHeader + 16 * (size_t)a.K;
+    const uint32_t wbytes = 16u * (uint32_t)a.K;
+    int tile = blockIdx.x * 8 + warp;
+    // the weights do not depend on the previous kernel
+    if (tile < n_tiles) prefetch_tile_l2(a.w + (size_t)tile * blob + kTileHeader, wbytes, lane);
+    if (threadIdx.x == 0) {
+        mbar_init(&xbar, 1);
+        fence_mbar_init();
+    }
+    if (threadIdx.x < 4 * NT) best[threadIdx.x] = 0ull;
+    __syncthreads();
+    pdl_wait();
+    if (warp == 0) {
+        if (lane == 0) mbar_arrive_expect_tx(&xbar, (uint32_t)kpairs * NT * 512u);
+        __syncwarp();
+        for (int p = lane; p < kpairs; p += 32)
+            bulk_g2s(xs + (size_t)p * NT * 512, reinterpret_cast<const uint8_t*>(a.xh) + (size_t)p * 8 * 512,
+                     NT * 512u, &xbar);
+    }
+    if (a.ss_clear && blockIdx.x == 0)
+        for (int b = threadIdx.x; b < a.B; b += blockDim.x) a.ss_clear[b] = 0;
+    if (threadIdx.x < 4 * NT)
+        s_inv[threadIdx.x] = (a.ss_in && threadIdx.x < a.B)
+                                 ? 1.0f / sqrtf(ss_float(__ldcg(a.ss_in + threadIdx.x)) / (float)a.norm_H + a.eps)
+                                 : 1.0f;
+    __syncthreads();
+    const bool ok = mbar_wait_bounded(&xbar, 0);
+    if (!ok) set_status(a.status, kStatusTimeout);
+
+    unsigned long long kb[NT];
+#pragma unroll
+    for (int n = 0; n < NT; ++n) kb[n] = 0ull;
+    const uint32_t xbase = smem_u32(xs) + lane * 16;
+    for (; ok && tile < n_tiles; tile += nw) {
+        if (tile + nw < n_tiles) prefetch_tile_l2(a.w + (size_t)(tile + nw) * blob + kTileHeader, wbytes, lane);
+        const int r0 = tile * 16 + g, r1 = r0 + 8;
+        const float sc0 = a.scale[r0], sc1 = a.scale[r1];
+        const uint8_t* wt = a.w + (size_t)tile * blob + kTileHeader + lane * 16;
+        float acc[NT][4];
+#pragma unroll
+        for (int n = 0; n < NT; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
+        uint4 wv[kHeadBatch], wn[kHeadBatch];
+#pragma unroll
+        for (int u = 0; u < kHeadBatch; ++u)
+            if (u < kpairs) wv[u] = ld_stream_u4(wt + (size_t)u * 512);
+        for (int p0 = 0; p0 < kpairs; p0 += kHeadBatch) {
+            // the next batch is in flight while this one is multiplied
+#pragma unroll
+            for (int u = 0; u < kHeadBatch; ++u)
+                if (p0 + kHeadBatch + u < kpairs) wn[u] = ld_stream_u4(wt + (size_t)(p0 + kHeadBatch + u) * 512);
+#pragma unroll
+            for (int u = 0; u < kHeadBatch; ++u) {
+                if (p0 + u >= kpairs) break;
+                uint32_t A0[4], A1[4];
+                u8x4_to_f16x2x2(wv[u].x, A0[0], A0[1]);
+                u8x4_to_f16x2x2(wv[u].y, A0[2], A0[3]);
+                u8x4_to_f16x2x2(wv[u].z, A1[0], A1[1]);
+                u8x4_to_f16x2x2(wv[u].w, A1[2], A1[3]);
+                // all tiles' first k-steps, then their second ones
+                uint4 bw[NT];
+#pragma unroll
+                for (int n = 0; n < NT; ++n) bw[n] = lds128(xbase + (uint32_t)((p0 + u) * NT + n) * 512u);
+#pragma unroll
+                for (int n = 0; n < NT; ++n) mma_f16_16816(acc[n], A0, bw[n].x, bw[n].y);
+#pragma unroll
+                for (int n = 0; n < NT; ++n) mma_f16_16816(acc[n], A1, bw[n].z, bw[n].w);
+            }
+#pragma unroll
+            for (int u = 0; u < kHeadBatch; ++u) wv[u] = wn[u];
+        }
+#pragma unroll
+        for (int n = 0; n < NT; ++n) {
+            const int b = 4 * n + t;
+            if (b >= a.B) continue;
+            const float v0 = sc0 * (acc[n][0] + acc[n][1]) * s_inv[b];  // row r0, sequence b (hi + lo)
+            const float v1 = sc1 * (acc[n][2] + acc[n][3]) * s_inv[b];  // row r1
+            if (r0 < a.valid_rows) {
+                if (a.logits) a.logits[(size_t)b * a.valid_rows + r0] = v0;
+                kb[n] = max(kb[n], argmax_key(v0, (uint32_t)r0));
+            }
+            if (r1 < a.valid_rows) {
+                if (a.logits) a.logits[(size_t)b * a.valid_rows + r1] = v1;
+                kb[n] = max(kb[n], argmax_key(v1, (uint32_t)r1));
+            }
+        }
+    }
+    // lanes t, t + 4, ... hold the same sequences: their maximum, then the CTA's
+#pragma unroll
+    for (int n = 0; n < NT; ++n) {
+#pragma unroll
+        for (int o = 4; o < 32; o <<= 1) kb[n] = max(kb[n], __shfl_xor_sync(0xffffffffu, kb[n], o));
+        if (g == 0 && 4 * n + t < a.B) atomicMax(&best[4 * n + t], kb[n]);
+    }
+    __syncthreads();
+    // block result -> grid result; the last block to finish publishes the tokens
+    if (threadIdx.x < a.B) atomicMax(&a.keys[threadIdx.x], best[threadIdx.x]);
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) is_last = (atomicAdd(a.counter, 1u) == gridDim.x - 1);
+    __syncthreads();
+    if (is_last) {
+        __threadfence();
+        const int step = *reinterpret_cast<volatile int32_t*>(a.step);
+        if (threadIdx.x < a.B) {
+            const int b = threadIdx.x;
+            const unsigned long long k = atomicExch(&a.keys[b], 0ull);
+            const int tok = (int)argmax_key_index(k);
+            a.tokens[b] = tok;
+            if (step < a.out_cap) a.out_ids[(size_t)b * a.out_cap + step] = tok;
+            if (a.advance_pos) a.pos[b] += 1;
+        }
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            *a.step = step + 1;
+            *a.counter = 0u;
+        }
+    }
+    if (!ok && threadIdx.x == 0) mbar_wait_bounded(&xbar, 0);
+}
+
 // Launch with programmatic stream serialization (see pdl_wait).
 template <typename... KArgs, typename... Args>
 static void launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, Args... args) {
@@ -479,8 +637,40 @@ static bool launch_gemv_staged(const GemvArgs& a, int grid, int ks, uint32_t dyn
     return cudaLaunchKernelEx(&cfg, gemv_staged_kernel<NT, MODE>, a) == cudaSuccess;
 }
 
+// Shared memory above which the wide lm_head kernel is not used (bytes of
+// activation planes per CTA).
+constexpr uint32_t kHeadPlanesMax = 160u * 1024u;
+
+template <int NT>
+static bool launch_lm_head_wide(const GemvArgs& a, cudaStream_t st) {
+    const uint32_t dyn = (uint32_t)(a.K >> 5) * NT * 512u;
+    if (dyn > kHeadPlanesMax) return false;
+    const void* fn = (const void*)lm_head_wide_kernel<NT>;
+    if (allow_max_dynamic_smem(fn) != cudaSuccess) return false;
+    int dev = 0, sms = 0, per_sm = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, lm_head_wide_kernel<NT>, 256, dyn) != cudaSuccess ||
+        per_sm < 1)
+        return false;
+    const int tiles = a.rows >> 4;
+    const int grid = std::min(sms * per_sm, (tiles + 7) / 8);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = dyn;
+    cfg.stream = st;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, lm_head_wide_kernel<NT>, a) == cudaSuccess;
+}
+
 template <int NT>
 static void launch_gemv_nt(const GemvArgs& a, int mode, int grid, cudaStream_t st) {
+    if (mode == kArgmax && a.xfrag && launch_lm_head_wide<NT>(a, st)) return;
     // fragment-ordered operands with one CTA per (tile, K part) whose
     // weight slice fits: the staged kernel
     const int ks = (mode == kResid && a.ksplit > 1) ? a.ksplit : 1;
@@ -1087,7 +1277,8 @@ __global__ void __launch_bounds__(128) attn_decode_kernel(const float* qkv, cons
 
 // out[r][h][:] = sum_s acc_s e^{m_s - M} / sum_s l_s e^{m_s - M} over the
 // row's non-empty splits (the split kernels' range rule); the split weights
-// are computed once per block by warp 0, then every thread sums its column.
+// are computed once per block by warp 0, then every thread sums its column
+// (loads batched eight splits at a time; the sum stays in split order).
 template <int HD>
 __global__ void attn_merge_kernel(const float* part, int nh, int splits, const int32_t* row_len, int len_add,
                                   float* out, __half* outh, int ldh, int frag) {
@@ -1119,8 +1310,14 @@ __global__ void attn_merge_kernel(const float* part, int nh, int splits, const i
     }
     __syncthreads();
     float A = 0.f;
-    for (int s2 = 0; s2 < nne; ++s2)
-        if (sm_m[s2] != -INFINITY) A += p[(size_t)s2 * (HD + 2) + d] * sm_f[s2];
+    for (int s0 = 0; s0 < nne; s0 += 8) {
+        float v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) v[u] = s0 + u < nne ? p[(size_t)(s0 + u) * (HD + 2) + d] : 0.f;
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+            if (s0 + u < nne && sm_m[s0 + u] != -INFINITY) A += v[u] * sm_f[s0 + u];
+    }
     const float o = A / s_l;
     if (out) out[(size_t)rh * HD + d] = o;
     if (outh) {
