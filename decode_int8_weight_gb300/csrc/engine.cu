@@ -555,7 +555,11 @@ int step_setup(q3i8_ctx* c) {
     CK(c, cudaMemsetAsync(c->xf, 0, n * sizeof(long long), c->stream));
     c->splan = p;
     c->use_step = true;
-    c->step_max_batch = kStepMaxBatch;
+    // The small-batch kernels are built for up to kStepMaxBatch rows, but from
+    // 3 rows on the chained kernels are faster (0.6B shape, prompts of 32-53
+    // tokens, 64 new: 460 / 543 / 641 / 735 us per step at B = 1..4 here
+    // against 616 / 611 / 615 / 621 us chained).
+    c->step_max_batch = 2;
     c->step_max_ctx = 2048;
     if (const char* mc = getenv("Q3I8_STEP_MAX_CTX")) c->step_max_ctx = std::max(0, atoi(mc));
     if (const char* mb = getenv("Q3I8_STEP_MAX_BATCH")) c->step_max_batch = std::max(0, std::min(kStepMaxBatch, atoi(mb)));

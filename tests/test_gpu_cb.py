@@ -6,7 +6,7 @@ and the native loop q3i8_sched_run, through the C ABI.
 Each request's tokens must be its own greedy sequence: checked against the
 oracle (teacher-forced on the GPU's tokens, identical wherever the oracle's
 top-1/top-2 gap exceeds 1e-2).  Where a sequence's prompt is prefilled alone
-and its steps run on the small-batch step kernels (at most 4 rows), its
+and its steps run on the small-batch step kernels (at most 2 rows), its
 tokens must also equal a plain single-sequence decode bit for bit: every
 row of those kernels is computed independently of the others
 (column-independent MMAs, per-row attention, integer accumulation of the

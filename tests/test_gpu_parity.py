@@ -76,6 +76,14 @@ def test_tiny_one_attention_split(pkg):
     assert worst < 1e-3
 
 
+def test_small_batch_kernels_at_four_rows(pkg, monkeypatch):
+    # the small-batch step kernels take up to 4 rows when asked (by default
+    # 2: from 3 rows on the chained kernels are faster)
+    monkeypatch.setenv("Q3I8_STEP_MAX_BATCH", "4")
+    worst, _ = _teacher_forced_check(pkg, "tiny-b1-p8-n16", B=4)
+    assert worst < 1e-3
+
+
 def test_tiny_random_gains(pkg):
     _teacher_forced_check(pkg, "tiny-b1-p8-n16", random_gains=True)
 
