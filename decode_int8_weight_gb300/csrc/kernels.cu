@@ -276,7 +276,8 @@ __global__ void __launch_bounds__(256) gemv_kernel(GemvArgs a) {
 constexpr uint32_t kGemvStageMax = 64u * 1024u;  // largest weight slice staged (bytes)
 
 template <int NT, int MODE>
-__global__ void __launch_bounds__(256, NT >= 8 ? 2 : 1) gemv_staged_kernel(GemvArgs a) {
+__global__ void __launch_bounds__(256, NT >= 8 ? (MODE == kSiluGate ? 3 : 2) : (NT == 1 && MODE == kSiluGate ? 6 : 1))
+gemv_staged_kernel(GemvArgs a) {
     pdl_launch_dependents();
     extern __shared__ __align__(128) unsigned char wsm[];
     __shared__ float red[8][NT][32][2];
