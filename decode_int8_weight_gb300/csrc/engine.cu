@@ -483,10 +483,13 @@ int enqueue_step(q3i8_ctx* c, int B, bool want_logits) {
         a.y = c->qkv, a.ldy = L.qkv.rows;
         a.ss_in = l > 0 ? ss_a : nullptr, a.ss_clear = ss_b, a.norm_H = H, a.eps = d.rms_eps;
         a.status = c->status;
+        // the attention launched next may then read the positions and the
+        // cached K/V before its own wait
+        a.late_dependents = 1;
         launch_gemv(a, kStore, gemv_grid(a.rows, kStore, c->num_sms), st);
         if (launch_attention_decode(c->qkv, L.q_norm, L.k_norm, d.rms_eps, c->rope, c->kc + l * layer_kv,
                                     c->vc + l * layer_kv, c->seq_ids, c->pos, B, nh, nkv, hd, c->cap, splits, c->part,
-                                    c->oh, Dq, c->status, st, 1))
+                                    c->oh, Dq, c->status, st, 1, 1))
             return fail(c, Q3_ERR_CUDA, "decode attention could not be launched");
         a = GemvArgs{};
         a.B = B;

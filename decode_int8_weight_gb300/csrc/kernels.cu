@@ -278,7 +278,7 @@ constexpr uint32_t kGemvStageMax = 64u * 1024u;  // largest weight slice staged 
 template <int NT, int MODE>
 __global__ void __launch_bounds__(256, NT >= 8 ? (MODE == kSiluGate ? 3 : 2) : (NT == 1 && MODE == kSiluGate ? 6 : 1))
 gemv_staged_kernel(GemvArgs a) {
-    pdl_launch_dependents();
+    if (!a.late_dependents) pdl_launch_dependents();
     extern __shared__ __align__(128) unsigned char wsm[];
     __shared__ float red[8][NT][32][2];
     __shared__ float s_part[NT * 64];  // this CTA's sums (the tile's, or its K part's)
@@ -306,6 +306,7 @@ gemv_staged_kernel(GemvArgs a) {
     }
     __syncthreads();  // the barrier is initialised before anyone waits on it
     pdl_wait();
+    if (a.late_dependents) pdl_launch_dependents();
 
     // reads of what earlier kernels wrote, in flight during the MMAs
     long long ss = 0;
@@ -911,6 +912,18 @@ Q3_DEV void ld_bf16(const __nv_bfloat16* p, float* out) {
     }
 }
 
+// The first two K/V stages of positions [start, end) (thread 0).
+template <int HD>
+Q3_DEV void attn_issue_first(AttnSmem<HD>& sm, const __nv_bfloat16* kb, const __nv_bfloat16* vb, int start, int end) {
+    constexpr uint32_t kBytes = kChunk * HD * 2;
+    const int nchunks = end > start ? (end - start + kChunk - 1) / kChunk : 0;
+    for (int c = 0; c < 2 && c < nchunks; ++c) {
+        mbar_arrive_expect_tx(&sm.bar[c], 2 * kBytes);
+        bulk_g2s(sm.k[c], kb + (size_t)c * kChunk * HD, kBytes, &sm.bar[c]);
+        bulk_g2s(sm.v[c], vb + (size_t)c * kChunk * HD, kBytes, &sm.bar[c]);
+    }
+}
+
 // The chunk loop shared by the decode attention kernels: positions
 // [start, end) of one (sequence, kv head) in chunks of kChunk, staged two
 // at a time by bulk copies; each warp folds its 16 positions of a chunk into
@@ -918,24 +931,20 @@ Q3_DEV void ld_bf16(const __nv_bfloat16* p, float* out) {
 // positions per step (AttnLanes).  On return l and acc are summed over the
 // warp's position lanes: every lane holds l, and the lanes of one dim group
 // t hold that group's acc.  False when a bounded wait gave up (the status
-// is set, copies drained).
+// is set, copies drained).  first_issued: the caller has already issued the
+// first two stages (attn_issue_first).
 template <int HD, int GROUP>
 Q3_DEV bool attn_chunks(AttnSmem<HD>& sm, const __nv_bfloat16* kb, const __nv_bfloat16* vb, int start, int end,
                         const float (&qr)[GROUP][AttnLanes<HD, GROUP>::DL], float scale, float (&m)[GROUP],
-                        float (&l)[GROUP], float (&acc)[GROUP][AttnLanes<HD, GROUP>::DL], int32_t* status) {
+                        float (&l)[GROUP], float (&acc)[GROUP][AttnLanes<HD, GROUP>::DL], int32_t* status,
+                        bool first_issued = false) {
     using Ln = AttnLanes<HD, GROUP>;
     constexpr int J = Ln::J, T = Ln::T, DL = Ln::DL, P = Ln::P, IT = 16 / J;
     constexpr uint32_t kBytes = kChunk * HD * 2;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int j = lane / T, t = lane % T;
     const int nchunks = end > start ? (end - start + kChunk - 1) / kChunk : 0;
-    if (threadIdx.x == 0) {
-        for (int c = 0; c < 2 && c < nchunks; ++c) {
-            mbar_arrive_expect_tx(&sm.bar[c], 2 * kBytes);
-            bulk_g2s(sm.k[c], kb + (size_t)c * kChunk * HD, kBytes, &sm.bar[c]);
-            bulk_g2s(sm.v[c], vb + (size_t)c * kChunk * HD, kBytes, &sm.bar[c]);
-        }
-    }
+    if (threadIdx.x == 0 && !first_issued) attn_issue_first<HD>(sm, kb, vb, start, end);
     bool ok = true;
     for (int c = 0; c < nchunks; ++c) {
         const int s = c & 1;
@@ -1136,28 +1145,8 @@ __global__ void __launch_bounds__(128) attn_decode_kernel(const float* qkv, cons
                                                           __nv_bfloat16* vc, const int32_t* row_seq,
                                                           const int32_t* row_pos, int nh, int nkv, int cap,
                                                           int splits, float* part, __half* outh, int ldh, int frag,
-                                                          int32_t* status) {
+                                                          int pos_final, int32_t* status) {
     pdl_launch_dependents();
-    if (kAttnPrefetch) {
-        // The cached positions this split reads were written by earlier
-        // steps: start moving them into L2 while the previous kernel
-        // finishes (only a hint, so the position read here may be early).
-        const int r = blockIdx.z, sp = blockIdx.x, g = blockIdx.y;
-        const int pos = min(row_pos[r], cap - 1);
-        int per = (pos + splits) / splits;
-        per = (per + kChunk - 1) / kChunk * kChunk;
-        const int lo = sp * per, hi = min(pos, lo + per);
-        if (pos >= 0 && lo < hi) {
-            const size_t base = (((size_t)row_seq[r] * nkv + g) * cap + lo) * HD;
-            const uint32_t bytes = (uint32_t)(hi - lo) * HD * 2u;
-            for (uint32_t off = threadIdx.x * 4096u; off < bytes; off += blockDim.x * 4096u) {
-                const uint32_t n = bytes - off < 4096u ? bytes - off : 4096u;
-                prefetch_l2_bulk(reinterpret_cast<const uint8_t*>(kc + base) + off, n);
-                prefetch_l2_bulk(reinterpret_cast<const uint8_t*>(vc + base) + off, n);
-            }
-        }
-    }
-    pdl_wait();
     using Ln = AttnLanes<HD, GROUP>;
     constexpr int D = Ln::DL;
     constexpr int E = HD / 32;
@@ -1169,6 +1158,44 @@ __global__ void __launch_bounds__(128) attn_decode_kernel(const float* qkv, cons
 
     const int sp = blockIdx.x, g = blockIdx.y, r = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // With pos_final the positions and the cached K/V of positions < pos are
+    // final already (every launch before the previous one has completed):
+    // the first two stages are issued now.  Otherwise the cached range is
+    // only asked of L2 (the position read here may be early).
+    bool early = false;
+    if (pos_final) {
+        const int pos = row_pos[r], seq = row_seq[r];
+        int per = (pos + splits) / splits;
+        per = (per + kChunk - 1) / kChunk * kChunk;
+        const int start = sp * per, end = min(pos + 1, start + per);
+        const int cend = (pos >= start && pos < end) ? pos : end;
+        early = start < end;
+        if (early && threadIdx.x == 0) {
+            const size_t head_base = ((size_t)seq * nkv + g) * cap * HD;
+            mbar_init(&sm.bar[0], 1);
+            mbar_init(&sm.bar[1], 1);
+            fence_mbar_init();
+            attn_issue_first<HD>(sm, kc + head_base + (size_t)start * HD, vc + head_base + (size_t)start * HD, start,
+                                 cend);
+        }
+    }
+    if (kAttnPrefetch) {
+        const int pos = min(row_pos[r], cap - 1);
+        int per = (pos + splits) / splits;
+        per = (per + kChunk - 1) / kChunk * kChunk;
+        const int lo = sp * per + (early ? 2 * kChunk : 0), hi = min(pos, sp * per + per);
+        if (pos >= 0 && lo < hi) {
+            const size_t base = (((size_t)row_seq[r] * nkv + g) * cap + lo) * HD;
+            const uint32_t bytes = (uint32_t)(hi - lo) * HD * 2u;
+            for (uint32_t off = threadIdx.x * 4096u; off < bytes; off += blockDim.x * 4096u) {
+                const uint32_t n = bytes - off < 4096u ? bytes - off : 4096u;
+                prefetch_l2_bulk(reinterpret_cast<const uint8_t*>(kc + base) + off, n);
+                prefetch_l2_bulk(reinterpret_cast<const uint8_t*>(vc + base) + off, n);
+            }
+        }
+    }
+    pdl_wait();
+
     const int pos = row_pos[r], seq = row_seq[r];
     const int len = pos + 1;
     int per = (len + splits - 1) / splits;
@@ -1185,7 +1212,7 @@ __global__ void __launch_bounds__(128) attn_decode_kernel(const float* qkv, cons
     }
     const bool owns_p = pos >= start && pos < end;
     const size_t head_base = ((size_t)seq * nkv + g) * cap * HD;
-    if (threadIdx.x == 0) {
+    if (threadIdx.x == 0 && !early) {
         mbar_init(&sm.bar[0], 1);
         mbar_init(&sm.bar[1], 1);
         fence_mbar_init();
@@ -1251,7 +1278,7 @@ __global__ void __launch_bounds__(128) attn_decode_kernel(const float* qkv, cons
     }
     const int cend = owns_p ? pos : end;  // cached positions only
     if (!attn_chunks<HD, GROUP>(sm, kc + head_base + (size_t)start * HD, vc + head_base + (size_t)start * HD, start,
-                                cend, qr, scale, m, l, acc, status))
+                                cend, qr, scale, m, l, acc, status, early))
         return;
     if (owns_p && warp == 0) {
         // position p from the rounded values kept in shared memory (every
@@ -1374,12 +1401,13 @@ template <int HD, int GROUP>
 static bool launch_attn_decode_t(const float* qkv, const float* q_norm, const float* k_norm, float eps,
                                  const float2* rope_cs, __nv_bfloat16* kc, __nv_bfloat16* vc, const int32_t* row_seq,
                                  const int32_t* row_pos, int R, int nh, int nkv, int cap, int splits, float* part,
-                                 __half* outh, int ldh, int frag, int32_t* status, cudaStream_t st) {
+                                 __half* outh, int ldh, int frag, int pos_final, int32_t* status,
+                                 cudaStream_t st) {
     const int smem = (int)sizeof(AttnSmem<HD>);
     if (allow_max_dynamic_smem((const void*)attn_decode_kernel<HD, GROUP>) != cudaSuccess) return false;
     dim3 grid(splits, nkv, R);
     launch_pdl(attn_decode_kernel<HD, GROUP>, grid, 128, smem, st, qkv, q_norm, k_norm, eps, rope_cs, kc, vc, row_seq,
-               row_pos, nh, nkv, cap, splits, part, outh, ldh, frag, status);
+               row_pos, nh, nkv, cap, splits, part, outh, ldh, frag, pos_final, status);
     return true;
 }
 
@@ -1411,13 +1439,14 @@ int attention_decode_blocks_per_sm(int hd, int group) {
 int launch_attention_decode(const float* qkv, const float* q_norm, const float* k_norm, float eps,
                             const float2* rope_cs, __nv_bfloat16* kc, __nv_bfloat16* vc, const int32_t* row_seq,
                             const int32_t* row_pos, int R, int nh, int nkv, int hd, int cap, int splits, float* part,
-                            __half* outh, int ldh, int32_t* status, cudaStream_t st, int frag) {
+                            __half* outh, int ldh, int32_t* status, cudaStream_t st, int frag, int pos_final) {
     if (R <= 0) return 0;
     const int group = nh / nkv;
 #define Q3_ATTN_CASE(HDV, GV)                                                                                      \
     if (hd == HDV && group == GV) {                                                                                \
         if (!launch_attn_decode_t<HDV, GV>(qkv, q_norm, k_norm, eps, rope_cs, kc, vc, row_seq, row_pos, R, nh, nkv,  \
-                                           cap, splits, part, splits == 1 ? outh : nullptr, ldh, frag, status, st)) \
+                                           cap, splits, part, splits == 1 ? outh : nullptr, ldh, frag, pos_final,  \
+                                           status, st))                                                            \
             return -2;                                                                                             \
         if (splits > 1)                                                                                            \
             launch_pdl(attn_merge_kernel<HDV>, R * nh, HDV, 0, st, part, nh, splits, row_pos, 1, (float*)nullptr, \

@@ -72,6 +72,10 @@ struct GemvArgs {
     int norm_H;
     float eps;
     int32_t* status;           // Q3 status word (a bounded wait that ran out), may be null
+    // 1: the next kernel may launch only once this one has passed its wait,
+    // so that the next kernel's prologue may read what every launch before
+    // this one wrote (the decode attention's positions and cached K/V)
+    int late_dependents;
 };
 
 // Activation planes hold column c = 2b + part (part 0 = f16 hi, 1 = lo of
@@ -124,10 +128,14 @@ int launch_attention(const float* q, const __nv_bfloat16* k, const __nv_bfloat16
 // current device (0 if the shape is not built or the query failed).
 int attention_decode_blocks_per_sm(int hd, int group);
 
+// With pos_final the positions, sequence slots and the cached K/V of the
+// earlier positions are final when the kernel starts (the previous launch
+// triggers its dependents only after its own wait): the first K/V stages
+// are then copied before the wait.
 int launch_attention_decode(const float* qkv, const float* q_norm, const float* k_norm, float eps,
                             const float2* rope_cs, __nv_bfloat16* kc, __nv_bfloat16* vc, const int32_t* row_seq,
                             const int32_t* row_pos, int R, int nh, int nkv, int hd, int cap, int splits, float* part,
-                            __half* outh, int ldh, int32_t* status, cudaStream_t st, int frag);
+                            __half* outh, int ldh, int32_t* status, cudaStream_t st, int frag, int pos_final = 0);
 
 // Causal prefill attention on tensor cores (GROUP == 2, hd == 128): blocks
 // of 32 prompt positions of one sequence, {sequence, first position, flat
