@@ -935,7 +935,11 @@ static int run_prefill(q3i8_ctx* c, int B, const int32_t* d_ids, const int32_t* 
             a.xh = xh + (size_t)2 * m0 * K;
             if (y) a.y = y + (size_t)m0 * ldy, a.ldy = ldy;
             if (yh) a.yh = yh + (size_t)2 * m0 * ldyh, a.ldyh = ldyh;
-            launch_gemv(a, mode, gemv_grid(a.rows, mode, c->num_sms), st);
+            a.status = c->status;
+            // the residual projections split K over a cluster of CTAs, as in the decode step
+            const int ks = mode == kResid ? kResidSplit : 1;
+            a.ksplit = ks;
+            launch_gemv(a, mode, gemv_grid(a.rows, mode, c->num_sms) * ks, st);
         }
     };
     // causal attention: the tensor-core kernel over 32-position query blocks

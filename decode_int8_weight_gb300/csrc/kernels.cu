@@ -270,12 +270,13 @@ __global__ void __launch_bounds__(256) gemv_kernel(GemvArgs a) {
 // memory and CTA 0 of the cluster adds the parts in order through
 // distributed shared memory, so the result has the same bits as the parked
 // parts of gemv_kernel and needs no counter or second pass through global
-// memory.  Used for the fragment-ordered operands of the decode step; the
-// epilogues are gemv_kernel's.
+// memory.  Used by the decode step (fragment-ordered operand planes) and by
+// the prefill of up to 32 rows per chunk (plain planes); the epilogues are
+// gemv_kernel's.
 // =====================================================================
 constexpr uint32_t kGemvStageMax = 64u * 1024u;  // largest weight slice staged (bytes)
 
-template <int NT, int MODE>
+template <int NT, int MODE, bool FRAG>
 __global__ void __launch_bounds__(256, NT >= 8 ? (MODE == kSiluGate ? 3 : 2) : (NT == 1 && MODE == kSiluGate ? 6 : 1))
 gemv_staged_kernel(GemvArgs a) {
     if (!a.late_dependents) pdl_launch_dependents();
@@ -342,8 +343,17 @@ gemv_staged_kernel(GemvArgs a) {
             // all tiles' first k-steps, then their second ones: no MMA waits on the one before it
             uint4 bw[NT];
 #pragma unroll
-            for (int n = 0; n < NT; ++n)
-                bw[n] = *reinterpret_cast<const uint4*>(a.xh + ((((size_t)p * 8 + n) * 32 + lane) << 3));
+            for (int n = 0; n < NT; ++n) {
+                if constexpr (FRAG) {
+                    bw[n] = *reinterpret_cast<const uint4*>(a.xh + ((((size_t)p * 8 + n) * 32 + lane) << 3));
+                } else {
+                    const __half* xr = a.xh + (size_t)(8 * n + (lane >> 2)) * a.K + p * 32 + 2 * (lane & 3);
+                    bw[n].x = *reinterpret_cast<const uint32_t*>(xr);
+                    bw[n].y = *reinterpret_cast<const uint32_t*>(xr + 8);
+                    bw[n].z = *reinterpret_cast<const uint32_t*>(xr + 16);
+                    bw[n].w = *reinterpret_cast<const uint32_t*>(xr + 24);
+                }
+            }
 #pragma unroll
             for (int n = 0; n < NT; ++n) mma_f16_16816(acc[n], A0, bw[n].x, bw[n].y);
 #pragma unroll
@@ -618,9 +628,9 @@ static void launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
 
 // The staged kernel with ks-CTA clusters (ks > 1), programmatic stream
 // serialization and dyn bytes of dynamic shared memory.
-template <int NT, int MODE>
+template <int NT, int MODE, bool FRAG>
 static bool launch_gemv_staged(const GemvArgs& a, int grid, int ks, uint32_t dyn, cudaStream_t st) {
-    const void* fn = (const void*)gemv_staged_kernel<NT, MODE>;
+    const void* fn = (const void*)gemv_staged_kernel<NT, MODE, FRAG>;
     if (allow_max_dynamic_smem(fn) != cudaSuccess) return false;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
@@ -636,7 +646,7 @@ static bool launch_gemv_staged(const GemvArgs& a, int grid, int ks, uint32_t dyn
     at[1].val.clusterDim.z = 1;
     cfg.attrs = at;
     cfg.numAttrs = ks > 1 ? 2 : 1;
-    return cudaLaunchKernelEx(&cfg, gemv_staged_kernel<NT, MODE>, a) == cudaSuccess;
+    return cudaLaunchKernelEx(&cfg, gemv_staged_kernel<NT, MODE, FRAG>, a) == cudaSuccess;
 }
 
 // Shared memory above which the wide lm_head kernel is not used (bytes of
@@ -673,17 +683,24 @@ static bool launch_lm_head_wide(const GemvArgs& a, cudaStream_t st) {
 template <int NT>
 static void launch_gemv_nt(const GemvArgs& a, int mode, int grid, cudaStream_t st) {
     if (mode == kArgmax && a.xfrag && launch_lm_head_wide<NT>(a, st)) return;
-    // fragment-ordered operands with one CTA per (tile, K part) whose
-    // weight slice fits: the staged kernel
+    // one CTA per (tile, K part) whose weight slice fits: the staged kernel
     const int ks = (mode == kResid && a.ksplit > 1) ? a.ksplit : 1;
     const int kpairs = a.K >> 5;
     const uint32_t dyn = (uint32_t)((kpairs + ks - 1) / ks) * 512u;
-    if (mode != kArgmax && a.xfrag && grid == (a.rows >> 4) * ks && ks <= 8 && dyn <= kGemvStageMax) {
+    if (mode != kArgmax && grid == (a.rows >> 4) * ks && ks <= 8 && dyn <= kGemvStageMax) {
         bool ok = false;
-        switch (mode) {
-            case kStore: ok = launch_gemv_staged<NT, kStore>(a, grid, ks, dyn, st); break;
-            case kResid: ok = launch_gemv_staged<NT, kResid>(a, grid, ks, dyn, st); break;
-            default: ok = launch_gemv_staged<NT, kSiluGate>(a, grid, ks, dyn, st); break;
+        if (a.xfrag) {
+            switch (mode) {
+                case kStore: ok = launch_gemv_staged<NT, kStore, true>(a, grid, ks, dyn, st); break;
+                case kResid: ok = launch_gemv_staged<NT, kResid, true>(a, grid, ks, dyn, st); break;
+                default: ok = launch_gemv_staged<NT, kSiluGate, true>(a, grid, ks, dyn, st); break;
+            }
+        } else {
+            switch (mode) {
+                case kStore: ok = launch_gemv_staged<NT, kStore, false>(a, grid, ks, dyn, st); break;
+                case kResid: ok = launch_gemv_staged<NT, kResid, false>(a, grid, ks, dyn, st); break;
+                default: ok = launch_gemv_staged<NT, kSiluGate, false>(a, grid, ks, dyn, st); break;
+            }
         }
         if (ok) return;
     }
