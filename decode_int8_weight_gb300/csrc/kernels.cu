@@ -465,22 +465,30 @@ gemv_staged_kernel(GemvArgs a) {
 // weight bytes at NT = 8).  Here the activation planes (NT column tiles of
 // every k-pair, fragment order) are bulk-copied into shared memory once per
 // CTA, and each warp takes whole weight tiles (all of K) in turn: it streams
-// a tile's bytes from global memory in batches of kHeadBatch k-pairs (asking
+// a tile's bytes from global memory in batches of head_batch k-pairs (asking
 // L2 for its next tile meanwhile) and keeps the running argmax key of each
 // of its lanes' sequences in registers.  No partial sums cross warps.  The
 // keys meet in shared memory, then in global memory; the last CTA publishes
 // the tokens as gemv_kernel does.  The dot products are summed over K in
 // k-pair order by one warp.
 // =====================================================================
-constexpr int kHeadBatch = 4;  // k-pairs of weights in flight per warp
+// k-pairs of weights per batch (two batches in flight per warp); 2 at 8
+// column tiles, where 16 warps per SM share the latency
+template <int NT>
+__host__ __device__ constexpr int head_batch() { return NT >= 8 ? 2 : 4; }
 
 Q3_DEV void prefetch_tile_l2(const uint8_t* tile_base, uint32_t bytes, int lane) {
     for (uint32_t off = (uint32_t)lane * 4096u; off < bytes; off += 32u * 4096u)
         prefetch_l2_bulk(tile_base + off, bytes - off < 4096u ? bytes - off : 4096u);
 }
 
+// Threads per CTA: at 8 column tiles one CTA fills an SM's shared memory, so
+// it takes 16 warps to hide the MMA and conversion latencies.
 template <int NT>
-__global__ void __launch_bounds__(256) lm_head_wide_kernel(GemvArgs a) {
+__host__ __device__ constexpr int head_threads() { return NT >= 8 ? 512 : 256; }
+
+template <int NT>
+__global__ void __launch_bounds__(head_threads<NT>()) lm_head_wide_kernel(GemvArgs a) {
     pdl_launch_dependents();
     extern __shared__ __align__(128) unsigned char xs[];  // [kpairs][NT][32 lanes][16 B]
     __shared__ __align__(8) uint64_t xbar;
@@ -489,10 +497,12 @@ __global__ void __launch_bounds__(256) lm_head_wide_kernel(GemvArgs a) {
     __shared__ int is_last;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
     const int n_tiles = a.rows >> 4, kpairs = a.K >> 5;
-    const int nw = gridDim.x * 8;
+    constexpr int kW = head_threads<NT>() / 32;  // warps per CTA
+    constexpr int kHeadBatch = head_batch<NT>();
+    const int nw = gridDim.x * kW;
     const size_t blob = kTileHeader + 16 * (size_t)a.K;
     const uint32_t wbytes = 16u * (uint32_t)a.K;
-    int tile = blockIdx.x * 8 + warp;
+    int tile = blockIdx.x * kW + warp;
     // the weights do not depend on the previous kernel
     if (tile < n_tiles) prefetch_tile_l2(a.w + (size_t)tile * blob + kTileHeader, wbytes, lane);
     if (threadIdx.x == 0) {
@@ -662,14 +672,15 @@ static bool launch_lm_head_wide(const GemvArgs& a, cudaStream_t st) {
     int dev = 0, sms = 0, per_sm = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, lm_head_wide_kernel<NT>, 256, dyn) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, lm_head_wide_kernel<NT>, head_threads<NT>(), dyn) !=
+            cudaSuccess ||
         per_sm < 1)
         return false;
-    const int tiles = a.rows >> 4;
-    const int grid = std::min(sms * per_sm, (tiles + 7) / 8);
+    const int tiles = a.rows >> 4, warps = head_threads<NT>() / 32;
+    const int grid = std::min(sms * per_sm, (tiles + warps - 1) / warps);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(256);
+    cfg.blockDim = dim3(head_threads<NT>());
     cfg.dynamicSmemBytes = dyn;
     cfg.stream = st;
     cudaLaunchAttribute at[1];
