@@ -437,17 +437,16 @@ extern "C" void q3i8_destroy(q3i8_ctx* c) {
 
 // ------------------------------------------------------------------ the decode step
 
-// KV splits of the decode attention: as many as fill one wave of resident
-// attention CTAs (at least one).  One split writes the output itself and
-// needs no merge launch.  Measured per step at 0.6B: B = 32, one split
-// instead of five 1.10 vs 1.17 ms; B = 8 and 16 the same as the earlier
-// rule of 8 CTAs per SM; B = 1 within 0.5 % (the context caps the count).
+// CTAs per kv head of the decode attention: as many as fill one wave of
+// resident attention CTAs, at least one per row, and no more than the rows
+// can use (one per 64-position chunk of the capacity, at most
+// dec_splits_max per row).  The kernel shares them between the rows by their
+// lengths (long rows take several splits, short ones one), so no CTA's split
+// is much longer than the others.
 int decode_splits(const q3i8_ctx* c, int B) {
-    const int pairs = B * c->d.n_kv_heads;
-    int s = c->attn_resident > 0 ? c->attn_resident / pairs : (8 * c->num_sms + pairs - 1) / pairs;
-    s = std::min(s, c->cap / kChunkPos);
-    s = std::min(s, c->dec_splits_max);
-    return std::max(s, 1);
+    const int per_head = c->attn_resident > 0 ? c->attn_resident / c->d.n_kv_heads : 8 * c->num_sms / c->d.n_kv_heads;
+    const int per_row = std::max(1, std::min(c->dec_splits_max, c->cap / kChunkPos));
+    return std::max(B, std::min(per_head, B * per_row));
 }
 
 // Enqueue one decode step for B sequences: tokens[b] at positions pos[b].
@@ -488,8 +487,8 @@ int enqueue_step(q3i8_ctx* c, int B, bool want_logits) {
         a.late_dependents = 1;
         launch_gemv(a, kStore, gemv_grid(a.rows, kStore, c->num_sms), st);
         if (launch_attention_decode(c->qkv, L.q_norm, L.k_norm, d.rms_eps, c->rope, c->kc + l * layer_kv,
-                                    c->vc + l * layer_kv, c->seq_ids, c->pos, B, nh, nkv, hd, c->cap, splits, c->part,
-                                    c->oh, Dq, c->status, st, 1, 1))
+                                    c->vc + l * layer_kv, c->seq_ids, c->pos, B, nh, nkv, hd, c->cap, splits,
+                                    c->dec_splits_max, c->part, c->oh, Dq, c->status, st, 1))
             return fail(c, Q3_ERR_CUDA, "decode attention could not be launched");
         a = GemvArgs{};
         a.B = B;
@@ -770,7 +769,7 @@ static int enqueue_decode_step(q3i8_ctx* c, int B, bool want_logits) {
 int step_launches(const q3i8_ctx* c, int B) {
     if (persistent_for(c, B)) return 1;
     if (fused_for(c, B)) return 2 * c->d.n_layers + 1;
-    return 2 + c->d.n_layers * (decode_splits(c, B) == 1 ? 5 : 6) + 1;
+    return 2 + c->d.n_layers * (decode_splits(c, B) > B ? 6 : 5) + 1;
 }
 // Kernels of one prefill over M prompt rows: embed; per layer 2 RMSNorms, the
 // QK-norm/RoPE/append, attention split + merge and the 4 projections (one

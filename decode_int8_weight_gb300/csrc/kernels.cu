@@ -1160,6 +1160,45 @@ __global__ void __launch_bounds__(128) attn_split_kernel(const float* q, const _
     attn_write_partial<HD, GROUP>(m, l, acc, wm, wl, wacc, outp, splits, sp);
 }
 
+// The decode attention's balanced split plan.  Row r of the step (len_r =
+// row_pos[r] + 1 positions, R <= 32 rows) gets s_r = ceil(len_r / P) splits
+// of P positions, P the smallest multiple of kChunk with sum_r s_r <= G and
+// every s_r <= smax (G >= R): long rows take more CTAs than short ones and
+// every split is at most P long.  Evaluated by one whole warp; every lane
+// returns P.
+Q3_DEV int plan_split_len(const int32_t* row_pos, int R, int G, int smax, int cap) {
+    const int lane = threadIdx.x & 31;
+    const int len = lane < R ? row_pos[lane] + 1 : 0;
+    const int total = __reduce_add_sync(0xffffffffu, len);
+    const int maxlen = __reduce_max_sync(0xffffffffu, len);
+    int P = max((total + G - 1) / G, (maxlen + smax - 1) / smax);
+    P = max(kChunk, (P + kChunk - 1) / kChunk * kChunk);
+#pragma unroll 1
+    for (int it = 0; it <= cap / kChunk; ++it) {  // P >= maxlen fits (G >= R)
+        if (__reduce_add_sync(0xffffffffu, (len + P - 1) / P) <= G) break;
+        P += kChunk;
+    }
+    return P;
+}
+
+// CTA `i` of a kv head under the plan: its row (or -1 when the rows need
+// fewer than i + 1 splits), its split index and its row's split count.
+Q3_DEV void plan_cta(const int32_t* row_pos, int R, int P, int i, int& r, int& sp, int& nr) {
+    const int lane = threadIdx.x & 31;
+    const int s = lane < R ? (row_pos[lane] + 1 + P - 1) / P : 0;
+    int incl = s;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+    }
+    const int excl = incl - s;
+    const unsigned hit = __ballot_sync(0xffffffffu, s > 0 && excl <= i && i < incl);
+    r = hit ? __ffs(hit) - 1 : -1;
+    sp = r >= 0 ? i - __shfl_sync(0xffffffffu, excl, r) : 0;
+    nr = r >= 0 ? __shfl_sync(0xffffffffu, s, r) : 0;
+}
+
 // Whether the decode attention asks L2 for its cached K/V before waiting on
 // the previous kernel.
 constexpr bool kAttnPrefetch = true;
@@ -1172,8 +1211,8 @@ __global__ void __launch_bounds__(128) attn_decode_kernel(const float* qkv, cons
                                                           float eps, const float2* rope_cs, __nv_bfloat16* kc,
                                                           __nv_bfloat16* vc, const int32_t* row_seq,
                                                           const int32_t* row_pos, int nh, int nkv, int cap,
-                                                          int splits, float* part, __half* outh, int ldh, int frag,
-                                                          int pos_final, int32_t* status) {
+                                                          int G, int R, int smax, float* part, __half* outh,
+                                                          int ldh, int frag, int32_t* status) {
     pdl_launch_dependents();
     using Ln = AttnLanes<HD, GROUP>;
     constexpr int D = Ln::DL;
@@ -1183,38 +1222,43 @@ __global__ void __launch_bounds__(128) attn_decode_kernel(const float* qkv, cons
     __shared__ float wm[4][GROUP], wl[4][GROUP];
     __shared__ float wacc[4][GROUP][HD];
     __shared__ float qs[GROUP][HD], kp[HD], vp[HD];
+    __shared__ int s_plan[4];  // P, row, split, the row's splits
 
-    const int sp = blockIdx.x, g = blockIdx.y, r = blockIdx.z;
+    const int g = blockIdx.y;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    // With pos_final the positions and the cached K/V of positions < pos are
-    // final already (every launch before the previous one has completed):
-    // the first two stages are issued now.  Otherwise the cached range is
-    // only asked of L2 (the position read here may be early).
-    bool early = false;
-    if (pos_final) {
-        const int pos = row_pos[r], seq = row_seq[r];
-        int per = (pos + splits) / splits;
-        per = (per + kChunk - 1) / kChunk * kChunk;
-        const int start = sp * per, end = min(pos + 1, start + per);
-        const int cend = (pos >= start && pos < end) ? pos : end;
-        early = start < end;
-        if (early && threadIdx.x == 0) {
-            const size_t head_base = ((size_t)seq * nkv + g) * cap * HD;
-            mbar_init(&sm.bar[0], 1);
-            mbar_init(&sm.bar[1], 1);
-            fence_mbar_init();
-            attn_issue_first<HD>(sm, kc + head_base + (size_t)start * HD, vc + head_base + (size_t)start * HD, start,
-                                 cend);
-        }
+    // The positions and the cached K/V of positions < pos are final here:
+    // the previous launch lets this one start only after its own wait, when
+    // every launch before it has completed.  The split plan is made now and
+    // the first two stages are issued before the wait.
+    if (warp == 0) {
+        const int P = plan_split_len(row_pos, R, G, smax, cap);
+        int pr, psp, pnr;
+        plan_cta(row_pos, R, P, blockIdx.x, pr, psp, pnr);
+        if (lane == 0) s_plan[0] = P, s_plan[1] = pr, s_plan[2] = psp, s_plan[3] = pnr;
+    }
+    __syncthreads();
+    const int P = s_plan[0], r = s_plan[1], sp = s_plan[2], nr = s_plan[3];
+    if (r < 0) return;  // the rows need fewer splits than this kv head has CTAs
+    const int pos = row_pos[r], seq = row_seq[r];
+    const int len = pos + 1;
+    const int start = sp * P;
+    const int end = min(len, start + P);  // non-empty: sp < ceil(len / P)
+    const bool owns_p = pos >= start && pos < end;
+    const int cend = owns_p ? pos : end;  // cached positions only
+    const size_t head_base = ((size_t)seq * nkv + g) * cap * HD;
+    if (threadIdx.x == 0) {
+        mbar_init(&sm.bar[0], 1);
+        mbar_init(&sm.bar[1], 1);
+        fence_mbar_init();
+        attn_issue_first<HD>(sm, kc + head_base + (size_t)start * HD, vc + head_base + (size_t)start * HD, start,
+                             cend);
     }
     if (kAttnPrefetch) {
-        const int pos = min(row_pos[r], cap - 1);
-        int per = (pos + splits) / splits;
-        per = (per + kChunk - 1) / kChunk * kChunk;
-        const int lo = sp * per + (early ? 2 * kChunk : 0), hi = min(pos, sp * per + per);
-        if (pos >= 0 && lo < hi) {
-            const size_t base = (((size_t)row_seq[r] * nkv + g) * cap + lo) * HD;
-            const uint32_t bytes = (uint32_t)(hi - lo) * HD * 2u;
+        // the rest of the split: asked of L2
+        const int lo = start + 2 * kChunk;
+        if (lo < cend) {
+            const size_t base = head_base + (size_t)lo * HD;
+            const uint32_t bytes = (uint32_t)(cend - lo) * HD * 2u;
             for (uint32_t off = threadIdx.x * 4096u; off < bytes; off += blockDim.x * 4096u) {
                 const uint32_t n = bytes - off < 4096u ? bytes - off : 4096u;
                 prefetch_l2_bulk(reinterpret_cast<const uint8_t*>(kc + base) + off, n);
@@ -1223,28 +1267,8 @@ __global__ void __launch_bounds__(128) attn_decode_kernel(const float* qkv, cons
         }
     }
     pdl_wait();
+    float* outp = part + ((size_t)r * nh + (size_t)g * GROUP) * smax * (HD + 2);
 
-    const int pos = row_pos[r], seq = row_seq[r];
-    const int len = pos + 1;
-    int per = (len + splits - 1) / splits;
-    per = (per + kChunk - 1) / kChunk * kChunk;
-    const int start = sp * per;
-    const int end = min(len, start + per);
-    float* outp = part + ((size_t)r * nh + (size_t)g * GROUP) * splits * (HD + 2);
-    if (start >= end) {
-        for (int i = threadIdx.x; i < GROUP * (HD + 2); i += blockDim.x) {
-            const int h = i / (HD + 2), e = i % (HD + 2);
-            outp[((size_t)h * splits + sp) * (HD + 2) + e] = (e == HD) ? -INFINITY : 0.f;
-        }
-        return;
-    }
-    const bool owns_p = pos >= start && pos < end;
-    const size_t head_base = ((size_t)seq * nkv + g) * cap * HD;
-    if (threadIdx.x == 0 && !early) {
-        mbar_init(&sm.bar[0], 1);
-        mbar_init(&sm.bar[1], 1);
-        fence_mbar_init();
-    }
     // the group's queries (and, in the owning split, the new K and V): one
     // warp per head, lane l holding elements l + 32j
     const float* row = qkv + (size_t)r * (nh + 2 * nkv) * HD;
@@ -1304,9 +1328,8 @@ __global__ void __launch_bounds__(128) attn_decode_kernel(const float* qkv, cons
 #pragma unroll
         for (int d = 0; d < D; ++d) acc[h][d] = 0.f;
     }
-    const int cend = owns_p ? pos : end;  // cached positions only
     if (!attn_chunks<HD, GROUP>(sm, kc + head_base + (size_t)start * HD, vc + head_base + (size_t)start * HD, start,
-                                cend, qr, scale, m, l, acc, status, early))
+                                cend, qr, scale, m, l, acc, status, true))
         return;
     if (owns_p && warp == 0) {
         // position p from the rounded values kept in shared memory (every
@@ -1328,7 +1351,8 @@ __global__ void __launch_bounds__(128) attn_decode_kernel(const float* qkv, cons
             m[h] = mn;
         }
     }
-    attn_write_partial<HD, GROUP>(m, l, acc, wm, wl, wacc, outp, splits, sp, outh, ldh, frag, r, g * GROUP);
+    attn_write_partial<HD, GROUP>(m, l, acc, wm, wl, wacc, outp, smax, sp, nr == 1 ? outh : nullptr, ldh, frag, r,
+                                  g * GROUP);
 }
 
 // out[r][h][:] = sum_s acc_s e^{m_s - M} / sum_s l_s e^{m_s - M} over the
@@ -1337,18 +1361,37 @@ __global__ void __launch_bounds__(128) attn_decode_kernel(const float* qkv, cons
 // (loads batched eight splits at a time; the sum stays in split order).
 template <int HD>
 __global__ void attn_merge_kernel(const float* part, int nh, int splits, const int32_t* row_len, int len_add,
-                                  float* out, __half* outh, int ldh, int frag) {
+                                  float* out, __half* outh, int ldh, int frag, int plan_G, int plan_R,
+                                  int plan_cap) {
     pdl_launch_dependents();
-    pdl_wait();
     __shared__ float sm_m[64], sm_f[64];
     __shared__ float s_l;
+    __shared__ int s_per;
     const int rh = blockIdx.x;  // r * nh + h
     const int d = threadIdx.x;
     const int r = rh / nh, h = rh % nh;
-    const int len = row_len[r] + len_add;
-    int per = (len + splits - 1) / splits;
-    per = (per + kChunk - 1) / kChunk * kChunk;
-    const int nne = min(splits, (len + per - 1) / per);
+    int nne;
+    if (plan_G > 0) {
+        // the decode attention's balanced plan (row_len = positions, len_add =
+        // 1), made before the wait as the attention makes it: the positions
+        // are final once the attention has started.  A row of one split has
+        // had its output written by the attention (every CTA still waits, so
+        // this launch cannot complete before the attention)
+        if (d < 32) {
+            const int P = plan_split_len(row_len, plan_R, plan_G, splits, plan_cap);
+            if (d == 0) s_per = P;
+        }
+        __syncthreads();
+        nne = (row_len[r] + len_add + s_per - 1) / s_per;
+        pdl_wait();
+        if (nne == 1) return;
+    } else {
+        pdl_wait();
+        const int len = row_len[r] + len_add;
+        int per = (len + splits - 1) / splits;
+        per = (per + kChunk - 1) / kChunk * kChunk;
+        nne = min(splits, (len + per - 1) / per);
+    }
     const float* p = part + (size_t)rh * splits * (HD + 2);
     if (d < 32) {
         // lane j holds splits j and j + 32
@@ -1410,7 +1453,7 @@ int launch_attention(const float* q, const __nv_bfloat16* k, const __nv_bfloat16
                                     st))                                                              \
             return -2;                                                                                \
         attn_merge_kernel<HDV><<<R * nh, HDV, 0, st>>>(part, nh, splits, row_len, len_add, out, outh, ldh, \
-                                                       frag);                                                 \
+                                                       frag, 0, 0, 0);                                        \
         return 0;                                                                                     \
     }
     Q3_ATTN_CASE(128, 1)
@@ -1428,14 +1471,13 @@ int launch_attention(const float* q, const __nv_bfloat16* k, const __nv_bfloat16
 template <int HD, int GROUP>
 static bool launch_attn_decode_t(const float* qkv, const float* q_norm, const float* k_norm, float eps,
                                  const float2* rope_cs, __nv_bfloat16* kc, __nv_bfloat16* vc, const int32_t* row_seq,
-                                 const int32_t* row_pos, int R, int nh, int nkv, int cap, int splits, float* part,
-                                 __half* outh, int ldh, int frag, int pos_final, int32_t* status,
-                                 cudaStream_t st) {
+                                 const int32_t* row_pos, int R, int nh, int nkv, int cap, int G, int smax,
+                                 float* part, __half* outh, int ldh, int frag, int32_t* status, cudaStream_t st) {
     const int smem = (int)sizeof(AttnSmem<HD>);
     if (allow_max_dynamic_smem((const void*)attn_decode_kernel<HD, GROUP>) != cudaSuccess) return false;
-    dim3 grid(splits, nkv, R);
+    dim3 grid(G, nkv, 1);
     launch_pdl(attn_decode_kernel<HD, GROUP>, grid, 128, smem, st, qkv, q_norm, k_norm, eps, rope_cs, kc, vc, row_seq,
-               row_pos, nh, nkv, cap, splits, part, outh, ldh, frag, pos_final, status);
+               row_pos, nh, nkv, cap, G, R, smax, part, outh, ldh, frag, status);
     return true;
 }
 
@@ -1466,19 +1508,19 @@ int attention_decode_blocks_per_sm(int hd, int group) {
 
 int launch_attention_decode(const float* qkv, const float* q_norm, const float* k_norm, float eps,
                             const float2* rope_cs, __nv_bfloat16* kc, __nv_bfloat16* vc, const int32_t* row_seq,
-                            const int32_t* row_pos, int R, int nh, int nkv, int hd, int cap, int splits, float* part,
-                            __half* outh, int ldh, int32_t* status, cudaStream_t st, int frag, int pos_final) {
+                            const int32_t* row_pos, int R, int nh, int nkv, int hd, int cap, int G, int smax,
+                            float* part, __half* outh, int ldh, int32_t* status, cudaStream_t st, int frag) {
     if (R <= 0) return 0;
+    if (R > 32 || G < R || smax < 1 || smax > 64) return -3;
     const int group = nh / nkv;
 #define Q3_ATTN_CASE(HDV, GV)                                                                                      \
     if (hd == HDV && group == GV) {                                                                                \
         if (!launch_attn_decode_t<HDV, GV>(qkv, q_norm, k_norm, eps, rope_cs, kc, vc, row_seq, row_pos, R, nh, nkv,  \
-                                           cap, splits, part, splits == 1 ? outh : nullptr, ldh, frag, pos_final,  \
-                                           status, st))                                                            \
+                                           cap, G, smax, part, outh, ldh, frag, status, st))                      \
             return -2;                                                                                             \
-        if (splits > 1)                                                                                            \
-            launch_pdl(attn_merge_kernel<HDV>, R * nh, HDV, 0, st, part, nh, splits, row_pos, 1, (float*)nullptr, \
-                       outh, ldh, frag);                                                                           \
+        if (G > R) /* some row may have more than one split */                                                    \
+            launch_pdl(attn_merge_kernel<HDV>, R * nh, HDV, 0, st, part, nh, smax, row_pos, 1, (float*)nullptr,   \
+                       outh, ldh, frag, G, R, cap);                                                                \
         return 0;                                                                                                  \
     }
     Q3_ATTN_CASE(128, 1)

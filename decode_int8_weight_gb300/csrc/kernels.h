@@ -119,23 +119,27 @@ int launch_attention(const float* q, const __nv_bfloat16* k, const __nv_bfloat16
                      float* part, float* out, __half* outh, int ldh, int32_t* status, cudaStream_t st,
                      int frag = 0);
 
-// One decode step's attention with the QK-RMSNorm, RoPE and bf16 KV append
-// folded in: qkv [R][(nh + 2 nkv) hd] fp32 as projected, row_pos[r] the new
-// position (appended, then attended with positions 0..row_pos[r]); output
-// hi/lo f16 planes (outh, ldh, frag as launch_attention).  With splits == 1
-// the attention kernel writes the output itself and no merge is launched.
 // Decode attention CTAs (head_dim hd, group nh / nkv) resident per SM of the
 // current device (0 if the shape is not built or the query failed).
 int attention_decode_blocks_per_sm(int hd, int group);
 
-// With pos_final the positions, sequence slots and the cached K/V of the
-// earlier positions are final when the kernel starts (the previous launch
-// triggers its dependents only after its own wait): the first K/V stages
-// are then copied before the wait.
+// One decode step's attention with the QK-RMSNorm, RoPE and bf16 KV append
+// folded in: qkv [R][(nh + 2 nkv) hd] fp32 as projected, row_pos[r] the new
+// position (appended, then attended with positions 0..row_pos[r]); output
+// hi/lo f16 planes (outh, ldh, frag as launch_attention).  G CTAs per kv
+// head (R <= G, R <= 32) share the rows' positions by the balanced plan:
+// row r gets ceil(len_r / P) splits of P positions, P the smallest multiple
+// of 64 for which the splits fit in G and no row has more than smax
+// (<= 64); part holds [R][nh][smax] partial states.  A row of one split is
+// written by the attention itself; a merge kernel follows when G > R.  The
+// launch before this one must trigger its dependents only after its own
+// wait: the positions and the cached K/V are read before this kernel waits.
+// Returns 0, -1 (head_dim / group not built), -2 (launch set-up failed) or
+// -3 (sizes out of range).
 int launch_attention_decode(const float* qkv, const float* q_norm, const float* k_norm, float eps,
                             const float2* rope_cs, __nv_bfloat16* kc, __nv_bfloat16* vc, const int32_t* row_seq,
-                            const int32_t* row_pos, int R, int nh, int nkv, int hd, int cap, int splits, float* part,
-                            __half* outh, int ldh, int32_t* status, cudaStream_t st, int frag, int pos_final = 0);
+                            const int32_t* row_pos, int R, int nh, int nkv, int hd, int cap, int G, int smax,
+                            float* part, __half* outh, int ldh, int32_t* status, cudaStream_t st, int frag);
 
 // Causal prefill attention on tensor cores (GROUP == 2, hd == 128): blocks
 // of 32 prompt positions of one sequence, {sequence, first position, flat
