@@ -47,16 +47,19 @@ struct GemvArgs {
     int advance_pos;
     int valid_rows;            // rows >= valid_rows (padding) take no part in the argmax
     float* logits;             // optional [B][valid_rows]
-    int ksplit;                // kResid only: K split over this many CTAs per tile (0 = 1).  With kpart the
-                               // parts are parked in kpart [tiles][ksplit][4 NT 16] and the last CTA of a
-                               // tile (tile_cnt [tiles], zero between launches, left zero) adds them in
-                               // order; without, each part atomically adds its share to y
+    int ksplit;                // kResid only: K split over this many CTAs per tile (0 = 1).  The staged
+                               // kernel (launch_gemv's choice whenever a CTA's weight slice fits in shared
+                               // memory) meets the parts in a thread-block cluster, in rank order.  The
+                               // per-item kernel parks them in kpart [tiles][ksplit][4 NT 16] and the last
+                               // CTA of a tile (tile_cnt [tiles], zero between launches, left zero) adds
+                               // them in order; without kpart each part atomically adds its share to y
     float* kpart;
     unsigned int* tile_cnt;
     int xfrag;                 // xh is in fragment order (plane_index), else plain [8*NT][K] planes
     int yfrag;                 // kSiluGate: yh in fragment order
-    // RMSNorm folded into its neighbours.  kResid (with kpart): the tile's
-    // last CTA also writes the next norm's operand planes, norm_g * x in
+    // RMSNorm folded into its neighbours.  kResid (staged kernel, or the
+    // per-item kernel with kpart): the CTA that finishes a tile also writes
+    // the next norm's operand planes, norm_g * x in
     // fragment order (hi/lo), for its rows into norm_xh ([8*NT][norm_H]),
     // and adds its rows' sum of squares of x per sequence to ss_out (64-bit
     // fixed point, value * 2^32: the sum does not depend on the order of the
